@@ -1,0 +1,399 @@
+/*
+ * dh_oracle.c -- plain, slow CPU oracle for the 2-bit draft head with exact rerank.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link or call this
+ * file; only the test-suite, the smoke check and the benchmark's CPU-baseline leg do.
+ * It shares no code, header, table or constant with the CUDA library.
+ *
+ * Source of every step: the page "radiance_drafthead.py" (module docstring bullets and the
+ * functions _quantize_head_now, _draft_head_int2, _emit, _apply_head_int2, _rerank_exact).
+ * Precision: the quantiser runs in IEEE fp32 exactly as the page's torch code does
+ * (correctly rounded division, no fused multiply-add, round half to even); everything the
+ * page leaves to "the math" (coarse value, exact logit, exact head) runs in fp64.
+ * Selection decisions are taken on fp32-rounded values, the precision the page's kernel
+ * holds its accumulator in.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread (no -ffast-math, ever).
+ *
+ * Parity status per function (pins live in tests/test_oracle_pins.py):
+ *   orc_quantize       pinned: hand-worked golden groups, invariants, error bound
+ *   orc_pack/unpack    pinned: golden bytes, round trip, plane placement
+ *   orc_coarse         pinned: collapsed form == direct dequant-and-dot (exact scales)
+ *   orc_block_topk     pinned: brute force full sort on tiny inputs, KC=64 special case
+ *   orc_select_topr    pinned: brute force, R = all candidates special case
+ *   orc_rerank         pinned: exact integer arithmetic on scaled bf16 values
+ *   orc_exact_head     pinned: exact integer arithmetic; KC=64,R=V reduces forward to it
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+#include <pthread.h>
+
+/* ------------------------------------------------------------------------------------- */
+/* bf16 <-> fp32, written out from the IEEE definitions                                  */
+/* ------------------------------------------------------------------------------------- */
+
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Round an fp32 value to bf16, nearest with ties to even (what torch's .to(bfloat16) does). */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) /* NaN: keep it a NaN */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t upper = u >> 16;
+    uint32_t lower = u & 0xFFFFu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* Round half to even on an fp32 value (torch.round semantics), written out explicitly. */
+static float round_half_even(float x)
+{
+    float fl = floorf(x);
+    float diff = x - fl; /* exact: x and floor(x) share the exponent range */
+    if (diff > 0.5f) return fl + 1.0f;
+    if (diff < 0.5f) return fl;
+    /* exactly halfway: pick the even neighbour */
+    double half = (double)fl * 0.5;
+    return (floor(half) == half) ? fl : fl + 1.0f;
+}
+
+static float clampf(float v, float lo, float hi)
+{
+    if (v < lo) return lo;
+    if (v > hi) return hi;
+    return v;
+}
+
+/* ------------------------------------------------------------------------------------- */
+/* Quantiser and packing: radiance_drafthead.py, _quantize_head_now                       */
+/* ------------------------------------------------------------------------------------- */
+
+#define GROUP 128
+#define LEVELS 3.0f /* (1 << BITS) - 1 at BITS = 2 */
+#define BIAS 4.0f   /* 2^m for the mantissa slot m = 5 of the bit-pattern dequant */
+
+/*
+ * Per (row n, group gi of 128 consecutive k), in fp32:
+ *   lo, hi = min, max of the group;   sc = max((hi - lo) / 3, 1e-8)
+ *   zp = clamp(round(-lo / sc), 0, 3);   q_k = clamp(round(w_k / sc + zp), 0, 3)
+ *   S = bf16(4 sc);   ZS = bf16(4 sc + zp sc)          (the premultiplied pair)
+ * Packing (quarter split): byte j of a row holds q[j] | q[Q+j]<<2 | q[2Q+j]<<4 | q[3Q+j]<<6,
+ * Q = H/4.  Optional outputs sc_out / zp_out expose the fp32 scale and zero point.
+ * Returns 0, or -2 when H is not a multiple of 512 (whole groups in every quarter).
+ */
+int orc_quantize(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint16_t *S,
+                 uint16_t *ZS, float *sc_out, float *zp_out)
+{
+    if (H <= 0 || H % 512 != 0 || V <= 0) return -2;
+    const int64_t NGt = H / GROUP, Q = H / 4;
+    uint8_t *q = (uint8_t *)malloc((size_t)H);
+    if (!q) return -1;
+    for (int64_t n = 0; n < V; ++n) {
+        const uint16_t *row = W + n * H;
+        for (int64_t gi = 0; gi < NGt; ++gi) {
+            float lo = bf16_to_f32(row[gi * GROUP]), hi = lo;
+            for (int t = 1; t < GROUP; ++t) {
+                float w = bf16_to_f32(row[gi * GROUP + t]);
+                if (w < lo) lo = w;
+                if (w > hi) hi = w;
+            }
+            float sc = (hi - lo) / LEVELS;
+            if (sc < 1e-8f) sc = 1e-8f;
+            float zp = clampf(round_half_even((-lo) / sc), 0.0f, LEVELS);
+            for (int t = 0; t < GROUP; ++t) {
+                float w = bf16_to_f32(row[gi * GROUP + t]);
+                float r = round_half_even(w / sc + zp);
+                q[gi * GROUP + t] = (uint8_t)clampf(r, 0.0f, LEVELS);
+            }
+            float s4 = BIAS * sc;
+            float zsc = zp * sc;
+            S[n * NGt + gi] = f32_to_bf16_rne(s4);
+            ZS[n * NGt + gi] = f32_to_bf16_rne(s4 + zsc);
+            if (sc_out) sc_out[n * NGt + gi] = sc;
+            if (zp_out) zp_out[n * NGt + gi] = zp;
+        }
+        for (int64_t j = 0; j < Q; ++j)
+            packed[n * Q + j] = (uint8_t)(q[j] | (q[Q + j] << 2) | (q[2 * Q + j] << 4) |
+                                          (q[3 * Q + j] << 6));
+    }
+    free(q);
+    return 0;
+}
+
+/* Inverse of the quarter-split packing: codes[n, k] for k = plane*Q + j. */
+void orc_unpack(const uint8_t *packed, int64_t V, int64_t H, uint8_t *codes)
+{
+    const int64_t Q = H / 4;
+    for (int64_t n = 0; n < V; ++n)
+        for (int64_t k = 0; k < H; ++k) {
+            int64_t plane = k / Q, j = k % Q;
+            codes[n * H + k] = (uint8_t)((packed[n * Q + j] >> (2 * plane)) & 3u);
+        }
+}
+
+/* ------------------------------------------------------------------------------------- */
+/* Coarse value: radiance_drafthead.py, docstring "Bit-pattern dequant" bullet and        */
+/* _draft_head_int2.  c[m,n] = sum_gi ( S[n,gi] * p - ZS[n,gi] * xs ),                    */
+/*   p  = sum_{k in gi} x[m,k] * (1 + v[n,k]/4),   xs = sum_{k in gi} x[m,k]              */
+/* with S, ZS the stored bf16 values; fp64 throughout.                                    */
+/* ------------------------------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *x;
+    const uint8_t *packed;
+    const uint16_t *S, *ZS;
+    int M;
+    int64_t H, V, n0, n1;
+    double *c;
+} coarse_job;
+
+static void *coarse_worker(void *arg)
+{
+    coarse_job *jb = (coarse_job *)arg;
+    const int64_t H = jb->H, Q = H / 4, NGt = H / GROUP;
+    double *v = (double *)malloc((size_t)H * sizeof(double));
+    for (int64_t n = jb->n0; n < jb->n1; ++n) {
+        const uint8_t *prow = jb->packed + n * Q;
+        for (int64_t k = 0; k < H; ++k) /* v[n,k] from the packed byte j = k mod Q */
+            v[k] = (double)((prow[k % Q] >> (2 * (k / Q))) & 3u);
+        for (int m = 0; m < jb->M; ++m) {
+            const uint16_t *xr = jb->x + (int64_t)m * H;
+            double c = 0.0;
+            for (int64_t gi = 0; gi < NGt; ++gi) {
+                double p = 0.0, xs = 0.0;
+                for (int t = 0; t < GROUP; ++t) {
+                    double xk = (double)bf16_to_f32(xr[gi * GROUP + t]);
+                    p += xk * (1.0 + v[gi * GROUP + t] / 4.0);
+                    xs += xk;
+                }
+                c += (double)bf16_to_f32(jb->S[n * NGt + gi]) * p -
+                     (double)bf16_to_f32(jb->ZS[n * NGt + gi]) * xs;
+            }
+            jb->c[(int64_t)m * jb->V + n] = c;
+        }
+    }
+    free(v);
+    return NULL;
+}
+
+/* c is [M, V] fp64.  nthreads <= 1 runs on the calling thread. */
+void orc_coarse(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
+                int M, int64_t H, int64_t V, double *c, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    coarse_job jobs[256];
+    int64_t chunk = (V + nthreads - 1) / nthreads;
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        int64_t n0 = (int64_t)i * chunk, n1 = n0 + chunk;
+        if (n1 > V) n1 = V;
+        if (n0 >= n1) break;
+        jobs[i] = (coarse_job){x, packed, S, ZS, M, H, V, n0, n1, c};
+        if (nthreads == 1) {
+            coarse_worker(&jobs[i]);
+        } else {
+            pthread_create(&th[i], NULL, coarse_worker, &jobs[i]);
+            ++started;
+        }
+    }
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+}
+
+/* ------------------------------------------------------------------------------------- */
+/* Selection.  Order everywhere: value descending, equal values -> lower vocab index      */
+/* (the first maximum, as the page's argmax returns).                                     */
+/* ------------------------------------------------------------------------------------- */
+
+typedef struct {
+    float val;
+    int32_t idx;
+} cand;
+
+static int cand_cmp(const void *a, const void *b)
+{
+    const cand *x = (const cand *)a, *y = (const cand *)b;
+    if (x->val > y->val) return -1;
+    if (x->val < y->val) return 1;
+    return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
+}
+
+/*
+ * Block candidates: radiance_drafthead.py, _emit.  For each row m and each block b of 64
+ * columns [64b, min(64b+64, V)), the KC best columns by fp32 coarse value.  A block with
+ * fewer than KC valid columns emits only those.  Output slots are [M, nblk*KC] in block
+ * order, best first inside a block; unused slots get idx -1 and val -inf.
+ * Returns the number of valid candidates per row.
+ */
+int64_t orc_block_topk(const float *cf, int M, int64_t V, int kcand, float *cval, int32_t *cidx)
+{
+    const int64_t nblk = (V + 63) / 64;
+    int64_t nvalid = 0;
+    cand buf[64];
+    for (int m = 0; m < M; ++m) {
+        nvalid = 0;
+        for (int64_t b = 0; b < nblk; ++b) {
+            int64_t c0 = 64 * b, c1 = c0 + 64 < V ? c0 + 64 : V;
+            int cnt = (int)(c1 - c0);
+            for (int i = 0; i < cnt; ++i) {
+                buf[i].val = cf[(int64_t)m * V + c0 + i];
+                buf[i].idx = (int32_t)(c0 + i);
+            }
+            qsort(buf, (size_t)cnt, sizeof(cand), cand_cmp);
+            for (int s = 0; s < kcand; ++s) {
+                int64_t o = (int64_t)m * nblk * kcand + b * kcand + s;
+                if (s < cnt) {
+                    cval[o] = buf[s].val;
+                    cidx[o] = buf[s].idx;
+                    ++nvalid;
+                } else {
+                    cval[o] = -INFINITY;
+                    cidx[o] = -1;
+                }
+            }
+        }
+    }
+    return nvalid;
+}
+
+/*
+ * Global top-R: radiance_drafthead.py, _apply_head_int2 (BI gathered at BM.topk(RERANK)).
+ * Per row, the R best of the ncand slots (slots with idx < 0 are skipped).
+ * Returns 0, or -3 when a row has fewer than R valid candidates.
+ */
+int orc_select_topr(const float *cval, const int32_t *cidx, int M, int64_t ncand, int R,
+                    int32_t *sel_idx, float *sel_val)
+{
+    cand *buf = (cand *)malloc((size_t)ncand * sizeof(cand));
+    if (!buf) return -1;
+    for (int m = 0; m < M; ++m) {
+        int64_t cnt = 0;
+        for (int64_t i = 0; i < ncand; ++i) {
+            int32_t id = cidx[(int64_t)m * ncand + i];
+            if (id < 0) continue;
+            buf[cnt].val = cval[(int64_t)m * ncand + i];
+            buf[cnt].idx = id;
+            ++cnt;
+        }
+        if (cnt < R) {
+            free(buf);
+            return -3;
+        }
+        qsort(buf, (size_t)cnt, sizeof(cand), cand_cmp);
+        for (int j = 0; j < R; ++j) {
+            sel_idx[(int64_t)m * R + j] = buf[j].idx;
+            if (sel_val) sel_val[(int64_t)m * R + j] = buf[j].val;
+        }
+    }
+    free(buf);
+    return 0;
+}
+
+/*
+ * Exact rerank: radiance_drafthead.py, _rerank_exact (bf16 branch).
+ * e[m,j] = sum_k x[m,k] * W[idx[m,j], k], fp64.
+ */
+void orc_rerank(const uint16_t *x, const uint16_t *W, int M, int64_t H, const int32_t *idx, int R,
+                double *e)
+{
+    for (int m = 0; m < M; ++m)
+        for (int j = 0; j < R; ++j) {
+            const uint16_t *wr = W + (int64_t)idx[(int64_t)m * R + j] * H;
+            const uint16_t *xr = x + (int64_t)m * H;
+            double s = 0.0;
+            for (int64_t k = 0; k < H; ++k)
+                s += (double)bf16_to_f32(xr[k]) * (double)bf16_to_f32(wr[k]);
+            e[(int64_t)m * R + j] = s;
+        }
+}
+
+/*
+ * Result: the top-k of the R reranked entries (only reranked entries are eligible, the
+ * reading of the top-k caller in _apply_head_int2; argmax is k = 1).  Ranked on the
+ * fp32-rounded exact value, ties -> lower vocab index.  out_val receives the fp64 value.
+ */
+void orc_topk(const double *e, const int32_t *idx, int M, int R, int topk, int32_t *out_idx,
+              double *out_val)
+{
+    cand *buf = (cand *)malloc((size_t)R * sizeof(cand));
+    for (int m = 0; m < M; ++m) {
+        for (int j = 0; j < R; ++j) {
+            buf[j].val = (float)e[(int64_t)m * R + j];
+            buf[j].idx = idx[(int64_t)m * R + j];
+        }
+        qsort(buf, (size_t)R, sizeof(cand), cand_cmp);
+        for (int t = 0; t < topk; ++t) {
+            out_idx[(int64_t)m * topk + t] = buf[t].idx;
+            /* recover the fp64 value of that index */
+            for (int j = 0; j < R; ++j)
+                if (idx[(int64_t)m * R + j] == buf[t].idx) {
+                    out_val[(int64_t)m * topk + t] = e[(int64_t)m * R + j];
+                    break;
+                }
+        }
+    }
+    free(buf);
+}
+
+/* ------------------------------------------------------------------------------------- */
+/* Exact bf16 head, for recall: logits[m,n] = sum_k x[m,k] W[n,k], fp64.                  */
+/* ------------------------------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *x, *W;
+    int M;
+    int64_t H, V, n0, n1;
+    double *out;
+} head_job;
+
+static void *head_worker(void *arg)
+{
+    head_job *jb = (head_job *)arg;
+    for (int64_t n = jb->n0; n < jb->n1; ++n) {
+        const uint16_t *wr = jb->W + n * jb->H;
+        for (int m = 0; m < jb->M; ++m) {
+            const uint16_t *xr = jb->x + (int64_t)m * jb->H;
+            double s = 0.0;
+            for (int64_t k = 0; k < jb->H; ++k)
+                s += (double)bf16_to_f32(xr[k]) * (double)bf16_to_f32(wr[k]);
+            jb->out[(int64_t)m * jb->V + n] = s;
+        }
+    }
+    return NULL;
+}
+
+void orc_exact_head(const uint16_t *x, const uint16_t *W, int M, int64_t H, int64_t V,
+                    double *out, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    head_job jobs[256];
+    int64_t chunk = (V + nthreads - 1) / nthreads;
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        int64_t n0 = (int64_t)i * chunk, n1 = n0 + chunk;
+        if (n1 > V) n1 = V;
+        if (n0 >= n1) break;
+        jobs[i] = (head_job){x, W, M, H, V, n0, n1, out};
+        if (nthreads == 1) {
+            head_worker(&jobs[i]);
+        } else {
+            pthread_create(&th[i], NULL, head_worker, &jobs[i]);
+            ++started;
+        }
+    }
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+}

@@ -1,0 +1,343 @@
+"""Pins for the CPU oracle: it is checked against what the page and the mathematics fix,
+never against itself.  Page: radiance_drafthead.py (module docstring and functions).
+
+* hand-worked quantiser groups and packed bytes (tests/golden/*.json)
+* the bit-pattern identity 0x3F80 | ((b << (5-2q)) & 0x60) == bf16(1 + v/4), exhaustively
+* collapsed accumulator form == direct dequant-and-dot
+* special cases that reduce to textbook routines (grid weights -> exact head; KCAND=64 and
+  RERANK=V -> exact top-k of x W^T)
+* brute force on tiny inputs for the selections; exact integer arithmetic for the dots
+"""
+import json
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f2bf_exact(vals):
+    """Float values that are exactly representable in bf16 -> their bit patterns."""
+    out = []
+    for v in np.asarray(vals, dtype=np.float64).ravel():
+        b = struct.unpack("<I", struct.pack("<f", float(v)))[0]
+        assert b & 0xFFFF == 0, f"{v} is not a bf16 value"
+        out.append(b >> 16)
+    return np.array(out, dtype=np.uint16).reshape(np.shape(vals))
+
+
+def bf2f(bits):
+    return orc.bf16_bits_to_f64(bits)
+
+
+def f32_bits(x):
+    return struct.unpack("<I", struct.pack("<f", float(x)))[0]
+
+
+def my_unpack(packed, H):
+    """Test-side unpack, written from the docstring: byte j carries k = j + p*Q in bits 2p."""
+    Q = H // 4
+    planes = [(packed >> (2 * p)) & 3 for p in range(4)]
+    return np.concatenate(planes, axis=1).astype(np.uint8)  # k = p*Q + j
+
+
+# ------------------------------------------------------------------------------------------
+# quantiser and packing
+# ------------------------------------------------------------------------------------------
+
+def test_quantize_golden_groups():
+    spec = json.load(open(os.path.join(GOLD, "quantize_groups.json")))
+    for case in spec["cases"]:
+        group = np.tile(np.array(case["pattern"]), 32)          # 128 values
+        W = f2bf_exact(np.tile(group, 4)[None, :])              # H = 512: four equal groups
+        packed, S, ZS, sc, zp = orc.quantize(W, with_params=True)
+        codes = my_unpack(packed, 512)[0]
+        want = np.tile(np.array(case["codes"]), 128)
+        assert np.array_equal(codes, want), case["name"]
+        for g in range(4):
+            assert f32_bits(sc[0, g]) == int(case["sc_bits"], 16), case["name"]
+            assert zp[0, g] == case["zp"], case["name"]
+            assert S[0, g] == int(case["S"], 16), case["name"]
+            assert ZS[0, g] == int(case["ZS"], 16), case["name"]
+
+
+def test_packing_golden_bytes():
+    spec = json.load(open(os.path.join(GOLD, "packing.json")))
+    for row in spec["rows"]:
+        H = row["H"]
+        groups = [np.array([-0.75, 0.75] + [f] * 126) for f in row["group_fill"]]
+        W = f2bf_exact(np.concatenate(groups)[None, :])
+        packed, S, ZS = orc.quantize(W)
+        want = np.zeros(H // 4, np.uint8)
+        for start, count, val in row["bytes"]:
+            want[start:start + count] = int(val, 16)
+        assert np.array_equal(packed[0], want), H
+        assert np.all(S == int(row["S"], 16)) and np.all(ZS == int(row["ZS"], 16))
+
+
+def test_unpack_inverts_quarter_split_packing():
+    rng = np.random.default_rng(1)
+    for H in (512, 1024, 5120):
+        Q = H // 4
+        codes = rng.integers(0, 4, size=(7, H), dtype=np.uint8)
+        packed = (codes[:, :Q] | (codes[:, Q:2 * Q] << 2) | (codes[:, 2 * Q:3 * Q] << 4)
+                  | (codes[:, 3 * Q:] << 6)).astype(np.uint8)
+        assert np.array_equal(orc.unpack(packed, H), codes)
+    # plane placement: a byte with only plane p set decodes to k = p*Q + j only
+    H, Q = 1024, 256
+    for p in range(4):
+        packed = np.zeros((1, Q), np.uint8)
+        packed[0, 5] = 1 << (2 * p)
+        codes = orc.unpack(packed, H)[0]
+        assert np.flatnonzero(codes).tolist() == [p * Q + 5]
+
+
+def test_quantize_invariants_and_error_bound():
+    rng = np.random.default_rng(2)
+    w = (rng.standard_normal((48, 1024)) * 0.02).astype(np.float32)
+    w[3] *= 4.0
+    w[7, :128] = 0.37                     # constant group
+    w[9, 128:256] = np.abs(w[9, 128:256]) + 0.01   # all-positive group
+    W = (w.view(np.uint32) >> 16).astype(np.uint16)  # truncate to bf16 bits
+    packed, S, ZS, sc, zp = orc.quantize(W, with_params=True)
+    wv = bf2f(W)
+    codes = my_unpack(packed, 1024).astype(np.float64)
+    assert np.all(sc >= np.float32(1e-8))
+    assert set(np.unique(zp).tolist()) <= {0.0, 1.0, 2.0, 3.0}
+    g = wv.reshape(48, 8, 128)
+    lo, hi = g.min(-1), g.max(-1)
+    deq = sc[..., None].astype(np.float64) * (codes.reshape(48, 8, 128) - zp[..., None])
+    err = np.abs(g - deq)
+    straddle = (lo <= 0) & (hi >= 0)
+    bound = 0.5 * sc.astype(np.float64) * (1 + 1e-5)
+    assert np.all(err[straddle] <= bound[straddle][:, None])
+    assert straddle.sum() >= 40
+    # the stored pair is the premultiplied scale and zero within bf16 rounding (half an
+    # ulp of an 8-bit significand: 2^-8 relative)
+    s = bf2f(S)
+    zs = bf2f(ZS)
+    sc64 = sc.astype(np.float64)
+    assert np.all(np.abs(s - 4 * sc64) <= 2.0 ** -8 * 4 * sc64)
+    assert np.all(np.abs(zs - (4 + zp) * sc64) <= 2.0 ** -8 * (1 + 1e-6) * (4 + zp) * sc64)
+
+
+def test_quantize_cross_check_with_torch_fp32():
+    """Cross-check of platform fp32 semantics against the page's own library ops (torch
+    amin/amax/round/clamp on CPU).  Not counted as a pin: it restates the arithmetic."""
+    torch = pytest.importorskip("torch")
+    g = torch.Generator().manual_seed(3)
+    wt = (torch.randn(64, 1024, generator=g) * 0.02).to(torch.bfloat16)
+    W = wt.view(torch.int16).numpy().view(np.uint16)
+    packed, S, ZS = orc.quantize(W)
+    wg = wt.float().reshape(64, 8, 128)
+    lo, hi = wg.amin(dim=2), wg.amax(dim=2)
+    sc = ((hi - lo) / 3).clamp(min=1e-8)
+    zp = torch.round(-lo / sc).clamp(0, 3)
+    q = torch.round(wg / sc[:, :, None] + zp[:, :, None]).clamp(0, 3).to(torch.uint8)
+    q = q.reshape(64, 1024)
+    Q = 256
+    tp = (q[:, :Q] | (q[:, Q:2 * Q] << 2) | (q[:, 2 * Q:3 * Q] << 4) | (q[:, 3 * Q:] << 6))
+    assert np.array_equal(tp.numpy(), packed)
+    assert np.array_equal((4.0 * sc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16), S)
+    assert np.array_equal((4.0 * sc + zp * sc).to(torch.bfloat16).view(torch.int16).numpy()
+                          .view(np.uint16), ZS)
+
+
+def test_quantize_rejects_partial_quarter_groups():
+    with pytest.raises(ValueError):
+        orc.quantize(np.zeros((2, 256), np.uint16))
+
+
+# ------------------------------------------------------------------------------------------
+# bit-pattern dequant (module docstring, 'Bit-pattern dequant, hoisted' bullet)
+# ------------------------------------------------------------------------------------------
+
+def test_bit_pattern_identity_exhaustive():
+    for b in range(256):
+        for q in range(4):
+            if q < 3:
+                bits = 0x3F80 | ((b << (5 - 2 * q)) & 0x60)
+            else:
+                bits = 0x3F80 | ((b >> 1) & 0x60)
+            v = (b >> (2 * q)) & 3
+            assert bf2f(np.array([bits], np.uint16))[0] == 1.0 + v / 4.0
+
+
+def test_bit_pattern_on_32bit_words_pairs_bytes_0_2_and_1_3():
+    """The word form of the identity: one shift and one mask turn bytes (0, 2) or (1, 3) of a
+    packed 32-bit word into a bf16 pair, both halves equal to 1 + v/4 of that byte."""
+    rng = np.random.default_rng(4)
+    words = rng.integers(0, 2 ** 32, size=4096, dtype=np.uint64)
+    for wd in words.tolist() + [0, 0xFFFFFFFF, 0x1B1B1B1B]:
+        bs = [(wd >> (8 * i)) & 0xFF for i in range(4)]
+        for q in range(4):
+            s = 5 - 2 * q
+            even = ((wd << s) if s >= 0 else (wd >> -s)) & 0x00600060 | 0x3F803F80
+            odd = (wd >> (3 + 2 * q)) & 0x00600060 | 0x3F803F80
+            for word, (blo, bhi) in ((even, (bs[0], bs[2])), (odd, (bs[1], bs[3]))):
+                lo = bf2f(np.array([word & 0xFFFF], np.uint16))[0]
+                hi = bf2f(np.array([(word >> 16) & 0xFFFF], np.uint16))[0]
+                assert lo == 1 + ((blo >> (2 * q)) & 3) / 4
+                assert hi == 1 + ((bhi >> (2 * q)) & 3) / 4
+
+
+# ------------------------------------------------------------------------------------------
+# coarse value
+# ------------------------------------------------------------------------------------------
+
+def _grid_weights(rng, V, H):
+    """Rows on the exact 2-bit grid {-1, -0.5, 0, 0.5} * 2^e (each group holds -1 and 0.5, so
+    lo, hi fix sc = 0.5 * 2^e and zp = 2 and every value is reproduced exactly)."""
+    vals = rng.choice(np.array([-1.0, -0.5, 0.0, 0.5]), size=(V, H))
+    vals.reshape(V, H // 128, 128)[:, :, 0] = -1.0
+    vals.reshape(V, H // 128, 128)[:, :, 1] = 0.5
+    e = rng.integers(-9, -3, size=(V, 1)).astype(np.float64)
+    return vals * 2.0 ** e
+
+
+def test_coarse_on_grid_weights_is_the_exact_head():
+    rng = np.random.default_rng(5)
+    V, H, M = 96, 1024, 3
+    W = f2bf_exact(_grid_weights(rng, V, H))
+    x = f2bf_exact(np.round(rng.standard_normal((M, H)) * 64) / 64)
+    packed, S, ZS = orc.quantize(W)
+    c = orc.coarse(x, packed, S, ZS)
+    ref = bf2f(x) @ bf2f(W).T
+    np.testing.assert_allclose(c, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_coarse_collapsed_form_equals_direct_dequant():
+    """c = sum_g S p - ZS xs must equal sum_k x_k (S_g (1 + v_k/4) - ZS_g), the per-element
+    dequant-and-dot, computed here from a test-side unpack and a plain matmul."""
+    rng = np.random.default_rng(6)
+    V, H, M = 200, 1536, 5
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS = orc.quantize(W)
+    v = my_unpack(packed, H).astype(np.float64)
+    s = np.repeat(bf2f(S), 128, axis=1)
+    zs = np.repeat(bf2f(ZS), 128, axis=1)
+    What = s * (1.0 + v / 4.0) - zs
+    ref = bf2f(x) @ What.T
+    c = orc.coarse(x, packed, S, ZS)
+    np.testing.assert_allclose(c, ref, rtol=1e-11, atol=1e-11)
+    # and the quantised head tracks the bf16 head (2-bit noise, not a wrong term)
+    exact = bf2f(x) @ bf2f(W).T
+    corr = np.corrcoef(c.ravel(), exact.ravel())[0, 1]
+    assert corr > 0.85
+
+
+# ------------------------------------------------------------------------------------------
+# selections (brute force on tiny inputs)
+# ------------------------------------------------------------------------------------------
+
+def _order(vals, idx):
+    """Value descending, equal values -> lower index."""
+    return np.lexsort((idx, -vals))
+
+
+@pytest.mark.parametrize("kcand", [1, 3, 8, 64])
+def test_block_topk_brute_force(kcand):
+    rng = np.random.default_rng(7 + kcand)
+    M, V = 3, 200                                   # blocks of 64, 64, 64, 8 (ragged tail)
+    cf = np.round(rng.standard_normal((M, V)) * 4).astype(np.float32)  # many exact ties
+    cval, cidx, _ = orc.block_topk(cf, kcand)
+    nblk = 4
+    for m in range(M):
+        for b in range(nblk):
+            cols = np.arange(64 * b, min(V, 64 * b + 64))
+            o = _order(cf[m, cols], cols)[:kcand]
+            got_i = cidx[m, b * kcand:(b + 1) * kcand]
+            got_v = cval[m, b * kcand:(b + 1) * kcand]
+            n = len(o)
+            assert np.array_equal(got_i[:n], cols[o])
+            assert np.array_equal(got_v[:n], cf[m, cols[o]])
+            assert np.all(got_i[n:] == -1) and np.all(np.isneginf(got_v[n:]))
+
+
+def test_select_topr_brute_force():
+    rng = np.random.default_rng(8)
+    M, V, kc = 4, 300, 8
+    cf = np.round(rng.standard_normal((M, V)) * 3).astype(np.float32)
+    cval, cidx, _ = orc.block_topk(cf, kc)
+    for R in (1, 5, 17, 37):
+        sel, selv = orc.select_topr(cval, cidx, R)
+        for m in range(M):
+            ok = cidx[m] >= 0
+            o = _order(cval[m][ok], cidx[m][ok])[:R]
+            assert np.array_equal(sel[m], cidx[m][ok][o])
+            assert np.array_equal(selv[m], cval[m][ok][o])
+    # KCAND = 64 makes the candidates every column: top-R of the full row
+    cval, cidx, n = orc.block_topk(cf, 64)
+    assert n == V
+    sel, _ = orc.select_topr(cval, cidx, 50)
+    for m in range(M):
+        assert np.array_equal(sel[m], _order(cf[m], np.arange(V))[:50])
+
+
+def test_forward_with_full_candidate_pool_is_exact_topk():
+    """KCAND=64 and RERANK=V rerank every column, so the result is the exact head's top-k."""
+    rng = np.random.default_rng(9)
+    M, V, H, k = 4, 130, 512, 5
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS = orc.quantize(W)
+    res = orc.forward(x, packed, S, ZS, W, 64, V, k)
+    ex = bf2f(x) @ bf2f(W).T
+    for m in range(M):
+        o = _order(ex[m].astype(np.float32), np.arange(V))[:k]
+        assert np.array_equal(res["idx"][m], o)
+        np.testing.assert_allclose(res["logit"][m], ex[m, o], rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------------------------------------
+# exact dots (integer arithmetic)
+# ------------------------------------------------------------------------------------------
+
+def test_rerank_and_exact_head_match_exact_rational_sums():
+    rng = np.random.default_rng(10)
+    M, V, H = 2, 40, 512
+    xv = rng.integers(-128, 128, size=(M, H)) / 64.0          # bf16-exact (8-bit mantissas)
+    wv = rng.integers(-128, 128, size=(V, H)) / 4096.0
+    x, W = f2bf_exact(xv), f2bf_exact(wv)
+    exact = np.array([[float(sum(Fraction(int(a)) * int(b) for a, b in
+                                 zip(np.round(xv[m] * 64), np.round(wv[n] * 4096))) / (64 * 4096))
+                       for n in range(V)] for m in range(M)])
+    idx = np.array([[3, 17, 0, 39], [5, 5, 22, 1]], np.int32)
+    e = orc.rerank(x, W, idx)
+    for m in range(M):
+        for j in range(4):
+            assert e[m, j] == exact[m, idx[m, j]]
+    assert np.array_equal(orc.exact_head(x, W), exact)
+
+
+# ------------------------------------------------------------------------------------------
+# decision gaps
+# ------------------------------------------------------------------------------------------
+
+def test_decision_gap_flags_a_planted_tie():
+    rng = np.random.default_rng(11)
+    M, V, H = 2, 256, 512
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    W[77] = W[12]                       # identical rows: identical coarse and exact values
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS = orc.quantize(W)
+    ex = bf2f(x) @ bf2f(W).T
+    res = orc.forward(x, packed, S, ZS, W, 8, 32, 1)
+    gaps = orc.decision_gaps(res, 8, 1)
+    assert gaps.shape == (M,)
+    # make row 0's winner one of the twins: its exact gap to the (k+1)-th is 0
+    x2 = x.copy()
+    x2[0] = (((bf2f(W[12]) * 50).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    res2 = orc.forward(x2, packed, S, ZS, W, 8, 32, 1)
+    assert set(res2["idx"][0].tolist()) <= {12, 77}
+    assert res2["idx"][0, 0] == 12               # equal values -> lower index
+    assert orc.decision_gaps(res2, 8, 1)[0] == 0.0
