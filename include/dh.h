@@ -1,0 +1,165 @@
+/*
+ * dh.h -- C ABI of the GB300 2-bit draft head with exact rerank.
+ *
+ * The operation (page "radiance_drafthead.py"): a speculative-decoding draft LM head that
+ * replaces the stock bf16 head x[M,H] @ W[H,V].  W is quantised once to 2 bits per weight
+ * with an asymmetric scale and zero per (vocabulary row, group of 128 hidden positions)
+ * (_quantize_head_now); a coarse pass streams the 2-bit weight, applies the scale and zero
+ * to the fp32 accumulator in the collapsed form (4s)*p - (4s + zp*s)*sum_k x_k, with
+ * p = sum_k x_k (1 + v_k/4) read through the bf16 bit pattern 0x3F80 | (v << 5)
+ * (module docstring, bullets "Bit-pattern dequant, hoisted" and "The scale is applied to the
+ * accumulator"; _draft_head_int2); every block of 64 vocabulary columns emits its KCAND best
+ * candidates (_emit); the RERANK best candidates of each row are rescored exactly against
+ * the bf16 weight (_rerank_exact) and the best TOPK of those are returned (TOPK = 1 is the
+ * argmax caller, TOPK = 16 the selector_top_k caller of _apply_head_int2).
+ *
+ * Conventions for every entry point
+ *   - bf16 tensors are passed as uint16_t* holding the raw bit patterns.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, contiguous row-major,
+ *     16-byte aligned.  The library never allocates, frees or synchronises: all work is
+ *     enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and the call
+ *     returns as soon as it is enqueued.  Outputs are valid once the stream reaches them.
+ *   - Every entry point checks its arguments on the host before launching anything and
+ *     returns a status (DH_OK or a negative DH_ERR_*); dh_last_error() then describes it.
+ *     No entry point aborts, traps or prints.
+ *   - Entry points are thread-safe as long as concurrent calls use distinct workspaces.
+ *   - Device-side waits are bounded: a wait that times out records DH_ERR_DEVICE_TIMEOUT in
+ *     a device flag (read with dh_device_status) and the kernel returns early.
+ *
+ * Shapes
+ *   M  rows of hidden states per call (draft positions), 1 <= M <= 128
+ *   H  hidden size, a positive multiple of 512 (every quarter of a row holds whole groups)
+ *   V  vocabulary rows of the head, V >= 1
+ *   G  = 128 (quantisation group), BLOCK_N = 64 (selection block), nblk = ceil(V / 64)
+ */
+#ifndef DH_H
+#define DH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define DH_OK 0
+#define DH_ERR_NULL (-1)           /* a required pointer is NULL */
+#define DH_ERR_SHAPE (-2)          /* M, H or V out of range (see Shapes) */
+#define DH_ERR_SELECT (-3)         /* kcand, rerank or topk out of range */
+#define DH_ERR_WORKSPACE (-4)      /* workspace smaller than dh_workspace_bytes() */
+#define DH_ERR_ALIGN (-5)          /* a pointer is not 16-byte aligned */
+#define DH_ERR_CUDA (-6)           /* a CUDA runtime call or launch failed */
+#define DH_ERR_DEVICE_TIMEOUT (-7) /* a bounded device-side wait gave up (dh_device_status) */
+#define DH_ERR_ARG (-8)            /* any other invalid argument */
+
+/*
+ * dh_quantize -- one-time quantise and pack of the bf16 head.
+ * Page: radiance_drafthead.py, _quantize_head_now (BITS = 2, GROUP = 128).
+ *
+ *   W_bf16  [V, H]       bf16 head weight, row n = vocabulary entry n          (input)
+ *   packed  [V, H/4]     u8: byte j of row n holds the 2-bit codes of k = j, H/4+j, H/2+j,
+ *                        3H/4+j in bits 0-1, 2-3, 4-5, 6-7 (quarter split)        (output)
+ *   scales  [V, H/128]   bf16 S  = bf16(4 * sc) per (row, group)                 (output)
+ *   zeros   [V, H/128]   bf16 ZS = bf16(4 * sc + zp * sc) per (row, group)       (output)
+ * with, per group of 128 consecutive k and in IEEE fp32: lo/hi = min/max,
+ * sc = max((hi - lo) / 3, 1e-8), zp = clamp(round(-lo / sc), 0, 3),
+ * q = clamp(round(w / sc + zp), 0, 3), round = half to even.  Bit-exact with that definition.
+ * Returns DH_OK, DH_ERR_NULL, DH_ERR_SHAPE, DH_ERR_ALIGN or DH_ERR_CUDA.
+ */
+int dh_quantize(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                uint16_t *zeros, void *stream);
+
+/*
+ * dh_workspace_bytes -- device scratch that dh_forward needs for these sizes (bytes), or 0
+ * when the sizes are invalid.  The pages need no such call because their host framework
+ * allocates per call; here the caller allocates once and reuses it.
+ */
+size_t dh_workspace_bytes(int M, int H, int V, int kcand, int rerank);
+
+/*
+ * dh_forward -- the draft-head forward.
+ * Page: radiance_drafthead.py, _apply_head_int2 with _draft_head_int2, _emit and
+ * _rerank_exact (bf16 branch).
+ *
+ *   x        [M, H]          bf16 hidden states                                  (input)
+ *   packed, scales, zeros    the output of dh_quantize for W_bf16                (input)
+ *   W_bf16   [V, H]          bf16 head weight the rerank scores against          (input)
+ *   kcand    1..64           candidates each 64-column block emits
+ *   rerank   1..min(valid candidates, 1024), and <= V
+ *                            candidates per row rescored exactly; valid candidates =
+ *                            sum over blocks of min(kcand, columns in the block)
+ *   topk     1..rerank       results per row; 1 is the argmax caller
+ *   idx      [M, topk] int32 vocabulary indices, best first                     (output)
+ *   logit    [M, topk] fp32  their exact logits sum_k x[m,k] W[idx,k]            (output)
+ *   workspace, ws_bytes      device scratch of at least dh_workspace_bytes(...)
+ * Ranking: coarse values and exact values are compared in fp32; equal values go to the
+ * lower vocabulary index.  Only reranked entries are eligible for the result.
+ * Returns DH_OK or a negative DH_ERR_* (checked before any launch).
+ */
+int dh_forward(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+               const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V, int kcand,
+               int rerank, int topk, int32_t *idx, float *logit, void *workspace,
+               size_t ws_bytes, void *stream);
+
+/*
+ * dh_forward_debug -- dh_forward that also writes the intermediates, for parity checks.
+ * Any of the extra outputs may be NULL.
+ *   coarse    [M, V] fp32                 coarse values c[m, n]
+ *   cand_val  [M, nblk*kcand] fp32        block candidates, block-major, best first inside
+ *   cand_idx  [M, nblk*kcand] int32       a block; missing slots (block shorter than kcand)
+ *                                         hold -inf / -1
+ *   sel_idx   [M, rerank] int32           the reranked vocabulary indices (any order)
+ *   sel_exact [M, rerank] fp32            their exact logits, same order as sel_idx
+ */
+int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                     const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                     int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                     void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                     int32_t *cand_idx, int32_t *sel_idx, float *sel_exact, void *stream);
+
+/*
+ * dh_forward_timed -- dh_forward that records caller-created CUDA events (cudaEvent_t, cast
+ * to void*) at the stage boundaries, for per-kernel timing inside a benchmark:
+ *   events[0] before staging x, [1] before the coarse pass, [2] before candidate
+ *   selection, [3] before the rerank, [4] before the top-k merge, [5] after it.
+ * `events` must hold DH_NUM_STAGE_EVENTS valid events.
+ */
+#define DH_NUM_STAGE_EVENTS 6
+int dh_forward_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                     const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                     int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                     void *workspace, size_t ws_bytes, void *const *events, void *stream);
+
+/*
+ * Coarse-pass implementation choice (process-wide).
+ *   DH_PATH_AUTO  pick by M (default)
+ *   DH_PATH_WARP  warp-level mma.sync tensor-core path, batch handled 16 rows at a time
+ *   DH_PATH_TC    tcgen05 / tensor-memory path
+ * dh_set_coarse_path returns the previous setting, or DH_ERR_ARG for an unknown value.
+ * dh_coarse_path_for(M) reports which path a forward with M rows would take.
+ */
+#define DH_PATH_AUTO 0
+#define DH_PATH_WARP 1
+#define DH_PATH_TC 2
+int dh_set_coarse_path(int path);
+int dh_coarse_path_for(int M);
+
+/*
+ * dh_device_status -- DH_OK, or DH_ERR_DEVICE_TIMEOUT when a kernel since the last reset
+ * gave up on a bounded wait.  Synchronises the current device to read the flag; reset != 0
+ * clears it.  Returns DH_ERR_CUDA if the device cannot be read.
+ */
+int dh_device_status(int reset);
+
+/* Human-readable description of the last error on this thread ("" if none). */
+const char *dh_last_error(void);
+
+/* ABI version: (major << 16) | minor. */
+int dh_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DH_H */

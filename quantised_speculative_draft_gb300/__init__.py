@@ -1,0 +1,215 @@
+"""GB300 2-bit draft head with exact rerank: Python binding of the C ABI in include/dh.h.
+
+This module only marshals arguments: every step of the path runs in the CUDA library
+``_build/libdh.so`` (build it with :func:`build`).  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+
+Functions mirror the C entry points one to one and take torch tensors (device memory owned by
+the caller); ``stream`` defaults to torch's current CUDA stream.  :class:`DraftHead` bundles the
+packed weight, its scale/zero pair, the bf16 weight and a workspace for repeated calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB as _LIB_PATH
+from .build import build
+
+__all__ = [
+    "build", "DHError", "dh_quantize", "dh_workspace_bytes", "dh_forward", "dh_forward_debug",
+    "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for", "dh_device_status",
+    "dh_last_error", "dh_version", "DraftHead", "PATH_AUTO", "PATH_WARP", "PATH_TC",
+    "NUM_STAGE_EVENTS", "library_path",
+]
+
+PATH_AUTO, PATH_WARP, PATH_TC = 0, 1, 2
+NUM_STAGE_EVENTS = 6
+GROUP = 128
+BLOCK_N = 64
+
+_STATUS = {0: "DH_OK", -1: "DH_ERR_NULL", -2: "DH_ERR_SHAPE", -3: "DH_ERR_SELECT",
+           -4: "DH_ERR_WORKSPACE", -5: "DH_ERR_ALIGN", -6: "DH_ERR_CUDA",
+           -7: "DH_ERR_DEVICE_TIMEOUT", -8: "DH_ERR_ARG"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DHError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{_STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"CUDA library {_LIB_PATH} is not built; call "
+                               "quantised_speculative_draft_gb300.build() first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.dh_quantize.argtypes = [P, I, I, P, P, P, P]
+        lib.dh_quantize.restype = I
+        lib.dh_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.dh_workspace_bytes.restype = S
+        fwd = [P, P, P, P, P, I, I, I, I, I, I, P, P, P, S]
+        lib.dh_forward.argtypes = fwd + [P]
+        lib.dh_forward.restype = I
+        lib.dh_forward_debug.argtypes = fwd + [P, P, P, P, P, P]
+        lib.dh_forward_debug.restype = I
+        lib.dh_forward_timed.argtypes = fwd + [P, P]
+        lib.dh_forward_timed.restype = I
+        lib.dh_set_coarse_path.argtypes = [I]
+        lib.dh_set_coarse_path.restype = I
+        lib.dh_coarse_path_for.argtypes = [I]
+        lib.dh_coarse_path_for.restype = I
+        lib.dh_device_status.argtypes = [I]
+        lib.dh_device_status.restype = I
+        lib.dh_last_error.argtypes = []
+        lib.dh_last_error.restype = ctypes.c_char_p
+        lib.dh_version.argtypes = []
+        lib.dh_version.restype = I
+        _lib = lib
+        return lib
+
+
+def dh_last_error() -> str:
+    return _load().dh_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise DHError(rc, dh_last_error())
+    return rc
+
+
+def _p(t):
+    """Device pointer of a tensor (or an int address, or None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dh_version() -> int:
+    return _load().dh_version()
+
+
+def dh_quantize(W, packed, scales, zeros, stream=None):
+    """Quantise the bf16 head W [V, H] into packed [V, H/4] u8, scales/zeros [V, H/128] bf16."""
+    V, H = W.shape
+    _check(_load().dh_quantize(_p(W), V, H, _p(packed), _p(scales), _p(zeros), _stream(stream)))
+
+
+def dh_workspace_bytes(M: int, H: int, V: int, kcand: int, rerank: int) -> int:
+    return int(_load().dh_workspace_bytes(M, H, V, kcand, rerank))
+
+
+def _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace):
+    M, H = x.shape
+    V = packed.shape[0]
+    nbytes = workspace.numel() * workspace.element_size()
+    return [_p(x), _p(packed), _p(scales), _p(zeros), _p(W), M, H, V, kcand, rerank, topk,
+            _p(idx), _p(logit), _p(workspace), nbytes]
+
+
+def dh_forward(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,
+               stream=None):
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    _check(_load().dh_forward(*args, _stream(stream)))
+
+
+def dh_forward_debug(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,
+                     coarse=None, cand_val=None, cand_idx=None, sel_idx=None, sel_exact=None,
+                     stream=None):
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    _check(_load().dh_forward_debug(*args, _p(coarse), _p(cand_val), _p(cand_idx), _p(sel_idx),
+                                    _p(sel_exact), _stream(stream)))
+
+
+def dh_forward_timed(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,
+                     events, stream=None):
+    """``events``: NUM_STAGE_EVENTS torch.cuda.Event objects (created with enable_timing)."""
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in events])
+    _check(_load().dh_forward_timed(*args, arr, _stream(stream)))
+
+
+def dh_set_coarse_path(path: int) -> int:
+    rc = _load().dh_set_coarse_path(path)
+    if rc < 0:
+        raise DHError(rc, dh_last_error())
+    return rc
+
+
+def dh_coarse_path_for(M: int) -> int:
+    rc = _load().dh_coarse_path_for(M)
+    if rc < 0:
+        raise DHError(rc, dh_last_error())
+    return rc
+
+
+def dh_device_status(reset: bool = False) -> int:
+    return _load().dh_device_status(1 if reset else 0)
+
+
+class DraftHead:
+    """A quantised head ready for repeated forwards: owns packed/scales/zeros and a workspace.
+
+    The bf16 weight W stays owned by the caller and is kept by reference (the rerank reads it).
+    """
+
+    def __init__(self, W, kcand: int = 8, rerank: int = 32, max_m: int = 128, stream=None):
+        import torch
+        if W.dtype != torch.bfloat16 or not W.is_cuda or not W.is_contiguous():
+            raise ValueError("W must be a contiguous bf16 CUDA tensor [V, H]")
+        self.W = W
+        self.V, self.H = W.shape
+        dev = W.device
+        self.packed = torch.empty(self.V, self.H // 4, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(self.V, self.H // GROUP, dtype=torch.bfloat16, device=dev)
+        self.zeros = torch.empty(self.V, self.H // GROUP, dtype=torch.bfloat16, device=dev)
+        dh_quantize(W, self.packed, self.scales, self.zeros, stream)
+        self.kcand, self.rerank = kcand, rerank
+        self._ws = None
+        self._ws_key = None
+
+    def workspace(self, M: int):
+        import torch
+        key = (M, self.kcand, self.rerank)
+        if self._ws_key != key:
+            n = dh_workspace_bytes(M, self.H, self.V, self.kcand, self.rerank)
+            if n == 0:
+                raise DHError(-2, dh_last_error())
+            self._ws = torch.empty(n, dtype=torch.uint8, device=self.W.device)
+            self._ws_key = key
+        return self._ws
+
+    def forward(self, x, topk: int = 1, stream=None):
+        """x [M, H] bf16 -> (idx int32 [M, topk], logit fp32 [M, topk])."""
+        import torch
+        M = x.shape[0]
+        idx = torch.empty(M, topk, dtype=torch.int32, device=x.device)
+        logit = torch.empty(M, topk, dtype=torch.float32, device=x.device)
+        dh_forward(x, self.packed, self.scales, self.zeros, self.W, self.kcand, self.rerank, topk,
+                   idx, logit, self.workspace(M), stream)
+        return idx, logit

@@ -1,0 +1,367 @@
+// dh_api.cu -- host layer of the draft-head library: the C ABI declared in include/dh.h.
+//
+// Every entry point validates its arguments on the host, carves the caller's workspace, and
+// enqueues the kernels on the caller's stream.  Nothing here allocates device memory,
+// synchronises (except dh_device_status, which exists to read a flag) or touches the host
+// copy of any tensor.
+#include "dh.h"
+#include "dh_internal.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace dh {
+
+namespace {
+
+thread_local std::string g_last_error;
+int g_path = DH_PATH_AUTO;
+std::mutex g_path_mu;
+
+// Set by any kernel whose bounded wait gave up.  The host learns its address per device.
+__device__ int g_timeout_flag;
+
+int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int ok()
+{
+    g_last_error.clear();
+    return DH_OK;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+size_t align256(size_t v)
+{
+    return (v + 255u) & ~static_cast<size_t>(255u);
+}
+
+int *timeout_flag_ptr()
+{
+    // one address per device; the symbol address is resolved with that device current
+    static std::mutex mu;
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_timeout_flag) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int *>(p);
+    }
+    return addr[dev];
+}
+
+long long valid_candidates(int V, int kcand)
+{
+    const long long nblk = (V + kBlockN - 1) / kBlockN;
+    const int kc = kcand < kBlockN ? kcand : kBlockN;
+    const int tail = V - static_cast<int>((nblk - 1) * kBlockN);
+    return (nblk - 1) * kc + (kcand < tail ? kcand : tail);
+}
+
+struct Layout {
+    int Mpad_w = 0, Npad = 0, rows = 0;
+    long long nblk = 0, ncand = 0, scratch_entries = 0;
+    int passes = 0;
+    size_t xs = 0, xw = 0, xt = 0, cval = 0, cidx = 0, sval[2] = {0, 0}, sidx[2] = {0, 0},
+           sel = 0, ex = 0, counters = 0, total = 0;
+};
+
+constexpr int kNumCounters = 64;
+
+Layout layout_for(int M, int H, int V, int kcand, int rerank)
+{
+    Layout L;
+    L.Mpad_w = ((M + kWarpBatch - 1) / kWarpBatch) * kWarpBatch;
+    L.Npad = tc_npad(M);
+    L.rows = L.Mpad_w > L.Npad ? L.Mpad_w : L.Npad;
+    L.nblk = (V + kBlockN - 1) / kBlockN;
+    L.ncand = L.nblk * kcand;
+    select_plan(M, L.ncand, rerank, &L.passes, &L.scratch_entries);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align256(off + bytes);
+        return o;
+    };
+    L.xs = take(static_cast<size_t>(L.rows) * (H / kGroup) * 4);
+    L.xw = take(warp_xw_elems(M, H) * 2);
+    L.xt = take(static_cast<size_t>(L.Npad) * H * 2);
+    L.cval = take(static_cast<size_t>(M) * L.ncand * 4);
+    L.cidx = take(static_cast<size_t>(M) * L.ncand * 4);
+    for (int b = 0; b < 2; ++b) {
+        L.sval[b] = take(static_cast<size_t>(L.scratch_entries) * 4);
+        L.sidx[b] = take(static_cast<size_t>(L.scratch_entries) * 4);
+    }
+    L.sel = take(static_cast<size_t>(M) * rerank * 4);
+    L.ex = take(static_cast<size_t>(M) * rerank * 4);
+    L.counters = take(kNumCounters * 4);
+    L.total = off;
+    return L;
+}
+
+int check_shapes(int M, int H, int V, int kcand, int rerank, int topk)
+{
+    if (M < 1 || M > kMaxM) return fail(DH_ERR_SHAPE, "M=%d outside [1, %d]", M, kMaxM);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    if (V < 1) return fail(DH_ERR_SHAPE, "V=%d must be >= 1", V);
+    if (static_cast<long long>(V) * H / 4 > (1LL << 40))
+        return fail(DH_ERR_SHAPE, "V*H=%lld too large", static_cast<long long>(V) * H);
+    if (kcand < 1 || kcand > kBlockN)
+        return fail(DH_ERR_SELECT, "kcand=%d outside [1, %d]", kcand, kBlockN);
+    long long nv = valid_candidates(V, kcand);
+    long long rmax = nv < kMaxRerank ? nv : kMaxRerank;
+    if (rerank < 1 || rerank > rmax)
+        return fail(DH_ERR_SELECT, "rerank=%d outside [1, %lld] (valid candidates %lld)", rerank,
+                    rmax, nv);
+    if (topk < 1 || topk > rerank)
+        return fail(DH_ERR_SELECT, "topk=%d outside [1, rerank=%d]", topk, rerank);
+    return DH_OK;
+}
+
+int choose_path(int M, int H)
+{
+    int p;
+    {
+        std::lock_guard<std::mutex> lk(g_path_mu);
+        p = g_path;
+    }
+    if (p == DH_PATH_TC) return tc_supported(M, H) ? DH_PATH_TC : -1;
+    if (p == DH_PATH_WARP) return DH_PATH_WARP;
+    // automatic: the tcgen05 path where it is available, else the warp path
+    if (tc_supported(M, H) && M > 8) return DH_PATH_TC;
+    return DH_PATH_WARP;
+}
+
+int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                 const uint16_t *zeros, const uint16_t *W, int M, int H, int V, int kcand,
+                 int rerank, int topk, int32_t *idx, float *logit, void *workspace,
+                 size_t ws_bytes, float *coarse, float *cand_val, int32_t *cand_idx,
+                 int32_t *sel_idx, float *sel_exact, void *const *events, cudaStream_t stream)
+{
+    if (!x || !packed || !scales || !zeros || !W || !idx || !logit || !workspace)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    int rc = check_shapes(M, H, V, kcand, rerank, topk);
+    if (rc != DH_OK) return rc;
+    const void *ptrs[] = {x, packed, scales, zeros, W, idx, logit, workspace};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    const Layout L = layout_for(M, H, V, kcand, rerank);
+    if (ws_bytes < L.total)
+        return fail(DH_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
+    const int path = choose_path(M, H);
+    if (path < 0) return fail(DH_ERR_ARG, "the tcgen05 path does not support M=%d, H=%d", M, H);
+    int *tflag = timeout_flag_ptr();
+    if (!tflag) return fail(DH_ERR_CUDA, "cannot resolve the device status flag");
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *xs = reinterpret_cast<float *>(ws + L.xs);
+    uint16_t *xw = reinterpret_cast<uint16_t *>(ws + L.xw);
+    uint16_t *xt = reinterpret_cast<uint16_t *>(ws + L.xt);
+    float *cval = cand_val ? cand_val : reinterpret_cast<float *>(ws + L.cval);
+    int32_t *cidx = cand_idx ? cand_idx : reinterpret_cast<int32_t *>(ws + L.cidx);
+    float *sv[2] = {reinterpret_cast<float *>(ws + L.sval[0]), reinterpret_cast<float *>(ws + L.sval[1])};
+    int32_t *si[2] = {reinterpret_cast<int32_t *>(ws + L.sidx[0]),
+                      reinterpret_cast<int32_t *>(ws + L.sidx[1])};
+    int32_t *sel = sel_idx ? sel_idx : reinterpret_cast<int32_t *>(ws + L.sel);
+    float *ex = sel_exact ? sel_exact : reinterpret_cast<float *>(ws + L.ex);
+    int *counters = reinterpret_cast<int *>(ws + L.counters);
+
+    auto rec = [&](int i) -> bool {
+        return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess;
+    };
+    cudaError_t err;
+    if (!rec(0)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+    err = launch_prep(x, M, H, path == DH_PATH_WARP ? L.Mpad_w : 0, xs,
+                      path == DH_PATH_WARP ? xw : nullptr, path == DH_PATH_TC ? xt : nullptr,
+                      path == DH_PATH_TC ? L.Npad : 0, counters, kNumCounters, stream);
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "prep launch: %s", cudaGetErrorString(err));
+    if (!rec(1)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+
+    CoarseArgs a;
+    a.packed = packed;
+    a.S = scales;
+    a.ZS = zeros;
+    a.xs = xs;
+    a.xw = xw;
+    a.xt = xt;
+    a.M = M;
+    a.H = H;
+    a.V = V;
+    a.kcand = kcand;
+    a.cand_val = cval;
+    a.cand_idx = cidx;
+    a.coarse = coarse;
+    a.counters = counters;
+    a.timeout_flag = tflag;
+    err = (path == DH_PATH_TC) ? launch_coarse_tc(a, stream) : launch_coarse_warp(a, stream);
+    if (err != cudaSuccess)
+        return fail(DH_ERR_CUDA, "coarse launch (%s path): %s",
+                    path == DH_PATH_TC ? "tcgen05" : "warp", cudaGetErrorString(err));
+    if (!rec(2)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+    err = launch_select(cval, cidx, M, L.ncand, rerank, sv, si, L.scratch_entries, sel, stream);
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
+    if (!rec(3)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+    err = launch_rerank(x, W, M, H, V, sel, rerank, ex, stream);
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));
+    if (!rec(4)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+    err = launch_topk(ex, sel, M, rerank, topk, idx, logit, stream);
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(err));
+    if (!rec(5)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+    return ok();
+}
+
+} // namespace
+
+CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,
+                              uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+} // namespace dh
+
+using namespace dh;
+
+extern "C" {
+
+int dh_quantize(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                uint16_t *zeros, void *stream)
+{
+    if (!W_bf16 || !packed || !scales || !zeros)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (V < 1) return fail(DH_ERR_SHAPE, "V=%d must be >= 1", V);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    const void *ptrs[] = {W_bf16, packed, scales, zeros};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    cudaError_t err = launch_quantize(W_bf16, V, H, packed, scales, zeros,
+                                      static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
+    return ok();
+}
+
+size_t dh_workspace_bytes(int M, int H, int V, int kcand, int rerank)
+{
+    if (check_shapes(M, H, V, kcand, rerank, 1) != DH_OK) return 0;
+    return layout_for(M, H, V, kcand, rerank).total;
+}
+
+int dh_forward(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+               const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V, int kcand,
+               int rerank, int topk, int32_t *idx, float *logit, void *workspace,
+               size_t ws_bytes, void *stream)
+{
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                     const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                     int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                     void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                     int32_t *cand_idx, int32_t *sel_idx, float *sel_exact, void *stream)
+{
+    const void *opt[] = {coarse, cand_val, cand_idx, sel_idx, sel_exact};
+    for (const void *p : opt)
+        if (p && !aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
+                        sel_exact, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int dh_forward_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                     const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                     int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                     void *workspace, size_t ws_bytes, void *const *events, void *stream)
+{
+    if (!events) return fail(DH_ERR_NULL, "events is NULL");
+    for (int i = 0; i < DH_NUM_STAGE_EVENTS; ++i)
+        if (!events[i]) return fail(DH_ERR_NULL, "events[%d] is NULL", i);
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        events, static_cast<cudaStream_t>(stream));
+}
+
+int dh_set_coarse_path(int path)
+{
+    if (path != DH_PATH_AUTO && path != DH_PATH_WARP && path != DH_PATH_TC)
+        return fail(DH_ERR_ARG, "unknown coarse path %d", path);
+    std::lock_guard<std::mutex> lk(g_path_mu);
+    const int prev = g_path;
+    g_path = path;
+    return prev;
+}
+
+int dh_coarse_path_for(int M)
+{
+    if (M < 1 || M > kMaxM) return fail(DH_ERR_SHAPE, "M=%d outside [1, %d]", M, kMaxM);
+    return choose_path(M, 5120);
+}
+
+int dh_device_status(int reset)
+{
+    int *p = timeout_flag_ptr();
+    if (!p) return fail(DH_ERR_CUDA, "cannot resolve the device status flag");
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return fail(DH_ERR_CUDA, "device synchronize failed");
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return fail(DH_ERR_CUDA, "cannot read the device status flag");
+    if (reset) {
+        const int z = 0;
+        if (cudaMemcpy(p, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess)
+            return fail(DH_ERR_CUDA, "cannot reset the device status flag");
+    }
+    if (v) return fail(DH_ERR_DEVICE_TIMEOUT, "a device-side wait timed out");
+    return ok();
+}
+
+const char *dh_last_error(void)
+{
+    return g_last_error.c_str();
+}
+
+int dh_version(void)
+{
+    return (1 << 16) | 0;
+}
+
+} // extern "C"

@@ -1,0 +1,75 @@
+// dh_internal.h -- host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dh {
+
+// ---- geometry shared by the host layer and the kernels ----------------------------------
+constexpr int kGroup = 128;             // quantisation group along H
+constexpr int kBlockN = 64;             // vocabulary columns per selection block
+constexpr int kSpanBytes = 128;         // packed bytes of a row covered by one pass over the planes
+constexpr int kNumSMs = 152;
+constexpr int kWarpBatch = 16;          // batch rows per warp-path pass (two n8 tiles)
+constexpr int kWarpRowsPerWarp = 64;    // vocabulary rows per warp work item (one block)
+constexpr int kSelectChunk = 4096;      // candidates per CTA in one top-R selection pass
+constexpr int kMaxRerank = 1024;
+constexpr int kMaxM = 128;
+
+// ---- launchers (each returns the launch status) ------------------------------------------
+cudaError_t launch_quantize(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
+                            uint16_t *ZS, cudaStream_t stream);
+
+// x [M,H] bf16 -> group sums xs [Mpad, NGt] fp32 and the operand layouts of the coarse paths:
+//   xw (warp path): per 16-row batch chunk, B fragments in mma.sync register order
+//   xt (tcgen05 path): [Npad, H] K-major rows with every aligned quad of k permuted [0,2,1,3]
+// Rows >= M are zero.  Either of xw / xt may be null.  Also zeroes `counters` (ncounters).
+cudaError_t launch_prep(const uint16_t *x, int M, int H, int Mpad, float *xs, uint16_t *xw,
+                        uint16_t *xt, int Npad, int *counters, int ncounters,
+                        cudaStream_t stream);
+
+struct CoarseArgs {
+    const uint8_t *packed;
+    const uint16_t *S;
+    const uint16_t *ZS;
+    const float *xs;    // [Mpad, NGt]
+    const uint16_t *xw; // warp path operand (per chunk)
+    const uint16_t *xt; // tcgen05 path operand
+    int M, H, V, kcand;
+    float *cand_val;    // [M, nblk*kcand]
+    int32_t *cand_idx;
+    float *coarse;      // optional [M, V]
+    int *counters;      // work-queue counters, zeroed by prep
+    int *timeout_flag;
+};
+
+cudaError_t launch_coarse_warp(const CoarseArgs &a, cudaStream_t stream);
+size_t warp_xw_elems(int M, int H); // bf16 elements of the warp-path operand
+
+bool tc_supported(int M, int H);
+cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream);
+int tc_npad(int M);
+
+// Top-R selection over candidate lists.  Returns the number of passes it will take and the
+// scratch entries it needs (two ping-pong buffers of `scratch_entries` (val, idx) pairs).
+void select_plan(int M, long long ncand, int R, int *passes, long long *scratch_entries);
+cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M, long long ncand,
+                          int R, float *scratch_val[2], int32_t *scratch_idx[2],
+                          long long scratch_entries, int32_t *sel_idx, cudaStream_t stream);
+
+cudaError_t launch_rerank(const uint16_t *x, const uint16_t *W, int M, int H, int V,
+                          const int32_t *sel_idx, int R, float *ex, cudaStream_t stream);
+
+cudaError_t launch_topk(const float *ex, const int32_t *sel_idx, int M, int R, int topk,
+                        int32_t *out_idx, float *out_logit, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,
+                              uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+} // namespace dh

@@ -1,0 +1,105 @@
+// dh_prep.cu -- step a2: group sums of x and the operand layouts of the coarse pass.
+//
+// xs[m, g] = sum_{k in group g} x[m, k] in fp32 (radiance_drafthead.py, _apply_head_int2:
+// "xs = x.reshape(M, ng, GROUP).float().sum(-1)"), the zero-point term's multiplier.
+//
+// The 2-bit dequant turns bytes (0, 2) and (1, 3) of a packed 32-bit word into bf16 pairs, so
+// the weight operand carries k in the order 4w+0, 4w+2, 4w+1, 4w+3 inside every aligned quad.
+// The contraction order of an MMA is free as long as both operands agree, so x is staged with
+// the same permutation (x'[4w + e] = x[4w + perm(e)], perm = 0, 2, 1, 3) in two layouts:
+//   xt  [Npad, H]: plain K-major rows, the tcgen05 path's B operand (loaded by TMA);
+//   xw  per 16-row batch chunk c, span s, plane p, n8-tile t: a 2 KB block holding the
+//       mma.sync B fragments in register order, [j = 0..3][lane = 0..31][8 values] with
+//       lane = 4 g + tig carrying x'[16c + 8t + g][p Q + 128 s + 32 tig + 8 j + 0..7].
+// One thread handles one row and one octet of k (one 16-byte load, one or two 16-byte stores).
+#include "dh_common.cuh"
+#include "dh_internal.h"
+
+namespace dh {
+
+__device__ __forceinline__ uint4 permute_quads(uint4 v)
+{
+    // within each 32-bit pair of bf16 the order is (k, k+1); swap k+1 and k+2 of each quad
+    uint4 o;
+    o.x = __byte_perm(v.x, v.y, 0x5410); // (k0, k2)
+    o.y = __byte_perm(v.x, v.y, 0x7632); // (k1, k3)
+    o.z = __byte_perm(v.z, v.w, 0x5410); // (k4, k6)
+    o.w = __byte_perm(v.z, v.w, 0x7632); // (k5, k7)
+    return o;
+}
+
+__global__ void __launch_bounds__(256) prep_kernel(const uint16_t *__restrict__ x, int M, int H,
+                                                   int rows, float *__restrict__ xs,
+                                                   uint16_t *__restrict__ xw, int xw_rows,
+                                                   int nt_per_chunk,
+                                                   uint16_t *__restrict__ xt,
+                                                   int *__restrict__ counters, int ncounters)
+{
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (tid < ncounters) counters[tid] = 0;
+    const int octs = H / 8;
+    const long long total = static_cast<long long>(rows) * octs;
+    // every thread of a 16-lane half-warp belongs to the same group: no early exit before the
+    // shuffles, only predicated stores
+    const bool live = tid < total;
+    const int b = live ? static_cast<int>(tid / octs) : 0;
+    const int o = live ? static_cast<int>(tid - static_cast<long long>(b) * octs) : 0;
+    const int k0 = 8 * o;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (live && b < M) v = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<long long>(b) * H + k0));
+    // group sum over 16 octets = 128 values
+    float s = 0.f;
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            s += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (!live) return;
+    const int NGt = H / kGroup;
+    if ((o & 15) == 0) xs[static_cast<long long>(b) * NGt + (k0 >> 7)] = s;
+
+    const uint4 pv = permute_quads(v);
+    if (xt) *reinterpret_cast<uint4 *>(xt + static_cast<long long>(b) * H + k0) = pv;
+    if (xw && b < xw_rows) {
+        const int Q = H / 4, NG = H / 512;
+        const int p = k0 / Q, rem = k0 - p * Q;
+        const int sp = rem >> 7, r2 = rem & 127;
+        const int tig = r2 >> 5, j = (r2 & 31) >> 3;
+        const int c = b / kWarpBatch, t = (b % kWarpBatch) >> 3, g = b & 7;
+        if (t < nt_per_chunk) {
+            const int lane = 4 * g + tig;
+            const long long blk =
+                ((static_cast<long long>(c) * NG + sp) * 4 + p) * nt_per_chunk + t;
+            const long long off = (blk * 4 + j) * 32 + lane;
+            reinterpret_cast<uint4 *>(xw)[off] = pv;
+        }
+    }
+}
+
+cudaError_t launch_prep(const uint16_t *x, int M, int H, int Mpad, float *xs, uint16_t *xw,
+                        uint16_t *xt, int Npad, int *counters, int ncounters,
+                        cudaStream_t stream)
+{
+    int rows = Mpad > Npad ? Mpad : Npad;
+    const int nt = (M <= 8) ? 1 : 2;
+    const long long total = static_cast<long long>(rows) * (H / 8);
+    long long threads = total > ncounters ? total : ncounters;
+    const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+    const int xw_rows = ((M + kWarpBatch - 1) / kWarpBatch) * kWarpBatch;
+    prep_kernel<<<blocks, 256, 0, stream>>>(x, M, H, rows, xs, xw, xw_rows, nt, xt, counters,
+                                            ncounters);
+    return cudaGetLastError();
+}
+
+size_t warp_xw_elems(int M, int H)
+{
+    const int nt = (M <= 8) ? 1 : 2;
+    const int chunks = (M + kWarpBatch - 1) / kWarpBatch;
+    // per chunk: NG spans x 4 planes x nt tiles x 2 KB (1024 bf16)
+    return static_cast<size_t>(chunks) * (H / 512) * 4 * nt * 1024;
+}
+
+} // namespace dh

@@ -1,0 +1,102 @@
+// dh_quantize.cu -- kernel (1): quantise and pack the bf16 head to 2 bits.
+//
+// radiance_drafthead.py, _quantize_head_now (BITS = 2, GROUP = 128): per (row, group of 128
+// consecutive k), in IEEE fp32,
+//     lo, hi = min, max;  sc = max((hi - lo) / 3, 1e-8);  zp = clamp(rne(-lo / sc), 0, 3)
+//     q_k = clamp(rne(w_k / sc + zp), 0, 3);  S = bf16(4 sc);  ZS = bf16(4 sc + zp sc)
+// and the quarter split: byte j of a row holds q[j] | q[Q+j] << 2 | q[2Q+j] << 4 | q[3Q+j] << 6.
+//
+// Every arithmetic step uses the explicitly rounded intrinsics (no contraction into FMA),
+// division is correctly rounded, rintf rounds half to even: the result is bit-exact with the
+// definition.  The kernel is HBM-bound (2 bytes read per weight, 0.28 written).
+//
+// Work unit: one warp per (row n, span s), where span s is packed bytes [128 s, 128 s + 128)
+// of the row -- the four groups s, NG + s, 2 NG + s, 3 NG + s (NG = H / 512), one per plane.
+// Lane l owns packed bytes 4l .. 4l+3 of the span, i.e. four consecutive weights of each of
+// the four groups, so the packed word it writes needs nothing from other lanes.
+#include "dh_common.cuh"
+#include "dh_internal.h"
+
+namespace dh {
+
+__device__ __forceinline__ float warp_min(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t *__restrict__ W,
+                                                       uint8_t *__restrict__ packed,
+                                                       uint16_t *__restrict__ S,
+                                                       uint16_t *__restrict__ ZS, int V, int H)
+{
+    const int lane = threadIdx.x & 31;
+    const int NG = H / 512;     // spans per row
+    const int NGt = H / kGroup; // groups per row
+    const int Q = H / 4;
+    const long long total = static_cast<long long>(V) * NG;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long item = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) +
+                          (threadIdx.x >> 5);
+         item < total; item += nwarps) {
+        const long long n = item / NG;
+        const int s = static_cast<int>(item - n * NG);
+        const uint16_t *row = W + n * H;
+        // four weights of each plane: k = p*Q + 128 s + 4 lane + i
+        uint2 raw[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * Q + 128 * s + 4 * lane));
+        uint32_t word = 0;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float w[4];
+            w[0] = __uint_as_float(raw[p].x << 16);
+            w[1] = __uint_as_float(raw[p].x & 0xFFFF0000u);
+            w[2] = __uint_as_float(raw[p].y << 16);
+            w[3] = __uint_as_float(raw[p].y & 0xFFFF0000u);
+            float lo = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
+            float hi = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+            lo = warp_min(lo);
+            hi = warp_max(hi);
+            float sc = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+            sc = fmaxf(sc, 1e-8f);
+            float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), 3.0f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float r = rintf(__fadd_rn(__fdiv_rn(w[i], sc), zp));
+                uint32_t qv = static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 3.0f));
+                word |= qv << (8 * i + 2 * p);
+            }
+            if (lane == p) {
+                const float s4 = __fmul_rn(4.0f, sc);
+                const long long gi = static_cast<long long>(p) * NG + s;
+                S[n * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(s4));
+                ZS[n * NGt + gi] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(s4, __fmul_rn(zp, sc))));
+            }
+        }
+        reinterpret_cast<uint32_t *>(packed + n * Q + 128 * s)[lane] = word;
+    }
+}
+
+cudaError_t launch_quantize(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
+                            uint16_t *ZS, cudaStream_t stream)
+{
+    const long long total = static_cast<long long>(V) * (H / 512);
+    long long blocks = (total + 7) / 8;
+    const long long cap = static_cast<long long>(kNumSMs) * 8;
+    if (blocks > cap) blocks = cap;
+    quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, packed, S, ZS, V, H);
+    return cudaGetLastError();
+}
+
+} // namespace dh

@@ -1,0 +1,136 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds, loads, exports every
+entry point declared in include/dh.h, and rejects bad arguments before launching anything.
+
+Invalid calls must return their status without touching the device, so these run on a
+machine without a GPU (fake, never dereferenced device addresses are passed).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantised_speculative_draft_gb300 as dh
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dh.h")
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dh.build()
+    return dh._load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dh_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    for must in ("dh_quantize", "dh_workspace_bytes", "dh_forward", "dh_forward_debug",
+                 "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for",
+                 "dh_device_status", "dh_last_error", "dh_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(dh.library_path())
+    for name in declared_functions():
+        assert hasattr(so, name), f"{name} declared in dh.h but not exported"
+
+
+def test_version(lib):
+    assert dh.dh_version() >> 16 == 1
+
+
+def _fwd(lib, M=4, H=1024, V=8192, kcand=8, rerank=32, topk=1, ws=1 << 40, **ptrs):
+    p = dict(x=FAKE, packed=FAKE, scales=FAKE, zeros=FAKE, W=FAKE, idx=FAKE, logit=FAKE,
+             ws=FAKE)
+    if "ws_ptr" in ptrs:
+        p["ws"] = ptrs.pop("ws_ptr")
+    p.update(ptrs)
+    return lib.dh_forward(p["x"], p["packed"], p["scales"], p["zeros"], p["W"], M, H, V, kcand,
+                          rerank, topk, p["idx"], p["logit"], p["ws"], ws, None)
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(x=None), -1), (dict(W=None), -1), (dict(ws=None), -1), (dict(idx=None), -1),
+    (dict(M=0), -2), (dict(M=129), -2), (dict(H=256), -2), (dict(H=1000), -2), (dict(H=0), -2),
+    (dict(V=0), -2),
+    (dict(kcand=0), -3), (dict(kcand=65), -3),
+    (dict(rerank=0), -3), (dict(rerank=1025), -3), (dict(topk=0), -3), (dict(topk=33), -3),
+    (dict(V=100, kcand=64, rerank=101), -3),   # 64 + 36 valid candidates
+    (dict(V=100, kcand=8, rerank=17), -3),     # 8 + 8 valid candidates
+    (dict(x=FAKE + 8), -5), (dict(packed=FAKE + 4), -5), (dict(ws=FAKE + 2), -5),
+    (dict(wsbytes=16), -4),
+])
+def test_forward_rejects_bad_arguments_before_launch(lib, kw, code):
+    wsbytes = kw.pop("wsbytes", 1 << 40)
+    rc = _fwd(lib, ws=wsbytes, **{("ws_ptr" if k == "ws" else k): v for k, v in kw.items()})
+    assert rc == code, dh.dh_last_error()
+    assert dh.dh_last_error() != ""
+
+
+def test_boundary_selection_parameters_are_accepted_by_the_checks(lib):
+    # V=100, kcand=64: exactly 100 valid candidates -> rerank 100 passes the checks and only
+    # fails later on the (fake) workspace size
+    assert _fwd(lib, V=100, kcand=64, rerank=100, topk=100, ws=16) == -4
+    assert _fwd(lib, V=8192, kcand=8, rerank=1024, topk=1024, ws=16) == -4
+
+
+def test_workspace_bytes(lib):
+    assert dh.dh_workspace_bytes(1, 1024, 8192, 8, 32) > 0
+    assert dh.dh_workspace_bytes(0, 1024, 8192, 8, 32) == 0
+    assert dh.dh_workspace_bytes(1, 1000, 8192, 8, 32) == 0
+    assert dh.dh_workspace_bytes(1, 1024, 8192, 8, 5000) == 0
+    small = dh.dh_workspace_bytes(16, 5120, 124160, 8, 32)
+    big = dh.dh_workspace_bytes(72, 5120, 248320, 8, 32)
+    assert 0 < small < big
+    # candidates dominate: M * nblk * kcand * 8 bytes
+    assert big >= 72 * 3880 * 8 * 8
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    q = lib.dh_quantize
+    assert q(None, 10, 1024, FAKE, FAKE, FAKE, None) == -1
+    assert q(FAKE, 0, 1024, FAKE, FAKE, FAKE, None) == -2
+    assert q(FAKE, 10, 768, FAKE, FAKE, FAKE, None) == -2
+    assert q(FAKE, 10, 1024, FAKE + 1, FAKE, FAKE, None) == -5
+
+
+def test_forward_debug_and_timed_reject_bad_optional_pointers(lib):
+    args = [FAKE] * 5 + [4, 1024, 8192, 8, 32, 1, FAKE, FAKE, FAKE, 1 << 40]
+    assert lib.dh_forward_debug(*args, FAKE + 4, None, None, None, None, None) == -5
+    assert lib.dh_forward_timed(*args, None, None) == -1
+    arr = (ctypes.c_void_p * 6)(*([FAKE] * 5 + [0]))
+    assert lib.dh_forward_timed(*args, arr, None) == -1
+
+
+def test_coarse_path_setting(lib):
+    prev = dh.dh_set_coarse_path(dh.PATH_WARP)
+    try:
+        assert dh.dh_coarse_path_for(16) == dh.PATH_WARP
+        with pytest.raises(dh.DHError):
+            dh.dh_set_coarse_path(7)
+        with pytest.raises(dh.DHError):
+            dh.dh_coarse_path_for(0)
+    finally:
+        dh.dh_set_coarse_path(prev)
+
+
+def test_product_path_never_touches_the_oracle():
+    """The CUDA library and its binding import, link and call nothing under oracle/."""
+    pkg = os.path.join(ROOT, "quantised_speculative_draft_gb300")
+    bad = re.compile(r"import\s+oracle|from\s+oracle|liboracle|dh_oracle|orc_[a-z]")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not bad.search(src), f
