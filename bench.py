@@ -1,0 +1,490 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 draft head (2-bit coarse LM head + exact rerank).
+
+One step = one dh_forward over one batch of M hidden states on the full-vocabulary head
+(V=248320, H=5120, KCAND=8, RERANK=32, argmax): stage x, coarse pass with block top-KCAND,
+top-RERANK selection, exact rerank, top-k.  Inputs are synthetic and seeded, resident in HBM
+when the timed region starts; two input sets (2.9 GB each, far above the 129 MB L2) alternate
+between steps so no step reads the previous one's weight from L2.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead (the
+reference arm: a plain fp64 restatement of the method on the host cores, run on a bounded
+vocabulary slice per step and scaled to the whole head).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft-head µs/call and HBM GB/s (or TF/s) at V=248320,H=5120,M=1..72"
+UNIT = "us/call"
+V_FULL, H_FULL = 248320, 5120
+KCAND, RERANK, TOPK = 8, 32, 1
+SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 72)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--M", type=int, default=16)
+    ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic_bytes(V, H):
+    """Bytes the method must stream per call: packed int2 (V*H/4) + S and ZS (2 * V*H/128 * 2)."""
+    return V * H // 4 + 2 * V * (H // 128) * 2
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.6)
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            except Exception:
+                ts = None
+            rows.append((ts, parts))
+        os.unlink(self.path)
+        inside = [p for ts, p in rows if ts is None or (t0 - 0.05 <= ts <= t1 + 0.05)] or \
+            [p for _, p in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(p[2]) for p in inside if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for p in inside if p[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for p in inside:
+            for name, val in zip(names, p[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+class Inputs:
+    """One resident input set: x for every swept M, the bf16 head and its int2 packing."""
+
+    def __init__(self, seed, dev, max_m):
+        import torch
+        import quantised_speculative_draft_gb300 as dh
+        from quantised_speculative_draft_gb300 import synth
+        wl = synth.full(max_m)
+        self.x = synth.make_x(wl, seed, dev)
+        self.W = synth.make_w(wl, seed, dev)
+        V, H = self.W.shape
+        self.packed = torch.empty(V, H // 4, dtype=torch.uint8, device=dev)
+        self.S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        self.ZS = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        dh.dh_quantize(self.W, self.packed, self.S, self.ZS)
+
+
+def make_outputs(M, dev):
+    import torch
+    import quantised_speculative_draft_gb300 as dh
+    ws = torch.empty(dh.dh_workspace_bytes(M, H_FULL, V_FULL, KCAND, RERANK), dtype=torch.uint8,
+                     device=dev)
+    idx = torch.empty(M, TOPK, dtype=torch.int32, device=dev)
+    logit = torch.empty(M, TOPK, dtype=torch.float32, device=dev)
+    return ws, idx, logit
+
+
+def fwd(sets, i, M, ws, idx, logit):
+    import quantised_speculative_draft_gb300 as dh
+    s = sets[i % len(sets)]
+    dh.dh_forward(s.x[:M], s.packed, s.S, s.ZS, s.W, KCAND, RERANK, TOPK, idx, logit, ws)
+
+
+def time_graph(sets, M, steps, warmup, dist=None):
+    """Mean device time per forward: one CUDA graph per input set, replayed alternately."""
+    import torch
+    ws, idx, logit = make_outputs(M, sets[0].x.device)
+    for i in range(warmup):
+        fwd(sets, i, M, ws, idx, logit)
+    torch.cuda.synchronize()
+    graphs = []
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for k in range(len(sets)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fwd(sets, k, M, ws, idx, logit)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    for i in range(max(3, warmup)):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        graphs[i % len(graphs)].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1), t0, t1
+
+
+def time_stages(sets, M, steps):
+    """Per-stage device time (CUDA events at the stage boundaries, on the launch stream)."""
+    import torch
+    import quantised_speculative_draft_gb300 as dh
+    ws, idx, logit = make_outputs(M, sets[0].x.device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(dh.NUM_STAGE_EVENTS)]
+           for _ in range(steps)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record()
+    for i in range(3):
+        fwd(sets, i, M, ws, idx, logit)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        s = sets[i % len(sets)]
+        dh.dh_forward_timed(s.x[:M], s.packed, s.S, s.ZS, s.W, KCAND, RERANK, TOPK, idx, logit,
+                            ws, evs[i])
+    torch.cuda.synchronize()
+    names = ["prep", "coarse", "select", "rerank", "topk"]
+    out = {}
+    for j, n in enumerate(names):
+        out[n] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) * 1e3
+    out["total"] = statistics.mean(evs[i][0].elapsed_time(evs[i][5]) for i in range(steps)) * 1e3
+    return out
+
+
+def time_e2e(sets, M, steps):
+    """The same call end to end with host buffers: pinned x in, dh_forward, idx/logit out."""
+    import torch
+    dev = sets[0].x.device
+    ws, idx, logit = make_outputs(M, dev)
+    xh = [s.x[:M].cpu().pin_memory() for s in sets]
+    xd = torch.empty(M, H_FULL, dtype=torch.bfloat16, device=dev)
+    ih = torch.empty(M, TOPK, dtype=torch.int32).pin_memory()
+    lh = torch.empty(M, TOPK, dtype=torch.float32).pin_memory()
+    import quantised_speculative_draft_gb300 as dh
+
+    def one(i):
+        s = sets[i % len(sets)]
+        xd.copy_(xh[i % len(sets)], non_blocking=True)
+        dh.dh_forward(xd, s.packed, s.S, s.ZS, s.W, KCAND, RERANK, TOPK, idx, logit, ws)
+        ih.copy_(idx, non_blocking=True)
+        lh.copy_(logit, non_blocking=True)
+
+    for i in range(5):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / steps, M * H_FULL * 2, M * TOPK * 8
+
+
+def time_quantize(dev):
+    """dh_quantize on the one-shard head (124160 x 5120 bf16) and on the full head."""
+    import torch
+    import quantised_speculative_draft_gb300 as dh
+    from quantised_speculative_draft_gb300 import synth
+    out = {}
+    for name, wl in (("shard", synth.shard(16)), ("full", synth.full(16))):
+        W = synth.make_w(wl, 7, dev)
+        V, H = W.shape
+        packed = torch.empty(V, H // 4, dtype=torch.uint8, device=dev)
+        S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        ZS = torch.empty_like(S)
+        for _ in range(3):
+            dh.dh_quantize(W, packed, S, ZS)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 10
+        e0.record()
+        for _ in range(n):
+            dh.dh_quantize(W, packed, S, ZS)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / n
+        nbytes = V * H * 2 + algorithmic_bytes(V, H)
+        out[name] = {"V": V, "H": H, "us": round(us, 2), "GB/s": round(nbytes / us / 1e3, 1)}
+        del W, packed, S, ZS
+    return out
+
+
+def roofline_entry(M, coarse_us, hbm, tflops, src):
+    nbytes = algorithmic_bytes(V_FULL, H_FULL)
+    flops = 2 * M * H_FULL * V_FULL
+    gbs = nbytes / coarse_us / 1e3
+    tfs = flops / coarse_us / 1e6
+    bound = "hbm" if M <= 32 else "tensor"
+    if bound == "hbm":
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gbs / hbm, 4), "peak_source": src, "bytes_per_launch": nbytes}
+    return {"bound": "tensor", "achieved": round(tfs, 1), "peak": tflops, "unit": "TFLOP/s",
+            "frac": round(tfs / tflops, 4), "peak_source": src, "flops_per_launch": flops}
+
+
+def traffic_from_profile(M):
+    """DRAM bytes per coarse launch from the committed ncu summary, if it was taken on the
+    current coarse-kernel sources (else null)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "coarse_traffic.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for f in rec.get("sources", []):
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if h.hexdigest() != rec.get("sha256"):
+        return None
+    return rec.get("traffic_per_launch", {}).get(str(M))
+
+
+def cpu_oracle_sample(xb, packed, S, ZS, Wb, M, frac_den):
+    """Time the oracle forward over the first V/frac_den vocabulary rows; scale to the head."""
+    from oracle import oracle as orc
+    Vs = (V_FULL // frac_den) // 64 * 64
+    t0 = time.perf_counter()
+    res = orc.forward(xb[:M], packed[:Vs], S[:Vs], ZS[:Vs], Wb, KCAND, RERANK, TOPK)
+    dt = time.perf_counter() - t0
+    del res
+    return dt * 1e6 * (V_FULL / Vs), Vs
+
+
+def host_copies(sets):
+    from quantised_speculative_draft_gb300 import synth
+    s = sets[0]
+    return (synth.bits(s.x), s.packed.cpu().numpy(), synth.bits(s.S), synth.bits(s.ZS),
+            synth.bits(s.W))
+
+
+def run_ours(args):
+    import torch
+    import quantised_speculative_draft_gb300 as dh
+    dist = None
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        dist = td
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    dh.build()
+    max_m = max(SWEEP_M + (args.M,))
+    sets = [Inputs(seed, dev, max_m) for seed in (0, 1)]
+    torch.cuda.synchronize()
+    hbm, tfl, src = peaks()
+
+    # headline: M = args.M
+    M = args.M
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms, t0, t1 = time_graph(sets, M, args.steps, args.warmup, dist)
+    clocks = sampler.stop(t0, t1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    us_per_call = ms * 1e3 / args.steps
+    stages = time_stages(sets, M, 50)
+    e2e_us, h2d, d2h = time_e2e(sets, M, 200)
+    launches = dh.dh_forward_launch_count(M, H_FULL, V_FULL, KCAND, RERANK)
+
+    roof = roofline_entry(M, stages["coarse"], hbm, tfl, src)
+    roof["kernel"] = "coarse pass + fused block top-KCAND (%s path)" % (
+        "tcgen05" if dh.dh_coarse_path_for(M) == dh.PATH_TC else "warp mma.sync")
+    roof["launch_us"] = round(stages["coarse"], 2)
+    roof["traffic"] = traffic_from_profile(M)
+
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        for m in SWEEP_M:
+            msw, _, _ = time_graph(sets, m, args.sweep_steps, 5)
+            st = time_stages(sets, m, 20)
+            r = roofline_entry(m, st["coarse"], hbm, tfl, src)
+            sweep.append({"M": m, "us_per_call": round(msw * 1e3 / args.sweep_steps, 2),
+                          "coarse_us": round(st["coarse"], 2),
+                          "path": "tcgen05" if dh.dh_coarse_path_for(m) == dh.PATH_TC else "warp",
+                          "coarse_GB/s": round(algorithmic_bytes(V_FULL, H_FULL) / st["coarse"] / 1e3, 1),
+                          "coarse_TF/s": round(2 * m * H_FULL * V_FULL / st["coarse"] / 1e6, 1),
+                          "roofline": {"bound": r["bound"], "frac": r["frac"]},
+                          "stages_us": {k: round(v, 2) for k, v in st.items()}})
+
+    pack = time_quantize(dev) if rank == 0 else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xb, pb, Sb, ZSb, Wb = host_copies(sets)
+        from oracle import oracle as orc
+        orc.build()
+        us, Vs = cpu_oracle_sample(xb, pb, Sb, ZSb, Wb, M, 4)
+        cpu = {"value": round(us, 1), "unit": UNIT, "cores": orc.default_threads(),
+               "kind": "oracle",
+               "sample": f"oracle forward (fp64 coarse, block top-{KCAND}, top-{RERANK}, exact "
+                         f"rerank, top-{TOPK}) over the first {Vs} of {V_FULL} vocabulary rows "
+                         f"at M={M}, wall time scaled by {V_FULL}/{Vs}"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(us_per_call / (world if world > 1 else 1), 3),
+            "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms / args.steps, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded normal x and W with hot rows; no trained weights)",
+            "config": {"workload": f"full-vocab head M={M} (V={V_FULL}, H={H_FULL}, "
+                                   f"KCAND={KCAND}, RERANK={RERANK}, argmax)",
+                       "M": M, "H": H_FULL, "V": V_FULL, "kcand": KCAND, "rerank": RERANK,
+                       "topk": TOPK, "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "two resident input sets of 2.9 GB alternate between steps "
+                             "(inputs larger than L2, no flush)",
+                       "timing": "CUDA graph per input set, replayed back to back; CUDA events"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "clocks": clocks,
+            "stages_us": {k: round(v, 2) for k, v in stages.items()},
+            "pack": pack,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    from quantised_speculative_draft_gb300 import synth
+    from oracle import oracle as orc
+    orc.build()
+    M = args.M
+    wl = synth.full(M)
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    x = synth.make_x(wl, 0, dev)
+    W = synth.make_w(wl, 0, dev)
+    xb, Wb = synth.bits(x), synth.bits(W)
+    del W
+    frac = 16
+    Vs = (V_FULL // frac) // 64 * 64
+    packed, S, ZS = orc.quantize(Wb[:Vs])
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        orc.forward(xb, packed, S, ZS, Wb, KCAND, RERANK, TOPK)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt * 1e6 * (V_FULL / Vs))
+    us = statistics.mean(times)
+    sample = (f"per step: oracle forward (fp64 coarse, block top-{KCAND}, top-{RERANK}, exact "
+              f"rerank, top-{TOPK}) over the first {Vs} of {V_FULL} vocabulary rows at M={M}, "
+              f"wall time scaled by {V_FULL}/{Vs}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"full-vocab head M={M} (V={V_FULL}, H={H_FULL}, KCAND={KCAND}, "
+                               f"RERANK={RERANK}, argmax)",
+                   "M": M, "H": H_FULL, "V": V_FULL, "kcand": KCAND, "rerank": RERANK,
+                   "topk": TOPK},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": orc.default_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

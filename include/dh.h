@@ -146,6 +146,13 @@ int dh_set_coarse_path(int path);
 int dh_coarse_path_for(int M);
 
 /*
+ * dh_forward_launch_count -- number of kernels one dh_forward with these sizes launches on the
+ * current coarse-path setting (0 when the sizes are invalid).  For benchmarks that count
+ * device launches.
+ */
+int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank);
+
+/*
  * dh_device_status -- DH_OK, or DH_ERR_DEVICE_TIMEOUT when a kernel since the last reset
  * gave up on a bounded wait.  Synchronises the current device to read the flag; reset != 0
  * clears it.  Returns DH_ERR_CUDA if the device cannot be read.

@@ -20,6 +20,7 @@ from .build import build
 __all__ = [
     "build", "DHError", "dh_quantize", "dh_workspace_bytes", "dh_forward", "dh_forward_debug",
     "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for", "dh_device_status",
+    "dh_forward_launch_count",
     "dh_last_error", "dh_version", "DraftHead", "PATH_AUTO", "PATH_WARP", "PATH_TC",
     "NUM_STAGE_EVENTS", "library_path",
 ]
@@ -72,6 +73,8 @@ def _load():
         lib.dh_set_coarse_path.restype = I
         lib.dh_coarse_path_for.argtypes = [I]
         lib.dh_coarse_path_for.restype = I
+        lib.dh_forward_launch_count.argtypes = [I, I, I, I, I]
+        lib.dh_forward_launch_count.restype = I
         lib.dh_device_status.argtypes = [I]
         lib.dh_device_status.restype = I
         lib.dh_last_error.argtypes = []
@@ -166,6 +169,10 @@ def dh_coarse_path_for(M: int) -> int:
     if rc < 0:
         raise DHError(rc, dh_last_error())
     return rc
+
+
+def dh_forward_launch_count(M: int, H: int, V: int, kcand: int, rerank: int) -> int:
+    return int(_load().dh_forward_launch_count(M, H, V, kcand, rerank))
 
 
 def dh_device_status(reset: bool = False) -> int:

@@ -336,6 +336,16 @@ int dh_coarse_path_for(int M)
     return choose_path(M, 5120);
 }
 
+int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank)
+{
+    if (check_shapes(M, H, V, kcand, rerank, 1) != DH_OK) return 0;
+    const Layout L = layout_for(M, H, V, kcand, rerank);
+    const int path = choose_path(M, H);
+    if (path < 0) return 0;
+    const int coarse = (path == DH_PATH_TC) ? tc_launches(M) : (M + kWarpBatch - 1) / kWarpBatch;
+    return 1 /*prep*/ + coarse + L.passes /*selection*/ + 1 /*rerank*/ + 1 /*top-k*/;
+}
+
 int dh_device_status(int reset)
 {
     int *p = timeout_flag_ptr();

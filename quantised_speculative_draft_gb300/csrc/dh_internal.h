@@ -53,6 +53,7 @@ size_t warp_xw_elems(int M, int H); // bf16 elements of the warp-path operand
 bool tc_supported(int M, int H);
 cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream);
 int tc_npad(int M);
+int tc_launches(int M); // coarse-pass launches of the tcgen05 path
 
 // Top-R selection over candidate lists.  Returns the number of passes it will take and the
 // scratch entries it needs (two ping-pong buffers of `scratch_entries` (val, idx) pairs).

@@ -142,13 +142,16 @@ def check_exact_values(gpu, x_bits, W_bits):
 
 
 def check_result(gpu, ref, kcand, topk, x_bits, W_bits):
-    """Final indices: exact where the decision gap is clear, valid where it is a tie."""
+    """Final indices: bit-exact where the decision gap is clear; where it is not (a tie row),
+    the returned list must still be the top-k of the GPU's own reranked set under the
+    oracle's exact values, within the exact-logit tolerance.  Returns the tie rows as
+    (row, gap, oracle indices, GPU indices, differs)."""
     gaps = orc.decision_gaps(ref, kcand, topk)
     ties = []
     M = gpu["idx"].shape[0]
     for m in range(M):
         gi, gl = gpu["idx"][m], gpu["logit"][m]
-        assert (gi >= 0).all(), f"row {m}: missing result"
+        assert (gi >= 0).all() and len(set(gi.tolist())) == topk, f"row {m}: bad result {gi}"
         e = orc.rerank(x_bits[m:m + 1], W_bits, gi[None, :].astype(np.int32))[0]
         tol = EXACT_RTOL * np.maximum(np.abs(e), 1.0)
         assert (np.abs(gl - e) <= tol).all(), f"row {m}: returned logits off"
@@ -161,8 +164,21 @@ def check_result(gpu, ref, kcand, topk, x_bits, W_bits):
                 f"{gaps[m]:.3g}")
             rtol = EXACT_RTOL * np.maximum(np.abs(ref["logit"][m]), 1.0)
             assert (np.abs(gl - ref["logit"][m]) <= rtol).all()
-        else:
-            ties.append((m, float(gaps[m]), ref["idx"][m].tolist(), gi.tolist()))
+            continue
+        differs = not np.array_equal(gi, ref["idx"][m])
+        if differs and "sel_idx" in gpu:
+            sel = gpu["sel_idx"][m]
+            assert set(gi.tolist()) <= set(sel.tolist()), f"row {m}: result outside reranked set"
+            es = orc.rerank(x_bits[m:m + 1], W_bits, sel[None, :].astype(np.int32))[0]
+            rest = es[~np.isin(sel, gi)]
+            floor = e.min()
+            slack = 2 * EXACT_RTOL * max(abs(floor), 1.0)
+            assert rest.size == 0 or rest.max() <= floor + slack, (
+                f"row {m}: a reranked entry above the returned top-k beyond tolerance")
+            for i in range(topk - 1):
+                assert e[i] + 2 * EXACT_RTOL * max(abs(e[i]), 1.0) >= e[i + 1], (
+                    f"row {m}: order of the returned list contradicts the exact values")
+        ties.append((m, float(gaps[m]), ref["idx"][m].tolist(), gi.tolist(), differs))
     return ties
 
 
