@@ -43,6 +43,11 @@ def parse():
     ap.add_argument("--sweep-steps", type=int, default=200)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--V", type=int, default=V_FULL,
+                    help="vocabulary rows (smaller heads are for profiling captures only)")
+    ap.add_argument("--sets", type=int, default=2, help="resident input sets rotated per step")
+    ap.add_argument("--profile", action="store_true",
+                    help="only run warmup + steps forwards (no timing, no JSON): for ncu")
     return ap.parse_args()
 
 
@@ -131,11 +136,14 @@ class ClockSampler:
 class Inputs:
     """One resident input set: x for every swept M, the bf16 head and its int2 packing."""
 
-    def __init__(self, seed, dev, max_m):
+    def __init__(self, seed, dev, max_m, V=V_FULL):
+        import dataclasses
         import torch
         import quantised_speculative_draft_gb300 as dh
         from quantised_speculative_draft_gb300 import synth
         wl = synth.full(max_m)
+        if V != wl.V:
+            wl = dataclasses.replace(wl, V=V, hot_rows=max(1, V // 100))
         self.x = synth.make_x(wl, seed, dev)
         self.W = synth.make_w(wl, seed, dev)
         V, H = self.W.shape
@@ -145,11 +153,11 @@ class Inputs:
         dh.dh_quantize(self.W, self.packed, self.S, self.ZS)
 
 
-def make_outputs(M, dev):
+def make_outputs(M, dev, V=None):
     import torch
     import quantised_speculative_draft_gb300 as dh
-    ws = torch.empty(dh.dh_workspace_bytes(M, H_FULL, V_FULL, KCAND, RERANK), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(dh.dh_workspace_bytes(M, H_FULL, V or V_FULL, KCAND, RERANK),
+                     dtype=torch.uint8, device=dev)
     idx = torch.empty(M, TOPK, dtype=torch.int32, device=dev)
     logit = torch.empty(M, TOPK, dtype=torch.float32, device=dev)
     return ws, idx, logit
@@ -343,8 +351,15 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     dh.build()
+    if args.profile:
+        sets = [Inputs(seed, dev, args.M, args.V) for seed in range(args.sets)]
+        ws, idx, logit = make_outputs(args.M, dev, args.V)
+        for i in range(args.warmup + args.steps):
+            fwd(sets, i, args.M, ws, idx, logit)
+        torch.cuda.synchronize()
+        return
     max_m = max(SWEEP_M + (args.M,))
-    sets = [Inputs(seed, dev, max_m) for seed in (0, 1)]
+    sets = [Inputs(seed, dev, max_m) for seed in range(args.sets)]
     torch.cuda.synchronize()
     hbm, tfl, src = peaks()
 

@@ -99,18 +99,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and sets *flag) if
-// it has not completed within kWaitTimeoutNs; the caller must then stop its work.
+// it has not completed within kWaitTimeoutNs, or after kWaitMaxPolls polls whatever the
+// timer says; the caller must then stop its work.
+constexpr uint32_t kWaitMaxPolls = 1u << 26;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *flag)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            atomicExch(flag, 1);
-            return false;
-        }
+        if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) break;
     }
+    atomicExch(flag, 1);
+    return false;
 }
 
 // ----------------------------------------------------------------------------------------
