@@ -132,6 +132,35 @@ int dh_forward_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *s
                      void *workspace, size_t ws_bytes, void *const *events, void *stream);
 
 /*
+ * dh_forward_noalloc -- dh_forward for callers that cannot allocate device memory.
+ * The pages have no counterpart: their host framework allocates per call.
+ *
+ * Some callers have no way to hand this library a workspace: a serving engine that has
+ * already reserved nearly all free device memory for its KV cache (an extra cudaMalloc would
+ * fail or eat into that cache), runtimes with a fixed memory pool, and latency-critical
+ * paths where cudaMalloc's implicit device synchronisation is not acceptable.  For them this
+ * entry point takes no workspace at all: its scratch is one file-scope device array of
+ * DH_NOALLOC_WORKSPACE_BYTES inside the library, which every GPU that loads the library holds
+ * until the process exits.  The caller still passes (and owns) every input and output.
+ *
+ *   Arguments, layouts, results and status codes are those of dh_forward without
+ *   workspace/ws_bytes.  Sizes whose workspace (dh_workspace_bytes) exceeds
+ *   DH_NOALLOC_WORKSPACE_BYTES are rejected with DH_ERR_WORKSPACE before anything runs.
+ *   No cudaMalloc, cudaFree or other allocating routine is ever called.
+ *   The first call on a device resolves the array's device address for that device (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call uses the same array, which keeps the previous call's contents (the forward
+ *   clears what must start at zero itself): calls that can overlap on the GPU -- on different
+ *   streams, or concurrently from several host threads -- race on it and must be serialised
+ *   by the caller.
+ */
+#define DH_NOALLOC_WORKSPACE_BYTES (16u << 20)
+int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                       const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                       int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                       void *stream);
+
+/*
  * Coarse-pass implementation choice (process-wide).
  *   DH_PATH_AUTO  pick by M (default)
  *   DH_PATH_WARP  warp-level mma.sync tensor-core path, batch handled 16 rows at a time

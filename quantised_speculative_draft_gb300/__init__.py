@@ -20,13 +20,14 @@ from .build import build
 __all__ = [
     "build", "DHError", "dh_quantize", "dh_workspace_bytes", "dh_forward", "dh_forward_debug",
     "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for", "dh_device_status",
-    "dh_forward_launch_count",
+    "dh_forward_launch_count", "dh_forward_noalloc", "NOALLOC_WORKSPACE_BYTES",
     "dh_last_error", "dh_version", "DraftHead", "PATH_AUTO", "PATH_WARP", "PATH_TC",
     "NUM_STAGE_EVENTS", "library_path",
 ]
 
 PATH_AUTO, PATH_WARP, PATH_TC = 0, 1, 2
 NUM_STAGE_EVENTS = 6
+NOALLOC_WORKSPACE_BYTES = 16 << 20
 GROUP = 128
 BLOCK_N = 64
 
@@ -69,6 +70,8 @@ def _load():
         lib.dh_forward_debug.restype = I
         lib.dh_forward_timed.argtypes = fwd + [P, P]
         lib.dh_forward_timed.restype = I
+        lib.dh_forward_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, P]
+        lib.dh_forward_noalloc.restype = I
         lib.dh_set_coarse_path.argtypes = [I]
         lib.dh_set_coarse_path.restype = I
         lib.dh_coarse_path_for.argtypes = [I]
@@ -155,6 +158,16 @@ def dh_forward_timed(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logi
     args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
     arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in events])
     _check(_load().dh_forward_timed(*args, arr, _stream(stream)))
+
+
+def dh_forward_noalloc(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit,
+                       stream=None):
+    """dh_forward without a workspace: scratch is the library's fixed device array
+    (NOALLOC_WORKSPACE_BYTES), for callers that cannot allocate device memory."""
+    M, H = x.shape
+    V = packed.shape[0]
+    _check(_load().dh_forward_noalloc(_p(x), _p(packed), _p(scales), _p(zeros), _p(W), M, H, V,
+                                      kcand, rerank, topk, _p(idx), _p(logit), _stream(stream)))
 
 
 def dh_set_coarse_path(path: int) -> int:

@@ -229,6 +229,28 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     return ok();
 }
 
+// Fixed scratch of dh_forward_noalloc: the whole forward workspace for callers that cannot
+// allocate.  Host code must not use this name as an address (it is a host-side stand-in);
+// its device address is resolved per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DH_NOALLOC_WORKSPACE_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, resolved once per device with
+// that device current; nullptr if the runtime cannot resolve it.
+void *noalloc_scratch_ptr()
+{
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 } // namespace
 
 CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,
@@ -318,6 +340,28 @@ int dh_forward_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *s
     return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
                         logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
                         events, static_cast<cudaStream_t>(stream));
+}
+
+int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                       const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                       int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                       void *stream)
+{
+    if (!x || !packed || !scales || !zeros || !W_bf16 || !idx || !logit)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    int rc = check_shapes(M, H, V, kcand, rerank, topk);
+    if (rc != DH_OK) return rc;
+    const size_t need = layout_for(M, H, V, kcand, rerank).total;
+    if (need > DH_NOALLOC_WORKSPACE_BYTES)
+        return fail(DH_ERR_WORKSPACE,
+                    "M=%d H=%d V=%d kcand=%d rerank=%d need %zu bytes of scratch; the fixed "
+                    "buffer of dh_forward_noalloc holds %u (use dh_forward with a workspace)",
+                    M, H, V, kcand, rerank, need, DH_NOALLOC_WORKSPACE_BYTES);
+    void *ws = noalloc_scratch_ptr();
+    if (!ws) return fail(DH_ERR_CUDA, "cannot resolve the device address of the fixed scratch");
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, ws, DH_NOALLOC_WORKSPACE_BYTES, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int dh_set_coarse_path(int path)
