@@ -222,7 +222,7 @@ def time_stages(sets, M, steps):
         dh.dh_forward_timed(s.x[:M], s.packed, s.S, s.ZS, s.W, KCAND, RERANK, TOPK, idx, logit,
                             ws, evs[i])
     torch.cuda.synchronize()
-    names = ["prep", "coarse", "select", "rerank", "topk"]
+    names = ["prep", "coarse", "select", "rerank_topk"]
     out = {}
     for j, n in enumerate(names):
         out[n] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) * 1e3

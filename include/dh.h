@@ -122,7 +122,7 @@ int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *s
  * dh_forward_timed -- dh_forward that records caller-created CUDA events (cudaEvent_t, cast
  * to void*) at the stage boundaries, for per-kernel timing inside a benchmark:
  *   events[0] before staging x, [1] before the coarse pass, [2] before candidate
- *   selection, [3] before the rerank, [4] before the top-k merge, [5] after it.
+ *   selection, [3] before the rerank (which also runs the top-k merge), [4] and [5] after it.
  * `events` must hold DH_NUM_STAGE_EVENTS valid events.
  */
 #define DH_NUM_STAGE_EVENTS 6
@@ -162,15 +162,20 @@ int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t 
 
 /*
  * Coarse-pass implementation choice (process-wide).
- *   DH_PATH_AUTO  pick by M (default)
- *   DH_PATH_WARP  warp-level mma.sync tensor-core path, batch handled 16 rows at a time
- *   DH_PATH_TC    tcgen05 / tensor-memory path
- * dh_set_coarse_path returns the previous setting, or DH_ERR_ARG for an unknown value.
- * dh_coarse_path_for(M) reports which path a forward with M rows would take.
+ *   DH_PATH_AUTO     pick by M (default)
+ *   DH_PATH_WARP     warp-level mma.sync on bf16 operands (the page's 1 + v/4 bit pattern),
+ *                    batch handled 16 rows at a time
+ *   DH_PATH_TC       tcgen05 with 8-bit operands: weights as the e4m3 pattern 1 + v/8, x split
+ *                    exactly into e4m3 terms stacked along N, batch in launches of 64 rows
+ *   DH_PATH_TC_BF16  tcgen05 on bf16 operands (the page's 1 + v/4 bit pattern)
+ * All paths compute the same coarse values up to fp32 rounding.  dh_set_coarse_path returns
+ * the previous setting, or DH_ERR_ARG for an unknown value.  dh_coarse_path_for(M) reports
+ * which path a forward with M rows would take.
  */
 #define DH_PATH_AUTO 0
 #define DH_PATH_WARP 1
 #define DH_PATH_TC 2
+#define DH_PATH_TC_BF16 3
 int dh_set_coarse_path(int path);
 int dh_coarse_path_for(int M);
 

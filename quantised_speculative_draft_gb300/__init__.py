@@ -21,11 +21,11 @@ __all__ = [
     "build", "DHError", "dh_quantize", "dh_workspace_bytes", "dh_forward", "dh_forward_debug",
     "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for", "dh_device_status",
     "dh_forward_launch_count", "dh_forward_noalloc", "NOALLOC_WORKSPACE_BYTES",
-    "dh_last_error", "dh_version", "DraftHead", "PATH_AUTO", "PATH_WARP", "PATH_TC",
+    "dh_last_error", "dh_version", "DraftHead", "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16",
     "NUM_STAGE_EVENTS", "library_path",
 ]
 
-PATH_AUTO, PATH_WARP, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_WARP, PATH_TC, PATH_TC_BF16 = 0, 1, 2, 3
 NUM_STAGE_EVENTS = 6
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 GROUP = 128

@@ -81,10 +81,10 @@ struct Layout {
     long long nblk = 0, ncand = 0, scratch_entries = 0;
     int passes = 0;
     size_t xs = 0, xw = 0, xt = 0, cval = 0, cidx = 0, sval[2] = {0, 0}, sidx[2] = {0, 0},
-           sel = 0, ex = 0, counters = 0, total = 0;
+           sel = 0, ex = 0, counters = 0, xt8 = 0, xs8 = 0, inv8 = 0, total = 0;
+    size_t xt8_chunk = 0;
 };
 
-constexpr int kNumCounters = 64;
 
 Layout layout_for(int M, int H, int V, int kcand, int rerank)
 {
@@ -113,6 +113,11 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     L.sel = take(static_cast<size_t>(M) * rerank * 4);
     L.ex = take(static_cast<size_t>(M) * rerank * 4);
     L.counters = take(kNumCounters * 4);
+    const int chunks8 = tc8_chunks(M);
+    L.xt8_chunk = align256(static_cast<size_t>(2 * kTc8MaxRows) * H); // T*MP <= 64 rows
+    L.xt8 = take(L.xt8_chunk * chunks8);
+    L.xs8 = take(static_cast<size_t>(chunks8) * kTc8MaxRows * (H / kGroup) * 4);
+    L.inv8 = take(static_cast<size_t>(chunks8) * kTc8MaxRows * 4);
     L.total = off;
     return L;
 }
@@ -144,10 +149,10 @@ int choose_path(int M, int H)
         std::lock_guard<std::mutex> lk(g_path_mu);
         p = g_path;
     }
-    if (p == DH_PATH_TC) return tc_supported(M, H) ? DH_PATH_TC : -1;
+    if (p == DH_PATH_TC || p == DH_PATH_TC_BF16) return tc_supported(M, H) ? p : -1;
     if (p == DH_PATH_WARP) return DH_PATH_WARP;
-    // automatic: the tcgen05 path where it is available, else the warp path
-    if (tc_supported(M, H) && M > 8) return DH_PATH_TC;
+    // automatic: the 8-bit tcgen05 path where it is available, else the warp path
+    if (tc_supported(M, H)) return DH_PATH_TC;
     return DH_PATH_WARP;
 }
 
@@ -190,9 +195,18 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     };
     cudaError_t err;
     if (!rec(0)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
-    err = launch_prep(x, M, H, path == DH_PATH_WARP ? L.Mpad_w : 0, xs,
-                      path == DH_PATH_WARP ? xw : nullptr, path == DH_PATH_TC ? xt : nullptr,
-                      path == DH_PATH_TC ? L.Npad : 0, counters, kNumCounters, stream);
+    Tc8Workspace w8;
+    w8.xt8 = ws + L.xt8;
+    w8.chunk_bytes = L.xt8_chunk;
+    w8.xs = reinterpret_cast<float *>(ws + L.xs8);
+    w8.inv_scale = reinterpret_cast<float *>(ws + L.inv8);
+    if (path == DH_PATH_TC)
+        err = launch_prep_fp8(x, M, H, w8, counters, kNumCounters, stream);
+    else
+        err = launch_prep(x, M, H, path == DH_PATH_WARP ? L.Mpad_w : 0, xs,
+                          path == DH_PATH_WARP ? xw : nullptr,
+                          path == DH_PATH_TC_BF16 ? xt : nullptr,
+                          path == DH_PATH_TC_BF16 ? L.Npad : 0, counters, kNumCounters, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "prep launch: %s", cudaGetErrorString(err));
     if (!rec(1)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
 
@@ -212,19 +226,22 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     a.coarse = coarse;
     a.counters = counters;
     a.timeout_flag = tflag;
-    err = (path == DH_PATH_TC) ? launch_coarse_tc(a, stream) : launch_coarse_warp(a, stream);
+    if (path == DH_PATH_TC) err = launch_coarse_tc8(a, w8, stream);
+    else if (path == DH_PATH_TC_BF16) err = launch_coarse_tc(a, stream);
+    else err = launch_coarse_warp(a, stream);
     if (err != cudaSuccess)
         return fail(DH_ERR_CUDA, "coarse launch (%s path): %s",
-                    path == DH_PATH_TC ? "tcgen05" : "warp", cudaGetErrorString(err));
+                    path == DH_PATH_TC ? "tcgen05 8-bit"
+                                       : (path == DH_PATH_TC_BF16 ? "tcgen05 bf16" : "warp"),
+                    cudaGetErrorString(err));
     if (!rec(2)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     err = launch_select(cval, cidx, M, L.ncand, rerank, sv, si, L.scratch_entries, sel, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
     if (!rec(3)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
-    err = launch_rerank(x, W, M, H, V, sel, rerank, ex, stream);
+    err = launch_rerank_topk(x, W, M, H, V, sel, rerank, ex, counters + kRowDoneOffset, topk,
+                             idx, logit, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));
     if (!rec(4)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
-    err = launch_topk(ex, sel, M, rerank, topk, idx, logit, stream);
-    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(err));
     if (!rec(5)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     return ok();
 }
@@ -366,7 +383,8 @@ int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t 
 
 int dh_set_coarse_path(int path)
 {
-    if (path != DH_PATH_AUTO && path != DH_PATH_WARP && path != DH_PATH_TC)
+    if (path != DH_PATH_AUTO && path != DH_PATH_WARP && path != DH_PATH_TC &&
+        path != DH_PATH_TC_BF16)
         return fail(DH_ERR_ARG, "unknown coarse path %d", path);
     std::lock_guard<std::mutex> lk(g_path_mu);
     const int prev = g_path;
@@ -386,8 +404,10 @@ int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank)
     const Layout L = layout_for(M, H, V, kcand, rerank);
     const int path = choose_path(M, H);
     if (path < 0) return 0;
-    const int coarse = (path == DH_PATH_TC) ? tc_launches(M) : (M + kWarpBatch - 1) / kWarpBatch;
-    return 1 /*prep*/ + coarse + L.passes /*selection*/ + 1 /*rerank*/ + 1 /*top-k*/;
+    int prep = 1, coarse = (M + kWarpBatch - 1) / kWarpBatch;
+    if (path == DH_PATH_TC) prep = coarse = tc8_chunks(M);
+    else if (path == DH_PATH_TC_BF16) coarse = tc_launches(M);
+    return prep + coarse + L.passes /*selection*/ + 1 /*rerank + top-k*/;
 }
 
 int dh_device_status(int reset)

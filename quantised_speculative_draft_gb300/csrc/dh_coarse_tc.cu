@@ -24,6 +24,7 @@
 //   * every handoff is an mbarrier; every wait is bounded and gives up with a flag.
 #include "dh_common.cuh"
 #include "dh_internal.h"
+#include "dh_tcgen05.cuh"
 
 #include <climits>
 
@@ -38,10 +39,17 @@ constexpr int kPkBytes = kTileRows * kSpanBytes; // 16 KB packed box per span
 constexpr int kMaxN = 64;                       // batch rows per launch
 constexpr int kSmemLimitTc = 232448;
 
-// TMEM column map: A buffers (one per plane, 64 columns = 128 bf16 of K each), then two
-// D buffers of N fp32 columns.
-constexpr uint32_t kAcol = 0;
-constexpr uint32_t kDcol = 256;
+// Tensor memory (512 columns x 128 lanes): a ring of A buffers (64 columns = 128 bf16 of K,
+// one group's dequantised weights) followed by a ring of D buffers (N fp32 columns, one
+// group's partial p).  Deep rings let dequant, MMA and epilogue run several groups apart.
+template <int N> struct Rings {
+    static constexpr int kA = (N <= 32) ? 6 : 4;
+    static constexpr int kD0 = (kTmemCols - kA * 64) / N;
+    static constexpr int kD = kD0 > 8 ? 8 : kD0;
+    static constexpr uint32_t kAcol = 0;
+    static constexpr uint32_t kDcol = kA * 64;
+    static_assert(kD >= 2, "tensor memory too small for two accumulators");
+};
 
 struct TcParams {
     const uint16_t *S;
@@ -54,114 +62,6 @@ struct TcParams {
     float *coarse;
     int *timeout_flag;
 };
-
-// ---- tcgen05 wrappers -------------------------------------------------------------------
-
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before()
-{
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after()
-{
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_x64(uint32_t taddr, const uint32_t (&r)[64])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"
-                 "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-                 "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, "
-                 "%33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, "
-                 "%49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};" ::
-                     "r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
-                 "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
-                 "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
-                 "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]),
-                 "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]),
-                 "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]),
-                 "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]),
-                 "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]),
-                 "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]),
-                 "r"(r[62]), "r"(r[63])
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st()
-{
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16])
-{
-    uint32_t r[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {"
-                 "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr)
-                 : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_wait_ld()
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Bounded wait taken by every lane of a warp; the warp agrees on the outcome so that the
-// .sync.aligned tcgen05 instructions after it are never reached by part of a warp.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *flag)
-{
-    const bool ok = mbar_wait_bounded(bar, parity, flag);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
-// apart (SBO), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
-{
-    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (64ull << 32) |
-           (1ull << 46) | (2ull << 61);
-}
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M = 128, N.
 __host__ __device__ constexpr uint32_t make_idesc(int N)
@@ -193,11 +93,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *const bars = reinterpret_cast<uint64_t *>(xs_s + NGt * N);
     uint64_t *const full = bars;                  // [nstage]  TMA -> consumers
     uint64_t *const empty = full + nstage;        // [nstage]  consumers -> TMA
-    uint64_t *const a_full = empty + nstage;      // [4]       dequant -> MMA
-    uint64_t *const a_empty = a_full + 4;         // [4]       MMA -> dequant
-    uint64_t *const d_full = a_empty + 4;         // [2]       MMA -> epilogue
-    uint64_t *const d_empty = d_full + 2;         // [2]       epilogue -> MMA
-    uint64_t *const fin = d_empty + 2;            // [1]       MMA drain before teardown
+    constexpr int kA = Rings<N>::kA, kD = Rings<N>::kD;
+    uint64_t *const a_full = empty + nstage;      // [kA]      dequant -> MMA
+    uint64_t *const a_empty = a_full + kA;        // [kA]      MMA -> dequant
+    uint64_t *const d_full = a_empty + kA;        // [kD]      MMA -> epilogue
+    uint64_t *const d_empty = d_full + kD;        // [kD]      epilogue -> MMA
+    uint64_t *const fin = d_empty + kD;           // [1]       MMA drain before teardown
     uint64_t *const red_full = fin + 1;           // [1]       epilogue warps: tile written
     uint64_t *const red_free = red_full + 1;      // [1]       epilogue warps: tile selected
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(red_free + 1);
@@ -209,11 +110,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 8 + 1); // 8 dequant warps + 1 MMA commit
         }
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kA; ++i) {
             mbar_init(&a_full[i], 4);
             mbar_init(&a_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kD; ++i) {
             mbar_init(&d_full[i], 1);
             mbar_init(&d_empty[i], 4);
         }
@@ -274,21 +175,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t xbase = smem_u32(stages + static_cast<size_t>(st) * kStage + kPkBytes);
                     for (int q = 0; q < 4; ++q, ++t) {
-                        const uint32_t d = t & 1u;
-                        if (!mbar_wait_bounded(&a_full[q], s & 1u, prm.timeout_flag) ||
-                            !mbar_wait_bounded(&d_empty[d], ((t >> 1) & 1u) ^ 1u, prm.timeout_flag)) {
+                        const uint32_t a = t % kA, d = t % kD;
+                        if (!mbar_wait_bounded(&a_full[a], (t / kA) & 1u, prm.timeout_flag) ||
+                            !mbar_wait_bounded(&d_empty[d], ((t / kD) & 1u) ^ 1u, prm.timeout_flag)) {
                             failed = true;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d_tmem = tmem + kDcol + d * N;
-                        const uint32_t a_tmem = tmem + kAcol + q * 64;
+                        const uint32_t d_tmem = tmem + Rings<N>::kDcol + d * N;
+                        const uint32_t a_tmem = tmem + Rings<N>::kAcol + a * 64;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const uint32_t b_addr = xbase + (q * 2 + (i >> 2)) * (N * 128) + (i & 3) * 32;
                             mma_ts(d_tmem, a_tmem + i * 8, sw128_desc(b_addr), idesc, i > 0 ? 1u : 0u);
                         }
-                        mma_commit(&a_empty[q]);
+                        mma_commit(&a_empty[a]);
                         mma_commit(&d_full[d]);
                     }
                     if (!failed) mma_commit(&empty[st]);
@@ -299,9 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(fin, 0, prm.timeout_flag);
         }
     } else if (warp >= 4 && warp < 12) {
-        // ---------------- dequant: warps 4-7 planes 0-1, warps 8-11 planes 2-3 ----------------
+        // ---------------- dequant: warps 4-7 planes 0 and 2, warps 8-11 planes 1 and 3 -------
         const int row = ((warp & 3) << 5) | lane; // TMEM lane == tile row
-        const int qbase = (warp < 8) ? 0 : 2;
+        const int qoff = (warp < 8) ? 0 : 1;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
         uint32_t s = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
@@ -325,8 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&empty[st]);
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq) {
-                    const int q = qbase + qq;
-                    if (!warp_wait(&a_empty[q], (s & 1u) ^ 1u, prm.timeout_flag)) {
+                    const int q = qoff + 2 * qq;
+                    const uint32_t t = s * 4 + q;      // global group counter
+                    const uint32_t a = t % kA;
+                    if (!warp_wait(&a_empty[a], ((t / kA) & 1u) ^ 1u, prm.timeout_flag)) {
                         failed = true;
                         break;
                     }
@@ -357,11 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             r[2 * i + 1] = deq_pair_odd<3>(w[i]);
                         }
                     }
-                    tmem_st_x64(tmem + lane_base + kAcol + q * 64, r);
+                    tmem_st_x64(tmem + lane_base + Rings<N>::kAcol + a * 64, r);
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_full[q]);
+                    if (lane == 0) mbar_arrive(&a_full[a]);
                 }
                 if (failed) break;
             }
@@ -381,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int m = 0; m < N; ++m) acc[m] = 0.f;
             for (int span = 0; span < NG && !failed; ++span) {
                 for (int q = 0; q < 4; ++q, ++t) {
-                    const uint32_t d = t & 1u;
-                    if (!warp_wait(&d_full[d], (t >> 1) & 1u, prm.timeout_flag)) {
+                    const uint32_t d = t % kD;
+                    if (!warp_wait(&d_full[d], (t / kD) & 1u, prm.timeout_flag)) {
                         failed = true;
                         break;
                     }
@@ -394,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < N / 16; ++c) {
                         float v[16];
-                        tmem_ld_x16(tmem + lane_base + kDcol + d * N + c * 16, v);
+                        tmem_ld_x16(tmem + lane_base + Rings<N>::kDcol + d * N + c * 16, v);
                         tmem_wait_ld();
                         if (c == N / 16 - 1) {
                             // the partial has been read out: hand the D buffer back
@@ -504,7 +407,7 @@ cudaError_t launch_n(const CUtensorMap &tm_packed, const uint16_t *xt_chunk, con
     const int NGt = base.H / kGroup;
     constexpr int kStage = kPkBytes + N * 1024;
     const size_t fixed = 1024 + static_cast<size_t>(N) * kTileRows * 4 +
-                         static_cast<size_t>(NGt) * N * 4 + 64 * 8 + 32;
+                         static_cast<size_t>(NGt) * N * 4 + 96 * 8 + 32;
     int nstage = static_cast<int>((kSmemLimitTc - static_cast<long long>(fixed)) / kStage);
     if (nstage > 4) nstage = 4;
     if (nstage < 2) return cudaErrorInvalidConfiguration;

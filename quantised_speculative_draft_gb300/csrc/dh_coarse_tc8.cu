@@ -1,0 +1,508 @@
+// dh_coarse_tc8.cu -- kernels (2)+(3), tcgen05 path with 8-bit operands: coarse pass on the
+// 5th-generation tensor cores (kind::f8f6f4, A from tensor memory) and the fused block
+// top-KCAND epilogue.
+//
+// radiance_drafthead.py, _draft_head_int2 and _emit.  The page's kernel feeds its dot product
+// with the bf16 bit pattern 1 + v/4 and collapses the scale and zero into two accumulator
+// operations per group.  On GB300 a tcgen05.mma of M = 128 costs a fixed number of cycles
+// per instruction below N = 64 whatever the operand type, and an 8-bit instruction covers
+// twice the K of a bf16 one, so this kernel feeds the same collapsed form through 8-bit
+// operands:
+//   * weight: the e4m3 value 1 + v/8 is the bit pattern 0x38 | v, so one and-or (plus one
+//     shift for planes 1-3) turns a 32-bit word of packed bytes into four e4m3 weights of one
+//     plane -- in k order, no permutation;
+//   * x: every row is scaled by a power of two 2^e (max |x 2^e| in [128, 256)) and split
+//     exactly into T e4m3 terms, x 2^e = x1 + x2 (+ x3); the terms are stacked along the MMA's
+//     N dimension (rows t*MP + m), which costs nothing below N = 64;
+//   * per group g (128 consecutive k of one plane), with p = sum over the T terms of the
+//     partial D, sum_k x_k (1 + v/4) = 2 p - xs, so
+//         c[m, n] = 2^-e * sum_g ( 2 S[n,g] p - (S[n,g] + ZS[n,g]) xs'[m,g] )
+//     with xs' the group sums of the represented x (in the scaled units): the scale and zero
+//     are applied to the fp32 partial of every group, never to the weight.
+//
+// Roles (16 warps, one CTA per SM, persistent over 128-row vocabulary tiles):
+//   warp 0       TMA: per span one [128 rows x 128 B] box of packed bytes and four
+//                [128 k x N] boxes of the staged x terms (128-byte swizzle) into a stage ring
+//   warp 1       MMA issuer: per group 4 x tcgen05.mma kind::f8f6f4, M = 128, K = 32
+//   warps 2-3    block top-KCAND of the previous tile (overlaps the current tile)
+//   warps 4-7,   dequant: one TMEM lane (= one vocabulary row) per thread; warps 4-7 write
+//   warps 8-11   planes 0-1, warps 8-11 planes 2-3 of every span (two tcgen05.st of 32
+//                columns, one wait) into a ring of A buffers
+//   warps 12-15  epilogue: tcgen05.ld of the partials (two groups per wait when they fit in
+//                registers), sum of the T terms, scale/zero fold into fp32 registers, and at
+//                the tile end the coarse values into the shared tile buffer
+// Every handoff is an mbarrier; every wait is bounded.
+#include "dh_common.cuh"
+#include "dh_internal.h"
+#include "dh_tcgen05.cuh"
+
+#include <climits>
+
+namespace dh {
+
+namespace {
+
+constexpr int kTileRows = 128;
+constexpr int kThreads = 512;
+constexpr int kTmemCols = 512;
+constexpr int kPkBytes = kTileRows * kSpanBytes; // 16 KB packed box per span
+constexpr int kSmemLimit8 = 232448;
+
+// Batch rows per launch MP in {16, 32}; x in T = 2 e4m3 terms; MMA N = T * MP.
+// Tensor memory: two span-sized A buffers (4 groups x 32 columns) and a ring of kD group-sized
+// accumulators (N columns).
+template <int MP> struct Cfg8 {
+    static constexpr int T = 2;
+    static constexpr int N = MP * T;
+    static constexpr int kAs = 2;                           // A buffers, one span each
+    static constexpr int kD = (kTmemCols - kAs * 128) / N;  // 8 at N = 32, 4 at N = 64
+    static constexpr uint32_t kAcol = 0;
+    static constexpr uint32_t kDcol = kAs * 128;
+    static constexpr uint32_t kXBytes = N * 512;            // 4 planes x 128 k x N rows
+    static constexpr uint32_t kStage = kPkBytes + kXBytes;  // multiple of 1024
+    static_assert(kD >= 4, "a span of accumulators must fit");
+    static_assert(N % 16 == 0 && N <= 256, "MMA N out of range");
+};
+
+struct Tc8Params {
+    const uint16_t *S;
+    const uint16_t *ZS;
+    const float *xs;        // [MP rows of this launch][NGt], sums of the represented x, scaled
+    const float *inv_scale; // [MP] 2^-e per batch row
+    int V, H, m0, mrows, kcand, ntiles, nstage;
+    long long ncand;
+    float *cand_val;
+    int32_t *cand_idx;
+    float *coarse;
+    int *timeout_flag;
+};
+
+// kind::f8f6f4 instruction descriptor: D f32, A e4m3, B e4m3, both K-major, M = 128, N.
+__host__ __device__ constexpr uint32_t make_idesc_f8(int N)
+{
+    return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// e4m3 weights 1 + v/8 of plane P from a word of four packed bytes (four consecutive k)
+template <int P>
+__device__ __forceinline__ uint32_t deq4_e4m3(uint32_t w)
+{
+    return ((w >> (2 * P)) & 0x03030303u) | 0x38383838u;
+}
+
+// Block top-KCAND of up to 4 (batch column, block) pairs at once.  Lane l holds rows l and
+// l + 32 of each pair's 64-row block as order keys (0 = no row); one round takes the largest
+// key by redux.sync, equal values go to the lower row.
+template <int NB>
+__device__ __forceinline__ void select_pairs(uint32_t (&k0)[NB], uint32_t (&k1)[NB],
+                                             const int (&base_row)[NB], float *const (&oval)[NB],
+                                             int32_t *const (&oidx)[NB], int kcand, int lane)
+{
+    for (int r = 0; r < kcand; ++r) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const uint32_t km = __reduce_max_sync(0xffffffffu, k0[b] > k1[b] ? k0[b] : k1[b]);
+            const unsigned b0 = __ballot_sync(0xffffffffu, k0[b] == km && km != 0u);
+            const unsigned b1 = __ballot_sync(0xffffffffu, k1[b] == km && km != 0u);
+            const int row = b0 ? (__ffs(b0) - 1) : (b1 ? 32 + __ffs(b1) - 1 : -1);
+            if (row == lane) k0[b] = 0u;
+            if (row == lane + 32) k1[b] = 0u;
+            if (lane == 0 && oval[b] != nullptr) {
+                oval[b][r] = row >= 0 ? f32_from_order_key(km) : -INFINITY;
+                oidx[b][r] = row >= 0 ? base_row[b] + row : -1;
+            }
+        }
+    }
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 1)
+    coarse_tc8_kernel(const __grid_constant__ CUtensorMap tm_packed,
+                      const __grid_constant__ CUtensorMap tm_x, const Tc8Params prm)
+{
+    using C = Cfg8<MP>;
+    constexpr int N = C::N, T = C::T, kAs = C::kAs, kD = C::kD;
+    extern __shared__ uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NG = prm.H / 512, NGt = prm.H / kGroup;
+    const int nstage = prm.nstage;
+
+    // ---- shared memory ------------------------------------------------------------------
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    uint8_t *const stages = smem_raw + pad;                                   // nstage x kStage
+    float *const red = reinterpret_cast<float *>(stages + static_cast<size_t>(nstage) * C::kStage);
+    float *const xs_s = red + MP * kTileRows;                                 // [NGt][MP]
+    float *const inv_s = xs_s + NGt * MP;                                     // [MP]
+    uint64_t *const bars = reinterpret_cast<uint64_t *>(inv_s + MP);
+    uint64_t *const full = bars;              // [nstage] TMA -> dequant, MMA
+    uint64_t *const empty = full + nstage;    // [nstage] dequant (8 warps) + MMA -> TMA
+    uint64_t *const a_full = empty + nstage;  // [kAs]    dequant (8 warps) -> MMA, per span
+    uint64_t *const a_empty = a_full + kAs;   // [kAs]    MMA -> dequant, per span
+    uint64_t *const d_full = a_empty + kAs;   // [kD]     MMA -> epilogue, per group
+    uint64_t *const d_empty = d_full + kD;    // [kD]     epilogue -> MMA, per group
+    uint64_t *const fin = d_empty + kD;       // [1]      MMA drain before teardown
+    uint64_t *const red_full = fin + 1;       // [1]      epilogue -> selection: tile in `red`
+    uint64_t *const red_free = red_full + 1;  // [1]      selection -> epilogue: `red` free
+    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(red_free + 1);
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_packed);
+        prefetch_tensormap(&tm_x);
+        for (int i = 0; i < nstage; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 8 + 1);
+        }
+        for (int i = 0; i < kAs; ++i) {
+            mbar_init(&a_full[i], 8);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < kD; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], 4);
+        }
+        mbar_init(fin, 1);
+        mbar_init(red_full, 4);
+        mbar_init(red_free, 2);
+        fence_barrier_init();
+    }
+    for (int i = threadIdx.x; i < NGt * MP; i += blockDim.x) {
+        const int g = i / MP, m = i - g * MP;
+        xs_s[i] = prm.xs[static_cast<long long>(m) * NGt + g];
+    }
+    for (int i = threadIdx.x; i < MP; i += blockDim.x) inv_s[i] = prm.inv_scale[i];
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int first_tile = blockIdx.x, tile_step = gridDim.x;
+    bool failed = false;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            uint32_t s = 0;
+            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+                for (int span = 0; span < NG; ++span, ++s) {
+                    const uint32_t st = s % nstage;
+                    if (!mbar_wait_bounded(&empty[st], ((s / nstage) & 1u) ^ 1u, prm.timeout_flag)) {
+                        failed = true;
+                        break;
+                    }
+                    uint8_t *const stage = stages + static_cast<size_t>(st) * C::kStage;
+                    mbar_arrive_expect_tx(&full[st], C::kStage);
+                    tma_load_2d_hint(stage, &tm_packed, span * kSpanBytes, tile * kTileRows,
+                                     &full[st], policy);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tma_load_2d(stage + kPkBytes + q * (N * 128), &tm_x,
+                                    q * (prm.H / 4) + span * 128, 0, &full[st]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: one A handshake per span ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc_f8(N);
+            uint32_t s = 0, t = 0;
+            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+                for (int span = 0; span < NG && !failed; ++span, ++s) {
+                    const uint32_t st = s % nstage, sa = s % kAs;
+                    if (!mbar_wait_bounded(&full[st], (s / nstage) & 1u, prm.timeout_flag) ||
+                        !mbar_wait_bounded(&a_full[sa], (s / kAs) & 1u, prm.timeout_flag)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t xdesc =
+                        sw128_desc(smem_u32(stages + static_cast<size_t>(st) * C::kStage + kPkBytes));
+                    for (int q = 0; q < 4; ++q, ++t) {
+                        const uint32_t d = t % kD;
+                        if (!mbar_wait_bounded(&d_empty[d], ((t / kD) & 1u) ^ 1u, prm.timeout_flag)) {
+                            failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem + C::kDcol + d * N;
+                        const uint32_t a_tmem = tmem + C::kAcol + sa * 128 + q * 32;
+                        // the descriptor's address field counts 16-byte units
+                        const uint64_t qdesc = xdesc + static_cast<uint64_t>(q * (N * 128) / 16);
+                        mma_ts_f8(d_tmem, a_tmem, qdesc, idesc, 0u);
+#pragma unroll
+                        for (int i = 1; i < 4; ++i)
+                            mma_ts_f8(d_tmem, a_tmem + i * 8, qdesc + static_cast<uint64_t>(i * 2),
+                                      idesc, 1u);
+                        mma_commit(&d_full[d]);
+                    }
+                    if (failed) break;
+                    mma_commit(&a_empty[sa]);
+                    mma_commit(&empty[st]);
+                }
+            }
+            mma_commit(fin);
+            mbar_wait_bounded(fin, 0, prm.timeout_flag);
+        }
+    } else if (warp >= 4 && warp < 12) {
+        // ---------------- dequant: warps 4-7 planes 0-1, warps 8-11 planes 2-3 ----------------
+        const int row = ((warp & 3) << 5) | lane; // TMEM lane == tile row
+        const int q0 = (warp < 8) ? 0 : 2;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        uint32_t s = 0;
+        for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+            for (int span = 0; span < NG; ++span, ++s) {
+                const uint32_t st = s % nstage, sa = s % kAs;
+                if (!warp_wait(&full[st], (s / nstage) & 1u, prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
+                const uint32_t pk =
+                    smem_u32(stages + static_cast<size_t>(st) * C::kStage) + row * kSpanBytes;
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t addr = pk + ((c ^ (row & 7)) << 4);
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]),
+                                   "=r"(w[4 * c + 3])
+                                 : "r"(addr));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+                if (!warp_wait(&a_empty[sa], ((s / kAs) & 1u) ^ 1u, prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                if (q0 == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        r0[i] = deq4_e4m3<0>(w[i]);
+                        r1[i] = deq4_e4m3<1>(w[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        r0[i] = deq4_e4m3<2>(w[i]);
+                        r1[i] = deq4_e4m3<3>(w[i]);
+                    }
+                }
+                const uint32_t abuf = tmem + lane_base + C::kAcol + sa * 128 + q0 * 32;
+                tmem_st_x32(abuf, r0);
+                tmem_st_x32(abuf + 32, r1);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[sa]);
+            }
+        }
+    } else if (warp >= 12) {
+        // ---------------- epilogue: one wait per span, each slot released once read ----------
+        const int row = ((warp & 3) << 5) | lane;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        uint32_t t = 0, it = 0;
+        for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
+            const int grow = tile * kTileRows + row;
+            const bool row_ok = grow < prm.V;
+            const uint16_t *Srow = prm.S + static_cast<long long>(row_ok ? grow : 0) * NGt;
+            const uint16_t *Zrow = prm.ZS + static_cast<long long>(row_ok ? grow : 0) * NGt;
+            float acc[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m) acc[m] = 0.f;
+            for (int span = 0; span < NG; ++span, t += 4) {
+                float s2[4], sz[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int gi = q * NG + span;
+                    const float sv = row_ok ? bf16_bits_to_f32(__ldg(Srow + gi)) : 0.f;
+                    const float zv = row_ok ? bf16_bits_to_f32(__ldg(Zrow + gi)) : 0.f;
+                    s2[q] = 2.0f * sv;
+                    sz[q] = -(sv + zv);
+                }
+                // the span's MMAs complete in order: its last group done means all are
+                if (!warp_wait(&d_full[(t + 3) % kD], ((t + 3) / kD) & 1u, prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t d = (t + q) % kD;
+                    const float4 *xg = reinterpret_cast<const float4 *>(xs_s + (q * NG + span) * MP);
+#pragma unroll
+                    for (int c = 0; c < MP / 16; ++c) {
+                        float v[T][16];
+#pragma unroll
+                        for (int tt = 0; tt < T; ++tt)
+                            tmem_ld_x16(tmem + lane_base + C::kDcol + d * N + tt * MP + c * 16, v[tt]);
+                        tmem_wait_ld();
+                        if (c == MP / 16 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&d_empty[d]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 x4 = xg[c * 4 + j];
+                            const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float p = v[0][4 * j + i] + v[1][4 * j + i];
+                                const int m = c * 16 + 4 * j + i;
+                                acc[m] = fmaf(s2[q], p, fmaf(sz[q], xv[i], acc[m]));
+                            }
+                        }
+                    }
+                }
+            }
+            if (failed) break;
+            // the selection warps are done with the previous tile's values
+            if (!warp_wait(red_free, (it & 1u) ^ 1u, prm.timeout_flag)) {
+                failed = true;
+                break;
+            }
+#pragma unroll
+            for (int m = 0; m < MP; ++m) {
+                const float c = acc[m] * inv_s[m];
+                red[m * kTileRows + row] = row_ok ? c : -INFINITY;
+                if (prm.coarse && row_ok && m < prm.mrows)
+                    prm.coarse[static_cast<long long>(prm.m0 + m) * prm.V + grow] = c;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(red_full);
+        }
+    } else if (warp == 2 || warp == 3) {
+        // ---------------- block top-KCAND: pair = (batch column m, block b of the tile) ------
+        const int sw = warp - 2;
+        uint32_t it = 0;
+        for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
+            if (!warp_wait(red_full, it & 1u, prm.timeout_flag)) {
+                failed = true;
+                break;
+            }
+            for (int p0 = sw * 4; p0 < 2 * prm.mrows; p0 += 8) {
+                uint32_t k0[4], k1[4];
+                int base_row[4];
+                float *oval[4];
+                int32_t *oidx[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int pidx = p0 + b;
+                    const int m = pidx >> 1, blk = tile * 2 + (pidx & 1);
+                    const bool live = pidx < 2 * prm.mrows &&
+                                      static_cast<long long>(blk) * kBlockN < prm.V;
+                    const int r0 = (pidx & 1) * 64 + lane;
+                    const int g0 = tile * kTileRows + r0;
+                    k0[b] = (live && g0 < prm.V) ? f32_order_key(red[m * kTileRows + r0]) : 0u;
+                    k1[b] = (live && g0 + 32 < prm.V) ? f32_order_key(red[m * kTileRows + r0 + 32])
+                                                      : 0u;
+                    base_row[b] = tile * kTileRows + (pidx & 1) * 64;
+                    const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
+                                          static_cast<long long>(blk) * prm.kcand;
+                    oval[b] = live ? prm.cand_val + off : nullptr;
+                    oidx[b] = live ? prm.cand_idx + off : nullptr;
+                }
+                select_pairs<4>(k0, k1, base_row, oval, oidx, prm.kcand, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(red_free);
+        }
+    }
+
+    // ---- teardown: every role is done (or gave up); release tensor memory ----
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int MP>
+cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
+                       const Tc8Params &base, cudaStream_t stream)
+{
+    using C = Cfg8<MP>;
+    CUtensorMap tm_x;
+    CUresult r = encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                      const_cast<uint8_t *>(xt8_chunk), base.H, C::N, base.H,
+                                      128, C::N, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const int NGt = base.H / kGroup;
+    const size_t fixed = 1024 + static_cast<size_t>(MP) * kTileRows * 4 +
+                         static_cast<size_t>(NGt) * MP * 4 + MP * 4 + 64 * 8 + 32;
+    int nstage = static_cast<int>((kSmemLimit8 - static_cast<long long>(fixed)) / C::kStage);
+    if (nstage > 6) nstage = 6;
+    if (nstage < 2) return cudaErrorInvalidConfiguration;
+    const size_t smem = fixed + static_cast<size_t>(nstage) * C::kStage;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(coarse_tc8_kernel<MP>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemLimit8);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    Tc8Params prm = base;
+    prm.nstage = nstage;
+    const int grid = prm.ntiles < kNumSMs ? prm.ntiles : kNumSMs;
+    coarse_tc8_kernel<MP><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+Tc8Chunk tc8_chunk(int M, int c)
+{
+    Tc8Chunk k;
+    k.m0 = c * kTc8MaxRows;
+    k.rows = M - k.m0 < kTc8MaxRows ? M - k.m0 : kTc8MaxRows;
+    k.MP = ((k.rows + 15) / 16) * 16;
+    k.T = 2;
+    return k;
+}
+
+int tc8_chunks(int M)
+{
+    return (M + kTc8MaxRows - 1) / kTc8MaxRows;
+}
+
+cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream)
+{
+    CUtensorMap tm_packed;
+    CUresult r = encode_tensor_map_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                      const_cast<uint8_t *>(a.packed), a.H / 4, a.V, a.H / 4,
+                                      kSpanBytes, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    Tc8Params base;
+    base.S = a.S;
+    base.ZS = a.ZS;
+    base.V = a.V;
+    base.H = a.H;
+    base.kcand = a.kcand;
+    base.ntiles = (a.V + kTileRows - 1) / kTileRows;
+    base.ncand = static_cast<long long>((a.V + kBlockN - 1) / kBlockN) * a.kcand;
+    base.cand_val = a.cand_val;
+    base.cand_idx = a.cand_idx;
+    base.coarse = a.coarse;
+    base.timeout_flag = a.timeout_flag;
+    base.nstage = 2;
+    const int NGt = a.H / kGroup;
+    for (int c = 0; c < tc8_chunks(a.M); ++c) {
+        const Tc8Chunk k = tc8_chunk(a.M, c);
+        base.m0 = k.m0;
+        base.mrows = k.rows;
+        base.xs = w.xs + static_cast<size_t>(c) * kTc8MaxRows * NGt;
+        base.inv_scale = w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows;
+        const uint8_t *xt = w.xt8 + static_cast<size_t>(c) * w.chunk_bytes;
+        cudaError_t e;
+        if (k.MP == 16) e = launch_cfg<16>(tm_packed, xt, base, stream);
+        else e = launch_cfg<32>(tm_packed, xt, base, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+} // namespace dh

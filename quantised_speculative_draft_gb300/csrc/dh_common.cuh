@@ -86,29 +86,43 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// try_wait suspends the waiting thread (instead of spinning on the issue slots that working
+// warps need) until the phase completes or kSuspendHintNs elapses.
+constexpr uint32_t kSuspendHintNs = 1000000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
                  : "memory");
     return ok != 0;
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and sets *flag) if
-// it has not completed within kWaitTimeoutNs, or after kWaitMaxPolls polls whatever the
-// timer says; the caller must then stop its work.
-constexpr uint32_t kWaitMaxPolls = 1u << 26;
+// it has not completed within kWaitTimeoutNs of the global timer or kWaitTimeoutCycles of
+// the SM clock (two independent clocks, so the bound holds even if one of them stalls); the
+// caller must then stop its work.
+constexpr long long kWaitTimeoutCycles = 5000000000ll;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *flag)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
+    // the clocks are read only every 16 suspended polls: a wait that completes soon costs no
+    // timer reads
+    unsigned long long t0 = 0;
+    long long c0 = 0;
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+        if ((i & 15u) == 0) {
+            if (i == 16) {
+                t0 = globaltimer_ns();
+                c0 = clock64();
+            } else if (globaltimer_ns() - t0 > kWaitTimeoutNs || clock64() - c0 > kWaitTimeoutCycles) {
+                break;
+            }
+        }
     }
     atomicExch(flag, 1);
     return false;

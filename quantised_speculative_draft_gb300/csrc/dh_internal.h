@@ -19,6 +19,8 @@ constexpr int kWarpRowsPerWarp = 64;    // vocabulary rows per warp work item (o
 constexpr int kSelectChunk = 4096;      // candidates per CTA in one top-R selection pass
 constexpr int kMaxRerank = 1024;
 constexpr int kMaxM = 128;
+constexpr int kNumCounters = 256;   // [0, 64): work queues, [128, 256): per-row completion
+constexpr int kRowDoneOffset = 128;
 
 // ---- launchers (each returns the launch status) ------------------------------------------
 cudaError_t launch_quantize(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
@@ -50,6 +52,24 @@ struct CoarseArgs {
 cudaError_t launch_coarse_warp(const CoarseArgs &a, cudaStream_t stream);
 size_t warp_xw_elems(int M, int H); // bf16 elements of the warp-path operand
 
+// tcgen05 path with 8-bit operands: the batch is processed in launches of at most
+// kTc8MaxRows rows; launch c stages its rows as T e4m3 terms of MP (multiple of 16) rows.
+constexpr int kTc8MaxRows = 32;
+struct Tc8Chunk {
+    int m0, rows, MP, T;
+};
+Tc8Chunk tc8_chunk(int M, int c);
+int tc8_chunks(int M);
+struct Tc8Workspace {
+    uint8_t *xt8;       // per launch [T*MP, H] e4m3 terms, chunk_bytes apart
+    size_t chunk_bytes;
+    float *xs;          // per launch kTc8MaxRows x NGt scaled group sums of the represented x
+    float *inv_scale;   // per launch kTc8MaxRows entries 2^-e
+};
+cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
+                            int *counters, int ncounters, cudaStream_t stream);
+cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream);
+
 bool tc_supported(int M, int H);
 cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream);
 int tc_npad(int M);
@@ -62,11 +82,11 @@ cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M,
                           int R, float *scratch_val[2], int32_t *scratch_idx[2],
                           long long scratch_entries, int32_t *sel_idx, cudaStream_t stream);
 
-cudaError_t launch_rerank(const uint16_t *x, const uint16_t *W, int M, int H, int V,
-                          const int32_t *sel_idx, int R, float *ex, cudaStream_t stream);
-
-cudaError_t launch_topk(const float *ex, const int32_t *sel_idx, int M, int R, int topk,
-                        int32_t *out_idx, float *out_logit, cudaStream_t stream);
+// Exact rerank of the selected rows and, fused (last CTA per row), the per-row top-k.
+// row_done: M zeroed counters.
+cudaError_t launch_rerank_topk(const uint16_t *x, const uint16_t *W, int M, int H, int V,
+                               const int32_t *sel_idx, int R, float *ex, int *row_done, int topk,
+                               int32_t *out_idx, float *out_logit, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,

@@ -15,6 +15,9 @@
 #include "dh_common.cuh"
 #include "dh_internal.h"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 namespace dh {
 
 __device__ __forceinline__ uint4 permute_quads(uint4 v)
@@ -100,6 +103,114 @@ size_t warp_xw_elems(int M, int H)
     const int chunks = (M + kWarpBatch - 1) / kWarpBatch;
     // per chunk: NG spans x 4 planes x nt tiles x 2 KB (1024 bf16)
     return static_cast<size_t>(chunks) * (H / 512) * 4 * nt * 1024;
+}
+
+// ------------------------------------------------------------------------------------------
+// x staging for the 8-bit tcgen05 path.  Row m is scaled by 2^e (max |x 2^e| in [128, 256),
+// exact) and split into T e4m3 terms by successive round-to-nearest: x1 = e4m3(x 2^e),
+// x2 = e4m3(x 2^e - x1), x3 = e4m3(x 2^e - x1 - x2); every difference is exact in fp32.  A bf16
+// value (8 significant bits) is represented exactly by two terms unless it lies more than 10
+// binades below the row maximum; the third term shrinks that residual to below 2^-18 of the
+// maximum.  Term t of row m is row t*MP + m of the staged operand.  xs receives the group
+// sums of the represented values x1 + x2 + x3 (scaled units) and inv_scale the factor 2^-e.
+// One CTA per staged row.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float e4m3_to_f32(__nv_fp8_storage_t v)
+{
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(v, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+__global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restrict__ x, int H,
+                                                       int m0, int rows, int MP, int T,
+                                                       uint8_t *__restrict__ xt8,
+                                                       float *__restrict__ xs,
+                                                       float *__restrict__ inv_scale,
+                                                       int *__restrict__ counters, int ncounters)
+{
+    __shared__ float wmax[8];
+    const int m = blockIdx.x;
+    const bool valid = m < rows;
+    const int octs = H / 8, NGt = H / kGroup;
+    if (counters && m == 0)
+        for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
+    const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
+
+    float mx = 0.f;
+    if (valid)
+        for (int o = threadIdx.x; o < octs; o += blockDim.x) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
+                                     fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mx = fmaxf(mx, wmax[i]);
+    int e = 0;
+    if (mx > 0.f) {
+        int ex;
+        frexpf(mx, &ex); // mx = f 2^ex, f in [0.5, 1)
+        e = 8 - ex;      // mx 2^e in [128, 256)
+        e = e > 126 ? 126 : (e < -126 ? -126 : e);
+    }
+    const float scale = __int_as_float((e + 127) << 23);
+    if (threadIdx.x == 0) inv_scale[m] = valid ? __int_as_float((127 - e) << 23) : 1.0f;
+
+    for (int o = threadIdx.x; o < octs; o += blockDim.x) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (valid) v = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t lo[3] = {0, 0, 0}, hi[3] = {0, 0, 0};
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float xv = (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u)
+                                     : __uint_as_float(w[i >> 1] << 16);
+            float r = xv * scale; // exact: a power of two
+            float rep = 0.f;
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                if (t < T) {
+                    const __nv_fp8_storage_t b = __nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3);
+                    const float bf = e4m3_to_f32(b);
+                    r -= bf;
+                    rep += bf;
+                    if (i < 4) lo[t] |= static_cast<uint32_t>(b) << (8 * i);
+                    else hi[t] |= static_cast<uint32_t>(b) << (8 * (i - 4));
+                }
+            }
+            sum += rep;
+        }
+        for (int t = 0; t < T; ++t)
+            *reinterpret_cast<uint2 *>(xt8 + (static_cast<long long>(t) * MP + m) * H + 8 * o) =
+                make_uint2(lo[t], hi[t]);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if ((o & 15) == 0) xs[static_cast<long long>(m) * NGt + (o >> 4)] = sum;
+    }
+}
+
+cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
+                            int *counters, int ncounters, cudaStream_t stream)
+{
+    const int NGt = H / kGroup;
+    for (int c = 0; c < tc8_chunks(M); ++c) {
+        const Tc8Chunk k = tc8_chunk(M, c);
+        prep_fp8_kernel<<<k.MP, 256, 0, stream>>>(
+            x, H, k.m0, k.rows, k.MP, k.T, w.xt8 + static_cast<size_t>(c) * w.chunk_bytes,
+            w.xs + static_cast<size_t>(c) * kTc8MaxRows * NGt,
+            w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows, c == 0 ? counters : nullptr,
+            ncounters);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 } // namespace dh

@@ -164,76 +164,78 @@ __global__ void __launch_bounds__(kSelThreads) topr_kernel(const float *__restri
 }
 
 // ----------------------------------------------------------------------------------------
-// a6: exact rerank.  One warp per (m, j): fp32 products of bf16 values are exact; each lane
-// accumulates 160 of them (H = 5120) in four fp32 partials, the 32 x 4 partials are then
-// summed in fp64.
+// a6 + a7: exact rerank, then the top-k of the row.  One CTA of 128 threads per (row m,
+// candidate j): every thread takes H/1024 16-byte slices of x and of the candidate's bf16 row
+// (products of bf16 values are exact in fp32), sums them in two fp32 partials, and the CTA
+// combines the 256 partials in fp64.  The last CTA to finish a row (an atomic count per row,
+// zeroed by the staging kernel) sorts that row's R exact values and writes its top-k.
 // ----------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) rerank_kernel(const uint16_t *__restrict__ x,
-                                                     const uint16_t *__restrict__ W, int M, int H,
-                                                     int V, const int32_t *__restrict__ sel_idx,
-                                                     int R, float *__restrict__ ex)
+constexpr int kRerankThreads = 128;
+
+__global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
+    const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, int H, int V,
+    const int32_t *__restrict__ sel_idx, int R, float *__restrict__ ex,
+    int *__restrict__ row_done, int topk, int32_t *__restrict__ out_idx,
+    float *__restrict__ out_logit)
 {
-    const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= static_cast<long long>(M) * R) return;
-    const int m = static_cast<int>(gw / R);
-    const int n = sel_idx[gw];
-    if (n < 0 || n >= V) {
-        if (lane == 0) ex[gw] = -INFINITY;
-        return;
-    }
-    const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<long long>(m) * H);
-    const uint4 *wr = reinterpret_cast<const uint4 *>(W + static_cast<long long>(n) * H);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    for (int i = lane; i < H / 8; i += 32) {
-        const uint4 xv = __ldg(xr + i);
-        const uint4 wv = __ldg(wr + i);
-        const uint32_t xs4[4] = {xv.x, xv.y, xv.z, xv.w};
-        const uint32_t ws4[4] = {wv.x, wv.y, wv.z, wv.w};
+    __shared__ double part[kRerankThreads / 32];
+    __shared__ unsigned long long k[kMaxRerank];
+    __shared__ int s_last;
+    const long long pair = blockIdx.x;
+    const int m = static_cast<int>(pair / R);
+    const int n = sel_idx[pair];
+    const int tid = threadIdx.x, lane = tid & 31;
+
+    float a0 = 0.f, a1 = 0.f;
+    if (n >= 0 && n < V) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<long long>(m) * H);
+        const uint4 *wr = reinterpret_cast<const uint4 *>(W + static_cast<long long>(n) * H);
+        const int nv = H / 8;
+#pragma unroll 4
+        for (int i = tid; i < nv; i += kRerankThreads) {
+            const uint4 xv = __ldg(xr + i);
+            const uint4 wv = __ldg(wr + i);
+            const uint32_t xs4[4] = {xv.x, xv.y, xv.z, xv.w};
+            const uint32_t ws4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float xl = __uint_as_float(xs4[q] << 16), xh = __uint_as_float(xs4[q] & 0xFFFF0000u);
-            const float wl = __uint_as_float(ws4[q] << 16), wh = __uint_as_float(ws4[q] & 0xFFFF0000u);
-            if (q & 1) {
-                a2 = fmaf(xl, wl, a2);
-                a3 = fmaf(xh, wh, a3);
-            } else {
-                a0 = fmaf(xl, wl, a0);
-                a1 = fmaf(xh, wh, a1);
+            for (int q = 0; q < 4; ++q) {
+                a0 = fmaf(__uint_as_float(xs4[q] << 16), __uint_as_float(ws4[q] << 16), a0);
+                a1 = fmaf(__uint_as_float(xs4[q] & 0xFFFF0000u),
+                          __uint_as_float(ws4[q] & 0xFFFF0000u), a1);
             }
         }
     }
-    double d = (static_cast<double>(a0) + static_cast<double>(a1)) +
-               (static_cast<double>(a2) + static_cast<double>(a3));
+    double d = static_cast<double>(a0) + static_cast<double>(a1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (lane == 0) ex[gw] = static_cast<float>(d);
-}
+    if (lane == 0) part[tid >> 5] = d;
+    __syncthreads();
+    if (tid == 0) {
+        double t = 0.0;
+        for (int i = 0; i < kRerankThreads / 32; ++i) t += part[i];
+        ex[pair] = (n >= 0 && n < V) ? static_cast<float>(t) : -INFINITY;
+        __threadfence();
+        s_last = atomicAdd(&row_done[m], 1) == R - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
 
-// ----------------------------------------------------------------------------------------
-// a7: top-k of the R reranked entries of a row: bitonic sort of the rank keys (descending).
-// ----------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ ex,
-                                                   const int32_t *__restrict__ sel_idx, int R,
-                                                   int topk, int32_t *__restrict__ out_idx,
-                                                   float *__restrict__ out_logit)
-{
-    __shared__ unsigned long long k[kMaxRerank];
-    const int m = blockIdx.x;
+    // this CTA finished row m last: top-k of its R reranked entries (bitonic, descending)
     int n2 = 1;
     while (n2 < R) n2 <<= 1;
-    for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    for (int i = tid; i < n2; i += kRerankThreads) {
         unsigned long long key = 0;
         if (i < R) {
-            const int id = sel_idx[static_cast<long long>(m) * R + i];
-            if (id >= 0) key = rank_key(ex[static_cast<long long>(m) * R + i], id);
+            const int id = __ldcg(sel_idx + static_cast<long long>(m) * R + i);
+            if (id >= 0 && id < V) key = rank_key(__ldcg(ex + static_cast<long long>(m) * R + i), id);
         }
         k[i] = key;
     }
     __syncthreads();
     for (int size = 2; size <= n2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+            for (int i = tid; i < n2; i += kRerankThreads) {
                 const int j = i ^ stride;
                 if (j > i) {
                     const bool desc = (i & size) == 0;
@@ -247,10 +249,11 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ ex,
             __syncthreads();
         }
     }
-    for (int t = threadIdx.x; t < topk; t += blockDim.x) {
+    for (int t = tid; t < topk; t += kRerankThreads) {
         const unsigned long long key = k[t];
         const bool ok = key != 0;
-        out_idx[static_cast<long long>(m) * topk + t] = ok ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
+        out_idx[static_cast<long long>(m) * topk + t] =
+            ok ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
         out_logit[static_cast<long long>(m) * topk + t] =
             ok ? f32_from_order_key(static_cast<uint32_t>(key >> 32)) : -INFINITY;
     }
@@ -304,19 +307,13 @@ cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M,
     }
 }
 
-cudaError_t launch_rerank(const uint16_t *x, const uint16_t *W, int M, int H, int V,
-                          const int32_t *sel_idx, int R, float *ex, cudaStream_t stream)
+cudaError_t launch_rerank_topk(const uint16_t *x, const uint16_t *W, int M, int H, int V,
+                               const int32_t *sel_idx, int R, float *ex, int *row_done, int topk,
+                               int32_t *out_idx, float *out_logit, cudaStream_t stream)
 {
-    const long long warps = static_cast<long long>(M) * R;
-    const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
-    rerank_kernel<<<blocks, 256, 0, stream>>>(x, W, M, H, V, sel_idx, R, ex);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_topk(const float *ex, const int32_t *sel_idx, int M, int R, int topk,
-                        int32_t *out_idx, float *out_logit, cudaStream_t stream)
-{
-    topk_kernel<<<M, 256, 0, stream>>>(ex, sel_idx, R, topk, out_idx, out_logit);
+    const unsigned blocks = static_cast<unsigned>(static_cast<long long>(M) * R);
+    rerank_topk_kernel<<<blocks, kRerankThreads, 0, stream>>>(x, W, H, V, sel_idx, R, ex,
+                                                              row_done, topk, out_idx, out_logit);
     return cudaGetLastError();
 }
 

@@ -30,14 +30,15 @@ def _inputs(M, H, V, seed=0, **kw):
 def _paths():
     """The coarse paths this build can run: the warp path always, tcgen05 where supported."""
     out = [dh.PATH_WARP]
-    prev = dh.dh_set_coarse_path(dh.PATH_TC)
-    try:
-        if dh.dh_coarse_path_for(16) == dh.PATH_TC:
-            out.append(dh.PATH_TC)
-    except dh.DHError:
-        pass
-    finally:
-        dh.dh_set_coarse_path(prev)
+    for path in (dh.PATH_TC, dh.PATH_TC_BF16):
+        prev = dh.dh_set_coarse_path(path)
+        try:
+            if dh.dh_coarse_path_for(16) == path:
+                out.append(path)
+        except dh.DHError:
+            pass
+        finally:
+            dh.dh_set_coarse_path(prev)
     return out
 
 
