@@ -23,8 +23,10 @@
 // Roles (16 warps, one CTA per SM, persistent over 128-row vocabulary tiles):
 //   warp 0       TMA: per span one [128 rows x 128 B] box of packed bytes and four
 //                [128 k x N] boxes of the staged x terms (128-byte swizzle) into a stage ring
-//   warp 1       MMA issuer: per group 4 x tcgen05.mma kind::f8f6f4, M = 128, K = 32
-//   warps 2-3    block top-KCAND of the previous tile (overlaps the current tile)
+//   warp 1       MMA issuer: per group 4 x tcgen05.mma kind::f8f6f4, M = 128, K = 32; one
+//                commit per span and consumer (a commit costs an issue slot like an MMA)
+//   warps 2-3    block top-KCAND of the previous tile (overlaps the current tile): one lane
+//                per (batch column, block) pair keeps an insertion list of the best 8
 //   warps 4-7,   dequant: one TMEM lane (= one vocabulary row) per thread; warps 4-7 write
 //   warps 8-11   planes 0-1, warps 8-11 planes 2-3 of every span (two tcgen05.st of 32
 //                columns, one wait) into a ring of A buffers
@@ -47,6 +49,9 @@ constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
 constexpr int kPkBytes = kTileRows * kSpanBytes; // 16 KB packed box per span
 constexpr int kSmemLimit8 = 232448;
+// The tile's coarse values for the selection warps: one 64-value block per (batch column,
+// block) pair, pairs kRedPitch floats apart (16-byte aligned, bank-conflict free per lane).
+constexpr int kRedPitch = 68;
 
 // Batch rows per launch MP in {16, 32}; x in T = 2 e4m3 terms; MMA N = T * MP.
 // Tensor memory: two span-sized A buffers (4 groups x 32 columns) and a ring of kD group-sized
@@ -56,6 +61,10 @@ template <int MP> struct Cfg8 {
     static constexpr int N = MP * T;
     static constexpr int kAs = 2;                           // A buffers, one span each
     static constexpr int kD = (kTmemCols - kAs * 128) / N;  // 8 at N = 32, 4 at N = 64
+    static constexpr int kDS = kD / 4;                      // span-sized accumulator sets
+    // when there are at least as many accumulator sets as A buffers, "span s accumulated"
+    // also means "A buffer of span s free": one commit serves both
+    static constexpr bool kAFromD = kDS >= kAs;
     static constexpr uint32_t kAcol = 0;
     static constexpr uint32_t kDcol = kAs * 128;
     static constexpr uint32_t kXBytes = N * 512;            // 4 planes x 128 k x N rows
@@ -116,13 +125,57 @@ __device__ __forceinline__ void select_pairs(uint32_t (&k0)[NB], uint32_t (&k1)[
     }
 }
 
+// Block top-KCAND for KCAND <= 8, one lane per (batch column, block) pair: the lane walks the
+// block's 64 values in row order and keeps the 8 best in a descending list.  A value enters
+// only where it is strictly greater, so equal values keep the lower row first; rows past the
+// head hold -inf and never enter, leaving (-inf, -1) in unfilled slots.
+__device__ __forceinline__ void select_lane8(const float *vals, int base_row, int kcand,
+                                             float *oval, int32_t *oidx)
+{
+    float v[8];
+    int r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        v[k] = -INFINITY;
+        r[k] = -1;
+    }
+#pragma unroll 2
+    for (int j4 = 0; j4 < kBlockN / 4; ++j4) {
+        const float4 u = reinterpret_cast<const float4 *>(vals)[j4];
+        const float uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float xv = uu[e];
+            const int row = base_row + 4 * j4 + e;
+            bool c[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) c[k] = xv > v[k];
+            // the list is descending, so c is false up to the insertion point, true after it
+#pragma unroll
+            for (int k = 7; k > 0; --k) {
+                v[k] = c[k] ? (c[k - 1] ? v[k - 1] : xv) : v[k];
+                r[k] = c[k] ? (c[k - 1] ? r[k - 1] : row) : r[k];
+            }
+            v[0] = c[0] ? xv : v[0];
+            r[0] = c[0] ? row : r[0];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < kcand) {
+            oval[k] = v[k];
+            oidx[k] = r[k];
+        }
+}
+
 template <int MP>
 __global__ void __launch_bounds__(kThreads, 1)
     coarse_tc8_kernel(const __grid_constant__ CUtensorMap tm_packed,
                       const __grid_constant__ CUtensorMap tm_x, const Tc8Params prm)
 {
     using C = Cfg8<MP>;
-    constexpr int N = C::N, T = C::T, kAs = C::kAs, kD = C::kD;
+    constexpr int N = C::N, T = C::T, kAs = C::kAs, kD = C::kD, kDS = C::kDS;
+    constexpr bool kAFromD = C::kAFromD;
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = prm.H / 512, NGt = prm.H / kGroup;
@@ -133,15 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t *const stages = smem_raw + pad;                                   // nstage x kStage
     float *const red = reinterpret_cast<float *>(stages + static_cast<size_t>(nstage) * C::kStage);
-    float *const xs_s = red + MP * kTileRows;                                 // [NGt][MP]
+    float *const xs_s = red + MP * 2 * kRedPitch;                             // [NGt][MP]
     float *const inv_s = xs_s + NGt * MP;                                     // [MP]
     uint64_t *const bars = reinterpret_cast<uint64_t *>(inv_s + MP);
     uint64_t *const full = bars;              // [nstage] TMA -> dequant, MMA
     uint64_t *const empty = full + nstage;    // [nstage] dequant (8 warps) + MMA -> TMA
     uint64_t *const a_full = empty + nstage;  // [kAs]    dequant (8 warps) -> MMA, per span
-    uint64_t *const a_empty = a_full + kAs;   // [kAs]    MMA -> dequant, per span
-    uint64_t *const d_full = a_empty + kAs;   // [kD]     MMA -> epilogue, per group
-    uint64_t *const d_empty = d_full + kD;    // [kD]     epilogue -> MMA, per group
+    uint64_t *const a_empty = a_full + kAs;   // [kAs]    MMA -> dequant (unless kAFromD)
+    uint64_t *const d_full = a_empty + kAs;   // [kDS]    MMA -> epilogue (+ dequant), per span
+    uint64_t *const d_empty = d_full + kDS;   // [kD]     epilogue -> MMA, per group
     uint64_t *const fin = d_empty + kD;       // [1]      MMA drain before teardown
     uint64_t *const red_full = fin + 1;       // [1]      epilogue -> selection: tile in `red`
     uint64_t *const red_free = red_full + 1;  // [1]      selection -> epilogue: `red` free
@@ -158,10 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&a_full[i], 8);
             mbar_init(&a_empty[i], 1);
         }
-        for (int i = 0; i < kD; ++i) {
-            mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], 4);
-        }
+        for (int i = 0; i < kDS; ++i) mbar_init(&d_full[i], 1);
+        for (int i = 0; i < kD; ++i) mbar_init(&d_empty[i], 4);
         mbar_init(fin, 1);
         mbar_init(red_full, 4);
         mbar_init(red_free, 2);
@@ -236,10 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 1; i < 4; ++i)
                             mma_ts_f8(d_tmem, a_tmem + i * 8, qdesc + static_cast<uint64_t>(i * 2),
                                       idesc, 1u);
-                        mma_commit(&d_full[d]);
                     }
                     if (failed) break;
-                    mma_commit(&a_empty[sa]);
+                    // a commit takes an issue slot like an MMA: one per consumer per span
+                    mma_commit(&d_full[s % kDS]);
+                    if (!kAFromD) mma_commit(&a_empty[sa]);
                     mma_commit(&empty[st]);
                 }
             }
@@ -272,7 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
-                if (!warp_wait(&a_empty[sa], ((s / kAs) & 1u) ^ 1u, prm.timeout_flag)) {
+                // A buffer sa is free once the MMAs of span s - kAs completed
+                const bool a_free =
+                    kAFromD ? (s < static_cast<uint32_t>(kAs) ||
+                               warp_wait(&d_full[(s - kAs) % kDS], ((s - kAs) / kDS) & 1u,
+                                         prm.timeout_flag))
+                            : warp_wait(&a_empty[sa], ((s / kAs) & 1u) ^ 1u, prm.timeout_flag);
+                if (!a_free) {
                     failed = true;
                     break;
                 }
@@ -323,8 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s2[q] = 2.0f * sv;
                     sz[q] = -(sv + zv);
                 }
-                // the span's MMAs complete in order: its last group done means all are
-                if (!warp_wait(&d_full[(t + 3) % kD], ((t + 3) / kD) & 1u, prm.timeout_flag)) {
+                // one commit per span: all four groups' partials are in tensor memory
+                const uint32_t sp = t / 4;
+                if (!warp_wait(&d_full[sp % kDS], (sp / kDS) & 1u, prm.timeout_flag)) {
                     failed = true;
                     break;
                 }
@@ -368,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int m = 0; m < MP; ++m) {
                 const float c = acc[m] * inv_s[m];
-                red[m * kTileRows + row] = row_ok ? c : -INFINITY;
+                red[(2 * m + (row >> 6)) * kRedPitch + (row & 63)] = row_ok ? c : -INFINITY;
                 if (prm.coarse && row_ok && m < prm.mrows)
                     prm.coarse[static_cast<long long>(prm.m0 + m) * prm.V + grow] = c;
             }
@@ -378,35 +437,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 2 || warp == 3) {
         // ---------------- block top-KCAND: pair = (batch column m, block b of the tile) ------
         const int sw = warp - 2;
+        const int npairs = 2 * prm.mrows;
+        const int share = (npairs + 1) / 2; // pairs per selection warp (<= 32)
         uint32_t it = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
             if (!warp_wait(red_full, it & 1u, prm.timeout_flag)) {
                 failed = true;
                 break;
             }
-            for (int p0 = sw * 4; p0 < 2 * prm.mrows; p0 += 8) {
-                uint32_t k0[4], k1[4];
-                int base_row[4];
-                float *oval[4];
-                int32_t *oidx[4];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int pidx = p0 + b;
+            if (prm.kcand <= 8) {
+                // one lane per pair
+                const int pidx = sw * share + lane;
+                if (lane < share && pidx < npairs) {
                     const int m = pidx >> 1, blk = tile * 2 + (pidx & 1);
-                    const bool live = pidx < 2 * prm.mrows &&
-                                      static_cast<long long>(blk) * kBlockN < prm.V;
-                    const int r0 = (pidx & 1) * 64 + lane;
-                    const int g0 = tile * kTileRows + r0;
-                    k0[b] = (live && g0 < prm.V) ? f32_order_key(red[m * kTileRows + r0]) : 0u;
-                    k1[b] = (live && g0 + 32 < prm.V) ? f32_order_key(red[m * kTileRows + r0 + 32])
-                                                      : 0u;
-                    base_row[b] = tile * kTileRows + (pidx & 1) * 64;
-                    const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
-                                          static_cast<long long>(blk) * prm.kcand;
-                    oval[b] = live ? prm.cand_val + off : nullptr;
-                    oidx[b] = live ? prm.cand_idx + off : nullptr;
+                    if (static_cast<long long>(blk) * kBlockN < prm.V) {
+                        const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
+                                              static_cast<long long>(blk) * prm.kcand;
+                        select_lane8(red + pidx * kRedPitch, blk * kBlockN, prm.kcand,
+                                     prm.cand_val + off, prm.cand_idx + off);
+                    }
                 }
-                select_pairs<4>(k0, k1, base_row, oval, oidx, prm.kcand, lane);
+            } else {
+                // larger KCAND: four pairs per warp at a time, one warp-wide round per entry
+                for (int p0 = sw * 4; p0 < npairs; p0 += 8) {
+                    uint32_t k0[4], k1[4];
+                    int base_row[4];
+                    float *oval[4];
+                    int32_t *oidx[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int pidx = p0 + b;
+                        const int m = pidx >> 1, blk = tile * 2 + (pidx & 1);
+                        const bool live = pidx < npairs &&
+                                          static_cast<long long>(blk) * kBlockN < prm.V;
+                        const int g0 = blk * kBlockN + lane;
+                        const float *pv = red + (live ? pidx : 0) * kRedPitch;
+                        k0[b] = (live && g0 < prm.V) ? f32_order_key(pv[lane]) : 0u;
+                        k1[b] = (live && g0 + 32 < prm.V) ? f32_order_key(pv[lane + 32]) : 0u;
+                        base_row[b] = blk * kBlockN;
+                        const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
+                                              static_cast<long long>(blk) * prm.kcand;
+                        oval[b] = live ? prm.cand_val + off : nullptr;
+                        oidx[b] = live ? prm.cand_idx + off : nullptr;
+                    }
+                    select_pairs<4>(k0, k1, base_row, oval, oidx, prm.kcand, lane);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(red_free);
@@ -431,7 +506,7 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
                                       128, C::N, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     const int NGt = base.H / kGroup;
-    const size_t fixed = 1024 + static_cast<size_t>(MP) * kTileRows * 4 +
+    const size_t fixed = 1024 + static_cast<size_t>(MP) * 2 * kRedPitch * 4 +
                          static_cast<size_t>(NGt) * MP * 4 + MP * 4 + 64 * 8 + 32;
     int nstage = static_cast<int>((kSmemLimit8 - static_cast<long long>(fixed)) / C::kStage);
     if (nstage > 6) nstage = 6;
