@@ -8,24 +8,29 @@
 // per instruction below N = 64 whatever the operand type, and an 8-bit instruction covers
 // twice the K of a bf16 one, so this kernel feeds the same collapsed form through 8-bit
 // operands:
-//   * weight: the e4m3 value 1 + v/8 is the bit pattern 0x38 | v, so one and-or (plus one
-//     shift for planes 1-3) turns a 32-bit word of packed bytes into four e4m3 weights of one
-//     plane -- in k order, no permutation;
+//   * weight: the e4m3 byte patterns 0..15 are exactly p 2^-9, so the 2-bit code of a plane
+//     masked in place is an exact e4m3 weight: v 2^-9 for planes 0 and 2 (mask 0x03), 4 v 2^-9
+//     for planes 1 and 3 (mask 0x0C), planes 2-3 after a 4-bit shift.  One AND (plus one
+//     shift) turns a 32-bit word of packed bytes into four weights of one plane, in k order;
 //   * x: every row is scaled by a power of two 2^e (max |x 2^e| in [128, 256)) and split
 //     exactly into T e4m3 terms, x 2^e = x1 + x2 (+ x3); the terms are stacked along the MMA's
 //     N dimension (rows t*MP + m), which costs nothing below N = 64;
-//   * per group g (128 consecutive k of one plane), with p = sum over the T terms of the
-//     partial D, sum_k x_k (1 + v/4) = 2 p - xs, so
-//         c[m, n] = 2^-e * sum_g ( 2 S[n,g] p - (S[n,g] + ZS[n,g]) xs'[m,g] )
+//   * per group g (128 consecutive k of one plane q), with p = sum over the T terms of the
+//     partial D, sum_k x_k v_k = 2^9 p / f (f = 1 for even q, 4 for odd q), and the page's
+//     group term S sum_k x_k (1 + v_k/4) - ZS xs = (S/4) sum_k x_k v_k + (S - ZS) xs, so
+//         c[m, n] = 2^-e * sum_g ( (2^7/f) S[n,g] p + (S[n,g] - ZS[n,g]) xs'[m,g] )
 //     with xs' the group sums of the represented x (in the scaled units): the scale and zero
 //     are applied to the fp32 partial of every group, never to the weight.
 //
 // Roles (16 warps, one CTA per SM, persistent over 128-row vocabulary tiles):
 //   warp 0       TMA: per span one [128 rows x 128 B] box of packed bytes and four
 //                [128 k x N] boxes of the staged x terms (128-byte swizzle) into a stage ring
-//   warp 1       MMA issuer: per group 4 x tcgen05.mma kind::f8f6f4, M = 128, K = 32; one
-//                commit per span and consumer (a commit costs an issue slot like an MMA)
-//   warps 2-3    block top-KCAND of the previous tile (overlaps the current tile): one lane
+//   warps 1, 3   MMA issuers: per group 4 x tcgen05.mma kind::f8f6f4, M = 128, K = 32; one
+//                commit per span and consumer (a commit costs an issue slot like an MMA).
+//                With two accumulator sets (N = 32) they take alternate spans, each with its
+//                own A buffer and accumulators, so one's waits overlap the other's MMAs;
+//                with one set (N = 64) warp 1 issues every span
+//   warp 2       block top-KCAND of the previous tile (overlaps the current tile): one lane
 //                per (batch column, block) pair keeps an insertion list of the best 8
 //   warps 4-7,   dequant: one TMEM lane (= one vocabulary row) per thread; warps 4-7 write
 //   warps 8-11   planes 0-1, warps 8-11 planes 2-3 of every span (two tcgen05.st of 32
@@ -93,11 +98,12 @@ __host__ __device__ constexpr uint32_t make_idesc_f8(int N)
            (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
-// e4m3 weights 1 + v/8 of plane P from a word of four packed bytes (four consecutive k)
+// e4m3 weights of plane P from a word of four packed bytes (four consecutive k): the codes
+// masked in place, v 2^-9 (even P) or 4 v 2^-9 (odd P), exact e4m3 values
 template <int P>
 __device__ __forceinline__ uint32_t deq4_e4m3(uint32_t w)
 {
-    return ((w >> (2 * P)) & 0x03030303u) | 0x38383838u;
+    return (P >= 2 ? (w >> 4) : w) & ((P & 1) ? 0x0C0C0C0Cu : 0x03030303u);
 }
 
 // Block top-KCAND of up to 4 (batch column, block) pairs at once.  Lane l holds rows l and
@@ -213,9 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kDS; ++i) mbar_init(&d_full[i], 1);
         for (int i = 0; i < kD; ++i) mbar_init(&d_empty[i], 4);
-        mbar_init(fin, 1);
+        mbar_init(fin, 2);
         mbar_init(red_full, 4);
-        mbar_init(red_free, 2);
+        mbar_init(red_free, 1);
         fence_barrier_init();
     }
     for (int i = threadIdx.x; i < NGt * MP; i += blockDim.x) {
@@ -255,14 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer: one A handshake per span ----------------
+    } else if (warp == 1 || warp == 3) {
+        // ---------------- MMA issuers: one A handshake per span ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc_f8(N);
+            constexpr bool kTwo = kDS >= 2 && kAs == 2;
+            const uint32_t who = warp == 1 ? 0u : 1u;
             uint32_t s = 0, t = 0;
             for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
                 for (int span = 0; span < NG && !failed; ++span, ++s) {
                     const uint32_t st = s % nstage, sa = s % kAs;
+                    if (kTwo ? ((s & 1u) != who) : (who != 0u)) { // the other issuer's span
+                        t += 4;
+                        continue;
+                    }
                     if (!mbar_wait_bounded(&full[st], (s / nstage) & 1u, prm.timeout_flag) ||
                         !mbar_wait_bounded(&a_full[sa], (s / kAs) & 1u, prm.timeout_flag)) {
                         failed = true;
@@ -359,15 +371,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp >= 12) {
-        // ---------------- epilogue: one wait per span, each slot released once read ----------
+        // ---------------- epilogue: one wait per span, slots released as they are read -------
         const int row = ((warp & 3) << 5) | lane;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        constexpr int GPW = (MP == 16) ? 2 : 1; // groups per tcgen05.wait::ld
+        // S and ZS of the next span to fold, loaded one span ahead so that their latency
+        // overlaps the current span (rows past the head read as 0)
+        uint16_t s_next[4], z_next[4];
+        auto fetch = [&](int tl, int sp_) {
+            const int gr = tl * kTileRows + row;
+            const bool ok = tl < prm.ntiles && gr < prm.V;
+            const long long base = static_cast<long long>(ok ? gr : 0) * NGt + sp_;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                s_next[q] = ok ? __ldg(prm.S + base + q * NG) : static_cast<uint16_t>(0);
+                z_next[q] = ok ? __ldg(prm.ZS + base + q * NG) : static_cast<uint16_t>(0);
+            }
+        };
+        fetch(first_tile, 0);
         uint32_t t = 0, it = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
             const int grow = tile * kTileRows + row;
             const bool row_ok = grow < prm.V;
-            const uint16_t *Srow = prm.S + static_cast<long long>(row_ok ? grow : 0) * NGt;
-            const uint16_t *Zrow = prm.ZS + static_cast<long long>(row_ok ? grow : 0) * NGt;
             float acc[MP];
 #pragma unroll
             for (int m = 0; m < MP; ++m) acc[m] = 0.f;
@@ -375,12 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s2[4], sz[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int gi = q * NG + span;
-                    const float sv = row_ok ? bf16_bits_to_f32(__ldg(Srow + gi)) : 0.f;
-                    const float zv = row_ok ? bf16_bits_to_f32(__ldg(Zrow + gi)) : 0.f;
-                    s2[q] = 2.0f * sv;
-                    sz[q] = -(sv + zv);
+                    const float sv = bf16_bits_to_f32(s_next[q]);
+                    const float zv = bf16_bits_to_f32(z_next[q]);
+                    s2[q] = ((q & 1) ? 32.0f : 128.0f) * sv;
+                    sz[q] = sv - zv;
                 }
+                if (span + 1 < NG) fetch(tile, span + 1);
+                else fetch(tile + tile_step, 0);
                 // one commit per span: all four groups' partials are in tensor memory
                 const uint32_t sp = t / 4;
                 if (!warp_wait(&d_full[sp % kDS], (sp / kDS) & 1u, prm.timeout_flag)) {
@@ -389,30 +415,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t d = (t + q) % kD;
-                    const float4 *xg = reinterpret_cast<const float4 *>(xs_s + (q * NG + span) * MP);
+                for (int q0 = 0; q0 < 4; q0 += GPW) {
 #pragma unroll
                     for (int c = 0; c < MP / 16; ++c) {
-                        float v[T][16];
+                        float v[GPW][T][16];
 #pragma unroll
-                        for (int tt = 0; tt < T; ++tt)
-                            tmem_ld_x16(tmem + lane_base + C::kDcol + d * N + tt * MP + c * 16, v[tt]);
+                        for (int g = 0; g < GPW; ++g)
+#pragma unroll
+                            for (int tt = 0; tt < T; ++tt)
+                                tmem_ld_x16(tmem + lane_base + C::kDcol + ((t + q0 + g) % kD) * N +
+                                                tt * MP + c * 16,
+                                            v[g][tt]);
                         tmem_wait_ld();
                         if (c == MP / 16 - 1) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&d_empty[d]);
+                            if (lane == 0)
+#pragma unroll
+                                for (int g = 0; g < GPW; ++g) mbar_arrive(&d_empty[(t + q0 + g) % kD]);
                         }
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 x4 = xg[c * 4 + j];
-                            const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+                        for (int g = 0; g < GPW; ++g) {
+                            const int q = q0 + g;
+                            const float4 *xg =
+                                reinterpret_cast<const float4 *>(xs_s + (q * NG + span) * MP);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float p = v[0][4 * j + i] + v[1][4 * j + i];
-                                const int m = c * 16 + 4 * j + i;
-                                acc[m] = fmaf(s2[q], p, fmaf(sz[q], xv[i], acc[m]));
+                            for (int j = 0; j < 4; ++j) {
+                                const float4 x4 = xg[c * 4 + j];
+                                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float p = v[g][0][4 * j + i] + v[g][1][4 * j + i];
+                                    const int m = c * 16 + 4 * j + i;
+                                    acc[m] = fmaf(s2[q], p, fmaf(sz[q], xv[i], acc[m]));
+                                }
                             }
                         }
                     }
@@ -434,11 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(red_full);
         }
-    } else if (warp == 2 || warp == 3) {
+    } else if (warp == 2) {
         // ---------------- block top-KCAND: pair = (batch column m, block b of the tile) ------
-        const int sw = warp - 2;
         const int npairs = 2 * prm.mrows;
-        const int share = (npairs + 1) / 2; // pairs per selection warp (<= 32)
         uint32_t it = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
             if (!warp_wait(red_full, it & 1u, prm.timeout_flag)) {
@@ -447,8 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (prm.kcand <= 8) {
                 // one lane per pair
-                const int pidx = sw * share + lane;
-                if (lane < share && pidx < npairs) {
+                for (int pidx = lane; pidx < npairs; pidx += 32) {
                     const int m = pidx >> 1, blk = tile * 2 + (pidx & 1);
                     if (static_cast<long long>(blk) * kBlockN < prm.V) {
                         const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
@@ -459,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // larger KCAND: four pairs per warp at a time, one warp-wide round per entry
-                for (int p0 = sw * 4; p0 < npairs; p0 += 8) {
+                for (int p0 = 0; p0 < npairs; p0 += 4) {
                     uint32_t k0[4], k1[4];
                     int base_row[4];
                     float *oval[4];

@@ -86,17 +86,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// try_wait suspends the waiting thread (instead of spinning on the issue slots that working
-// warps need) until the phase completes or kSuspendHintNs elapses.
-constexpr uint32_t kSuspendHintNs = 1000000;
+// One bounded-latency probe of the phase: try_wait may park the thread for a short,
+// system-chosen time while the phase is incomplete (no explicit suspend-time hint: a long hint
+// delayed wake-ups on the handoffs of the pipelined kernels).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+                 : "r"(smem_u32(bar)), "r"(parity)
                  : "memory");
     return ok != 0;
 }
