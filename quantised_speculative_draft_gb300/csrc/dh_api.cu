@@ -149,10 +149,11 @@ int choose_path(int M, int H)
         std::lock_guard<std::mutex> lk(g_path_mu);
         p = g_path;
     }
-    if (p == DH_PATH_TC || p == DH_PATH_TC_BF16) return tc_supported(M, H) ? p : -1;
+    if (p == DH_PATH_TC) return tc8_supported(M, H) ? p : -1;
+    if (p == DH_PATH_TC_BF16) return tc_supported(M, H) ? p : -1;
     if (p == DH_PATH_WARP) return DH_PATH_WARP;
     // automatic: the 8-bit tcgen05 path where it is available, else the warp path
-    if (tc_supported(M, H)) return DH_PATH_TC;
+    if (tc8_supported(M, H)) return DH_PATH_TC;
     return DH_PATH_WARP;
 }
 

@@ -32,12 +32,14 @@
 //                with one set (N = 64) warp 1 issues every span
 //   warp 2       block top-KCAND of the previous tile (overlaps the current tile): one lane
 //                per (batch column, block) pair keeps an insertion list of the best 8
-//   warps 4-7,   dequant: one TMEM lane (= one vocabulary row) per thread; warps 4-7 write
-//   warps 8-11   planes 0-1, warps 8-11 planes 2-3 of every span (two tcgen05.st of 32
-//                columns, one wait) into a ring of A buffers
-//   warps 12-15  epilogue: tcgen05.ld of the partials (two groups per wait when they fit in
-//                registers), sum of the T terms, scale/zero fold into fp32 registers, and at
-//                the tile end the coarse values into the shared tile buffer
+//   warps 4-7    dequant: one TMEM lane (= one vocabulary row) per thread, all four planes of
+//                every span (four tcgen05.st of 32 columns, one wait) into a ring of A buffers
+//   warp 0 also  bulk-copies each tile's S and ZS rows (contiguous in memory) into a
+//                double-buffered shared copy for the epilogue
+//   warps 8-15   epilogue, two halves of four warps (one per TMEM lane quarter): half h folds
+//                groups 2h and 2h+1 of every span -- tcgen05.ld of the partials, sum of the T
+//                terms, scale/zero fold into fp32 registers -- and at the tile end writes its
+//                half of the coarse values; the selection warp adds the halves
 // Every handoff is an mbarrier; every wait is bounded.
 #include "dh_common.cuh"
 #include "dh_internal.h"
@@ -57,6 +59,7 @@ constexpr int kSmemLimit8 = 232448;
 // The tile's coarse values for the selection warps: one 64-value block per (batch column,
 // block) pair, pairs kRedPitch floats apart (16-byte aligned, bank-conflict free per lane).
 constexpr int kRedPitch = 68;
+constexpr int kDqWarps = 4; // dequant warps (4-7); the epilogue is warps 8-15
 
 // Batch rows per launch MP in {16, 32}; x in T = 2 e4m3 terms; MMA N = T * MP.
 // Tensor memory: two span-sized A buffers (4 groups x 32 columns) and a ring of kD group-sized
@@ -132,11 +135,13 @@ __device__ __forceinline__ void select_pairs(uint32_t (&k0)[NB], uint32_t (&k1)[
 }
 
 // Block top-KCAND for KCAND <= 8, one lane per (batch column, block) pair: the lane walks the
-// block's 64 values in row order and keeps the 8 best in a descending list.  A value enters
-// only where it is strictly greater, so equal values keep the lower row first; rows past the
-// head hold -inf and never enter, leaving (-inf, -1) in unfilled slots.
-__device__ __forceinline__ void select_lane8(const float *vals, int base_row, int kcand,
-                                             float *oval, int32_t *oidx)
+// block's 64 values (the sums of the two epilogue halves) in row order and keeps the 8 best in a
+// descending list.  A value enters only where it is strictly greater, so equal values keep the
+// lower row first; rows past the head hold -inf and never enter, leaving (-inf, -1) in unfilled
+// slots.  With `coarse` set it also writes the block's coarse values (rows below V).
+__device__ __forceinline__ void select_lane8(const float *vals0, const float *vals1, int base_row,
+                                             int V, int kcand, float *oval, int32_t *oidx,
+                                             float *coarse)
 {
     float v[8];
     int r[8];
@@ -147,12 +152,14 @@ __device__ __forceinline__ void select_lane8(const float *vals, int base_row, in
     }
 #pragma unroll 2
     for (int j4 = 0; j4 < kBlockN / 4; ++j4) {
-        const float4 u = reinterpret_cast<const float4 *>(vals)[j4];
-        const float uu[4] = {u.x, u.y, u.z, u.w};
+        const float4 u0 = reinterpret_cast<const float4 *>(vals0)[j4];
+        const float4 u1 = reinterpret_cast<const float4 *>(vals1)[j4];
+        const float uu[4] = {u0.x + u1.x, u0.y + u1.y, u0.z + u1.z, u0.w + u1.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float xv = uu[e];
             const int row = base_row + 4 * j4 + e;
+            if (coarse && row < V) coarse[row] = xv;
             bool c[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) c[k] = xv > v[k];
@@ -182,46 +189,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg8<MP>;
     constexpr int N = C::N, T = C::T, kAs = C::kAs, kD = C::kD, kDS = C::kDS;
     constexpr bool kAFromD = C::kAFromD;
+    constexpr int kRedHalf = MP * 2 * kRedPitch; // floats of one epilogue half's tile values
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = prm.H / 512, NGt = prm.H / kGroup;
     const int nstage = prm.nstage;
+    const uint32_t sz_bytes = static_cast<uint32_t>(kTileRows) * NGt * 2; // S (or ZS) of a tile
 
     // ---- shared memory ------------------------------------------------------------------
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t *const stages = smem_raw + pad;                                   // nstage x kStage
-    float *const red = reinterpret_cast<float *>(stages + static_cast<size_t>(nstage) * C::kStage);
-    float *const xs_s = red + MP * 2 * kRedPitch;                             // [NGt][MP]
+    uint8_t *const szbuf = stages + static_cast<size_t>(nstage) * C::kStage; // [2][S, ZS] tiles
+    float *const red = reinterpret_cast<float *>(szbuf + 4 * static_cast<size_t>(sz_bytes));
+    float *const xs_s = red + 2 * kRedHalf;                                   // [NGt][MP]
     float *const inv_s = xs_s + NGt * MP;                                     // [MP]
     uint64_t *const bars = reinterpret_cast<uint64_t *>(inv_s + MP);
     uint64_t *const full = bars;              // [nstage] TMA -> dequant, MMA
-    uint64_t *const empty = full + nstage;    // [nstage] dequant (8 warps) + MMA -> TMA
-    uint64_t *const a_full = empty + nstage;  // [kAs]    dequant (8 warps) -> MMA, per span
+    uint64_t *const empty = full + nstage;    // [nstage] dequant (4 warps) + MMA -> TMA
+    uint64_t *const a_full = empty + nstage;  // [kAs]    dequant (4 warps) -> MMA, per span
     uint64_t *const a_empty = a_full + kAs;   // [kAs]    MMA -> dequant (unless kAFromD)
     uint64_t *const d_full = a_empty + kAs;   // [kDS]    MMA -> epilogue (+ dequant), per span
-    uint64_t *const d_empty = d_full + kDS;   // [kD]     epilogue -> MMA, per group
+    uint64_t *const d_empty = d_full + kDS;   // [kD]     epilogue half -> MMA, per group
     uint64_t *const fin = d_empty + kD;       // [1]      MMA drain before teardown
-    uint64_t *const red_full = fin + 1;       // [1]      epilogue -> selection: tile in `red`
+    uint64_t *const red_full = fin + 1;       // [1]      epilogue (8 warps) -> selection
     uint64_t *const red_free = red_full + 1;  // [1]      selection -> epilogue: `red` free
-    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(red_free + 1);
+    uint64_t *const sz_full = red_free + 1;   // [2]      bulk copy -> epilogue: S, ZS of a tile
+    uint64_t *const sz_empty = sz_full + 2;   // [2]      epilogue (8 warps) -> bulk copy
+    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(sz_empty + 2);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_packed);
         prefetch_tensormap(&tm_x);
         for (int i = 0; i < nstage; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 8 + 1);
+            mbar_init(&empty[i], kDqWarps + 1);
         }
         for (int i = 0; i < kAs; ++i) {
-            mbar_init(&a_full[i], 8);
+            mbar_init(&a_full[i], kDqWarps);
             mbar_init(&a_empty[i], 1);
         }
         for (int i = 0; i < kDS; ++i) mbar_init(&d_full[i], 1);
         for (int i = 0; i < kD; ++i) mbar_init(&d_empty[i], 4);
         mbar_init(fin, 2);
-        mbar_init(red_full, 4);
+        mbar_init(red_full, 8);
         mbar_init(red_free, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sz_full[i], 1);
+            mbar_init(&sz_empty[i], 8);
+        }
         fence_barrier_init();
     }
     for (int i = threadIdx.x; i < NGt * MP; i += blockDim.x) {
@@ -242,8 +258,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            uint32_t s = 0;
-            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+            uint32_t s = 0, it = 0;
+            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
+                // the tile's S and ZS rows (contiguous in memory) into buffer it % 2, free once
+                // the epilogue finished tile it - 2; a partial last tile is read from global
+                // memory by the epilogue instead (an arrival without data keeps the phases)
+                const uint32_t b = it & 1u;
+                if (!mbar_wait_bounded(&sz_empty[b], ((it >> 1) & 1u) ^ 1u, prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
+                if ((tile + 1) * kTileRows <= prm.V) {
+                    uint8_t *const sz = szbuf + static_cast<size_t>(b) * 2 * sz_bytes;
+                    const size_t off = static_cast<size_t>(tile) * kTileRows * NGt;
+                    mbar_arrive_expect_tx(&sz_full[b], 2 * sz_bytes);
+                    bulk_load(sz, prm.S + off, sz_bytes, &sz_full[b]);
+                    bulk_load(sz + sz_bytes, prm.ZS + off, sz_bytes, &sz_full[b]);
+                } else {
+                    mbar_arrive(&sz_full[b]);
+                }
                 for (int span = 0; span < NG; ++span, ++s) {
                     const uint32_t st = s % nstage;
                     if (!mbar_wait_bounded(&empty[st], ((s / nstage) & 1u) ^ 1u, prm.timeout_flag)) {
@@ -310,10 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(fin);
             mbar_wait_bounded(fin, 0, prm.timeout_flag);
         }
-    } else if (warp >= 4 && warp < 12) {
-        // ---------------- dequant: warps 4-7 planes 0-1, warps 8-11 planes 2-3 ----------------
-        const int row = ((warp & 3) << 5) | lane; // TMEM lane == tile row
-        const int q0 = (warp < 8) ? 0 : 2;
+    } else if (warp >= 4 && warp < 4 + kDqWarps) {
+        // ---------------- dequant: one TMEM lane (= tile row) per thread, all four planes ------
+        const int row = ((warp & 3) << 5) | lane;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
         uint32_t s = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
@@ -347,66 +379,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                const uint32_t abuf = tmem + lane_base + C::kAcol + sa * 128;
                 uint32_t r0[32], r1[32];
-                if (q0 == 0) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        r0[i] = deq4_e4m3<0>(w[i]);
-                        r1[i] = deq4_e4m3<1>(w[i]);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        r0[i] = deq4_e4m3<2>(w[i]);
-                        r1[i] = deq4_e4m3<3>(w[i]);
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    r0[i] = deq4_e4m3<0>(w[i]);
+                    r1[i] = deq4_e4m3<1>(w[i]);
                 }
-                const uint32_t abuf = tmem + lane_base + C::kAcol + sa * 128 + q0 * 32;
                 tmem_st_x32(abuf, r0);
                 tmem_st_x32(abuf + 32, r1);
+                // a tcgen05.st reads its registers at issue: r0 and r1 are free again
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    r0[i] = deq4_e4m3<2>(w[i]);
+                    r1[i] = deq4_e4m3<3>(w[i]);
+                }
+                tmem_st_x32(abuf + 64, r0);
+                tmem_st_x32(abuf + 96, r1);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[sa]);
             }
         }
-    } else if (warp >= 12) {
-        // ---------------- epilogue: one wait per span, slots released as they are read -------
+    } else if (warp >= 4 + kDqWarps) {
+        // ---------------- epilogue: two halves of four warps, each two groups of every span ---
+        const int h = (warp - 4 - kDqWarps) >> 2; // groups 2h, 2h + 1
         const int row = ((warp & 3) << 5) | lane;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
-        constexpr int GPW = (MP == 16) ? 2 : 1; // groups per tcgen05.wait::ld
-        // S and ZS of the next span to fold, loaded one span ahead so that their latency
-        // overlaps the current span (rows past the head read as 0)
-        uint16_t s_next[4], z_next[4];
-        auto fetch = [&](int tl, int sp_) {
-            const int gr = tl * kTileRows + row;
-            const bool ok = tl < prm.ntiles && gr < prm.V;
-            const long long base = static_cast<long long>(ok ? gr : 0) * NGt + sp_;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                s_next[q] = ok ? __ldg(prm.S + base + q * NG) : static_cast<uint16_t>(0);
-                z_next[q] = ok ? __ldg(prm.ZS + base + q * NG) : static_cast<uint16_t>(0);
-            }
-        };
-        fetch(first_tile, 0);
+        constexpr int CH = MP / 16; // 16-column chunks of one term of one group
         uint32_t t = 0, it = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
             const int grow = tile * kTileRows + row;
             const bool row_ok = grow < prm.V;
+            const bool full_tile = (tile + 1) * kTileRows <= prm.V;
+            const uint32_t b = it & 1u;
+            if (!warp_wait(&sz_full[b], (it >> 1) & 1u, prm.timeout_flag)) {
+                failed = true;
+                break;
+            }
+            const uint16_t *const sS = reinterpret_cast<const uint16_t *>(
+                szbuf + static_cast<size_t>(b) * 2 * sz_bytes) + row * NGt;
+            const uint16_t *const sZ = sS + sz_bytes / 2;
+            const uint16_t *const gS = prm.S + static_cast<long long>(row_ok ? grow : 0) * NGt;
+            const uint16_t *const gZ = prm.ZS + static_cast<long long>(row_ok ? grow : 0) * NGt;
             float acc[MP];
 #pragma unroll
             for (int m = 0; m < MP; ++m) acc[m] = 0.f;
             for (int span = 0; span < NG; ++span, t += 4) {
-                float s2[4], sz[4];
+                float s2[2], sz[2];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float sv = bf16_bits_to_f32(s_next[q]);
-                    const float zv = bf16_bits_to_f32(z_next[q]);
-                    s2[q] = ((q & 1) ? 32.0f : 128.0f) * sv;
-                    sz[q] = sv - zv;
+                for (int gl = 0; gl < 2; ++gl) {
+                    const int gi = (2 * h + gl) * NG + span;
+                    uint16_t sb = 0, zb = 0;
+                    if (full_tile) {
+                        sb = sS[gi];
+                        zb = sZ[gi];
+                    } else if (row_ok) {
+                        sb = __ldg(gS + gi);
+                        zb = __ldg(gZ + gi);
+                    }
+                    const float sv = bf16_bits_to_f32(sb), zv = bf16_bits_to_f32(zb);
+                    // odd planes carry 4 v 2^-9, even planes v 2^-9
+                    s2[gl] = (((2 * h + gl) & 1) ? 32.0f : 128.0f) * sv;
+                    sz[gl] = sv - zv;
                 }
-                if (span + 1 < NG) fetch(tile, span + 1);
-                else fetch(tile + tile_step, 0);
                 // one commit per span: all four groups' partials are in tensor memory
                 const uint32_t sp = t / 4;
                 if (!warp_wait(&d_full[sp % kDS], (sp / kDS) & 1u, prm.timeout_flag)) {
@@ -414,64 +451,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                // the half's 2 * CH chunks, two per tcgen05 wait (64 registers)
 #pragma unroll
-                for (int q0 = 0; q0 < 4; q0 += GPW) {
+                for (int wb = 0; wb < CH; ++wb) {
+                    float v[2][T][16];
 #pragma unroll
-                    for (int c = 0; c < MP / 16; ++c) {
-                        float v[GPW][T][16];
+                    for (int u = 0; u < 2; ++u) {
+                        const int k = 2 * wb + u, gl = k / CH, c = k % CH;
+                        const uint32_t d = (t + 2 * h + gl) % kD;
 #pragma unroll
-                        for (int g = 0; g < GPW; ++g)
+                        for (int tt = 0; tt < T; ++tt)
+                            tmem_ld_x16(tmem + lane_base + C::kDcol + d * N + tt * MP + c * 16,
+                                        v[u][tt]);
+                    }
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
 #pragma unroll
-                            for (int tt = 0; tt < T; ++tt)
-                                tmem_ld_x16(tmem + lane_base + C::kDcol + ((t + q0 + g) % kD) * N +
-                                                tt * MP + c * 16,
-                                            v[g][tt]);
-                        tmem_wait_ld();
-                        if (c == MP / 16 - 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0)
-#pragma unroll
-                                for (int g = 0; g < GPW; ++g) mbar_arrive(&d_empty[(t + q0 + g) % kD]);
+                        for (int u = 0; u < 2; ++u) {
+                            const int k = 2 * wb + u;
+                            if (k % CH == CH - 1) mbar_arrive(&d_empty[(t + 2 * h + k / CH) % kD]);
                         }
+                    }
 #pragma unroll
-                        for (int g = 0; g < GPW; ++g) {
-                            const int q = q0 + g;
-                            const float4 *xg =
-                                reinterpret_cast<const float4 *>(xs_s + (q * NG + span) * MP);
+                    for (int u = 0; u < 2; ++u) {
+                        const int k = 2 * wb + u, gl = k / CH, c = k % CH;
+                        const float4 *xg = reinterpret_cast<const float4 *>(
+                            xs_s + ((2 * h + gl) * NG + span) * MP);
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float4 x4 = xg[c * 4 + j];
-                                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 x4 = xg[c * 4 + j];
+                            const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float p = v[g][0][4 * j + i] + v[g][1][4 * j + i];
-                                    const int m = c * 16 + 4 * j + i;
-                                    acc[m] = fmaf(s2[q], p, fmaf(sz[q], xv[i], acc[m]));
-                                }
+                            for (int i = 0; i < 4; ++i) {
+                                const float p = v[u][0][4 * j + i] + v[u][1][4 * j + i];
+                                const int m = c * 16 + 4 * j + i;
+                                acc[m] = fmaf(s2[gl], p, fmaf(sz[gl], xv[i], acc[m]));
                             }
                         }
                     }
                 }
             }
             if (failed) break;
-            // the selection warps are done with the previous tile's values
+            // every read of the tile's S / ZS buffer is done
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sz_empty[b]);
+            // the selection warp is done with the previous tile's values
             if (!warp_wait(red_free, (it & 1u) ^ 1u, prm.timeout_flag)) {
                 failed = true;
                 break;
             }
+            float *const rh = red + h * kRedHalf + (row >> 6) * kRedPitch + (row & 63);
 #pragma unroll
-            for (int m = 0; m < MP; ++m) {
-                const float c = acc[m] * inv_s[m];
-                red[(2 * m + (row >> 6)) * kRedPitch + (row & 63)] = row_ok ? c : -INFINITY;
-                if (prm.coarse && row_ok && m < prm.mrows)
-                    prm.coarse[static_cast<long long>(prm.m0 + m) * prm.V + grow] = c;
-            }
+            for (int m = 0; m < MP; ++m) rh[2 * m * kRedPitch] = row_ok ? acc[m] * inv_s[m] : -INFINITY;
             __syncwarp();
             if (lane == 0) mbar_arrive(red_full);
         }
     } else if (warp == 2) {
         // ---------------- block top-KCAND: pair = (batch column m, block b of the tile) ------
+        // the tile's coarse values are the sums of the two epilogue halves (both -inf past V)
         const int npairs = 2 * prm.mrows;
         uint32_t it = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
@@ -486,32 +525,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (static_cast<long long>(blk) * kBlockN < prm.V) {
                         const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
                                               static_cast<long long>(blk) * prm.kcand;
-                        select_lane8(red + pidx * kRedPitch, blk * kBlockN, prm.kcand,
-                                     prm.cand_val + off, prm.cand_idx + off);
+                        float *const cdbg =
+                            prm.coarse ? prm.coarse + static_cast<long long>(prm.m0 + m) * prm.V
+                                       : nullptr;
+                        select_lane8(red + pidx * kRedPitch, red + kRedHalf + pidx * kRedPitch,
+                                     blk * kBlockN, prm.V, prm.kcand, prm.cand_val + off,
+                                     prm.cand_idx + off, cdbg);
                     }
                 }
             } else {
-                // larger KCAND: four pairs per warp at a time, one warp-wide round per entry
+                // larger KCAND: four pairs at a time, one warp-wide round per entry
                 for (int p0 = 0; p0 < npairs; p0 += 4) {
                     uint32_t k0[4], k1[4];
                     int base_row[4];
                     float *oval[4];
                     int32_t *oidx[4];
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const int pidx = p0 + b;
+                    for (int bb = 0; bb < 4; ++bb) {
+                        const int pidx = p0 + bb;
                         const int m = pidx >> 1, blk = tile * 2 + (pidx & 1);
                         const bool live = pidx < npairs &&
                                           static_cast<long long>(blk) * kBlockN < prm.V;
                         const int g0 = blk * kBlockN + lane;
                         const float *pv = red + (live ? pidx : 0) * kRedPitch;
-                        k0[b] = (live && g0 < prm.V) ? f32_order_key(pv[lane]) : 0u;
-                        k1[b] = (live && g0 + 32 < prm.V) ? f32_order_key(pv[lane + 32]) : 0u;
-                        base_row[b] = blk * kBlockN;
+                        const float c0 = pv[lane] + pv[kRedHalf + lane];
+                        const float c1 = pv[lane + 32] + pv[kRedHalf + lane + 32];
+                        k0[bb] = (live && g0 < prm.V) ? f32_order_key(c0) : 0u;
+                        k1[bb] = (live && g0 + 32 < prm.V) ? f32_order_key(c1) : 0u;
+                        if (prm.coarse && live) {
+                            float *const cd = prm.coarse + static_cast<long long>(prm.m0 + m) * prm.V;
+                            if (g0 < prm.V) cd[g0] = c0;
+                            if (g0 + 32 < prm.V) cd[g0 + 32] = c1;
+                        }
+                        base_row[bb] = blk * kBlockN;
                         const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
                                               static_cast<long long>(blk) * prm.kcand;
-                        oval[b] = live ? prm.cand_val + off : nullptr;
-                        oidx[b] = live ? prm.cand_idx + off : nullptr;
+                        oval[bb] = live ? prm.cand_val + off : nullptr;
+                        oidx[bb] = live ? prm.cand_idx + off : nullptr;
                     }
                     select_pairs<4>(k0, k1, base_row, oval, oidx, prm.kcand, lane);
                 }
@@ -528,6 +578,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Dynamic shared memory besides the stages: alignment slack, the double-buffered S/ZS tile
+// copies, the two epilogue halves' tile values, xs and 2^-e, barriers.
+size_t tc8_fixed_smem(int MP, int H)
+{
+    const int NGt = H / kGroup;
+    return 1024 + 4 * static_cast<size_t>(kTileRows) * NGt * 2 +
+           2 * static_cast<size_t>(MP) * 2 * kRedPitch * 4 + static_cast<size_t>(NGt) * MP * 4 +
+           MP * 4 + 64 * 8 + 32;
+}
+
 template <int MP>
 cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
                        const Tc8Params &base, cudaStream_t stream)
@@ -538,9 +598,7 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
                                       const_cast<uint8_t *>(xt8_chunk), base.H, C::N, base.H,
                                       128, C::N, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const int NGt = base.H / kGroup;
-    const size_t fixed = 1024 + static_cast<size_t>(MP) * 2 * kRedPitch * 4 +
-                         static_cast<size_t>(NGt) * MP * 4 + MP * 4 + 64 * 8 + 32;
+    const size_t fixed = tc8_fixed_smem(MP, base.H);
     int nstage = static_cast<int>((kSmemLimit8 - static_cast<long long>(fixed)) / C::kStage);
     if (nstage > 6) nstage = 6;
     if (nstage < 2) return cudaErrorInvalidConfiguration;
@@ -561,6 +619,18 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
 }
 
 } // namespace
+
+bool tc8_supported(int M, int H)
+{
+    if (M < 1 || M > kMaxM || H % 512 != 0) return false;
+    // at least two stages next to the fixed buffers, for every chunk size the batch uses
+    for (int c = 0; c < tc8_chunks(M); ++c) {
+        const int MP = tc8_chunk(M, c).MP;
+        const size_t stage = kPkBytes + static_cast<size_t>(MP) * 2 * 512;
+        if (tc8_fixed_smem(MP, H) + 2 * stage > static_cast<size_t>(kSmemLimit8)) return false;
+    }
+    return true;
+}
 
 Tc8Chunk tc8_chunk(int M, int c)
 {
@@ -584,6 +654,7 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
                                       const_cast<uint8_t *>(a.packed), a.H / 4, a.V, a.H / 4,
                                       kSpanBytes, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (!tc8_supported(a.M, a.H)) return cudaErrorInvalidConfiguration;
     Tc8Params base;
     base.S = a.S;
     base.ZS = a.ZS;

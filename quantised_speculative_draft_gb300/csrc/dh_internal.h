@@ -69,6 +69,7 @@ struct Tc8Workspace {
 cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
                             int *counters, int ncounters, cudaStream_t stream);
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream);
+bool tc8_supported(int M, int H); // shared memory of the 8-bit tcgen05 path fits
 
 bool tc_supported(int M, int H);
 cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream);
