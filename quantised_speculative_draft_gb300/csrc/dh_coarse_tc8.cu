@@ -73,6 +73,10 @@ template <int MP> struct Cfg8 {
     // when there are at least as many accumulator sets as A buffers, "span s accumulated"
     // also means "A buffer of span s free": one commit serves both
     static constexpr bool kAFromD = kDS >= kAs;
+    // accumulators go back to the MMA issuers per span when there are two or more sets (one
+    // wait per span), else per group (so the next span can start on a group already read)
+    static constexpr int kRel = kDS >= 2 ? 4 : 1;
+    static constexpr int kDrel = kD / kRel; // release barriers
     static constexpr uint32_t kAcol = 0;
     static constexpr uint32_t kDcol = kAs * 128;
     static constexpr uint32_t kXBytes = N * 512;            // 4 planes x 128 k x N rows
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg8<MP>;
     constexpr int N = C::N, T = C::T, kAs = C::kAs, kD = C::kD, kDS = C::kDS;
     constexpr bool kAFromD = C::kAFromD;
+    constexpr int kRel = C::kRel, kDrel = C::kDrel;
     constexpr int kRedHalf = MP * 2 * kRedPitch; // floats of one epilogue half's tile values
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -210,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *const a_full = empty + nstage;  // [kAs]    dequant (4 warps) -> MMA, per span
     uint64_t *const a_empty = a_full + kAs;   // [kAs]    MMA -> dequant (unless kAFromD)
     uint64_t *const d_full = a_empty + kAs;   // [kDS]    MMA -> epilogue (+ dequant), per span
-    uint64_t *const d_empty = d_full + kDS;   // [kD]     epilogue half -> MMA, per group
-    uint64_t *const fin = d_empty + kD;       // [1]      MMA drain before teardown
+    uint64_t *const d_empty = d_full + kDS;   // [kDrel]  epilogue -> MMA, per kRel groups
+    uint64_t *const fin = d_empty + kDrel;    // [1]      MMA drain before teardown
     uint64_t *const red_full = fin + 1;       // [1]      epilogue (8 warps) -> selection
     uint64_t *const red_free = red_full + 1;  // [1]      selection -> epilogue: `red` free
     uint64_t *const sz_full = red_free + 1;   // [2]      bulk copy -> epilogue: S, ZS of a tile
@@ -230,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&a_empty[i], 1);
         }
         for (int i = 0; i < kDS; ++i) mbar_init(&d_full[i], 1);
-        for (int i = 0; i < kD; ++i) mbar_init(&d_empty[i], 4);
+        // per span: all eight epilogue warps; per group: the four warps of its half
+        for (int i = 0; i < kDrel; ++i) mbar_init(&d_empty[i], kRel == 4 ? 8 : 4);
         mbar_init(fin, 2);
         mbar_init(red_full, 8);
         mbar_init(red_free, 1);
@@ -318,11 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sw128_desc(smem_u32(stages + static_cast<size_t>(st) * C::kStage + kPkBytes));
                     for (int q = 0; q < 4; ++q, ++t) {
                         const uint32_t d = t % kD;
-                        if (!mbar_wait_bounded(&d_empty[d], ((t / kD) & 1u) ^ 1u, prm.timeout_flag)) {
-                            failed = true;
-                            break;
+                        if (q % kRel == 0) {
+                            const uint32_t r = t / kRel;
+                            if (!mbar_wait_bounded(&d_empty[r % kDrel], ((r / kDrel) & 1u) ^ 1u,
+                                                   prm.timeout_flag)) {
+                                failed = true;
+                                break;
+                            }
+                            tc_fence_after();
                         }
-                        tc_fence_after();
                         const uint32_t d_tmem = tmem + C::kDcol + d * N;
                         const uint32_t a_tmem = tmem + C::kAcol + sa * 128 + q * 32;
                         // the descriptor's address field counts 16-byte units
@@ -468,10 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
+                        if (kRel == 1) {
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int k = 2 * wb + u;
-                            if (k % CH == CH - 1) mbar_arrive(&d_empty[(t + 2 * h + k / CH) % kD]);
+                            for (int u = 0; u < 2; ++u) {
+                                const int k = 2 * wb + u;
+                                if (k % CH == CH - 1)
+                                    mbar_arrive(&d_empty[(t + 2 * h + k / CH) % kDrel]);
+                            }
+                        } else if (wb == CH - 1) {
+                            mbar_arrive(&d_empty[(t / 4) % kDrel]); // the span's set, read
                         }
                     }
 #pragma unroll
