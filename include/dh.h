@@ -162,11 +162,13 @@ int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t 
 
 /*
  * Coarse-pass implementation choice (process-wide).
- *   DH_PATH_AUTO     pick by M (default)
+ *   DH_PATH_AUTO     DH_PATH_TC where its shared-memory layout fits (H up to 8192), else
+ *                    DH_PATH_WARP (default)
  *   DH_PATH_WARP     warp-level mma.sync on bf16 operands (the page's 1 + v/4 bit pattern),
  *                    batch handled 16 rows at a time
- *   DH_PATH_TC       tcgen05 with 8-bit operands: weights as the e4m3 pattern 1 + v/8, x split
- *                    exactly into e4m3 terms stacked along N, batch in launches of 64 rows
+ *   DH_PATH_TC       tcgen05 with 8-bit operands: each 2-bit code masked in place is an exact
+ *                    e4m3 subnormal weight, x split into two e4m3 terms stacked along N, batch
+ *                    in launches of 32 rows
  *   DH_PATH_TC_BF16  tcgen05 on bf16 operands (the page's 1 + v/4 bit pattern)
  * All paths compute the same coarse values up to fp32 rounding.  dh_set_coarse_path returns
  * the previous setting, or DH_ERR_ARG for an unknown value.  dh_coarse_path_for(M) reports
