@@ -94,7 +94,7 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     L.rows = L.Mpad_w > L.Npad ? L.Mpad_w : L.Npad;
     L.nblk = (V + kBlockN - 1) / kBlockN;
     L.ncand = L.nblk * kcand;
-    select_plan(M, L.ncand, rerank, &L.passes, &L.scratch_entries);
+    select_plan(M, L.ncand, kcand, rerank, &L.passes, &L.scratch_entries);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -236,7 +236,8 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
                                        : (path == DH_PATH_TC_BF16 ? "tcgen05 bf16" : "warp"),
                     cudaGetErrorString(err));
     if (!rec(2)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
-    err = launch_select(cval, cidx, M, L.ncand, rerank, sv, si, L.scratch_entries, sel, stream);
+    err = launch_select(cval, cidx, M, L.ncand, kcand, rerank, sv, si, L.scratch_entries,
+                        counters + kSelDoneOffset, sel, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
     if (!rec(3)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     err = launch_rerank_topk(x, W, M, H, V, sel, rerank, ex, counters + kRowDoneOffset, topk,

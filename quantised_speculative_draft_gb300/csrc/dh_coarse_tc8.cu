@@ -637,7 +637,8 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
 
 bool tc8_supported(int M, int H)
 {
-    if (M < 1 || M > kMaxM || H % 512 != 0) return false;
+    // the x staging keeps a row in registers: H <= 16384
+    if (M < 1 || M > kMaxM || H % 512 != 0 || H > 16384) return false;
     // at least two stages next to the fixed buffers, for every chunk size the batch uses
     for (int c = 0; c < tc8_chunks(M); ++c) {
         const int MP = tc8_chunk(M, c).MP;

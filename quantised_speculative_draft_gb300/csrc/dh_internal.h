@@ -19,8 +19,10 @@ constexpr int kWarpRowsPerWarp = 64;    // vocabulary rows per warp work item (o
 constexpr int kSelectChunk = 4096;      // candidates per CTA in one top-R selection pass
 constexpr int kMaxRerank = 1024;
 constexpr int kMaxM = 128;
-constexpr int kNumCounters = 256;   // [0, 64): work queues, [128, 256): per-row completion
+constexpr int kNumCounters = 384;   // [0, 64): work queues, [128, 256): per-row rerank
+                                    // completion, [256, 384): per-row selection completion
 constexpr int kRowDoneOffset = 128;
+constexpr int kSelDoneOffset = 256;
 
 // ---- launchers (each returns the launch status) ------------------------------------------
 cudaError_t launch_quantize(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
@@ -78,10 +80,12 @@ int tc_launches(int M); // coarse-pass launches of the tcgen05 path
 
 // Top-R selection over candidate lists.  Returns the number of passes it will take and the
 // scratch entries it needs (two ping-pong buffers of `scratch_entries` (val, idx) pairs).
-void select_plan(int M, long long ncand, int R, int *passes, long long *scratch_entries);
+void select_plan(int M, long long ncand, int kcand, int R, int *passes,
+                 long long *scratch_entries);
 cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M, long long ncand,
-                          int R, float *scratch_val[2], int32_t *scratch_idx[2],
-                          long long scratch_entries, int32_t *sel_idx, cudaStream_t stream);
+                          int kcand, int R, float *scratch_val[2], int32_t *scratch_idx[2],
+                          long long scratch_entries, int *row_cnt, int32_t *sel_idx,
+                          cudaStream_t stream);
 
 // Exact rerank of the selected rows and, fused (last CTA per row), the per-row top-k.
 // row_done: M zeroed counters.

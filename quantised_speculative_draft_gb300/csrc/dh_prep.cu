@@ -121,6 +121,8 @@ __device__ __forceinline__ float e4m3_to_f32(__nv_fp8_storage_t v)
     return __half2float(__half(h));
 }
 
+constexpr int kPrepOcts = 8; // 16-byte slices of x per thread (H up to 16384)
+
 __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restrict__ x, int H,
                                                        int m0, int rows, int MP, int T,
                                                        uint8_t *__restrict__ xt8,
@@ -136,16 +138,20 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restric
         for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
     const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
 
+    // the row stays in registers between the max and the split (H <= 256 * 8 * kPrepOcts)
+    uint4 xv[kPrepOcts];
     float mx = 0.f;
-    if (valid)
-        for (int o = threadIdx.x; o < octs; o += blockDim.x) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
-                                     fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
-        }
+    for (int j = 0; j < kPrepOcts; ++j) {
+        const int o = threadIdx.x + j * 256;
+        xv[j] = make_uint4(0, 0, 0, 0);
+        if (valid && o < octs) xv[j] = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
+        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
+                                 fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
@@ -162,17 +168,18 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restric
     const float scale = __int_as_float((e + 127) << 23);
     if (threadIdx.x == 0) inv_scale[m] = valid ? __int_as_float((127 - e) << 23) : 1.0f;
 
-    for (int o = threadIdx.x; o < octs; o += blockDim.x) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid) v = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < kPrepOcts; ++j) {
+        const int o = threadIdx.x + j * 256;
+        if (o >= octs) break;
+        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
         uint32_t lo[3] = {0, 0, 0}, hi[3] = {0, 0, 0};
         float sum = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float xv = (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u)
+            const float xe = (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u)
                                      : __uint_as_float(w[i >> 1] << 16);
-            float r = xv * scale; // exact: a power of two
+            float r = xe * scale; // exact: a power of two
             float rep = 0.f;
 #pragma unroll
             for (int t = 0; t < 3; ++t) {

@@ -164,13 +164,184 @@ __global__ void __launch_bounds__(kSelThreads) topr_kernel(const float *__restri
 }
 
 // ----------------------------------------------------------------------------------------
-// a6 + a7: exact rerank, then the top-k of the row.  One CTA of 128 threads per (row m,
-// candidate j): every thread takes H/1024 16-byte slices of x and of the candidate's bf16 row
+// a5, one launch per batch row when the sizes allow it.  Every block's candidate list is in
+// rank order (value descending, lower row first), so a candidate can be among the row's R
+// best only if its block's best is among the R best block maxima: if R blocks have a better
+// maximum, R candidates beat everything in the block.  For R <= 32 the 32 best block maxima
+// are found by CTAs of 512 maxima and merged by the row's last CTA, which then keeps the 32
+// best of those blocks' candidates and writes the R best indices in rank order.  Sorting is
+// warp-level (bitonic sorts of 32 keys, merges of sorted 32-lists), so nothing needs a
+// block-wide sort.  Keys are unique (the index is part of the key), so the cut is exact.
+// ----------------------------------------------------------------------------------------
+constexpr int kRowSelThreads = 128; // 4 warps
+constexpr int kRowSelChunk = 128;   // keys per warp sort unit (4 lists of 32)
+constexpr int kRowSelCtaKeys = 512; // block maxima per CTA in phase 1
+constexpr int kRowSelMaxCtas = 16;  // CTAs per row (block count <= 8192)
+constexpr int kRowSelR = 32;        // lists keep the 32 best
+
+__device__ __forceinline__ unsigned long long kmax(unsigned long long a, unsigned long long b)
+{
+    return a > b ? a : b;
+}
+__device__ __forceinline__ unsigned long long kmin(unsigned long long a, unsigned long long b)
+{
+    return a < b ? a : b;
+}
+
+// Sorts four warp lists (one key per lane each) descending, in lockstep (bitonic, 15 stages).
+__device__ __forceinline__ void warp_sort32x4_desc(unsigned long long (&v)[4])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], stride);
+                v[r] = keep_max ? kmax(v[r], o) : kmin(v[r], o);
+            }
+        }
+    }
+}
+
+// The 32 best of two descending warp lists, descending: the half-cleaner of a against b
+// reversed leaves the 32 largest as a bitonic sequence, five more stages sort it.
+__device__ __forceinline__ unsigned long long warp_merge32_desc(unsigned long long a,
+                                                                unsigned long long b)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned long long v = kmax(a, __shfl_sync(0xffffffffu, b, 31 - lane));
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, stride);
+        v = (lane & stride) == 0 ? kmax(v, o) : kmin(v, o);
+    }
+    return v;
+}
+
+// The 32 best (descending, one per lane) of the 128 keys k[0..127] (0 = empty).
+__device__ __forceinline__ unsigned long long warp_top32_of128(const unsigned long long *k)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned long long v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[r] = k[r * 32 + lane];
+    warp_sort32x4_desc(v);
+    return warp_merge32_desc(warp_merge32_desc(v[0], v[1]), warp_merge32_desc(v[2], v[3]));
+}
+
+// The 32 best of n keys in shared memory (n a multiple of 128, keys beyond the data 0), by the
+// CTA's four warps; returns the list in lists[0] (descending).  All threads must call it.
+__device__ void cta_top32(const unsigned long long *keys, int n, unsigned long long (*lists)[32])
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned long long acc = 0;
+    for (int c = warp; c * kRowSelChunk < n; c += 4)
+        acc = warp_merge32_desc(acc, warp_top32_of128(keys + c * kRowSelChunk));
+    lists[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned long long a = warp_merge32_desc(lists[0][lane], lists[1][lane]);
+        const unsigned long long b = warp_merge32_desc(lists[2][lane], lists[3][lane]);
+        lists[0][lane] = warp_merge32_desc(a, b);
+    }
+    __syncthreads();
+}
+
+// Phase 1, grid (P, M): CTA p keeps the 32 best of block maxima [512 p, 512 p + 512) of row m
+// and writes them to partial[(m P + p) 32 ..]; the last CTA of the row (per-row counter,
+// zeroed by the staging kernel) merges the P lists, takes the 32 best blocks' candidates and
+// writes the row's R best indices in rank order.  No CTA waits for another.
+__global__ void __launch_bounds__(kRowSelThreads) select_rows_kernel(
+    const float *__restrict__ cand_val, const int32_t *__restrict__ cand_idx, long long ncand,
+    int nblk, int kcand, int R, unsigned long long *__restrict__ partial, int *__restrict__ row_cnt,
+    int32_t *__restrict__ sel_idx)
+{
+    __shared__ unsigned long long keys[kRowSelR * kBlockN]; // 2048: the largest candidate set
+    __shared__ unsigned long long lists[4][32];
+    __shared__ int sblk[kRowSelR];
+    __shared__ int s_last;
+    const int P = gridDim.x, p = blockIdx.x, m = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const float *vrow = cand_val + static_cast<long long>(m) * ncand;
+    const int32_t *irow = cand_idx + static_cast<long long>(m) * ncand;
+
+    for (int i = threadIdx.x; i < kRowSelCtaKeys; i += kRowSelThreads) {
+        const int bk = p * kRowSelCtaKeys + i;
+        unsigned long long key = 0;
+        if (bk < nblk) {
+            const long long e = static_cast<long long>(bk) * kcand;
+            const int id = irow[e];
+            if (id >= 0) key = rank_key(vrow[e], id);
+        }
+        keys[i] = key;
+    }
+    __syncthreads();
+    cta_top32(keys, kRowSelCtaKeys, lists);
+    if (threadIdx.x < 32) partial[(static_cast<long long>(m) * P + p) * 32 + lane] = lists[0][lane];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&row_cnt[m], 1) == P - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // the row's last CTA: the 32 best blocks from the P lists
+    const int np = ((P * 32 + kRowSelChunk - 1) / kRowSelChunk) * kRowSelChunk;
+    for (int i = threadIdx.x; i < np; i += kRowSelThreads)
+        keys[i] = i < P * 32 ? __ldcg(partial + static_cast<long long>(m) * P * 32 + i) : 0ull;
+    __syncthreads();
+    cta_top32(keys, np, lists);
+    if (threadIdx.x < kRowSelR) {
+        const unsigned long long key = lists[0][threadIdx.x];
+        sblk[threadIdx.x] = key ? static_cast<int>(~static_cast<uint32_t>(key)) / kBlockN : -1;
+    }
+    __syncthreads();
+    // their candidates; the R best in rank order
+    const int nc = kRowSelR * kcand;
+    const int ncp = ((nc + kRowSelChunk - 1) / kRowSelChunk) * kRowSelChunk;
+    for (int e = threadIdx.x; e < ncp; e += kRowSelThreads) {
+        unsigned long long key = 0;
+        if (e < nc) {
+            const int bk = sblk[e / kcand];
+            if (bk >= 0) {
+                const long long c = static_cast<long long>(bk) * kcand + e % kcand;
+                const int id = irow[c];
+                if (id >= 0) key = rank_key(vrow[c], id);
+            }
+        }
+        keys[e] = key;
+    }
+    __syncthreads();
+    cta_top32(keys, ncp, lists);
+    if (threadIdx.x < R) {
+        const unsigned long long key = lists[0][threadIdx.x];
+        sel_idx[static_cast<long long>(m) * R + threadIdx.x] =
+            key ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
+    }
+}
+
+int row_select_ctas(long long ncand, int kcand)
+{
+    const long long nblk = ncand / kcand;
+    return static_cast<int>((nblk + kRowSelCtaKeys - 1) / kRowSelCtaKeys);
+}
+
+bool row_select_fits(long long ncand, int kcand, int R)
+{
+    return R <= kRowSelR && row_select_ctas(ncand, kcand) <= kRowSelMaxCtas;
+}
+
+// ----------------------------------------------------------------------------------------
+// a6 + a7: exact rerank, then the top-k of the row.  One CTA of 256 threads per (row m,
+// candidate j): every thread takes H/2048 16-byte slices of x and of the candidate's bf16 row
 // (products of bf16 values are exact in fp32), sums them in two fp32 partials, and the CTA
-// combines the 256 partials in fp64.  The last CTA to finish a row (an atomic count per row,
+// combines the 512 partials in fp64.  The last CTA to finish a row (an atomic count per row,
 // zeroed by the staging kernel) sorts that row's R exact values and writes its top-k.
 // ----------------------------------------------------------------------------------------
-constexpr int kRerankThreads = 128;
+constexpr int kRerankThreads = 256;
 
 __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, int H, int V,
@@ -261,8 +432,15 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
 
 } // namespace
 
-void select_plan(int M, long long ncand, int R, int *passes, long long *scratch_entries)
+void select_plan(int M, long long ncand, int kcand, int R, int *passes,
+                 long long *scratch_entries)
 {
+    if (row_select_fits(ncand, kcand, R)) {
+        // the partial lists: M x P x 32 keys of 8 bytes in the first value buffer
+        *passes = 1;
+        *scratch_entries = static_cast<long long>(M) * row_select_ctas(ncand, kcand) * 32 * 2;
+        return;
+    }
     long long n = ncand;
     int np = 0;
     long long most = 0;
@@ -279,10 +457,19 @@ void select_plan(int M, long long ncand, int R, int *passes, long long *scratch_
 }
 
 cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M, long long ncand,
-                          int R, float *scratch_val[2], int32_t *scratch_idx[2],
-                          long long scratch_entries, int32_t *sel_idx, cudaStream_t stream)
+                          int kcand, int R, float *scratch_val[2], int32_t *scratch_idx[2],
+                          long long scratch_entries, int *row_cnt, int32_t *sel_idx,
+                          cudaStream_t stream)
 {
     (void)scratch_entries;
+    if (row_select_fits(ncand, kcand, R)) {
+        const int nblk = static_cast<int>(ncand / kcand);
+        dim3 grid(static_cast<unsigned>(row_select_ctas(ncand, kcand)), static_cast<unsigned>(M));
+        select_rows_kernel<<<grid, kRowSelThreads, 0, stream>>>(
+            cand_val, cand_idx, ncand, nblk, kcand, R,
+            reinterpret_cast<unsigned long long *>(scratch_val[0]), row_cnt, sel_idx);
+        return cudaGetLastError();
+    }
     const float *in_v = cand_val;
     const int32_t *in_i = cand_idx;
     long long stride = ncand, n = ncand;
