@@ -22,24 +22,24 @@
 //     with xs' the group sums of the represented x (in the scaled units): the scale and zero
 //     are applied to the fp32 partial of every group, never to the weight.
 //
-// Roles (16 warps, one CTA per SM, persistent over 128-row vocabulary tiles):
+// Roles (16 warps, one CTA per SM, persistent over 128-row vocabulary tiles).  The unit of MMA
+// work is a span (N = 32) or half a span (N = 64, planes 2u, 2u+1); unit q uses tensor-memory
+// slot q % 2 (an A buffer and one accumulator per plane) and that slot's issuer:
 //   warp 0       TMA: per span one [128 rows x 128 B] box of packed bytes and four
-//                [128 k x N] boxes of the staged x terms (128-byte swizzle) into a stage ring
-//   warps 1, 3   MMA issuers: per group 4 x tcgen05.mma kind::f8f6f4, M = 128, K = 32; one
-//                commit per span and consumer (a commit costs an issue slot like an MMA).
-//                With two accumulator sets (N = 32) they take alternate spans, each with its
-//                own A buffer and accumulators, so one's waits overlap the other's MMAs;
-//                with one set (N = 64) warp 1 issues every span
+//                [128 k x N] boxes of the staged x terms (128-byte swizzle) into a stage ring;
+//                per tile a bulk copy of the tile's S and ZS rows (contiguous in memory) into
+//                a double-buffered shared copy for the epilogue
+//   warps 1, 3   MMA issuers of slots 0 and 1: per plane 4 x tcgen05.mma kind::f8f6f4
+//                (M = 128, K = 32), two commits per unit; a thread issuing tcgen05.mma is held
+//                ~57 cycles per instruction, so the two issuers overlap
 //   warp 2       block top-KCAND of the previous tile (overlaps the current tile): one lane
 //                per (batch column, block) pair keeps an insertion list of the best 8
-//   warps 4-7    dequant: one TMEM lane (= one vocabulary row) per thread, all four planes of
-//                every span (four tcgen05.st of 32 columns, one wait) into a ring of A buffers
-//   warp 0 also  bulk-copies each tile's S and ZS rows (contiguous in memory) into a
-//                double-buffered shared copy for the epilogue
+//   warps 4-7    dequant: one TMEM lane (= one vocabulary row) per thread, every plane of every
+//                span (a tcgen05.st of 32 columns per plane, one wait per unit)
 //   warps 8-15   epilogue, two halves of four warps (one per TMEM lane quarter): half h folds
-//                groups 2h and 2h+1 of every span -- tcgen05.ld of the partials, sum of the T
-//                terms, scale/zero fold into fp32 registers -- and at the tile end writes its
-//                half of the coarse values; the selection warp adds the halves
+//                planes 2h, 2h+1 of every span -- tcgen05.ld of the partials, sum of the T terms,
+//                scale/zero fold into fp32 registers -- and at the tile end writes its half of
+//                the coarse values; the selection warp adds the halves
 // Every handoff is an mbarrier; every wait is bounded.
 #include "dh_common.cuh"
 #include "dh_internal.h"
@@ -52,7 +52,7 @@ namespace dh {
 namespace {
 
 constexpr int kTileRows = 128;
-constexpr int kThreads = 512;
+constexpr int kThreads = 512; // 16 warps
 constexpr int kTmemCols = 512;
 constexpr int kPkBytes = kTileRows * kSpanBytes; // 16 KB packed box per span
 constexpr int kSmemLimit8 = 232448;
@@ -62,26 +62,24 @@ constexpr int kRedPitch = 68;
 constexpr int kDqWarps = 4; // dequant warps (4-7); the epilogue is warps 8-15
 
 // Batch rows per launch MP in {16, 32}; x in T = 2 e4m3 terms; MMA N = T * MP.
-// Tensor memory: two span-sized A buffers (4 groups x 32 columns) and a ring of kD group-sized
-// accumulators (N columns).
+// The unit of MMA work is a whole span at N = 32 (kU = 1: 4 planes, 16 MMAs) and half a span
+// at N = 64 (kU = 2: planes 2u, 2u+1, 8 MMAs).  Tensor memory holds kSlots unit slots, each an
+// A buffer (32 columns of e4m3 per plane) and one N-column fp32 accumulator per plane; unit
+// q = kU span + u uses slot q % kSlots and is issued by that slot's own thread, so the issuers
+// of different slots run concurrently (a thread issuing tcgen05.mma is held ~57 cycles per
+// instruction; two threads overlap).  Both sizes give two slots.
 template <int MP> struct Cfg8 {
     static constexpr int T = 2;
     static constexpr int N = MP * T;
-    static constexpr int kAs = 2;                           // A buffers, one span each
-    static constexpr int kD = (kTmemCols - kAs * 128) / N;  // 8 at N = 32, 4 at N = 64
-    static constexpr int kDS = kD / 4;                      // span-sized accumulator sets
-    // when there are at least as many accumulator sets as A buffers, "span s accumulated"
-    // also means "A buffer of span s free": one commit serves both
-    static constexpr bool kAFromD = kDS >= kAs;
-    // accumulators go back to the MMA issuers per span when there are two or more sets (one
-    // wait per span), else per group (so the next span can start on a group already read)
-    static constexpr int kRel = kDS >= 2 ? 4 : 1;
-    static constexpr int kDrel = kD / kRel; // release barriers
-    static constexpr uint32_t kAcol = 0;
-    static constexpr uint32_t kDcol = kAs * 128;
+    static constexpr int kU = MP == 16 ? 1 : 2;             // units per span
+    static constexpr int kPP = 4 / kU;                      // planes per unit
+    static constexpr uint32_t kACols = 32 * kPP;
+    static constexpr uint32_t kSlotCols = kACols + kPP * N;
+    static constexpr int kSlotsFit = static_cast<int>(kTmemCols / kSlotCols);
+    static constexpr int kSlots = kSlotsFit > 2 ? 2 : kSlotsFit; // one issuer warp per slot
     static constexpr uint32_t kXBytes = N * 512;            // 4 planes x 128 k x N rows
     static constexpr uint32_t kStage = kPkBytes + kXBytes;  // multiple of 1024
-    static_assert(kD >= 4, "a span of accumulators must fit");
+    static_assert(kSlots == 2, "two unit slots must fit");
     static_assert(N % 16 == 0 && N <= 256, "MMA N out of range");
 };
 
@@ -191,9 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_x, const Tc8Params prm)
 {
     using C = Cfg8<MP>;
-    constexpr int N = C::N, T = C::T, kAs = C::kAs, kD = C::kD, kDS = C::kDS;
-    constexpr bool kAFromD = C::kAFromD;
-    constexpr int kRel = C::kRel, kDrel = C::kDrel;
+    constexpr int N = C::N, T = C::T, K = C::kSlots, kU = C::kU, kPP = C::kPP;
+    constexpr uint32_t kSlotCols = C::kSlotCols, kACols = C::kACols;
     constexpr int kRedHalf = MP * 2 * kRedPitch; // floats of one epilogue half's tile values
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,12 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *const inv_s = xs_s + NGt * MP;                                     // [MP]
     uint64_t *const bars = reinterpret_cast<uint64_t *>(inv_s + MP);
     uint64_t *const full = bars;              // [nstage] TMA -> dequant, MMA
-    uint64_t *const empty = full + nstage;    // [nstage] dequant (4 warps) + MMA -> TMA
-    uint64_t *const a_full = empty + nstage;  // [kAs]    dequant (4 warps) -> MMA, per span
-    uint64_t *const a_empty = a_full + kAs;   // [kAs]    MMA -> dequant (unless kAFromD)
-    uint64_t *const d_full = a_empty + kAs;   // [kDS]    MMA -> epilogue (+ dequant), per span
-    uint64_t *const d_empty = d_full + kDS;   // [kDrel]  epilogue -> MMA, per kRel groups
-    uint64_t *const fin = d_empty + kDrel;    // [1]      MMA drain before teardown
+    uint64_t *const empty = full + nstage;    // [nstage] dequant (4 warps) + MMA units -> TMA
+    uint64_t *const a_full = empty + nstage;  // [K]      dequant (4 warps) -> MMA, per unit
+    uint64_t *const d_full = a_full + K;      // [K]      MMA -> epilogue + dequant, per unit
+    uint64_t *const d_empty = d_full + K;     // [K]      epilogue -> MMA, per unit
+    uint64_t *const fin = d_empty + K;        // [1]      MMA drain before teardown
     uint64_t *const red_full = fin + 1;       // [1]      epilogue (8 warps) -> selection
     uint64_t *const red_free = red_full + 1;  // [1]      selection -> epilogue: `red` free
     uint64_t *const sz_full = red_free + 1;   // [2]      bulk copy -> epilogue: S, ZS of a tile
@@ -228,15 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_x);
         for (int i = 0; i < nstage; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kDqWarps + 1);
+            mbar_init(&empty[i], kDqWarps + kU); // and one commit per unit
         }
-        for (int i = 0; i < kAs; ++i) {
+        for (int i = 0; i < K; ++i) {
             mbar_init(&a_full[i], kDqWarps);
-            mbar_init(&a_empty[i], 1);
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kU == 1 ? 8 : 4); // the epilogue warps reading the unit
         }
-        for (int i = 0; i < kDS; ++i) mbar_init(&d_full[i], 1);
-        // per span: all eight epilogue warps; per group: the four warps of its half
-        for (int i = 0; i < kDrel; ++i) mbar_init(&d_empty[i], kRel == 4 ? 8 : 4);
         mbar_init(fin, 2);
         mbar_init(red_full, 8);
         mbar_init(red_free, 1);
@@ -301,53 +295,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1 || warp == 3) {
-        // ---------------- MMA issuers: one A handshake per span ----------------
+        // ---------------- MMA issuers: warps 1 and 3 own unit slots 0 and 1 ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc_f8(N);
-            constexpr bool kTwo = kDS >= 2 && kAs == 2;
-            const uint32_t who = warp == 1 ? 0u : 1u;
-            uint32_t s = 0, t = 0;
-            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+            const int slot = warp == 1 ? 0 : 1;
+            uint32_t s = 0;
+            for (int tile = first_tile; tile < prm.ntiles && !failed && slot < K; tile += tile_step) {
                 for (int span = 0; span < NG && !failed; ++span, ++s) {
-                    const uint32_t st = s % nstage, sa = s % kAs;
-                    if (kTwo ? ((s & 1u) != who) : (who != 0u)) { // the other issuer's span
-                        t += 4;
-                        continue;
-                    }
-                    if (!mbar_wait_bounded(&full[st], (s / nstage) & 1u, prm.timeout_flag) ||
-                        !mbar_wait_bounded(&a_full[sa], (s / kAs) & 1u, prm.timeout_flag)) {
-                        failed = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t xdesc =
-                        sw128_desc(smem_u32(stages + static_cast<size_t>(st) * C::kStage + kPkBytes));
-                    for (int q = 0; q < 4; ++q, ++t) {
-                        const uint32_t d = t % kD;
-                        if (q % kRel == 0) {
-                            const uint32_t r = t / kRel;
-                            if (!mbar_wait_bounded(&d_empty[r % kDrel], ((r / kDrel) & 1u) ^ 1u,
-                                                   prm.timeout_flag)) {
-                                failed = true;
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-                        const uint32_t d_tmem = tmem + C::kDcol + d * N;
-                        const uint32_t a_tmem = tmem + C::kAcol + sa * 128 + q * 32;
-                        // the descriptor's address field counts 16-byte units
-                        const uint64_t qdesc = xdesc + static_cast<uint64_t>(q * (N * 128) / 16);
-                        mma_ts_f8(d_tmem, a_tmem, qdesc, idesc, 0u);
+                    const uint32_t st = s % nstage;
 #pragma unroll
-                        for (int i = 1; i < 4; ++i)
-                            mma_ts_f8(d_tmem, a_tmem + i * 8, qdesc + static_cast<uint64_t>(i * 2),
-                                      idesc, 1u);
+                    for (int u = 0; u < kU; ++u) {
+                        const uint32_t q = kU * s + u;
+                        if (q % K != static_cast<uint32_t>(slot)) continue;
+                        const uint32_t use = q / K; // this slot's use count
+                        if (!mbar_wait_bounded(&full[st], (s / nstage) & 1u, prm.timeout_flag) ||
+                            !mbar_wait_bounded(&a_full[slot], use & 1u, prm.timeout_flag) ||
+                            !mbar_wait_bounded(&d_empty[slot], (use & 1u) ^ 1u, prm.timeout_flag)) {
+                            failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_tmem = tmem + slot * kSlotCols;
+                        const uint32_t d_tmem = a_tmem + kACols;
+                        const uint64_t xdesc = sw128_desc(
+                            smem_u32(stages + static_cast<size_t>(st) * C::kStage + kPkBytes));
+#pragma unroll
+                        for (int g = 0; g < kPP; ++g) {
+                            const int plane = kPP * u + g;
+                            // the descriptor's address field counts 16-byte units
+                            const uint64_t qdesc = xdesc + static_cast<uint64_t>(plane * (N * 128) / 16);
+                            mma_ts_f8(d_tmem + g * N, a_tmem + g * 32, qdesc, idesc, 0u);
+#pragma unroll
+                            for (int i = 1; i < 4; ++i)
+                                mma_ts_f8(d_tmem + g * N, a_tmem + g * 32 + i * 8,
+                                          qdesc + static_cast<uint64_t>(i * 2), idesc, 1u);
+                        }
+                        // a commit takes an issue slot like an MMA: one per consumer
+                        mma_commit(&d_full[slot]);
+                        mma_commit(&empty[st]);
                     }
-                    if (failed) break;
-                    // a commit takes an issue slot like an MMA: one per consumer per span
-                    mma_commit(&d_full[s % kDS]);
-                    if (!kAFromD) mma_commit(&a_empty[sa]);
-                    mma_commit(&empty[st]);
                 }
             }
             mma_commit(fin);
@@ -360,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t s = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
             for (int span = 0; span < NG; ++span, ++s) {
-                const uint32_t st = s % nstage, sa = s % kAs;
+                const uint32_t st = s % nstage;
                 if (!warp_wait(&full[st], (s / nstage) & 1u, prm.timeout_flag)) {
                     failed = true;
                     break;
@@ -378,38 +364,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
-                // A buffer sa is free once the MMAs of span s - kAs completed
-                const bool a_free =
-                    kAFromD ? (s < static_cast<uint32_t>(kAs) ||
-                               warp_wait(&d_full[(s - kAs) % kDS], ((s - kAs) / kDS) & 1u,
-                                         prm.timeout_flag))
-                            : warp_wait(&a_empty[sa], ((s / kAs) & 1u) ^ 1u, prm.timeout_flag);
-                if (!a_free) {
-                    failed = true;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t abuf = tmem + lane_base + C::kAcol + sa * 128;
-                uint32_t r0[32], r1[32];
+                // the span's units: their planes into the A buffer of slot q % K, free once that
+                // slot's previous unit (q - K) has been accumulated
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    r0[i] = deq4_e4m3<0>(w[i]);
-                    r1[i] = deq4_e4m3<1>(w[i]);
-                }
-                tmem_st_x32(abuf, r0);
-                tmem_st_x32(abuf + 32, r1);
-                // a tcgen05.st reads its registers at issue: r0 and r1 are free again
+                for (int u = 0; u < kU; ++u) {
+                    const uint32_t q = kU * s + u, slot = q % K, use = q / K;
+                    if (use > 0 &&
+                        !warp_wait(&d_full[slot], (use - 1) & 1u, prm.timeout_flag)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t abuf = tmem + lane_base + slot * kSlotCols;
+                    uint32_t r0[32], r1[32];
+                    // planes kPP u .. kPP u + kPP - 1, two at a time (a tcgen05.st reads its
+                    // registers at issue: r0 and r1 are free again after it)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    r0[i] = deq4_e4m3<2>(w[i]);
-                    r1[i] = deq4_e4m3<3>(w[i]);
+                    for (int pp = 0; pp < kPP; pp += 2) {
+                        const int plane = kPP * u + pp;
+                        if (plane == 0) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                r0[i] = deq4_e4m3<0>(w[i]);
+                                r1[i] = deq4_e4m3<1>(w[i]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                r0[i] = deq4_e4m3<2>(w[i]);
+                                r1[i] = deq4_e4m3<3>(w[i]);
+                            }
+                        }
+                        tmem_st_x32(abuf + pp * 32, r0);
+                        tmem_st_x32(abuf + pp * 32 + 32, r1);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[slot]);
                 }
-                tmem_st_x32(abuf + 64, r0);
-                tmem_st_x32(abuf + 96, r1);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[sa]);
+                if (failed) break;
             }
         }
     } else if (warp >= 4 + kDqWarps) {
@@ -454,40 +448,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s2[gl] = (((2 * h + gl) & 1) ? 32.0f : 128.0f) * sv;
                     sz[gl] = sv - zv;
                 }
-                // one commit per span: all four groups' partials are in tensor memory
-                const uint32_t sp = t / 4;
-                if (!warp_wait(&d_full[sp % kDS], (sp / kDS) & 1u, prm.timeout_flag)) {
+                // the unit holding this half's two groups (planes 2h, 2h+1) of the span
+                const uint32_t q = kU * (t / 4) + (kU == 1 ? 0 : h), slot = q % K, use = q / K;
+                if (!warp_wait(&d_full[slot], use & 1u, prm.timeout_flag)) {
                     failed = true;
                     break;
                 }
                 tc_fence_after();
-                // the half's 2 * CH chunks, two per tcgen05 wait (64 registers)
+                // the half's first accumulator within the unit
+                const uint32_t dcol = tmem + lane_base + slot * kSlotCols + kACols +
+                                      (kU == 1 ? 2 * h : 0) * N;
+                // the unit's 2 * CH chunks, two per tcgen05 wait (64 registers)
 #pragma unroll
                 for (int wb = 0; wb < CH; ++wb) {
                     float v[2][T][16];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int k = 2 * wb + u, gl = k / CH, c = k % CH;
-                        const uint32_t d = (t + 2 * h + gl) % kD;
 #pragma unroll
                         for (int tt = 0; tt < T; ++tt)
-                            tmem_ld_x16(tmem + lane_base + C::kDcol + d * N + tt * MP + c * 16,
-                                        v[u][tt]);
+                            tmem_ld_x16(dcol + gl * N + tt * MP + c * 16, v[u][tt]);
                     }
                     tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (kRel == 1) {
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int k = 2 * wb + u;
-                                if (k % CH == CH - 1)
-                                    mbar_arrive(&d_empty[(t + 2 * h + k / CH) % kDrel]);
-                            }
-                        } else if (wb == CH - 1) {
-                            mbar_arrive(&d_empty[(t / 4) % kDrel]); // the span's set, read
-                        }
+                    if (wb == CH - 1) {
+                        // every partial of the unit is in registers: the slot goes back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&d_empty[slot]);
                     }
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
