@@ -201,6 +201,44 @@ const char *dh_last_error(void);
 /* ABI version: (major << 16) | minor. */
 int dh_version(void);
 
+/*
+ * Vocabulary-parallel head: each rank holds rows [vocab_offset, vocab_offset + Vs) of the
+ * head (its own packed/S/ZS and bf16 rows) and the result equals the unsharded dh_forward bit
+ * for bit.  The pages deploy the head as per-rank vocabulary shards
+ * (radiance_drafthead.py, _apply_head_int2 on a vocab-parallel lm_head); the exchange between
+ * the steps below is the caller's (two all-gathers of M x RERANK entries per rank).
+ *
+ * 1. dh_shard_candidates: the shard's coarse pass, block top-KCAND and top-RERANK of its own
+ *    candidates.  out_val [M, rerank] fp32 coarse values and out_idx [M, rerank] int32 GLOBAL
+ *    vocabulary ids (local row + vocab_offset), in rank order (value descending, lower id
+ *    first).
+ *    vocab_offset must be a multiple of 64 (the selection blocks then coincide with the
+ *    unsharded head's) and rerank must not exceed the shard's valid candidates.  Workspace:
+ *    dh_workspace_bytes(M, H, Vs, kcand, rerank).  Status codes as dh_forward.
+ *    Because every shard's top-RERANK contains every global top-RERANK candidate it owns, the
+ *    global top-RERANK of all shards' lists is the unsharded selection.
+ * 2. dh_shard_rerank: every rank passes the gathered lists all_val/all_idx [M, ncand_all]
+ *    (ncand_all = P x rerank; any order, -1 ids ignored, ids distinct).  Writes the global
+ *    top-RERANK ids to sel_idx [M, rerank] in rank order (identical on every rank: step 3
+ *    merges position by position) and their exact logits
+ *    x . W[id] to exact [M, rerank] for the ids this shard owns, -inf for the others.
+ *    W_shard [Vs, H] bf16 holds the shard's rows.  Workspace:
+ *    dh_shard_rerank_workspace_bytes(M, ncand_all, rerank) (0 = invalid sizes).
+ * 3. dh_shard_topk: exact_parts [P, M, rerank] (every rank's `exact`, gathered) merged by
+ *    max, then idx/logit [M, topk] exactly as dh_forward returns them.
+ */
+int dh_shard_candidates(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                        const uint16_t *zeros, int M, int H, int Vs, long long vocab_offset,
+                        int kcand, int rerank, float *out_val, int32_t *out_idx,
+                        void *workspace, size_t ws_bytes, void *stream);
+size_t dh_shard_rerank_workspace_bytes(int M, long long ncand_all, int rerank);
+int dh_shard_rerank(const uint16_t *x, const uint16_t *W_shard, int M, int H, int Vs,
+                    long long vocab_offset, const float *all_val, const int32_t *all_idx,
+                    long long ncand_all, int rerank, int32_t *sel_idx, float *exact,
+                    void *workspace, size_t ws_bytes, void *stream);
+int dh_shard_topk(const float *exact_parts, const int32_t *sel_idx, int P, int M, int rerank,
+                  int topk, int32_t *idx, float *logit, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

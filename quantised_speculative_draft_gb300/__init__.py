@@ -21,8 +21,9 @@ __all__ = [
     "build", "DHError", "dh_quantize", "dh_workspace_bytes", "dh_forward", "dh_forward_debug",
     "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for", "dh_device_status",
     "dh_forward_launch_count", "dh_forward_noalloc", "NOALLOC_WORKSPACE_BYTES",
-    "dh_last_error", "dh_version", "DraftHead", "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16",
-    "NUM_STAGE_EVENTS", "library_path",
+    "dh_last_error", "dh_version", "DraftHead", "dh_shard_candidates",
+    "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_shard_topk",
+    "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16", "NUM_STAGE_EVENTS", "library_path",
 ]
 
 PATH_AUTO, PATH_WARP, PATH_TC, PATH_TC_BF16 = 0, 1, 2, 3
@@ -84,6 +85,15 @@ def _load():
         lib.dh_last_error.restype = ctypes.c_char_p
         lib.dh_version.argtypes = []
         lib.dh_version.restype = I
+        L = ctypes.c_longlong
+        lib.dh_shard_candidates.argtypes = [P, P, P, P, I, I, I, L, I, I, P, P, P, S, P]
+        lib.dh_shard_candidates.restype = I
+        lib.dh_shard_rerank_workspace_bytes.argtypes = [I, L, I]
+        lib.dh_shard_rerank_workspace_bytes.restype = S
+        lib.dh_shard_rerank.argtypes = [P, P, I, I, I, L, P, P, L, I, P, P, P, S, P]
+        lib.dh_shard_rerank.restype = I
+        lib.dh_shard_topk.argtypes = [P, P, I, I, I, I, P, P, P]
+        lib.dh_shard_topk.restype = I
         _lib = lib
         return lib
 
@@ -168,6 +178,39 @@ def dh_forward_noalloc(x, packed, scales, zeros, W, kcand, rerank, topk, idx, lo
     V = packed.shape[0]
     _check(_load().dh_forward_noalloc(_p(x), _p(packed), _p(scales), _p(zeros), _p(W), M, H, V,
                                       kcand, rerank, topk, _p(idx), _p(logit), _stream(stream)))
+
+
+def dh_shard_candidates(x, packed, scales, zeros, vocab_offset, kcand, rerank, out_val, out_idx,
+                        workspace, stream=None):
+    """A vocabulary shard's top-``rerank`` candidates: out_val/out_idx [M, rerank] (global ids)."""
+    M, H = x.shape
+    Vs = packed.shape[0]
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().dh_shard_candidates(_p(x), _p(packed), _p(scales), _p(zeros), M, H, Vs,
+                                       int(vocab_offset), kcand, rerank, _p(out_val),
+                                       _p(out_idx), _p(workspace), nbytes, _stream(stream)))
+
+
+def dh_shard_rerank_workspace_bytes(M: int, ncand_all: int, rerank: int) -> int:
+    return int(_load().dh_shard_rerank_workspace_bytes(M, ncand_all, rerank))
+
+
+def dh_shard_rerank(x, W_shard, vocab_offset, all_val, all_idx, rerank, sel_idx, exact,
+                    workspace, stream=None):
+    """Global top-``rerank`` of the gathered lists, exact logits of the ids this shard owns."""
+    M, H = x.shape
+    Vs = W_shard.shape[0]
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().dh_shard_rerank(_p(x), _p(W_shard), M, H, Vs, int(vocab_offset), _p(all_val),
+                                   _p(all_idx), all_val.shape[1], rerank, _p(sel_idx), _p(exact),
+                                   _p(workspace), nbytes, _stream(stream)))
+
+
+def dh_shard_topk(exact_parts, sel_idx, topk, idx, logit, stream=None):
+    """Merge the ranks' partial exact logits [P, M, rerank] and write the top-``topk``."""
+    P, M, R = exact_parts.shape
+    _check(_load().dh_shard_topk(_p(exact_parts), _p(sel_idx), P, M, R, topk, _p(idx), _p(logit),
+                                 _stream(stream)))
 
 
 def dh_set_coarse_path(path: int) -> int:

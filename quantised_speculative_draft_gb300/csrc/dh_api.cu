@@ -94,7 +94,7 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     L.rows = L.Mpad_w > L.Npad ? L.Mpad_w : L.Npad;
     L.nblk = (V + kBlockN - 1) / kBlockN;
     L.ncand = L.nblk * kcand;
-    select_plan(M, L.ncand, kcand, rerank, &L.passes, &L.scratch_entries);
+    select_plan(M, L.ncand, kcand, rerank, true, &L.passes, &L.scratch_entries);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -161,15 +161,24 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
                  const uint16_t *zeros, const uint16_t *W, int M, int H, int V, int kcand,
                  int rerank, int topk, int32_t *idx, float *logit, void *workspace,
                  size_t ws_bytes, float *coarse, float *cand_val, int32_t *cand_idx,
-                 int32_t *sel_idx, float *sel_exact, void *const *events, cudaStream_t stream)
+                 int32_t *sel_idx, float *sel_exact, void *const *events, cudaStream_t stream,
+                 float *sel_val = nullptr, int id_offset = 0, bool candidates_only = false)
 {
-    if (!x || !packed || !scales || !zeros || !W || !idx || !logit || !workspace)
+    // candidates_only: stop after the top-R selection (a vocabulary shard's local candidates,
+    // indices offset by id_offset, values into sel_val); W, idx and logit are not used
+    if (candidates_only) {
+        if (!x || !packed || !scales || !zeros || !sel_idx || !sel_val || !workspace)
+            return fail(DH_ERR_NULL, "a required pointer is NULL");
+    } else if (!x || !packed || !scales || !zeros || !W || !idx || !logit || !workspace) {
         return fail(DH_ERR_NULL, "a required pointer is NULL");
-    int rc = check_shapes(M, H, V, kcand, rerank, topk);
+    }
+    int rc = check_shapes(M, H, V, kcand, rerank, candidates_only ? 1 : topk);
     if (rc != DH_OK) return rc;
-    const void *ptrs[] = {x, packed, scales, zeros, W, idx, logit, workspace};
+    const void *ptrs[] = {x, packed, scales, zeros, workspace};
     for (const void *p : ptrs)
         if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    if (!candidates_only && (!aligned16(W) || !aligned16(idx) || !aligned16(logit)))
+        return fail(DH_ERR_ALIGN, "W, idx or logit is not 16-byte aligned");
     const Layout L = layout_for(M, H, V, kcand, rerank);
     if (ws_bytes < L.total)
         return fail(DH_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
@@ -237,11 +246,12 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
                     cudaGetErrorString(err));
     if (!rec(2)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     err = launch_select(cval, cidx, M, L.ncand, kcand, rerank, sv, si, L.scratch_entries,
-                        counters + kSelDoneOffset, sel, stream);
+                        counters + kSelDoneOffset, true, sel, sel_val, id_offset, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
+    if (candidates_only) return ok();
     if (!rec(3)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     err = launch_rerank_topk(x, W, M, H, V, sel, rerank, ex, counters + kRowDoneOffset, topk,
-                             idx, logit, stream);
+                             idx, logit, 0, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));
     if (!rec(4)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     if (!rec(5)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
@@ -438,6 +448,100 @@ const char *dh_last_error(void)
 int dh_version(void)
 {
     return (1 << 16) | 0;
+}
+
+
+// ---- vocabulary-parallel head ------------------------------------------------------------
+
+int dh_shard_candidates(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                        const uint16_t *zeros, int M, int H, int Vs, long long vocab_offset,
+                        int kcand, int rerank, float *out_val, int32_t *out_idx,
+                        void *workspace, size_t ws_bytes, void *stream)
+{
+    if (vocab_offset < 0 || vocab_offset % kBlockN != 0)
+        return fail(DH_ERR_SHAPE, "vocab_offset=%lld is not a non-negative multiple of %d",
+                    vocab_offset, kBlockN);
+    if (Vs >= 1 && vocab_offset + Vs > 0x7FFFFFFFLL)
+        return fail(DH_ERR_SHAPE, "vocab_offset + Vs exceeds the 32-bit index range");
+    return forward_impl(x, packed, scales, zeros, nullptr, M, H, Vs, kcand, rerank, 1, nullptr,
+                        nullptr, workspace, ws_bytes, nullptr, nullptr, nullptr, out_idx, nullptr,
+                        nullptr, static_cast<cudaStream_t>(stream), out_val,
+                        static_cast<int>(vocab_offset), true);
+}
+
+size_t dh_shard_rerank_workspace_bytes(int M, long long ncand_all, int rerank)
+{
+    if (M < 1 || M > kMaxM || ncand_all < 1 || rerank < 1 || rerank > kMaxRerank ||
+        rerank > ncand_all)
+        return 0;
+    int passes = 0;
+    long long entries = 0;
+    select_plan(M, ncand_all, 1, rerank, false, &passes, &entries);
+    // two ping-pong (value, index) buffers of `entries`, then the counters
+    return 4 * align256(static_cast<size_t>(entries) * 4) + align256(kNumCounters * 4);
+}
+
+int dh_shard_rerank(const uint16_t *x, const uint16_t *W_shard, int M, int H, int Vs,
+                    long long vocab_offset, const float *all_val, const int32_t *all_idx,
+                    long long ncand_all, int rerank, int32_t *sel_idx, float *exact,
+                    void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!x || !W_shard || !all_val || !all_idx || !sel_idx || !exact || !workspace)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (M < 1 || M > kMaxM) return fail(DH_ERR_SHAPE, "M=%d outside [1, %d]", M, kMaxM);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    if (Vs < 1) return fail(DH_ERR_SHAPE, "Vs=%d must be >= 1", Vs);
+    if (vocab_offset < 0 || vocab_offset + Vs > 0x7FFFFFFFLL)
+        return fail(DH_ERR_SHAPE, "vocab_offset=%lld out of range", vocab_offset);
+    if (ncand_all < 1 || rerank < 1 || rerank > kMaxRerank || rerank > ncand_all)
+        return fail(DH_ERR_SELECT, "rerank=%d outside [1, min(%lld, %d)]", rerank, ncand_all,
+                    kMaxRerank);
+    const void *ptrs[] = {x, W_shard, workspace};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    const size_t need = dh_shard_rerank_workspace_bytes(M, ncand_all, rerank);
+    if (ws_bytes < need)
+        return fail(DH_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
+    int passes = 0;
+    long long entries = 0;
+    select_plan(M, ncand_all, 1, rerank, false, &passes, &entries);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t eb = align256(static_cast<size_t>(entries) * 4);
+    float *sv[2] = {reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + eb)};
+    int32_t *si[2] = {reinterpret_cast<int32_t *>(ws + 2 * eb),
+                      reinterpret_cast<int32_t *>(ws + 3 * eb)};
+    int *counters = reinterpret_cast<int *>(ws + 4 * eb);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaMemsetAsync(counters, 0, kNumCounters * 4, st);
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "counter reset: %s", cudaGetErrorString(err));
+    // the global top-R over every shard's local candidates: the same on every rank
+    err = launch_select(all_val, all_idx, M, ncand_all, 1, rerank, sv, si, entries,
+                        counters + kSelDoneOffset, false, sel_idx, nullptr, 0, st);
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
+    // exact values of the ids this shard owns; the others get -inf
+    err = launch_rerank_topk(x, W_shard, M, H, Vs, sel_idx, rerank, exact,
+                             counters + kRowDoneOffset, 0, nullptr, nullptr,
+                             static_cast<int>(vocab_offset), st);
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));
+    return ok();
+}
+
+int dh_shard_topk(const float *exact_parts, const int32_t *sel_idx, int P, int M, int rerank,
+                  int topk, int32_t *idx, float *logit, void *stream)
+{
+    if (!exact_parts || !sel_idx || !idx || !logit)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (P < 1) return fail(DH_ERR_ARG, "P=%d must be >= 1", P);
+    if (M < 1 || M > kMaxM) return fail(DH_ERR_SHAPE, "M=%d outside [1, %d]", M, kMaxM);
+    if (rerank < 1 || rerank > kMaxRerank)
+        return fail(DH_ERR_SELECT, "rerank=%d outside [1, %d]", rerank, kMaxRerank);
+    if (topk < 1 || topk > rerank)
+        return fail(DH_ERR_SELECT, "topk=%d outside [1, rerank=%d]", topk, rerank);
+    cudaError_t err = launch_merge_topk(exact_parts, sel_idx, P, M, rerank, topk, idx, logit,
+                                        static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "merge launch: %s", cudaGetErrorString(err));
+    return ok();
 }
 
 } // extern "C"

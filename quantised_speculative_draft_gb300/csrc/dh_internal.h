@@ -78,20 +78,29 @@ cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream);
 int tc_npad(int M);
 int tc_launches(int M); // coarse-pass launches of the tcgen05 path
 
-// Top-R selection over candidate lists.  Returns the number of passes it will take and the
+// Top-R selection over candidate lists.  `blocks`: the lists are the coarse pass's per-block
+// lists (rank-ordered, KCAND per 64-row block), which allows the one-launch path; otherwise a
+// generic radix selection runs.  select_plan returns the number of passes it will take and the
 // scratch entries it needs (two ping-pong buffers of `scratch_entries` (val, idx) pairs).
-void select_plan(int M, long long ncand, int kcand, int R, int *passes,
+// launch_select writes the R best indices plus id_offset to sel_idx [M, R] (-1 when empty) and,
+// with sel_val != null, their values.
+void select_plan(int M, long long ncand, int kcand, int R, bool blocks, int *passes,
                  long long *scratch_entries);
 cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M, long long ncand,
                           int kcand, int R, float *scratch_val[2], int32_t *scratch_idx[2],
-                          long long scratch_entries, int *row_cnt, int32_t *sel_idx,
-                          cudaStream_t stream);
+                          long long scratch_entries, int *row_cnt, bool blocks,
+                          int32_t *sel_idx, float *sel_val, int id_offset, cudaStream_t stream);
 
-// Exact rerank of the selected rows and, fused (last CTA per row), the per-row top-k.
-// row_done: M zeroed counters.
+// Exact rerank of the selected rows and, fused (last CTA per row), the per-row top-k (topk 0:
+// none).  W holds rows [id_offset, id_offset + V) of the head; selected ids outside that range
+// get -inf.  row_done: M zeroed counters.
 cudaError_t launch_rerank_topk(const uint16_t *x, const uint16_t *W, int M, int H, int V,
                                const int32_t *sel_idx, int R, float *ex, int *row_done, int topk,
-                               int32_t *out_idx, float *out_logit, cudaStream_t stream);
+                               int32_t *out_idx, float *out_logit, int id_offset,
+                               cudaStream_t stream);
+// Per-rank partial exact values parts [P, M, R] merged by max, then the per-row top-k.
+cudaError_t launch_merge_topk(const float *parts, const int32_t *sel_idx, int P, int M, int R,
+                              int topk, int32_t *out_idx, float *out_logit, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,

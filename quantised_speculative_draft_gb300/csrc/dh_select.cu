@@ -25,16 +25,22 @@ __device__ __forceinline__ unsigned long long rank_key(float v, int idx)
 // a5: top-R of one chunk of a row's candidates by MSB-first radix selection on rank_key.
 // grid (P, M); chunk p of row m covers entries [p CH, min(n_in, (p+1) CH)).  Writes the
 // chunk's R best (unordered) to out[(m P + p) R + j]; a chunk with fewer valid entries pads
-// with (-inf, -1).  With final_idx != null (P == 1) it writes the indices to final_idx[m R + j].
+// with (-inf, -1).  With final_idx != null (P == 1) it writes the R best in rank order (value
+// descending, lower index first; a shared-memory sort makes the order deterministic): the
+// indices plus id_offset to final_idx[m R + j] (-1 for empty slots) and, with
+// final_val != null, the values to final_val[m R + j].
 // ----------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSelThreads) topr_kernel(const float *__restrict__ in_val,
                                                            const int32_t *__restrict__ in_idx,
                                                            long long stride_in, long long n_in,
                                                            int R, float *__restrict__ out_val,
                                                            int32_t *__restrict__ out_idx,
-                                                           int32_t *__restrict__ final_idx)
+                                                           int32_t *__restrict__ final_idx,
+                                                           float *__restrict__ final_val,
+                                                           int id_offset)
 {
     __shared__ unsigned long long keys[kSelectChunk];
+    __shared__ unsigned long long outk[kMaxRerank]; // the final pass's R best, sorted
     __shared__ uint32_t hist[256];
     __shared__ unsigned long long s_prefix, s_mask;
     __shared__ int s_needed, s_eq, s_nvalid, s_count;
@@ -136,30 +142,55 @@ __global__ void __launch_bounds__(kSelThreads) topr_kernel(const float *__restri
     // nvalid, since prefix = mask = 0)
     float *const ov = out_val + (static_cast<long long>(m) * P + p) * R;
     int32_t *const oi = out_idx + (static_cast<long long>(m) * P + p) * R;
-    int32_t *const fi = final_idx ? final_idx + static_cast<long long>(m) * R : nullptr;
     for (int i = threadIdx.x; i < kSelectChunk; i += blockDim.x) {
         const unsigned long long k = keys[i];
         if (k != 0 && (k & mask) >= prefix) {
             const int slot = atomicAdd(&s_count, 1);
             if (slot < R) {
-                const int id = static_cast<int>(~static_cast<uint32_t>(k));
-                if (fi) {
-                    fi[slot] = id;
+                if (final_idx) {
+                    outk[slot] = k;
                 } else {
                     ov[slot] = f32_from_order_key(static_cast<uint32_t>(k >> 32));
-                    oi[slot] = id;
+                    oi[slot] = static_cast<int>(~static_cast<uint32_t>(k));
                 }
             }
         }
     }
     __syncthreads();
-    for (int j = s_count + threadIdx.x; j < R; j += blockDim.x) {
-        if (fi) {
-            fi[j] = -1;
-        } else {
+    const int got = s_count < R ? s_count : R;
+    if (!final_idx) {
+        for (int j = got + threadIdx.x; j < R; j += blockDim.x) {
             ov[j] = -INFINITY;
             oi[j] = -1;
         }
+        return;
+    }
+    // final pass: sort the R best (bitonic, descending) so that the output is in rank order
+    int n2 = 1;
+    while (n2 < R) n2 <<= 1;
+    for (int j = got + threadIdx.x; j < n2; j += blockDim.x) outk[j] = 0ull;
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const unsigned long long a = outk[i], b = outk[j];
+                    if (desc ? (a < b) : (a > b)) {
+                        outk[i] = b;
+                        outk[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    int32_t *const fi = final_idx + static_cast<long long>(m) * R;
+    float *const fv = final_val ? final_val + static_cast<long long>(m) * R : nullptr;
+    for (int j = threadIdx.x; j < R; j += blockDim.x) {
+        const unsigned long long k = outk[j];
+        fi[j] = k ? static_cast<int>(~static_cast<uint32_t>(k)) + id_offset : -1;
+        if (fv) fv[j] = k ? f32_from_order_key(static_cast<uint32_t>(k >> 32)) : -INFINITY;
     }
 }
 
@@ -257,7 +288,7 @@ __device__ void cta_top32(const unsigned long long *keys, int n, unsigned long l
 __global__ void __launch_bounds__(kRowSelThreads) select_rows_kernel(
     const float *__restrict__ cand_val, const int32_t *__restrict__ cand_idx, long long ncand,
     int nblk, int kcand, int R, unsigned long long *__restrict__ partial, int *__restrict__ row_cnt,
-    int32_t *__restrict__ sel_idx)
+    int32_t *__restrict__ sel_idx, float *__restrict__ sel_val, int id_offset)
 {
     __shared__ unsigned long long keys[kRowSelR * kBlockN]; // 2048: the largest candidate set
     __shared__ unsigned long long lists[4][32];
@@ -319,7 +350,10 @@ __global__ void __launch_bounds__(kRowSelThreads) select_rows_kernel(
     if (threadIdx.x < R) {
         const unsigned long long key = lists[0][threadIdx.x];
         sel_idx[static_cast<long long>(m) * R + threadIdx.x] =
-            key ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
+            key ? static_cast<int>(~static_cast<uint32_t>(key)) + id_offset : -1;
+        if (sel_val)
+            sel_val[static_cast<long long>(m) * R + threadIdx.x] =
+                key ? f32_from_order_key(static_cast<uint32_t>(key >> 32)) : -INFINITY;
     }
 }
 
@@ -343,18 +377,22 @@ bool row_select_fits(long long ncand, int kcand, int R)
 // ----------------------------------------------------------------------------------------
 constexpr int kRerankThreads = 256;
 
+__device__ void sort_write_topk(unsigned long long *k, int n2, int topk, int32_t *oidx,
+                                float *ologit);
+
 __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, int H, int V,
     const int32_t *__restrict__ sel_idx, int R, float *__restrict__ ex,
     int *__restrict__ row_done, int topk, int32_t *__restrict__ out_idx,
-    float *__restrict__ out_logit)
+    float *__restrict__ out_logit, int id_offset)
 {
     __shared__ double part[kRerankThreads / 32];
     __shared__ unsigned long long k[kMaxRerank];
     __shared__ int s_last;
     const long long pair = blockIdx.x;
     const int m = static_cast<int>(pair / R);
-    const int n = sel_idx[pair];
+    const int gid = sel_idx[pair];
+    const int n = gid >= 0 ? gid - id_offset : -1; // row of W (a shard starts at id_offset)
     const int tid = threadIdx.x, lane = tid & 31;
 
     float a0 = 0.f, a1 = 0.f;
@@ -389,7 +427,7 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
         s_last = atomicAdd(&row_done[m], 1) == R - 1;
     }
     __syncthreads();
-    if (!s_last) return;
+    if (!s_last || topk == 0) return;
     __threadfence();
 
     // this CTA finished row m last: top-k of its R reranked entries (bitonic, descending)
@@ -399,14 +437,55 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
         unsigned long long key = 0;
         if (i < R) {
             const int id = __ldcg(sel_idx + static_cast<long long>(m) * R + i);
-            if (id >= 0 && id < V) key = rank_key(__ldcg(ex + static_cast<long long>(m) * R + i), id);
+            const int local = id >= 0 ? id - id_offset : -1;
+            if (local >= 0 && local < V)
+                key = rank_key(__ldcg(ex + static_cast<long long>(m) * R + i), id);
         }
         k[i] = key;
     }
     __syncthreads();
+    sort_write_topk(k, n2, topk, out_idx + static_cast<long long>(m) * topk,
+                    out_logit + static_cast<long long>(m) * topk);
+}
+
+// ----------------------------------------------------------------------------------------
+// Sharded head, last step: per-rank partial exact values of the R selected ids (each id is
+// owned by one rank, the others hold -inf) merged by max, then the row's top-k.  One CTA per
+// row.
+// ----------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRerankThreads) merge_topk_kernel(
+    const float *__restrict__ parts, const int32_t *__restrict__ sel_idx, int P, int M, int R,
+    int topk, int32_t *__restrict__ out_idx, float *__restrict__ out_logit)
+{
+    __shared__ unsigned long long k[kMaxRerank];
+    const int m = blockIdx.x;
+    int n2 = 1;
+    while (n2 < R) n2 <<= 1;
+    for (int i = threadIdx.x; i < n2; i += kRerankThreads) {
+        unsigned long long key = 0;
+        if (i < R) {
+            const int id = sel_idx[static_cast<long long>(m) * R + i];
+            float e = -INFINITY;
+            for (int p = 0; p < P; ++p)
+                e = fmaxf(e, parts[(static_cast<long long>(p) * M + m) * R + i]);
+            if (id >= 0 && e > -INFINITY) key = rank_key(e, id);
+        }
+        k[i] = key;
+    }
+    __syncthreads();
+    sort_write_topk(k, n2, topk, out_idx + static_cast<long long>(m) * topk,
+                    out_logit + static_cast<long long>(m) * topk);
+}
+
+// Sorts n2 (a power of two) keys in shared memory descending with the whole CTA and writes the
+// first topk as (index, value); empty keys give (-1, -inf).
+__device__ void sort_write_topk(unsigned long long *k, int n2, int topk, int32_t *oidx,
+                                float *ologit)
+{
+    const int tid = threadIdx.x;
     for (int size = 2; size <= n2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < n2; i += kRerankThreads) {
+            for (int i = tid; i < n2; i += blockDim.x) {
                 const int j = i ^ stride;
                 if (j > i) {
                     const bool desc = (i & size) == 0;
@@ -420,22 +499,20 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
             __syncthreads();
         }
     }
-    for (int t = tid; t < topk; t += kRerankThreads) {
+    for (int t = tid; t < topk; t += blockDim.x) {
         const unsigned long long key = k[t];
         const bool ok = key != 0;
-        out_idx[static_cast<long long>(m) * topk + t] =
-            ok ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
-        out_logit[static_cast<long long>(m) * topk + t] =
-            ok ? f32_from_order_key(static_cast<uint32_t>(key >> 32)) : -INFINITY;
+        oidx[t] = ok ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
+        ologit[t] = ok ? f32_from_order_key(static_cast<uint32_t>(key >> 32)) : -INFINITY;
     }
 }
 
 } // namespace
 
-void select_plan(int M, long long ncand, int kcand, int R, int *passes,
+void select_plan(int M, long long ncand, int kcand, int R, bool blocks, int *passes,
                  long long *scratch_entries)
 {
-    if (row_select_fits(ncand, kcand, R)) {
+    if (blocks && row_select_fits(ncand, kcand, R)) {
         // the partial lists: M x P x 32 keys of 8 bytes in the first value buffer
         *passes = 1;
         *scratch_entries = static_cast<long long>(M) * row_select_ctas(ncand, kcand) * 32 * 2;
@@ -458,16 +535,17 @@ void select_plan(int M, long long ncand, int kcand, int R, int *passes,
 
 cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M, long long ncand,
                           int kcand, int R, float *scratch_val[2], int32_t *scratch_idx[2],
-                          long long scratch_entries, int *row_cnt, int32_t *sel_idx,
-                          cudaStream_t stream)
+                          long long scratch_entries, int *row_cnt, bool blocks,
+                          int32_t *sel_idx, float *sel_val, int id_offset, cudaStream_t stream)
 {
     (void)scratch_entries;
-    if (row_select_fits(ncand, kcand, R)) {
+    if (blocks && row_select_fits(ncand, kcand, R)) {
         const int nblk = static_cast<int>(ncand / kcand);
         dim3 grid(static_cast<unsigned>(row_select_ctas(ncand, kcand)), static_cast<unsigned>(M));
         select_rows_kernel<<<grid, kRowSelThreads, 0, stream>>>(
             cand_val, cand_idx, ncand, nblk, kcand, R,
-            reinterpret_cast<unsigned long long *>(scratch_val[0]), row_cnt, sel_idx);
+            reinterpret_cast<unsigned long long *>(scratch_val[0]), row_cnt, sel_idx, sel_val,
+            id_offset);
         return cudaGetLastError();
     }
     const float *in_v = cand_val;
@@ -479,11 +557,11 @@ cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M,
         dim3 grid(static_cast<unsigned>(P), static_cast<unsigned>(M));
         if (P <= 1) {
             topr_kernel<<<grid, kSelThreads, 0, stream>>>(in_v, in_i, stride, n, R, nullptr,
-                                                          nullptr, sel_idx);
+                                                          nullptr, sel_idx, sel_val, id_offset);
             return cudaGetLastError();
         }
         topr_kernel<<<grid, kSelThreads, 0, stream>>>(in_v, in_i, stride, n, R, scratch_val[buf],
-                                                      scratch_idx[buf], nullptr);
+                                                      scratch_idx[buf], nullptr, nullptr, 0);
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
         in_v = scratch_val[buf];
@@ -494,13 +572,23 @@ cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M,
     }
 }
 
+cudaError_t launch_merge_topk(const float *parts, const int32_t *sel_idx, int P, int M, int R,
+                              int topk, int32_t *out_idx, float *out_logit, cudaStream_t stream)
+{
+    merge_topk_kernel<<<M, kRerankThreads, 0, stream>>>(parts, sel_idx, P, M, R, topk, out_idx,
+                                                        out_logit);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rerank_topk(const uint16_t *x, const uint16_t *W, int M, int H, int V,
                                const int32_t *sel_idx, int R, float *ex, int *row_done, int topk,
-                               int32_t *out_idx, float *out_logit, cudaStream_t stream)
+                               int32_t *out_idx, float *out_logit, int id_offset,
+                               cudaStream_t stream)
 {
     const unsigned blocks = static_cast<unsigned>(static_cast<long long>(M) * R);
     rerank_topk_kernel<<<blocks, kRerankThreads, 0, stream>>>(x, W, H, V, sel_idx, R, ex,
-                                                              row_done, topk, out_idx, out_logit);
+                                                              row_done, topk, out_idx, out_logit,
+                                                              id_offset);
     return cudaGetLastError();
 }
 
