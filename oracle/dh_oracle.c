@@ -22,6 +22,9 @@
  *   orc_block_topk     pinned: brute force full sort on tiny inputs, KC=64 special case
  *   orc_select_topr    pinned: brute force, R = all candidates special case
  *   orc_rerank         pinned: exact integer arithmetic on scaled bf16 values
+ *   orc_decode_e4m3    pinned: every finite code against torch's float8_e4m3fn conversion
+ *   orc_quantize_fp8   pinned: power-of-two row scales reduce it to orc_quantize
+ *   orc_rerank_fp8     pinned: power-of-two row scales reduce it to orc_rerank
  *   orc_exact_head     pinned: exact integer arithmetic; KC=64,R=V reduces forward to it
  */
 #include <stdint.h>
@@ -92,46 +95,98 @@ static float clampf(float v, float lo, float hi)
  * Q = H/4.  Optional outputs sc_out / zp_out expose the fp32 scale and zero point.
  * Returns 0, or -2 when H is not a multiple of 512 (whole groups in every quarter).
  */
+/* e4m3 (fp8, "fn" variant) from its definition: 1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent 0 is subnormal, m/8 * 2^-6.  The codes with every exponent and
+ * mantissa bit set (NaN in the format) are not given a special value: the page's decoder
+ * does not test for them either, and the synthetic fp8 weights never contain them. */
+static float e4m3_to_f32(uint8_t b)
+{
+    const int sgn = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (float)(sgn ? -mag : mag);
+}
+
+void orc_decode_e4m3(const uint8_t *b, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_f32(b[i]);
+}
+
+/* One row of fp32 weights -> its packed bytes, S and ZS (the page's per-group steps). */
+static void quantize_row(const float *row, int64_t H, uint8_t *q, uint8_t *packed_row,
+                         uint16_t *S_row, uint16_t *ZS_row, float *sc_row, float *zp_row)
+{
+    const int64_t NGt = H / GROUP, Q = H / 4;
+    for (int64_t gi = 0; gi < NGt; ++gi) {
+        float lo = row[gi * GROUP], hi = lo;
+        for (int t = 1; t < GROUP; ++t) {
+            float w = row[gi * GROUP + t];
+            if (w < lo) lo = w;
+            if (w > hi) hi = w;
+        }
+        float sc = (hi - lo) / LEVELS;
+        if (sc < 1e-8f) sc = 1e-8f;
+        float zp = clampf(round_half_even((-lo) / sc), 0.0f, LEVELS);
+        for (int t = 0; t < GROUP; ++t) {
+            float w = row[gi * GROUP + t];
+            float r = round_half_even(w / sc + zp);
+            q[gi * GROUP + t] = (uint8_t)clampf(r, 0.0f, LEVELS);
+        }
+        float s4 = BIAS * sc;
+        float zsc = zp * sc;
+        S_row[gi] = f32_to_bf16_rne(s4);
+        ZS_row[gi] = f32_to_bf16_rne(s4 + zsc);
+        if (sc_row) sc_row[gi] = sc;
+        if (zp_row) zp_row[gi] = zp;
+    }
+    for (int64_t j = 0; j < Q; ++j)
+        packed_row[j] = (uint8_t)(q[j] | (q[Q + j] << 2) | (q[2 * Q + j] << 4) | (q[3 * Q + j] << 6));
+}
+
 int orc_quantize(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint16_t *S,
                  uint16_t *ZS, float *sc_out, float *zp_out)
 {
     if (H <= 0 || H % 512 != 0 || V <= 0) return -2;
     const int64_t NGt = H / GROUP, Q = H / 4;
     uint8_t *q = (uint8_t *)malloc((size_t)H);
-    if (!q) return -1;
+    float *row = (float *)malloc((size_t)H * sizeof(float));
+    if (!q || !row) {
+        free(q);
+        free(row);
+        return -1;
+    }
     for (int64_t n = 0; n < V; ++n) {
-        const uint16_t *row = W + n * H;
-        for (int64_t gi = 0; gi < NGt; ++gi) {
-            float lo = bf16_to_f32(row[gi * GROUP]), hi = lo;
-            for (int t = 1; t < GROUP; ++t) {
-                float w = bf16_to_f32(row[gi * GROUP + t]);
-                if (w < lo) lo = w;
-                if (w > hi) hi = w;
-            }
-            float sc = (hi - lo) / LEVELS;
-            if (sc < 1e-8f) sc = 1e-8f;
-            float zp = clampf(round_half_even((-lo) / sc), 0.0f, LEVELS);
-            for (int t = 0; t < GROUP; ++t) {
-                float w = bf16_to_f32(row[gi * GROUP + t]);
-                float r = round_half_even(w / sc + zp);
-                q[gi * GROUP + t] = (uint8_t)clampf(r, 0.0f, LEVELS);
-            }
-            float s4 = BIAS * sc;
-            float zsc = zp * sc;
-            S[n * NGt + gi] = f32_to_bf16_rne(s4);
-            ZS[n * NGt + gi] = f32_to_bf16_rne(s4 + zsc);
-            if (sc_out) sc_out[n * NGt + gi] = sc;
-            if (zp_out) zp_out[n * NGt + gi] = zp;
-        }
-        for (int64_t j = 0; j < Q; ++j)
-            packed[n * Q + j] = (uint8_t)(q[j] | (q[Q + j] << 2) | (q[2 * Q + j] << 4) |
-                                          (q[3 * Q + j] << 6));
+        for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
+        quantize_row(row, H, q, packed + n * Q, S + n * NGt, ZS + n * NGt,
+                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL);
     }
     free(q);
+    free(row);
     return 0;
 }
 
-/* Inverse of the quarter-split packing: codes[n, k] for k = plane*Q + j. */
+/* An fp8 head: e4m3 rows and a per-row fp32 scale.  The page widens the rows to fp32 and
+ * multiplies by the row's scale (one fp32 rounding) before the same per-group steps. */
+int orc_quantize_fp8(const uint8_t *W8, const float *wsc, int64_t V, int64_t H, uint8_t *packed,
+                     uint16_t *S, uint16_t *ZS)
+{
+    if (H <= 0 || H % 512 != 0 || V <= 0) return -2;
+    const int64_t NGt = H / GROUP, Q = H / 4;
+    uint8_t *q = (uint8_t *)malloc((size_t)H);
+    float *row = (float *)malloc((size_t)H * sizeof(float));
+    if (!q || !row) {
+        free(q);
+        free(row);
+        return -1;
+    }
+    for (int64_t n = 0; n < V; ++n) {
+        for (int64_t k = 0; k < H; ++k) row[k] = e4m3_to_f32(W8[n * H + k]) * wsc[n];
+        quantize_row(row, H, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL);
+    }
+    free(q);
+    free(row);
+    return 0;
+}
+
 void orc_unpack(const uint8_t *packed, int64_t V, int64_t H, uint8_t *codes)
 {
     const int64_t Q = H / 4;
@@ -315,6 +370,25 @@ void orc_rerank(const uint16_t *x, const uint16_t *W, int M, int64_t H, const in
             double s = 0.0;
             for (int64_t k = 0; k < H; ++k)
                 s += (double)bf16_to_f32(xr[k]) * (double)bf16_to_f32(wr[k]);
+            e[(int64_t)m * R + j] = s;
+        }
+}
+
+/* The page's fp8 rerank arm: weight k of row n is the fp32 product e4m3(b) * scale[n]; the
+ * exact logit sums x_k times that weight, here in fp64. */
+void orc_rerank_fp8(const uint16_t *x, const uint8_t *W8, const float *wsc, int M, int64_t H,
+                    const int32_t *idx, int R, double *e)
+{
+    for (int m = 0; m < M; ++m)
+        for (int j = 0; j < R; ++j) {
+            const int64_t n = idx[(int64_t)m * R + j];
+            const uint8_t *wr = W8 + n * H;
+            const uint16_t *xr = x + (int64_t)m * H;
+            double s = 0.0;
+            for (int64_t k = 0; k < H; ++k) {
+                const float w = e4m3_to_f32(wr[k]) * wsc[n];
+                s += (double)bf16_to_f32(xr[k]) * (double)w;
+            }
             e[(int64_t)m * R + j] = s;
         }
 }

@@ -78,6 +78,12 @@ def _load():
         lib.orc_topk.restype = None
         lib.orc_exact_head.argtypes = [P, P, I, I64, I64, P, I]
         lib.orc_exact_head.restype = None
+        lib.orc_decode_e4m3.argtypes = [P, I64, P]
+        lib.orc_decode_e4m3.restype = None
+        lib.orc_quantize_fp8.argtypes = [P, P, I64, I64, P, P, P]
+        lib.orc_quantize_fp8.restype = I
+        lib.orc_rerank_fp8.argtypes = [P, P, P, I, I64, P, I, P]
+        lib.orc_rerank_fp8.restype = None
         _lib = lib
         return lib
 
@@ -194,6 +200,54 @@ def topk(e: np.ndarray, idx: np.ndarray, k: int):
     out_val = np.empty((M, k), np.float64)
     _load().orc_topk(_ptr(e), _ptr(idx), M, R, k, _ptr(out_idx), _ptr(out_val))
     return out_idx, out_val
+
+
+def decode_e4m3(b: np.ndarray) -> np.ndarray:
+    """e4m3 codes (uint8) -> float32 values, from the format's definition."""
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    out = np.empty(b.shape, np.float32)
+    _load().orc_decode_e4m3(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def quantize_fp8(W8: np.ndarray, wsc: np.ndarray):
+    """An fp8 head (e4m3 rows [V, H] uint8, per-row fp32 scale [V]) -> (packed, S, ZS)."""
+    W8 = np.ascontiguousarray(W8, dtype=np.uint8)
+    wsc = np.ascontiguousarray(wsc, dtype=np.float32)
+    V, H = W8.shape
+    packed = np.empty((V, H // 4), np.uint8)
+    S = np.empty((V, H // GROUP), np.uint16)
+    ZS = np.empty((V, H // GROUP), np.uint16)
+    rc = _load().orc_quantize_fp8(_ptr(W8), _ptr(wsc), V, H, _ptr(packed), _ptr(S), _ptr(ZS))
+    if rc != 0:
+        raise ValueError(f"orc_quantize_fp8: status {rc}")
+    return packed, S, ZS
+
+
+def rerank_fp8(x: np.ndarray, W8: np.ndarray, wsc: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Exact fp64 logits [M, R] against fp8 rows: weight = fp32(e4m3 * row scale)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    W8 = np.ascontiguousarray(W8, dtype=np.uint8)
+    wsc = np.ascontiguousarray(wsc, dtype=np.float32)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    M, H = x.shape
+    R = idx.shape[1]
+    e = np.empty((M, R), np.float64)
+    _load().orc_rerank_fp8(_ptr(x), _ptr(W8), _ptr(wsc), M, H, _ptr(idx), R, _ptr(e))
+    return e
+
+
+def forward_fp8(x, packed, S, ZS, W8, wsc, kcand: int, rerank_n: int, k: int,
+                nthreads: int | None = None) -> dict:
+    """The draft-head path with the fp8 rerank arm (the coarse part is the same)."""
+    c = coarse(x, packed, S, ZS, nthreads)
+    cf = c.astype(np.float32)
+    cval, cidx, nvalid = block_topk(cf, kcand)
+    sel_idx, sel_val = select_topr(cval, cidx, rerank_n)
+    e = rerank_fp8(x, W8, wsc, sel_idx)
+    out_idx, out_val = topk(e, sel_idx, k)
+    return dict(coarse=c, coarse_f32=cf, cand_val=cval, cand_idx=cidx, sel_idx=sel_idx,
+                sel_val=sel_val, exact=e, idx=out_idx, logit=out_val)
 
 
 def exact_head(x: np.ndarray, W: np.ndarray, nthreads: int | None = None) -> np.ndarray:

@@ -341,3 +341,71 @@ def test_decision_gap_flags_a_planted_tie():
     assert set(res2["idx"][0].tolist()) <= {12, 77}
     assert res2["idx"][0, 0] == 12               # equal values -> lower index
     assert orc.decision_gaps(res2, 8, 1)[0] == 0.0
+
+
+# ------------------------------------------------------------------------------------------
+# fp8 head (e4m3 rows, per-row fp32 scale): decode, quantise, rerank
+# ------------------------------------------------------------------------------------------
+
+def _finite_e4m3_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    return codes[(codes & 0x7F) != 0x7F]           # 0x7F / 0xFF are NaN in e4m3fn
+
+
+def test_e4m3_decode_matches_torch_float8_for_every_finite_code():
+    torch = pytest.importorskip("torch")
+    codes = _finite_e4m3_codes()
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+    got = orc.decode_e4m3(codes)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))   # -0.0 included
+    # spot values from the format: largest finite, smallest subnormal, one
+    assert orc.decode_e4m3(np.array([0x7E, 0x01, 0x38], np.uint8)).tolist() == [448.0, 2.0**-9, 1.0]
+
+
+def _fp8_head(rng, V, H, pow2_scales):
+    codes = rng.choice(_finite_e4m3_codes(), size=(V, H)).astype(np.uint8)
+    if pow2_scales:
+        wsc = np.exp2(rng.integers(-12, -4, size=V)).astype(np.float32)
+    else:
+        wsc = (rng.uniform(0.5, 2.0, size=V) * 1e-3).astype(np.float32)
+    return codes, wsc
+
+
+def _as_bf16_bits(f32):
+    bits = np.asarray(f32, np.float32).view(np.uint32)
+    assert not (bits & 0xFFFF).any()                  # exactly representable in bf16
+    return (bits >> 16).astype(np.uint16)
+
+
+def test_fp8_quantise_and_rerank_with_power_of_two_scales_reduce_to_the_bf16_head():
+    """e4m3 has 4 significant bits, so e4m3 * 2^k is an exact bf16 value: the fp8 head is
+    then the bf16 head with those values, and both oracle paths must agree bit for bit."""
+    rng = np.random.default_rng(21)
+    V, H, M = 96, 1024, 3
+    codes, wsc = _fp8_head(rng, V, H, pow2_scales=True)
+    Wb = _as_bf16_bits(orc.decode_e4m3(codes) * wsc[:, None])
+    p8, S8, Z8 = orc.quantize_fp8(codes, wsc)
+    pb, Sb, Zb = orc.quantize(Wb)
+    assert np.array_equal(p8, pb) and np.array_equal(S8, Sb) and np.array_equal(Z8, Zb)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    idx = rng.integers(0, V, size=(M, 7)).astype(np.int32)
+    assert np.array_equal(orc.rerank_fp8(x, codes, wsc, idx), orc.rerank(x, Wb, idx))
+
+
+def test_fp8_rerank_rounds_each_weight_to_fp32_before_the_sum():
+    """General row scales: weight k is the fp32 product e4m3(b) * scale, as the page's
+    decoder computes it; the sum is checked against torch's float8 decode and numpy."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(22)
+    V, H, M = 40, 512, 2
+    codes, wsc = _fp8_head(rng, V, H, pow2_scales=False)
+    dec = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+    w32 = (dec * wsc[:, None]).astype(np.float32)                 # one fp32 rounding
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    idx = rng.integers(0, V, size=(M, 5)).astype(np.int32)
+    ref = np.einsum("mk,mjk->mj", bf2f(x).astype(np.float64), w32[idx].astype(np.float64))
+    np.testing.assert_allclose(orc.rerank_fp8(x, codes, wsc, idx), ref, rtol=1e-12, atol=1e-14)
+    # the fp32 rounding of the product matters: the fp64 product gives other sums
+    raw = np.einsum("mk,mjk->mj", bf2f(x).astype(np.float64),
+                    dec[idx].astype(np.float64) * wsc[idx][..., None].astype(np.float64))
+    assert not np.array_equal(orc.rerank_fp8(x, codes, wsc, idx), raw)
