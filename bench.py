@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--V", type=int, default=V_FULL,
                     help="vocabulary rows (smaller heads are for profiling captures only)")
     ap.add_argument("--sets", type=int, default=2, help="resident input sets rotated per step")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the fp8-head line")
     ap.add_argument("--profile", action="store_true",
                     help="only run warmup + steps forwards (no timing, no JSON): for ncu")
     return ap.parse_args()
@@ -158,6 +159,34 @@ class Inputs:
         self.ZS = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
         dh.dh_quantize(self.W, self.packed, self.S, self.ZS)
 
+    def call(self, M, ws, idx, logit):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND, RERANK, TOPK, idx,
+                      logit, ws)
+
+
+class Fp8Inputs:
+    """One resident input set of the fp8 head: e4m3 rows with per-row scales and their int2
+    packing (dh_quantize_fp8); the rerank reads the e4m3 rows."""
+
+    def __init__(self, seed, dev, max_m):
+        import torch
+        import quantised_speculative_draft_gb300 as dh
+        from quantised_speculative_draft_gb300 import synth
+        wl = synth.full(max_m)
+        self.x = synth.make_x(wl, seed, dev)
+        self.W8, self.rs = synth.make_w_fp8(wl, seed, dev)
+        V, H = self.W8.shape
+        self.packed = torch.empty(V, H // 4, dtype=torch.uint8, device=dev)
+        self.S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        self.ZS = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        dh.dh_quantize_fp8(self.W8, self.rs, self.packed, self.S, self.ZS)
+
+    def call(self, M, ws, idx, logit):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_fp8w(self.x[:M], self.packed, self.S, self.ZS, self.W8, self.rs, KCAND,
+                           RERANK, TOPK, idx, logit, ws)
+
 
 def make_outputs(M, dev, V=None):
     import torch
@@ -170,9 +199,7 @@ def make_outputs(M, dev, V=None):
 
 
 def fwd(sets, i, M, ws, idx, logit):
-    import quantised_speculative_draft_gb300 as dh
-    s = sets[i % len(sets)]
-    dh.dh_forward(s.x[:M], s.packed, s.S, s.ZS, s.W, KCAND, RERANK, TOPK, idx, logit, ws)
+    sets[i % len(sets)].call(M, ws, idx, logit)
 
 
 def time_graph(sets, M, steps, warmup, dist=None):
@@ -410,11 +437,32 @@ def run_ours(args):
                           "roofline": {"bound": r["bound"], "frac": r["frac"]},
                           "stages_us": {k: round(v, 2) for k, v in st.items()}})
 
+    cpu_inputs = host_copies(sets) if rank == 0 and world == 1 and not args.no_cpu_baseline \
+        else None
     pack = time_quantize(dev) if rank == 0 else None
+
+    fp8 = None
+    if rank == 0 and not args.no_fp8:
+        del sets
+        torch.cuda.empty_cache()
+        sets8 = [Fp8Inputs(seed, dev, M) for seed in range(args.sets)]
+        ms8, _, _ = time_graph(sets8, M, args.sweep_steps, 5)
+        n8 = 10
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s8 = sets8[0]
+        e0.record()
+        for _ in range(n8):
+            dh.dh_quantize_fp8(s8.W8, s8.rs, s8.packed, s8.S, s8.ZS)
+        e1.record()
+        torch.cuda.synchronize()
+        fp8 = {"workload": f"full-vocab fp8 head (e4m3 rows, per-row fp32 scale) M={M}",
+               "us_per_call": round(ms8 * 1e3 / args.sweep_steps, 2),
+               "quantize_us": round(e0.elapsed_time(e1) * 1e3 / n8, 1)}
+        del sets8
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        xb, pb, Sb, ZSb, Wb = host_copies(sets)
+        xb, pb, Sb, ZSb, Wb = cpu_inputs
         from oracle import oracle as orc
         orc.build()
         us, Vs = cpu_oracle_sample(xb, pb, Sb, ZSb, Wb, M, 4)
@@ -449,6 +497,7 @@ def run_ours(args):
             "clocks": clocks,
             "stages_us": {k: round(v, 2) for k, v in stages.items()},
             "pack": pack,
+            "fp8_head": fp8,
             "sweep": sweep,
         }
         print(json.dumps(line), flush=True)

@@ -239,6 +239,32 @@ int dh_shard_rerank(const uint16_t *x, const uint16_t *W_shard, int M, int H, in
 int dh_shard_topk(const float *exact_parts, const int32_t *sel_idx, int P, int M, int rerank,
                   int topk, int32_t *idx, float *logit, void *stream);
 
+/*
+ * fp8 head: the bf16 head weight replaced by e4m3 rows with one fp32 scale per row.
+ * Page: radiance_drafthead.py, _quantize_head_now (an fp8 lm_head's weight is pre-scaled by
+ * its per-row scale before the group statistics) and _rerank_exact (FP8 branch: the selected
+ * rows are dequantised to fp32 and dotted with x).
+ *
+ *   W_e4m3    [V, H]  u8: OCP e4m3 (float8_e4m3fn) codes, row n = vocabulary entry n; finite
+ *                     codes only (0x7F / 0xFF, the NaN codes, are not a weight)     (input)
+ *   row_scale [V]     fp32 scale of each row; weight w[n, k] = fp32(e4m3(W[n, k]) * row_scale[n]),
+ *                     the product rounded once to nearest even                     (input)
+ *
+ * dh_quantize_fp8 -- dh_quantize of those fp32 weights: the same group steps, outputs and
+ *   layout, bit-exact.  W_e4m3, packed, scales, zeros 16-byte aligned, row_scale 4-byte.
+ * dh_forward_fp8w -- dh_forward whose rerank scores against the fp8 rows: logit =
+ *   sum_k x[m, k] * w[idx, k] with w as above.  packed/scales/zeros are dh_quantize_fp8's
+ *   output; the coarse pass, selection, workspace (dh_workspace_bytes), ranking rules and
+ *   status codes are those of dh_forward.  The rerank reads H bytes per selected row instead
+ *   of 2H.
+ */
+int dh_quantize_fp8(const uint8_t *W_e4m3, const float *row_scale, int V, int H, uint8_t *packed,
+                    uint16_t *scales, uint16_t *zeros, void *stream);
+int dh_forward_fp8w(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                    const uint16_t *zeros, const uint8_t *W_e4m3, const float *row_scale, int M,
+                    int H, int V, int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                    void *workspace, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

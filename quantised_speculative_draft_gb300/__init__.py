@@ -22,7 +22,8 @@ __all__ = [
     "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for", "dh_device_status",
     "dh_forward_launch_count", "dh_forward_noalloc", "NOALLOC_WORKSPACE_BYTES",
     "dh_last_error", "dh_version", "DraftHead", "dh_shard_candidates",
-    "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_shard_topk",
+    "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_shard_topk", "dh_quantize_fp8",
+    "dh_forward_fp8w",
     "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16", "NUM_STAGE_EVENTS", "library_path",
 ]
 
@@ -94,6 +95,10 @@ def _load():
         lib.dh_shard_rerank.restype = I
         lib.dh_shard_topk.argtypes = [P, P, I, I, I, I, P, P, P]
         lib.dh_shard_topk.restype = I
+        lib.dh_quantize_fp8.argtypes = [P, P, I, I, P, P, P, P]
+        lib.dh_quantize_fp8.restype = I
+        lib.dh_forward_fp8w.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, S, P]
+        lib.dh_forward_fp8w.restype = I
         _lib = lib
         return lib
 
@@ -180,6 +185,25 @@ def dh_forward_noalloc(x, packed, scales, zeros, W, kcand, rerank, topk, idx, lo
                                       kcand, rerank, topk, _p(idx), _p(logit), _stream(stream)))
 
 
+def dh_quantize_fp8(W8, row_scale, packed, scales, zeros, stream=None):
+    """Quantise an fp8 head: W8 [V, H] e4m3 codes (uint8 or float8_e4m3fn), row_scale [V]
+    fp32; outputs as dh_quantize."""
+    V, H = W8.shape
+    _check(_load().dh_quantize_fp8(_p(W8), _p(row_scale), V, H, _p(packed), _p(scales),
+                                   _p(zeros), _stream(stream)))
+
+
+def dh_forward_fp8w(x, packed, scales, zeros, W8, row_scale, kcand, rerank, topk, idx, logit,
+                    workspace, stream=None):
+    """dh_forward with the rerank against the fp8 rows W8 [V, H] scaled by row_scale [V]."""
+    M, H = x.shape
+    V = packed.shape[0]
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().dh_forward_fp8w(_p(x), _p(packed), _p(scales), _p(zeros), _p(W8),
+                                   _p(row_scale), M, H, V, kcand, rerank, topk, _p(idx),
+                                   _p(logit), _p(workspace), nbytes, _stream(stream)))
+
+
 def dh_shard_candidates(x, packed, scales, zeros, vocab_offset, kcand, rerank, out_val, out_idx,
                         workspace, stream=None):
     """A vocabulary shard's top-``rerank`` candidates: out_val/out_idx [M, rerank] (global ids)."""
@@ -238,20 +262,33 @@ def dh_device_status(reset: bool = False) -> int:
 class DraftHead:
     """A quantised head ready for repeated forwards: owns packed/scales/zeros and a workspace.
 
-    The bf16 weight W stays owned by the caller and is kept by reference (the rerank reads it).
+    The head weight W stays owned by the caller and is kept by reference (the rerank reads
+    it): bf16 [V, H], or e4m3 codes [V, H] (uint8 or float8_e4m3fn) with ``row_scale`` [V]
+    fp32 for an fp8 head.
     """
 
-    def __init__(self, W, kcand: int = 8, rerank: int = 32, max_m: int = 128, stream=None):
+    def __init__(self, W, kcand: int = 8, rerank: int = 32, max_m: int = 128, stream=None,
+                 row_scale=None):
         import torch
-        if W.dtype != torch.bfloat16 or not W.is_cuda or not W.is_contiguous():
-            raise ValueError("W must be a contiguous bf16 CUDA tensor [V, H]")
-        self.W = W
+        fp8 = row_scale is not None
+        ok_dtype = W.dtype in (torch.uint8, torch.float8_e4m3fn) if fp8 else \
+            W.dtype == torch.bfloat16
+        if not ok_dtype or not W.is_cuda or not W.is_contiguous():
+            raise ValueError("W must be a contiguous CUDA tensor [V, H]: bf16, or e4m3 codes "
+                             "with row_scale")
+        if fp8 and (row_scale.dtype != torch.float32 or row_scale.shape != (W.shape[0],)
+                    or not row_scale.is_cuda or not row_scale.is_contiguous()):
+            raise ValueError("row_scale must be a contiguous fp32 CUDA tensor [V]")
+        self.W, self.row_scale = W, row_scale
         self.V, self.H = W.shape
         dev = W.device
         self.packed = torch.empty(self.V, self.H // 4, dtype=torch.uint8, device=dev)
         self.scales = torch.empty(self.V, self.H // GROUP, dtype=torch.bfloat16, device=dev)
         self.zeros = torch.empty(self.V, self.H // GROUP, dtype=torch.bfloat16, device=dev)
-        dh_quantize(W, self.packed, self.scales, self.zeros, stream)
+        if fp8:
+            dh_quantize_fp8(W, row_scale, self.packed, self.scales, self.zeros, stream)
+        else:
+            dh_quantize(W, self.packed, self.scales, self.zeros, stream)
         self.kcand, self.rerank = kcand, rerank
         self._ws = None
         self._ws_key = None
@@ -273,6 +310,10 @@ class DraftHead:
         M = x.shape[0]
         idx = torch.empty(M, topk, dtype=torch.int32, device=x.device)
         logit = torch.empty(M, topk, dtype=torch.float32, device=x.device)
-        dh_forward(x, self.packed, self.scales, self.zeros, self.W, self.kcand, self.rerank, topk,
-                   idx, logit, self.workspace(M), stream)
+        if self.row_scale is not None:
+            dh_forward_fp8w(x, self.packed, self.scales, self.zeros, self.W, self.row_scale,
+                            self.kcand, self.rerank, topk, idx, logit, self.workspace(M), stream)
+        else:
+            dh_forward(x, self.packed, self.scales, self.zeros, self.W, self.kcand, self.rerank,
+                       topk, idx, logit, self.workspace(M), stream)
         return idx, logit

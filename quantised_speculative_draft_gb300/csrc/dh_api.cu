@@ -157,12 +157,14 @@ int choose_path(int M, int H)
     return DH_PATH_WARP;
 }
 
+// W: the head's rows for the rerank, bf16 (w_scale null) or e4m3 with per-row fp32 scales.
 int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
-                 const uint16_t *zeros, const uint16_t *W, int M, int H, int V, int kcand,
+                 const uint16_t *zeros, const void *W, int M, int H, int V, int kcand,
                  int rerank, int topk, int32_t *idx, float *logit, void *workspace,
                  size_t ws_bytes, float *coarse, float *cand_val, int32_t *cand_idx,
                  int32_t *sel_idx, float *sel_exact, void *const *events, cudaStream_t stream,
-                 float *sel_val = nullptr, int id_offset = 0, bool candidates_only = false)
+                 float *sel_val = nullptr, int id_offset = 0, bool candidates_only = false,
+                 const float *w_scale = nullptr)
 {
     // candidates_only: stop after the top-R selection (a vocabulary shard's local candidates,
     // indices offset by id_offset, values into sel_val); W, idx and logit are not used
@@ -250,8 +252,8 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
     if (candidates_only) return ok();
     if (!rec(3)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
-    err = launch_rerank_topk(x, W, M, H, V, sel, rerank, ex, counters + kRowDoneOffset, topk,
-                             idx, logit, 0, stream);
+    err = launch_rerank_topk(x, W, w_scale, M, H, V, sel, rerank, ex, counters + kRowDoneOffset,
+                             topk, idx, logit, 0, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));
     if (!rec(4)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     if (!rec(5)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
@@ -322,7 +324,7 @@ int dh_quantize(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t 
     const void *ptrs[] = {W_bf16, packed, scales, zeros};
     for (const void *p : ptrs)
         if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
-    cudaError_t err = launch_quantize(W_bf16, V, H, packed, scales, zeros,
+    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, packed, scales, zeros,
                                       static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
     return ok();
@@ -342,6 +344,38 @@ int dh_forward(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
     return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
                         logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
                         nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int dh_quantize_fp8(const uint8_t *W_e4m3, const float *row_scale, int V, int H, uint8_t *packed,
+                    uint16_t *scales, uint16_t *zeros, void *stream)
+{
+    if (!W_e4m3 || !row_scale || !packed || !scales || !zeros)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (V < 1) return fail(DH_ERR_SHAPE, "V=%d must be >= 1", V);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    const void *ptrs[] = {W_e4m3, packed, scales, zeros};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    if (reinterpret_cast<uintptr_t>(row_scale) & 3u)
+        return fail(DH_ERR_ALIGN, "row_scale %p is not 4-byte aligned", row_scale);
+    cudaError_t err = launch_quantize(W_e4m3, row_scale, V, H, packed, scales, zeros,
+                                      static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
+    return ok();
+}
+
+int dh_forward_fp8w(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                    const uint16_t *zeros, const uint8_t *W_e4m3, const float *row_scale, int M,
+                    int H, int V, int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                    void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!row_scale) return fail(DH_ERR_NULL, "row_scale is NULL");
+    if (reinterpret_cast<uintptr_t>(row_scale) & 3u)
+        return fail(DH_ERR_ALIGN, "row_scale %p is not 4-byte aligned", row_scale);
+    return forward_impl(x, packed, scales, zeros, W_e4m3, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, static_cast<cudaStream_t>(stream), nullptr, 0, false, row_scale);
 }
 
 int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
@@ -447,7 +481,7 @@ const char *dh_last_error(void)
 
 int dh_version(void)
 {
-    return (1 << 16) | 0;
+    return (1 << 16) | 2;
 }
 
 
@@ -520,7 +554,7 @@ int dh_shard_rerank(const uint16_t *x, const uint16_t *W_shard, int M, int H, in
                         counters + kSelDoneOffset, false, sel_idx, nullptr, 0, st);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
     // exact values of the ids this shard owns; the others get -inf
-    err = launch_rerank_topk(x, W_shard, M, H, Vs, sel_idx, rerank, exact,
+    err = launch_rerank_topk(x, W_shard, nullptr, M, H, Vs, sel_idx, rerank, exact,
                              counters + kRowDoneOffset, 0, nullptr, nullptr,
                              static_cast<int>(vocab_offset), st);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));

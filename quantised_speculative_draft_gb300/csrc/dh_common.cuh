@@ -41,6 +41,18 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b)
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// OCP e4m3 (the float8_e4m3fn format) byte -> fp32, exact.  Sign, 4 exponent bits (bias 7),
+// 3 mantissa bits; exponent field 0 is subnormal, m * 2^-9.  A normal value's fp32 bits are
+// its exponent and mantissa fields moved up by 20 bits with the bias raised from 7 to 127.
+// The NaN codes (0x7F, 0xFF) decode as +-480: callers hold finite weights only.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b)
+{
+    const uint32_t mag = b & 0x7Fu;
+    const float v = mag >= 8u ? __uint_as_float((mag << 20) + (120u << 23))
+                              : static_cast<float>(mag) * 0.001953125f; // 2^-9
+    return (b & 0x80u) ? -v : v;
+}
+
 // Order-preserving map of an fp32 value onto uint32 (larger value -> larger key).
 __device__ __forceinline__ uint32_t f32_order_key(float v)
 {

@@ -25,8 +25,9 @@ constexpr int kRowDoneOffset = 128;
 constexpr int kSelDoneOffset = 256;
 
 // ---- launchers (each returns the launch status) ------------------------------------------
-cudaError_t launch_quantize(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
-                            uint16_t *ZS, cudaStream_t stream);
+// W: bf16 rows (wsc null) or e4m3 rows with per-row fp32 scales wsc.
+cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, uint8_t *packed,
+                            uint16_t *S, uint16_t *ZS, cudaStream_t stream);
 
 // x [M,H] bf16 -> group sums xs [Mpad, NGt] fp32 and the operand layouts of the coarse paths:
 //   xw (warp path): per 16-row batch chunk, B fragments in mma.sync register order
@@ -92,9 +93,11 @@ cudaError_t launch_select(const float *cand_val, const int32_t *cand_idx, int M,
                           int32_t *sel_idx, float *sel_val, int id_offset, cudaStream_t stream);
 
 // Exact rerank of the selected rows and, fused (last CTA per row), the per-row top-k (topk 0:
-// none).  W holds rows [id_offset, id_offset + V) of the head; selected ids outside that range
-// get -inf.  row_done: M zeroed counters.
-cudaError_t launch_rerank_topk(const uint16_t *x, const uint16_t *W, int M, int H, int V,
+// none).  W holds rows [id_offset, id_offset + V) of the head: bf16 (w_scale null) or e4m3
+// with per-row fp32 scales w_scale.  Selected ids outside that range get -inf.  row_done: M
+// zeroed counters.
+cudaError_t launch_rerank_topk(const uint16_t *x, const void *W, const float *w_scale, int M,
+                               int H, int V,
                                const int32_t *sel_idx, int R, float *ex, int *row_done, int topk,
                                int32_t *out_idx, float *out_logit, int id_offset,
                                cudaStream_t stream);

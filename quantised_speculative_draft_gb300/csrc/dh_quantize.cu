@@ -10,6 +10,11 @@
 // division is correctly rounded, rintf rounds half to even: the result is bit-exact with the
 // definition.  The kernel is HBM-bound (2 bytes read per weight, 0.28 written).
 //
+// An fp8 head (kernel (1) with the e4m3 input): row n's weights are the fp32 products
+// e4m3(b) * wsc[n] (radiance_drafthead.py, _quantize_head_now, the fp8 weight pre-scaled by its
+// per-row scale before the group statistics), each rounded once; the steps above then run on
+// those values.
+//
 // Work unit: one warp per (row n, span s), where span s is packed bytes [128 s, 128 s + 128)
 // of the row -- the four groups s, NG + s, 2 NG + s, 3 NG + s (NG = H / 512), one per plane.
 // Lane l owns packed bytes 4l .. 4l+3 of the span, i.e. four consecutive weights of each of
@@ -33,7 +38,10 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t *__restrict__ W,
+// kFp8: W holds e4m3 bytes and wsc the per-row fp32 scales; otherwise W holds bf16.
+template <bool kFp8>
+__global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ Wv,
+                                                       const float *__restrict__ wsc,
                                                        uint8_t *__restrict__ packed,
                                                        uint16_t *__restrict__ S,
                                                        uint16_t *__restrict__ ZS, int V, int H)
@@ -49,20 +57,38 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t *__restric
          item < total; item += nwarps) {
         const long long n = item / NG;
         const int s = static_cast<int>(item - n * NG);
-        const uint16_t *row = W + n * H;
         // four weights of each plane: k = p*Q + 128 s + 4 lane + i
-        uint2 raw[4];
+        float wv[4][4];
+        if constexpr (kFp8) {
+            const uint8_t *row = static_cast<const uint8_t *>(Wv) + n * H;
+            const float rs = __ldg(wsc + n);
+            uint32_t raw[4];
 #pragma unroll
-        for (int p = 0; p < 4; ++p)
-            raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * Q + 128 * s + 4 * lane));
+            for (int p = 0; p < 4; ++p)
+                raw[p] = __ldg(reinterpret_cast<const uint32_t *>(row + p * Q + 128 * s + 4 * lane));
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    wv[p][i] = __fmul_rn(e4m3_to_f32(raw[p] >> (8 * i)), rs);
+        } else {
+            const uint16_t *row = static_cast<const uint16_t *>(Wv) + n * H;
+            uint2 raw[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * Q + 128 * s + 4 * lane));
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                wv[p][0] = __uint_as_float(raw[p].x << 16);
+                wv[p][1] = __uint_as_float(raw[p].x & 0xFFFF0000u);
+                wv[p][2] = __uint_as_float(raw[p].y << 16);
+                wv[p][3] = __uint_as_float(raw[p].y & 0xFFFF0000u);
+            }
+        }
         uint32_t word = 0;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            float w[4];
-            w[0] = __uint_as_float(raw[p].x << 16);
-            w[1] = __uint_as_float(raw[p].x & 0xFFFF0000u);
-            w[2] = __uint_as_float(raw[p].y << 16);
-            w[3] = __uint_as_float(raw[p].y & 0xFFFF0000u);
+            const float *w = wv[p];
             float lo = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
             float hi = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
             lo = warp_min(lo);
@@ -88,14 +114,20 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t *__restric
     }
 }
 
-cudaError_t launch_quantize(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
-                            uint16_t *ZS, cudaStream_t stream)
+cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, uint8_t *packed,
+                            uint16_t *S, uint16_t *ZS, cudaStream_t stream)
 {
     const long long total = static_cast<long long>(V) * (H / 512);
     long long blocks = (total + 7) / 8;
     const long long cap = static_cast<long long>(kNumSMs) * 8;
     if (blocks > cap) blocks = cap;
-    quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, packed, S, ZS, V, H);
+    if (wsc)
+        quantize_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, wsc, packed,
+                                                                                 S, ZS, V, H);
+    else
+        quantize_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, nullptr,
+                                                                                  packed, S, ZS,
+                                                                                  V, H);
     return cudaGetLastError();
 }
 

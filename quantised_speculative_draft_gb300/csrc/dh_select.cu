@@ -380,10 +380,14 @@ constexpr int kRerankThreads = 256;
 __device__ void sort_write_topk(unsigned long long *k, int n2, int topk, int32_t *oidx,
                                 float *ologit);
 
+// kFp8: W holds e4m3 rows and w_scale the per-row fp32 scales; each weight is the fp32
+// product e4m3(b) * w_scale[n], rounded once (radiance_drafthead.py, _rerank_exact, FP8 branch:
+// the selected fp8 rows are dequantised to fp32 before the dot product).  Otherwise W is bf16.
+template <bool kFp8>
 __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
-    const uint16_t *__restrict__ x, const uint16_t *__restrict__ W, int H, int V,
-    const int32_t *__restrict__ sel_idx, int R, float *__restrict__ ex,
-    int *__restrict__ row_done, int topk, int32_t *__restrict__ out_idx,
+    const uint16_t *__restrict__ x, const void *__restrict__ Wv,
+    const float *__restrict__ w_scale, int H, int V, const int32_t *__restrict__ sel_idx, int R,
+    float *__restrict__ ex, int *__restrict__ row_done, int topk, int32_t *__restrict__ out_idx,
     float *__restrict__ out_logit, int id_offset)
 {
     __shared__ double part[kRerankThreads / 32];
@@ -398,19 +402,39 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
     float a0 = 0.f, a1 = 0.f;
     if (n >= 0 && n < V) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<long long>(m) * H);
-        const uint4 *wr = reinterpret_cast<const uint4 *>(W + static_cast<long long>(n) * H);
-        const int nv = H / 8;
+        const int nv = H / 8; // 8 weights per step
+        if constexpr (kFp8) {
+            const uint2 *wr = reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(Wv) +
+                                                              static_cast<long long>(n) * H);
+            const float rs = __ldg(w_scale + n);
 #pragma unroll 4
-        for (int i = tid; i < nv; i += kRerankThreads) {
-            const uint4 xv = __ldg(xr + i);
-            const uint4 wv = __ldg(wr + i);
-            const uint32_t xs4[4] = {xv.x, xv.y, xv.z, xv.w};
-            const uint32_t ws4[4] = {wv.x, wv.y, wv.z, wv.w};
+            for (int i = tid; i < nv; i += kRerankThreads) {
+                const uint4 xv = __ldg(xr + i);
+                const uint2 wv = __ldg(wr + i);
+                const uint32_t xs4[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                a0 = fmaf(__uint_as_float(xs4[q] << 16), __uint_as_float(ws4[q] << 16), a0);
-                a1 = fmaf(__uint_as_float(xs4[q] & 0xFFFF0000u),
-                          __uint_as_float(ws4[q] & 0xFFFF0000u), a1);
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t wb = (q < 2 ? wv.x : wv.y) >> (16 * (q & 1));
+                    a0 = fmaf(__uint_as_float(xs4[q] << 16), __fmul_rn(e4m3_to_f32(wb), rs), a0);
+                    a1 = fmaf(__uint_as_float(xs4[q] & 0xFFFF0000u),
+                              __fmul_rn(e4m3_to_f32(wb >> 8), rs), a1);
+                }
+            }
+        } else {
+            const uint4 *wr = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(Wv) +
+                                                              static_cast<long long>(n) * H);
+#pragma unroll 4
+            for (int i = tid; i < nv; i += kRerankThreads) {
+                const uint4 xv = __ldg(xr + i);
+                const uint4 wv = __ldg(wr + i);
+                const uint32_t xs4[4] = {xv.x, xv.y, xv.z, xv.w};
+                const uint32_t ws4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    a0 = fmaf(__uint_as_float(xs4[q] << 16), __uint_as_float(ws4[q] << 16), a0);
+                    a1 = fmaf(__uint_as_float(xs4[q] & 0xFFFF0000u),
+                              __uint_as_float(ws4[q] & 0xFFFF0000u), a1);
+                }
             }
         }
     }
@@ -580,15 +604,19 @@ cudaError_t launch_merge_topk(const float *parts, const int32_t *sel_idx, int P,
     return cudaGetLastError();
 }
 
-cudaError_t launch_rerank_topk(const uint16_t *x, const uint16_t *W, int M, int H, int V,
+cudaError_t launch_rerank_topk(const uint16_t *x, const void *W, const float *w_scale, int M,
+                               int H, int V,
                                const int32_t *sel_idx, int R, float *ex, int *row_done, int topk,
                                int32_t *out_idx, float *out_logit, int id_offset,
                                cudaStream_t stream)
 {
     const unsigned blocks = static_cast<unsigned>(static_cast<long long>(M) * R);
-    rerank_topk_kernel<<<blocks, kRerankThreads, 0, stream>>>(x, W, H, V, sel_idx, R, ex,
-                                                              row_done, topk, out_idx, out_logit,
-                                                              id_offset);
+    if (w_scale)
+        rerank_topk_kernel<true><<<blocks, kRerankThreads, 0, stream>>>(
+            x, W, w_scale, H, V, sel_idx, R, ex, row_done, topk, out_idx, out_logit, id_offset);
+    else
+        rerank_topk_kernel<false><<<blocks, kRerankThreads, 0, stream>>>(
+            x, W, nullptr, H, V, sel_idx, R, ex, row_done, topk, out_idx, out_logit, id_offset);
     return cudaGetLastError();
 }
 

@@ -11,6 +11,8 @@ the workloads name:
                 (2483) drawn at 3x the standard deviation
 * ``topk``      M=16, H=5120, V=248320: x ~ N(0,1); W ~ N(0, 0.02) with 2048 rows at 4x
 
+``make_w_fp8`` gives any of these heads as an fp8 checkpoint (e4m3 rows, per-row fp32 scale).
+
 All draws come from one ``torch.Generator`` seeded with ``seed`` (0 by default) on the
 requested device; values are drawn in fp32 and rounded once to bf16.  The same tensors feed
 the CUDA path and (copied to the host) the CPU oracle.
@@ -84,6 +86,30 @@ def make_w(wl: Workload, seed: int = 0, device: str = "cpu", chunk_rows: int = 1
         blk = torch.randn(r1 - r0, wl.H, generator=g, device=device, dtype=torch.float32)
         W[r0:r1] = (blk * scale[r0:r1, None]).to(torch.bfloat16)
     return W
+
+
+def make_w_fp8(wl: Workload, seed: int = 0, device: str = "cpu", chunk_rows: int = 16384):
+    """An fp8 head standing in for a checkpoint stored as e4m3 rows with one fp32 scale per
+    row: the fp32 draws of make_w (before their bf16 rounding), each row scaled so that its
+    largest magnitude maps to 448 (the largest finite e4m3 value) and rounded to e4m3.
+    Returns (codes [V, H] uint8, row_scale [V] fp32); no code is a NaN code."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000003 + 29)
+    codes = torch.empty(wl.V, wl.H, dtype=torch.uint8, device=device)
+    row_scale = torch.empty(wl.V, dtype=torch.float32, device=device)
+    scale = torch.full((wl.V,), wl.w_std, dtype=torch.float32, device=device)
+    if wl.hot_rows:
+        hot = torch.randperm(wl.V, generator=g, device=device)[: wl.hot_rows]
+        scale[hot] *= wl.hot_scale
+    for r0 in range(0, wl.V, chunk_rows):
+        r1 = min(wl.V, r0 + chunk_rows)
+        blk = torch.randn(r1 - r0, wl.H, generator=g, device=device, dtype=torch.float32)
+        blk = blk * scale[r0:r1, None]
+        rs = blk.abs().amax(dim=1).clamp_min(1e-30) / 448.0
+        q = (blk / rs[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+        codes[r0:r1] = q.view(torch.uint8)
+        row_scale[r0:r1] = rs
+    return codes, row_scale
 
 
 def bits(t: torch.Tensor):

@@ -141,18 +141,22 @@ def check_exact_values(gpu, x_bits, W_bits):
     return float((err / tol).max())
 
 
-def check_result(gpu, ref, kcand, topk, x_bits, W_bits):
+def check_result(gpu, ref, kcand, topk, x_bits, W_bits, rerank_fn=None):
     """Final indices: bit-exact where the decision gap is clear; where it is not (a tie row),
     the returned list must still be the top-k of the GPU's own reranked set under the
     oracle's exact values, within the exact-logit tolerance.  Returns the tie rows as
-    (row, gap, oracle indices, GPU indices, differs)."""
+    (row, gap, oracle indices, GPU indices, differs).  rerank_fn(x_rows, idx) gives the
+    oracle's exact values (default: the bf16 head W_bits)."""
+    if rerank_fn is None:
+        def rerank_fn(xr, ix):
+            return orc.rerank(xr, W_bits, ix)
     gaps = orc.decision_gaps(ref, kcand, topk)
     ties = []
     M = gpu["idx"].shape[0]
     for m in range(M):
         gi, gl = gpu["idx"][m], gpu["logit"][m]
         assert (gi >= 0).all() and len(set(gi.tolist())) == topk, f"row {m}: bad result {gi}"
-        e = orc.rerank(x_bits[m:m + 1], W_bits, gi[None, :].astype(np.int32))[0]
+        e = rerank_fn(x_bits[m:m + 1], gi[None, :].astype(np.int32))[0]
         tol = EXACT_RTOL * np.maximum(np.abs(e), 1.0)
         assert (np.abs(gl - e) <= tol).all(), f"row {m}: returned logits off"
         order_ok = all((gl[i] > gl[i + 1]) or (gl[i] == gl[i + 1] and gi[i] < gi[i + 1])
@@ -169,7 +173,7 @@ def check_result(gpu, ref, kcand, topk, x_bits, W_bits):
         if differs and "sel_idx" in gpu:
             sel = gpu["sel_idx"][m]
             assert set(gi.tolist()) <= set(sel.tolist()), f"row {m}: result outside reranked set"
-            es = orc.rerank(x_bits[m:m + 1], W_bits, sel[None, :].astype(np.int32))[0]
+            es = rerank_fn(x_bits[m:m + 1], sel[None, :].astype(np.int32))[0]
             rest = es[~np.isin(sel, gi)]
             floor = e.min()
             slack = 2 * EXACT_RTOL * max(abs(floor), 1.0)

@@ -134,3 +134,30 @@ def test_product_path_never_touches_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert not bad.search(src), f
+
+
+def test_fp8_head_entry_points_reject_bad_arguments(lib):
+    # dh_quantize_fp8(W8, row_scale, V, H, packed, scales, zeros, stream)
+    assert lib.dh_quantize_fp8(FAKE, None, 16, 1024, FAKE, FAKE, FAKE, None) == -1
+    assert lib.dh_quantize_fp8(FAKE, FAKE, 16, 1000, FAKE, FAKE, FAKE, None) == -2
+    assert lib.dh_quantize_fp8(FAKE, FAKE, 0, 1024, FAKE, FAKE, FAKE, None) == -2
+    assert lib.dh_quantize_fp8(FAKE, FAKE + 2, 16, 1024, FAKE, FAKE, FAKE, None) == -5
+    assert lib.dh_quantize_fp8(FAKE + 8, FAKE, 16, 1024, FAKE, FAKE, FAKE, None) == -5
+    # dh_forward_fp8w(x, packed, S, ZS, W8, row_scale, M, H, V, kcand, R, k, idx, logit, ws, n)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1024, 8192, 8, 32, 1, FAKE, FAKE, FAKE,
+            1 << 40, None]
+    bad = list(args)
+    bad[5] = None
+    assert lib.dh_forward_fp8w(*bad) == -1
+    bad = list(args)
+    bad[5] = FAKE + 2
+    assert lib.dh_forward_fp8w(*bad) == -5
+    bad = list(args)
+    bad[7] = 1000
+    assert lib.dh_forward_fp8w(*bad) == -2
+    bad = list(args)
+    bad[11] = 33
+    assert lib.dh_forward_fp8w(*bad) == -3
+    bad = list(args)
+    bad[15] = 16
+    assert lib.dh_forward_fp8w(*bad) == -4
