@@ -1,5 +1,6 @@
 /*
- * dh_oracle.c -- plain, slow CPU oracle for the 2-bit draft head with exact rerank.
+ * dh_oracle.c -- plain, slow CPU oracle for the 2-bit draft head with exact rerank
+ * (and the page's 4-bit and fp8-weight variants).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link or call this
  * file; only the test-suite, the smoke check and the benchmark's CPU-baseline leg do.
@@ -26,6 +27,9 @@
  *   orc_quantize_fp8   pinned: power-of-two row scales reduce it to orc_quantize
  *   orc_rerank_fp8     pinned: power-of-two row scales reduce it to orc_rerank
  *   orc_exact_head     pinned: exact integer arithmetic; KC=64,R=V reduces forward to it
+ *   orc_quantize4      pinned: hand-worked golden group, on-grid rows recovered exactly,
+ *                      half-split byte placement, error bound
+ *   orc_coarse4        pinned: collapsed form == direct dequant-and-dot (exact scales)
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -83,8 +87,11 @@ static float clampf(float v, float lo, float hi)
 /* ------------------------------------------------------------------------------------- */
 
 #define GROUP 128
-#define LEVELS 3.0f /* (1 << BITS) - 1 at BITS = 2 */
-#define BIAS 4.0f   /* 2^m for the mantissa slot m = 5 of the bit-pattern dequant */
+/* Per bit width (the page's BITS = 2 default and its BITS = 4 variant): the largest code
+ * (1 << BITS) - 1, and the premultiplier 2^BITS of the bit-pattern dequant, whose bf16 bias is
+ * 1 + v / 2^BITS (the code sits in mantissa slot 7 - BITS). */
+static float levels_of(int bits) { return bits == 4 ? 15.0f : 3.0f; }
+static float bias_of(int bits) { return bits == 4 ? 16.0f : 4.0f; }
 
 /*
  * Per (row n, group gi of 128 consecutive k), in fp32:
@@ -111,11 +118,14 @@ void orc_decode_e4m3(const uint8_t *b, int64_t n, float *out)
     for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_f32(b[i]);
 }
 
-/* One row of fp32 weights -> its packed bytes, S and ZS (the page's per-group steps). */
-static void quantize_row(const float *row, int64_t H, uint8_t *q, uint8_t *packed_row,
+/* One row of fp32 weights -> its packed bytes, S and ZS (the page's per-group steps).
+ * bits = 2: quarter split, byte j = q[j] | q[H/4+j] << 2 | q[H/2+j] << 4 | q[3H/4+j] << 6;
+ * bits = 4: half split, byte j = q[j] | q[H/2+j] << 4. */
+static void quantize_row(const float *row, int64_t H, int bits, uint8_t *q, uint8_t *packed_row,
                          uint16_t *S_row, uint16_t *ZS_row, float *sc_row, float *zp_row)
 {
     const int64_t NGt = H / GROUP, Q = H / 4;
+    const float LEVELS = levels_of(bits), BIAS = bias_of(bits);
     for (int64_t gi = 0; gi < NGt; ++gi) {
         float lo = row[gi * GROUP], hi = lo;
         for (int t = 1; t < GROUP; ++t) {
@@ -138,6 +148,10 @@ static void quantize_row(const float *row, int64_t H, uint8_t *q, uint8_t *packe
         if (sc_row) sc_row[gi] = sc;
         if (zp_row) zp_row[gi] = zp;
     }
+    if (bits == 4) {
+        for (int64_t j = 0; j < H / 2; ++j) packed_row[j] = (uint8_t)(q[j] | (q[H / 2 + j] << 4));
+        return;
+    }
     for (int64_t j = 0; j < Q; ++j)
         packed_row[j] = (uint8_t)(q[j] | (q[Q + j] << 2) | (q[2 * Q + j] << 4) | (q[3 * Q + j] << 6));
 }
@@ -156,7 +170,31 @@ int orc_quantize(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint1
     }
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
-        quantize_row(row, H, q, packed + n * Q, S + n * NGt, ZS + n * NGt,
+        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt,
+                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL);
+    }
+    free(q);
+    free(row);
+    return 0;
+}
+
+/* The BITS = 4 variant of _quantize_head_now: levels 0..15, S = bf16(16 sc),
+ * ZS = bf16(16 sc + zp sc), half-split packing into [V, H/2] bytes.  H % 256 == 0. */
+int orc_quantize4(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint16_t *S,
+                  uint16_t *ZS, float *sc_out, float *zp_out)
+{
+    if (H <= 0 || H % 256 != 0 || V <= 0) return -2;
+    const int64_t NGt = H / GROUP;
+    uint8_t *q = (uint8_t *)malloc((size_t)H);
+    float *row = (float *)malloc((size_t)H * sizeof(float));
+    if (!q || !row) {
+        free(q);
+        free(row);
+        return -1;
+    }
+    for (int64_t n = 0; n < V; ++n) {
+        for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
+        quantize_row(row, H, 4, q, packed + n * (H / 2), S + n * NGt, ZS + n * NGt,
                      sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL);
     }
     free(q);
@@ -180,7 +218,7 @@ int orc_quantize_fp8(const uint8_t *W8, const float *wsc, int64_t V, int64_t H, 
     }
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = e4m3_to_f32(W8[n * H + k]) * wsc[n];
-        quantize_row(row, H, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL);
+        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL);
     }
     free(q);
     free(row);
@@ -208,7 +246,7 @@ typedef struct {
     const uint16_t *x;
     const uint8_t *packed;
     const uint16_t *S, *ZS;
-    int M;
+    int M, bits;
     int64_t H, V, n0, n1;
     double *c;
 } coarse_job;
@@ -216,12 +254,16 @@ typedef struct {
 static void *coarse_worker(void *arg)
 {
     coarse_job *jb = (coarse_job *)arg;
-    const int64_t H = jb->H, Q = H / 4, NGt = H / GROUP;
+    const int bits = jb->bits;
+    const int64_t H = jb->H, NGt = H / GROUP;
+    const int64_t Q = H / (8 / bits); /* packed bytes per row: codes of k share byte k mod Q */
+    const double bias = bits == 4 ? 16.0 : 4.0;
+    const unsigned mask = (1u << bits) - 1u;
     double *v = (double *)malloc((size_t)H * sizeof(double));
     for (int64_t n = jb->n0; n < jb->n1; ++n) {
         const uint8_t *prow = jb->packed + n * Q;
-        for (int64_t k = 0; k < H; ++k) /* v[n,k] from the packed byte j = k mod Q */
-            v[k] = (double)((prow[k % Q] >> (2 * (k / Q))) & 3u);
+        for (int64_t k = 0; k < H; ++k) /* v[n,k]: field k / Q of the packed byte k mod Q */
+            v[k] = (double)((prow[k % Q] >> (bits * (k / Q))) & mask);
         for (int m = 0; m < jb->M; ++m) {
             const uint16_t *xr = jb->x + (int64_t)m * H;
             double c = 0.0;
@@ -229,7 +271,7 @@ static void *coarse_worker(void *arg)
                 double p = 0.0, xs = 0.0;
                 for (int t = 0; t < GROUP; ++t) {
                     double xk = (double)bf16_to_f32(xr[gi * GROUP + t]);
-                    p += xk * (1.0 + v[gi * GROUP + t] / 4.0);
+                    p += xk * (1.0 + v[gi * GROUP + t] / bias);
                     xs += xk;
                 }
                 c += (double)bf16_to_f32(jb->S[n * NGt + gi]) * p -
@@ -242,9 +284,11 @@ static void *coarse_worker(void *arg)
     return NULL;
 }
 
-/* c is [M, V] fp64.  nthreads <= 1 runs on the calling thread. */
-void orc_coarse(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
-                int M, int64_t H, int64_t V, double *c, int nthreads)
+/* c is [M, V] fp64.  nthreads <= 1 runs on the calling thread.  bits: 2 (packed [V, H/4],
+ * bias 4) or 4 (packed [V, H/2], bias 16). */
+static void coarse_bits(const uint16_t *x, const uint8_t *packed, const uint16_t *S,
+                        const uint16_t *ZS, int M, int64_t H, int64_t V, double *c, int nthreads,
+                        int bits)
 {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
@@ -256,7 +300,7 @@ void orc_coarse(const uint16_t *x, const uint8_t *packed, const uint16_t *S, con
         int64_t n0 = (int64_t)i * chunk, n1 = n0 + chunk;
         if (n1 > V) n1 = V;
         if (n0 >= n1) break;
-        jobs[i] = (coarse_job){x, packed, S, ZS, M, H, V, n0, n1, c};
+        jobs[i] = (coarse_job){x, packed, S, ZS, M, bits, H, V, n0, n1, c};
         if (nthreads == 1) {
             coarse_worker(&jobs[i]);
         } else {
@@ -265,6 +309,19 @@ void orc_coarse(const uint16_t *x, const uint8_t *packed, const uint16_t *S, con
         }
     }
     for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+}
+
+void orc_coarse(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
+                int M, int64_t H, int64_t V, double *c, int nthreads)
+{
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2);
+}
+
+/* The BITS = 4 head: group term S p - ZS xs with p = sum x (1 + v/16). */
+void orc_coarse4(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
+                 int M, int64_t H, int64_t V, double *c, int nthreads)
+{
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 4);
 }
 
 /* ------------------------------------------------------------------------------------- */

@@ -84,6 +84,10 @@ def _load():
         lib.orc_quantize_fp8.restype = I
         lib.orc_rerank_fp8.argtypes = [P, P, P, I, I64, P, I, P]
         lib.orc_rerank_fp8.restype = None
+        lib.orc_quantize4.argtypes = [P, I64, I64, P, P, P, P, P]
+        lib.orc_quantize4.restype = I
+        lib.orc_coarse4.argtypes = [P, P, P, P, I, I64, I64, P, I]
+        lib.orc_coarse4.restype = None
         _lib = lib
         return lib
 
@@ -131,6 +135,26 @@ def quantize(W: np.ndarray, with_params: bool = False):
     return packed, S, ZS
 
 
+def quantize4(W: np.ndarray, with_params: bool = False):
+    """The 4-bit head: W uint16 [V, H] bf16 bits -> (packed u8 [V, H/2] half split,
+    S u16 [V, H/128] = bf16(16 sc), ZS u16 = bf16(16 sc + zp sc)) [+ sc, zp]."""
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    V, H = W.shape
+    packed = np.empty((V, H // 2), np.uint8)
+    S = np.empty((V, H // GROUP), np.uint16)
+    ZS = np.empty((V, H // GROUP), np.uint16)
+    sc = np.empty((V, H // GROUP), np.float32) if with_params else None
+    zp = np.empty((V, H // GROUP), np.float32) if with_params else None
+    rc = _load().orc_quantize4(_ptr(W), V, H, _ptr(packed), _ptr(S), _ptr(ZS),
+                               _ptr(sc) if with_params else None,
+                               _ptr(zp) if with_params else None)
+    if rc != 0:
+        raise ValueError(f"orc_quantize4: status {rc} (H must be a positive multiple of 256)")
+    if with_params:
+        return packed, S, ZS, sc, zp
+    return packed, S, ZS
+
+
 def unpack(packed: np.ndarray, H: int) -> np.ndarray:
     """Quarter-split packed bytes [V, H/4] -> 2-bit codes [V, H] (u8)."""
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
@@ -151,6 +175,21 @@ def coarse(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
     c = np.empty((M, V), np.float64)
     _load().orc_coarse(_ptr(x), _ptr(packed), _ptr(S), _ptr(ZS), M, H, V, _ptr(c),
                        nthreads or default_threads())
+    return c
+
+
+def coarse4(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
+    """Coarse values c [M, V] in fp64 from the stored 4-bit head (packed [V, H/2])."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    S = np.ascontiguousarray(S, dtype=np.uint16)
+    ZS = np.ascontiguousarray(ZS, dtype=np.uint16)
+    M, H = x.shape
+    V = packed.shape[0]
+    assert packed.shape[1] * 2 == H
+    c = np.empty((M, V), np.float64)
+    _load().orc_coarse4(_ptr(x), _ptr(packed), _ptr(S), _ptr(ZS), M, H, V, _ptr(c),
+                        nthreads or default_threads())
     return c
 
 
@@ -245,6 +284,19 @@ def forward_fp8(x, packed, S, ZS, W8, wsc, kcand: int, rerank_n: int, k: int,
     cval, cidx, nvalid = block_topk(cf, kcand)
     sel_idx, sel_val = select_topr(cval, cidx, rerank_n)
     e = rerank_fp8(x, W8, wsc, sel_idx)
+    out_idx, out_val = topk(e, sel_idx, k)
+    return dict(coarse=c, coarse_f32=cf, cand_val=cval, cand_idx=cidx, sel_idx=sel_idx,
+                sel_val=sel_val, exact=e, idx=out_idx, logit=out_val)
+
+
+def forward4(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
+             nthreads: int | None = None) -> dict:
+    """The draft-head path on the 4-bit head (the rerank is the same bf16 one)."""
+    c = coarse4(x, packed, S, ZS, nthreads)
+    cf = c.astype(np.float32)
+    cval, cidx, nvalid = block_topk(cf, kcand)
+    sel_idx, sel_val = select_topr(cval, cidx, rerank_n)
+    e = rerank(x, W, sel_idx)
     out_idx, out_val = topk(e, sel_idx, k)
     return dict(coarse=c, coarse_f32=cf, cand_val=cval, cand_idx=cidx, sel_idx=sel_idx,
                 sel_val=sel_val, exact=e, idx=out_idx, logit=out_val)

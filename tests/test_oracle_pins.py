@@ -409,3 +409,126 @@ def test_fp8_rerank_rounds_each_weight_to_fp32_before_the_sum():
     raw = np.einsum("mk,mjk->mj", bf2f(x).astype(np.float64),
                     dec[idx].astype(np.float64) * wsc[idx][..., None].astype(np.float64))
     assert not np.array_equal(orc.rerank_fp8(x, codes, wsc, idx), raw)
+
+
+# ------------------------------------------------------------------------------------------
+# the 4-bit head (BITS = 4: half split, bias 16)
+# ------------------------------------------------------------------------------------------
+
+def my_unpack4(packed, H):
+    """Test-side unpack of the half split: low nibble -> k = j, high nibble -> k = H/2 + j."""
+    return np.concatenate([packed & 15, packed >> 4], axis=1).astype(np.uint8)
+
+
+def test_quantize4_golden_groups():
+    spec = json.load(open(os.path.join(GOLD, "quantize4_groups.json")))
+    for case in spec["cases"]:
+        group = np.tile(np.array(case["pattern"]), 32)
+        W = f2bf_exact(np.tile(group, 4)[None, :])              # H = 512: four equal groups
+        packed, S, ZS, sc, zp = orc.quantize4(W, with_params=True)
+        codes = my_unpack4(packed, 512)[0]
+        want = np.tile(np.array(case["codes"]), 128)
+        assert np.array_equal(codes, want), case["name"]
+        for g in range(4):
+            assert f32_bits(sc[0, g]) == int(case["sc_bits"], 16), case["name"]
+            assert zp[0, g] == case["zp"], case["name"]
+            assert S[0, g] == int(case["S"], 16), case["name"]
+            assert ZS[0, g] == int(case["ZS"], 16), case["name"]
+
+
+def test_packing4_golden_bytes():
+    spec = json.load(open(os.path.join(GOLD, "packing4.json")))
+    for row in spec["rows"]:
+        H = row["H"]
+        groups = [np.array([-0.875, 1.0] + [f] * 126) for f in row["group_fill"]]
+        W = f2bf_exact(np.concatenate(groups)[None, :])
+        packed, S, ZS = orc.quantize4(W)
+        want = np.zeros(H // 2, np.uint8)
+        for start, count, val in row["bytes"]:
+            want[start:start + count] = int(val, 16)
+        assert np.array_equal(packed[0], want), H
+        assert np.all(S == int(row["S"], 16)) and np.all(ZS == int(row["ZS"], 16))
+
+
+def test_quantize4_invariants_and_error_bound():
+    rng = np.random.default_rng(12)
+    w = (rng.standard_normal((40, 1536)) * 0.02).astype(np.float32)
+    w[5] *= 4.0
+    w[7, :128] = 0.37
+    W = (w.view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS, sc, zp = orc.quantize4(W, with_params=True)
+    codes = my_unpack4(packed, 1536).astype(np.float64)
+    assert codes.max() <= 15 and set(np.unique(zp).tolist()) <= set(range(16))
+    g = bf2f(W).reshape(40, 12, 128)
+    lo, hi = g.min(-1), g.max(-1)
+    deq = sc[..., None].astype(np.float64) * (codes.reshape(40, 12, 128) - zp[..., None])
+    straddle = (lo <= 0) & (hi >= 0)
+    assert straddle.sum() >= 400
+    bound = 0.5 * sc.astype(np.float64) * (1 + 1e-5)
+    assert np.all(np.abs(g - deq)[straddle] <= bound[straddle][:, None])
+    sc64 = sc.astype(np.float64)
+    assert np.all(np.abs(bf2f(S) - 16 * sc64) <= 2.0 ** -8 * 16 * sc64)
+    assert np.all(np.abs(bf2f(ZS) - (16 + zp) * sc64) <= 2.0 ** -8 * (1 + 1e-6) * (16 + zp) * sc64)
+    # the same groups at 2 bits: a step of range/3 against range/15
+    sc2 = orc.quantize(W, with_params=True)[3]
+    assert np.allclose(sc2[sc2 > 1e-8], 5 * sc[sc2 > 1e-8], rtol=1e-6)
+
+
+def test_quantize4_rejects_partial_half_groups():
+    with pytest.raises(ValueError):
+        orc.quantize4(np.zeros((2, 128), np.uint16))
+
+
+def _grid_weights4(rng, V, H):
+    """Rows on an exact 4-bit grid: per group codes in 0..15 with 0 and 15 present, a zero
+    point zp and a power-of-two step, w = (code - zp) * 2^e; lo, hi then fix sc = 2^e and
+    zp exactly and every value is reproduced."""
+    codes = rng.integers(0, 16, size=(V, H // 128, 128))
+    codes[:, :, 0] = 0
+    codes[:, :, 1] = 15
+    zp = rng.integers(0, 16, size=(V, H // 128, 1))
+    e = rng.integers(-12, -6, size=(V, 1, 1)).astype(np.float64)
+    return ((codes - zp) * 2.0 ** e).reshape(V, H)
+
+
+def test_coarse4_on_grid_weights_is_the_exact_head():
+    rng = np.random.default_rng(13)
+    V, H, M = 80, 1024, 3
+    W = f2bf_exact(_grid_weights4(rng, V, H))
+    x = f2bf_exact(np.round(rng.standard_normal((M, H)) * 64) / 64)
+    packed, S, ZS = orc.quantize4(W)
+    c = orc.coarse4(x, packed, S, ZS)
+    np.testing.assert_allclose(c, bf2f(x) @ bf2f(W).T, rtol=1e-12, atol=1e-12)
+
+
+def test_coarse4_collapsed_form_equals_direct_dequant():
+    """c = sum_g S p - ZS xs must equal sum_k x_k (S_g (1 + v_k/16) - ZS_g) from a test-side
+    unpack of the half split and a plain matmul."""
+    rng = np.random.default_rng(14)
+    V, H, M = 150, 1536, 4
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS = orc.quantize4(W)
+    v = my_unpack4(packed, H).astype(np.float64)
+    s = np.repeat(bf2f(S), 128, axis=1)
+    zs = np.repeat(bf2f(ZS), 128, axis=1)
+    ref = bf2f(x) @ (s * (1.0 + v / 16.0) - zs).T
+    c = orc.coarse4(x, packed, S, ZS)
+    np.testing.assert_allclose(c, ref, rtol=1e-11, atol=1e-11)
+    exact = bf2f(x) @ bf2f(W).T
+    assert np.corrcoef(c.ravel(), exact.ravel())[0, 1] > 0.97
+
+
+def test_forward4_with_full_candidate_pool_is_exact_topk():
+    rng = np.random.default_rng(15)
+    M, V, H, k = 3, 130, 512, 4
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS = orc.quantize4(W)
+    res = orc.forward4(x, packed, S, ZS, W, 64, V, k)
+    ex = bf2f(x) @ bf2f(W).T
+    for m in range(M):
+        o = _order(ex[m].astype(np.float32), np.arange(V))[:k]
+        assert np.array_equal(res["idx"][m], o)
