@@ -47,6 +47,9 @@ def parse():
                     help="vocabulary rows (smaller heads are for profiling captures only)")
     ap.add_argument("--sets", type=int, default=2, help="resident input sets rotated per step")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8-head line")
+    ap.add_argument("--no-int4", action="store_true", help="skip the 4-bit-head line")
+    ap.add_argument("--bits", type=int, choices=[2, 4], default=2,
+                    help="head width for --profile runs (4: the 4-bit head at KCAND=1)")
     ap.add_argument("--profile", action="store_true",
                     help="only run warmup + steps forwards (no timing, no JSON): for ncu")
     return ap.parse_args()
@@ -56,6 +59,11 @@ def path_name(p):
     import quantised_speculative_draft_gb300 as dh
     return {dh.PATH_TC: "tcgen05 8-bit", dh.PATH_TC_BF16: "tcgen05 bf16",
             dh.PATH_WARP: "warp mma.sync bf16"}.get(p, str(p))
+
+
+def algorithmic_bytes4(V, H):
+    """Bytes the 4-bit coarse pass must read: the half-split codes and the S/ZS pair."""
+    return V * H // 2 + 2 * V * (H // 128) * 2
 
 
 def algorithmic_bytes(V, H):
@@ -164,6 +172,43 @@ class Inputs:
         dh.dh_forward(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND, RERANK, TOPK, idx,
                       logit, ws)
 
+    def call_timed(self, M, ws, idx, logit, events):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_timed(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND, RERANK,
+                            TOPK, idx, logit, ws, events)
+
+
+class Int4Inputs:
+    """One resident input set of the 4-bit head (dh_quantize4 of the bf16 head): the page's
+    BITS = 4 variant, run at a chosen KCAND (1 is the page's setting for it)."""
+
+    def __init__(self, seed, dev, max_m, kcand=1, V=V_FULL):
+        import dataclasses
+        import torch
+        import quantised_speculative_draft_gb300 as dh
+        from quantised_speculative_draft_gb300 import synth
+        wl = synth.full(max_m)
+        if V != wl.V:
+            wl = dataclasses.replace(wl, V=V, hot_rows=max(1, V // 100))
+        self.x = synth.make_x(wl, seed, dev)
+        self.W = synth.make_w(wl, seed, dev)
+        V, H = self.W.shape
+        self.kcand = kcand
+        self.packed = torch.empty(V, H // 2, dtype=torch.uint8, device=dev)
+        self.S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        self.ZS = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        dh.dh_quantize4(self.W, self.packed, self.S, self.ZS)
+
+    def call(self, M, ws, idx, logit):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward4(self.x[:M], self.packed, self.S, self.ZS, self.W, self.kcand, RERANK,
+                       TOPK, idx, logit, ws)
+
+    def call_timed(self, M, ws, idx, logit, events):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward4_timed(self.x[:M], self.packed, self.S, self.ZS, self.W, self.kcand,
+                             RERANK, TOPK, idx, logit, ws, events)
+
 
 class Fp8Inputs:
     """One resident input set of the fp8 head: e4m3 rows with per-row scales and their int2
@@ -251,9 +296,7 @@ def time_stages(sets, M, steps):
         fwd(sets, i, M, ws, idx, logit)
     torch.cuda.synchronize()
     for i in range(steps):
-        s = sets[i % len(sets)]
-        dh.dh_forward_timed(s.x[:M], s.packed, s.S, s.ZS, s.W, KCAND, RERANK, TOPK, idx, logit,
-                            ws, evs[i])
+        sets[i % len(sets)].call_timed(M, ws, idx, logit, evs[i])
     torch.cuda.synchronize()
     names = ["prep", "coarse", "select", "rerank_topk"]
     out = {}
@@ -391,7 +434,10 @@ def run_ours(args):
     dev = f"cuda:{local}"
     dh.build()
     if args.profile:
-        sets = [Inputs(seed, dev, args.M, args.V) for seed in range(args.sets)]
+        if args.bits == 4:
+            sets = [Int4Inputs(seed, dev, args.M, 1, args.V) for seed in range(args.sets)]
+        else:
+            sets = [Inputs(seed, dev, args.M, args.V) for seed in range(args.sets)]
         ws, idx, logit = make_outputs(args.M, dev, args.V)
         for i in range(args.warmup + args.steps):
             fwd(sets, i, args.M, ws, idx, logit)
@@ -460,6 +506,25 @@ def run_ours(args):
                "quantize_us": round(e0.elapsed_time(e1) * 1e3 / n8, 1)}
         del sets8
 
+    int4 = None
+    if rank == 0 and not args.no_int4:
+        sets4 = [Int4Inputs(seed, dev, M) for seed in range(args.sets)]
+        nb4 = algorithmic_bytes4(V_FULL, H_FULL)
+        int4 = {"workload": f"full-vocab 4-bit head M={M} (half-split codes, bias 16)",
+                "coarse_bytes_per_launch": nb4}
+        for kc in (1, KCAND):
+            for s4 in sets4:
+                s4.kcand = kc
+            ms4, _, _ = time_graph(sets4, M, args.sweep_steps, 5)
+            st4 = time_stages(sets4, M, 20)
+            gbs = nb4 / st4["coarse"] / 1e3
+            int4[f"kcand_{kc}"] = {"us_per_call": round(ms4 * 1e3 / args.sweep_steps, 2),
+                                   "coarse_us": round(st4["coarse"], 2),
+                                   "coarse_GB/s": round(gbs, 1),
+                                   "coarse_frac_of_hbm": round(gbs / hbm, 4),
+                                   "stages_us": {k: round(v, 2) for k, v in st4.items()}}
+        del sets4
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xb, pb, Sb, ZSb, Wb = cpu_inputs
@@ -498,6 +563,7 @@ def run_ours(args):
             "stages_us": {k: round(v, 2) for k, v in stages.items()},
             "pack": pack,
             "fp8_head": fp8,
+            "int4_head": int4,
             "sweep": sweep,
         }
         print(json.dumps(line), flush=True)

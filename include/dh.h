@@ -265,6 +265,44 @@ int dh_forward_fp8w(const uint16_t *x, const uint8_t *packed, const uint16_t *sc
                     int H, int V, int kcand, int rerank, int topk, int32_t *idx, float *logit,
                     void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * 4-bit head: the page's BITS = 4 variant (radiance_drafthead.py, _quantize_head_now with
+ * BITS = 4; the coarse term with bias 16).  The page's note: at 4 bits KCAND = 1 already
+ * recovers nearly every argmax, where 2 bits needs KCAND = 8.
+ *
+ * dh_quantize4 -- as dh_quantize with 15 levels and the half split:
+ *   packed  [V, H/2]     u8: byte j of row n holds the 4-bit codes of k = j (bits 0-3) and
+ *                        k = H/2 + j (bits 4-7)                                   (output)
+ *   scales  [V, H/128]   bf16 S  = bf16(16 * sc)                                  (output)
+ *   zeros   [V, H/128]   bf16 ZS = bf16(16 * sc + zp * sc)                        (output)
+ *   with sc = max((hi - lo) / 15, 1e-8), zp = clamp(round(-lo / sc), 0, 15),
+ *   q = clamp(round(w / sc + zp), 0, 15).  H % 512 == 0.  Bit-exact with that definition.
+ * dh_forward4 / dh_forward4_debug / dh_forward4_timed -- dh_forward / _debug / _timed on that
+ *   head: coarse value
+ *   c = sum_g ( S_g sum_{k in g} x_k (1 + v_k/16) - ZS_g sum_{k in g} x_k ); selection,
+ *   rerank (against W_bf16), workspace (dh_workspace_bytes) and ranking rules unchanged.
+ *   Runs on the 8-bit tcgen05 coarse path only: DH_ERR_ARG when another path is forced by
+ *   dh_set_coarse_path or the sizes do not fit it (two pipeline stages of 32 KB of packed
+ *   bytes plus the staged x next to the fixed buffers: H <= 7168 for M > 16, H <= 13312
+ *   for M <= 16 -- the check runs before any launch).
+ */
+int dh_quantize4(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                 uint16_t *zeros, void *stream);
+int dh_forward4(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V, int kcand,
+                int rerank, int topk, int32_t *idx, float *logit, void *workspace,
+                size_t ws_bytes, void *stream);
+int dh_forward4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                      const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                      int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                      void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                      int32_t *cand_idx, int32_t *sel_idx, float *sel_exact, void *stream);
+/* dh_forward4_timed -- dh_forward_timed on the 4-bit head (same events). */
+int dh_forward4_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                      const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                      int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                      void *workspace, size_t ws_bytes, void *const *events, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

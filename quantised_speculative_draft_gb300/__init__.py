@@ -23,7 +23,7 @@ __all__ = [
     "dh_forward_launch_count", "dh_forward_noalloc", "NOALLOC_WORKSPACE_BYTES",
     "dh_last_error", "dh_version", "DraftHead", "dh_shard_candidates",
     "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_shard_topk", "dh_quantize_fp8",
-    "dh_forward_fp8w",
+    "dh_forward_fp8w", "dh_quantize4", "dh_forward4", "dh_forward4_debug", "dh_forward4_timed",
     "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16", "NUM_STAGE_EVENTS", "library_path",
 ]
 
@@ -99,6 +99,14 @@ def _load():
         lib.dh_quantize_fp8.restype = I
         lib.dh_forward_fp8w.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, S, P]
         lib.dh_forward_fp8w.restype = I
+        lib.dh_quantize4.argtypes = [P, I, I, P, P, P, P]
+        lib.dh_quantize4.restype = I
+        lib.dh_forward4.argtypes = fwd + [P]
+        lib.dh_forward4.restype = I
+        lib.dh_forward4_debug.argtypes = fwd + [P, P, P, P, P, P]
+        lib.dh_forward4_debug.restype = I
+        lib.dh_forward4_timed.argtypes = fwd + [P, P]
+        lib.dh_forward4_timed.restype = I
         _lib = lib
         return lib
 
@@ -204,6 +212,35 @@ def dh_forward_fp8w(x, packed, scales, zeros, W8, row_scale, kcand, rerank, topk
                                    _p(logit), _p(workspace), nbytes, _stream(stream)))
 
 
+def dh_quantize4(W, packed, scales, zeros, stream=None):
+    """Quantise the bf16 head W [V, H] to 4 bits: packed [V, H/2] u8 (half split),
+    scales/zeros [V, H/128] bf16."""
+    V, H = W.shape
+    _check(_load().dh_quantize4(_p(W), V, H, _p(packed), _p(scales), _p(zeros), _stream(stream)))
+
+
+def dh_forward4(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,
+                stream=None):
+    """dh_forward on the 4-bit head (packed [V, H/2] from dh_quantize4)."""
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    _check(_load().dh_forward4(*args, _stream(stream)))
+
+
+def dh_forward4_debug(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,
+                      coarse=None, cand_val=None, cand_idx=None, sel_idx=None, sel_exact=None,
+                      stream=None):
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    _check(_load().dh_forward4_debug(*args, _p(coarse), _p(cand_val), _p(cand_idx), _p(sel_idx),
+                                     _p(sel_exact), _stream(stream)))
+
+
+def dh_forward4_timed(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,
+                      events, stream=None):
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in events])
+    _check(_load().dh_forward4_timed(*args, arr, _stream(stream)))
+
+
 def dh_shard_candidates(x, packed, scales, zeros, vocab_offset, kcand, rerank, out_val, out_idx,
                         workspace, stream=None):
     """A vocabulary shard's top-``rerank`` candidates: out_val/out_idx [M, rerank] (global ids)."""
@@ -264,13 +301,17 @@ class DraftHead:
 
     The head weight W stays owned by the caller and is kept by reference (the rerank reads
     it): bf16 [V, H], or e4m3 codes [V, H] (uint8 or float8_e4m3fn) with ``row_scale`` [V]
-    fp32 for an fp8 head.
+    fp32 for an fp8 head.  ``bits=4`` builds the 4-bit head (bf16 weight only; the page pairs
+    it with ``kcand=1``).
     """
 
     def __init__(self, W, kcand: int = 8, rerank: int = 32, max_m: int = 128, stream=None,
-                 row_scale=None):
+                 row_scale=None, bits: int = 2):
         import torch
         fp8 = row_scale is not None
+        if bits not in (2, 4) or (bits == 4 and fp8):
+            raise ValueError("bits must be 2, or 4 with a bf16 weight")
+        self.bits = bits
         ok_dtype = W.dtype in (torch.uint8, torch.float8_e4m3fn) if fp8 else \
             W.dtype == torch.bfloat16
         if not ok_dtype or not W.is_cuda or not W.is_contiguous():
@@ -282,11 +323,13 @@ class DraftHead:
         self.W, self.row_scale = W, row_scale
         self.V, self.H = W.shape
         dev = W.device
-        self.packed = torch.empty(self.V, self.H // 4, dtype=torch.uint8, device=dev)
+        self.packed = torch.empty(self.V, self.H * bits // 8, dtype=torch.uint8, device=dev)
         self.scales = torch.empty(self.V, self.H // GROUP, dtype=torch.bfloat16, device=dev)
         self.zeros = torch.empty(self.V, self.H // GROUP, dtype=torch.bfloat16, device=dev)
         if fp8:
             dh_quantize_fp8(W, row_scale, self.packed, self.scales, self.zeros, stream)
+        elif bits == 4:
+            dh_quantize4(W, self.packed, self.scales, self.zeros, stream)
         else:
             dh_quantize(W, self.packed, self.scales, self.zeros, stream)
         self.kcand, self.rerank = kcand, rerank
@@ -310,7 +353,10 @@ class DraftHead:
         M = x.shape[0]
         idx = torch.empty(M, topk, dtype=torch.int32, device=x.device)
         logit = torch.empty(M, topk, dtype=torch.float32, device=x.device)
-        if self.row_scale is not None:
+        if self.bits == 4:
+            dh_forward4(x, self.packed, self.scales, self.zeros, self.W, self.kcand, self.rerank,
+                        topk, idx, logit, self.workspace(M), stream)
+        elif self.row_scale is not None:
             dh_forward_fp8w(x, self.packed, self.scales, self.zeros, self.W, self.row_scale,
                             self.kcand, self.rerank, topk, idx, logit, self.workspace(M), stream)
         else:

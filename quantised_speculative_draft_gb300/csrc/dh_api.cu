@@ -164,7 +164,7 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
                  size_t ws_bytes, float *coarse, float *cand_val, int32_t *cand_idx,
                  int32_t *sel_idx, float *sel_exact, void *const *events, cudaStream_t stream,
                  float *sel_val = nullptr, int id_offset = 0, bool candidates_only = false,
-                 const float *w_scale = nullptr)
+                 const float *w_scale = nullptr, int bits = 2)
 {
     // candidates_only: stop after the top-R selection (a vocabulary shard's local candidates,
     // indices offset by id_offset, values into sel_val); W, idx and logit are not used
@@ -186,6 +186,11 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
         return fail(DH_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
     const int path = choose_path(M, H);
     if (path < 0) return fail(DH_ERR_ARG, "the tcgen05 path does not support M=%d, H=%d", M, H);
+    if (bits == 4 && (path != DH_PATH_TC || !tc8_supported(M, H, 4)))
+        return fail(DH_ERR_ARG,
+                    "the 4-bit head runs on the 8-bit tcgen05 path only (M=%d, H=%d: %s)", M, H,
+                    path != DH_PATH_TC ? "another coarse path is selected"
+                                       : "its stages do not fit in shared memory");
     int *tflag = timeout_flag_ptr();
     if (!tflag) return fail(DH_ERR_CUDA, "cannot resolve the device status flag");
 
@@ -233,6 +238,7 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     a.H = H;
     a.V = V;
     a.kcand = kcand;
+    a.bits = bits;
     a.cand_val = cval;
     a.cand_idx = cidx;
     a.coarse = coarse;
@@ -324,7 +330,7 @@ int dh_quantize(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t 
     const void *ptrs[] = {W_bf16, packed, scales, zeros};
     for (const void *p : ptrs)
         if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
-    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, packed, scales, zeros,
+    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, 2, packed, scales, zeros,
                                       static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
     return ok();
@@ -359,7 +365,7 @@ int dh_quantize_fp8(const uint8_t *W_e4m3, const float *row_scale, int V, int H,
         if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
     if (reinterpret_cast<uintptr_t>(row_scale) & 3u)
         return fail(DH_ERR_ALIGN, "row_scale %p is not 4-byte aligned", row_scale);
-    cudaError_t err = launch_quantize(W_e4m3, row_scale, V, H, packed, scales, zeros,
+    cudaError_t err = launch_quantize(W_e4m3, row_scale, V, H, 2, packed, scales, zeros,
                                       static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
     return ok();
@@ -376,6 +382,63 @@ int dh_forward_fp8w(const uint16_t *x, const uint8_t *packed, const uint16_t *sc
     return forward_impl(x, packed, scales, zeros, W_e4m3, M, H, V, kcand, rerank, topk, idx,
                         logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
                         nullptr, static_cast<cudaStream_t>(stream), nullptr, 0, false, row_scale);
+}
+
+int dh_quantize4(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                 uint16_t *zeros, void *stream)
+{
+    if (!W_bf16 || !packed || !scales || !zeros)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (V < 1) return fail(DH_ERR_SHAPE, "V=%d must be >= 1", V);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    const void *ptrs[] = {W_bf16, packed, scales, zeros};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, 4, packed, scales, zeros,
+                                      static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
+    return ok();
+}
+
+int dh_forward4(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V, int kcand,
+                int rerank, int topk, int32_t *idx, float *logit, void *workspace,
+                size_t ws_bytes, void *stream)
+{
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, static_cast<cudaStream_t>(stream), nullptr, 0, false, nullptr,
+                        4);
+}
+
+int dh_forward4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                      const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                      int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                      void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                      int32_t *cand_idx, int32_t *sel_idx, float *sel_exact, void *stream)
+{
+    const void *opt[] = {coarse, cand_val, cand_idx, sel_idx, sel_exact};
+    for (const void *p : opt)
+        if (p && !aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
+                        sel_exact, nullptr, static_cast<cudaStream_t>(stream), nullptr, 0, false,
+                        nullptr, 4);
+}
+
+int dh_forward4_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                      const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                      int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                      void *workspace, size_t ws_bytes, void *const *events, void *stream)
+{
+    if (!events) return fail(DH_ERR_NULL, "events is NULL");
+    for (int i = 0; i < DH_NUM_STAGE_EVENTS; ++i)
+        if (!events[i]) return fail(DH_ERR_NULL, "events[%d] is NULL", i);
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        events, static_cast<cudaStream_t>(stream), nullptr, 0, false, nullptr,
+                        4);
 }
 
 int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,

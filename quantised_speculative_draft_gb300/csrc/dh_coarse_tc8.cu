@@ -41,6 +41,12 @@
 //                scale/zero fold into fp32 registers -- and at the tile end writes its half of
 //                the coarse values; the selection warp adds the halves
 // Every handoff is an mbarrier; every wait is bounded.
+//
+// The 4-bit head (BITS = 4, half split, bias 16; _quantize_head_now's 4-bit variant) runs the
+// same pipeline: a nibble masked in place is the exact e4m3 weight v 2^-9 (v in 0..15), and two
+// 128-byte boxes of a row (packed bytes 256 span ..) carry four groups -- low and high nibbles
+// of each box -- so one span is again four planes of 128 k, sixteen MMAs and four groups, with
+// NG = H / 512 spans per row.  The fold becomes (2^9 / 16) S p = 32 S p for every plane.
 #include "dh_common.cuh"
 #include "dh_internal.h"
 #include "dh_tcgen05.cuh"
@@ -68,8 +74,9 @@ constexpr int kDqWarps = 4; // dequant warps (4-7); the epilogue is warps 8-15
 // q = kU span + u uses slot q % kSlots and is issued by that slot's own thread, so the issuers
 // of different slots run concurrently (a thread issuing tcgen05.mma is held ~57 cycles per
 // instruction; two threads overlap).  Both sizes give two slots.
-template <int MP> struct Cfg8 {
+template <int MP, int BITS> struct Cfg8 {
     static constexpr int T = 2;
+    static constexpr int kPkBoxes = BITS == 4 ? 2 : 1;      // packed boxes per span
     static constexpr int N = MP * T;
     static constexpr int kU = MP == 16 ? 1 : 2;             // units per span
     static constexpr int kPP = 4 / kU;                      // planes per unit
@@ -78,7 +85,7 @@ template <int MP> struct Cfg8 {
     static constexpr int kSlotsFit = static_cast<int>(kTmemCols / kSlotCols);
     static constexpr int kSlots = kSlotsFit > 2 ? 2 : kSlotsFit; // one issuer warp per slot
     static constexpr uint32_t kXBytes = N * 512;            // 4 planes x 128 k x N rows
-    static constexpr uint32_t kStage = kPkBytes + kXBytes;  // multiple of 1024
+    static constexpr uint32_t kStage = kPkBoxes * kPkBytes + kXBytes; // multiple of 1024
     static_assert(kSlots == 2, "two unit slots must fit");
     static_assert(N % 16 == 0 && N <= 256, "MMA N out of range");
 };
@@ -109,6 +116,22 @@ template <int P>
 __device__ __forceinline__ uint32_t deq4_e4m3(uint32_t w)
 {
     return (P >= 2 ? (w >> 4) : w) & ((P & 1) ? 0x0C0C0C0Cu : 0x03030303u);
+}
+
+// The 4-bit head: the low / high nibble of each byte, v 2^-9 with v in 0..15 (e4m3 bytes 0..15
+// are exactly p 2^-9: subnormals up to 7, then 2^-6 (1 + m/8) = (8 + m) 2^-9).
+__device__ __forceinline__ uint32_t deq_nib_lo(uint32_t w) { return w & 0x0F0F0F0Fu; }
+__device__ __forceinline__ uint32_t deq_nib_hi(uint32_t w) { return (w >> 4) & 0x0F0F0F0Fu; }
+
+// Weight group (index into a row's H/128 groups, = first k / 128) of plane `plane` of span
+// `span` (NG = H / 512 spans per row).  2 bits: one 128-byte box per span, plane p at
+// k = p H/4 + 128 span.  4 bits: two 128-byte boxes per span (packed bytes 256 span ..), plane
+// p = 2 box + half at k = half H/2 + 128 (2 span + box).
+template <int BITS>
+__device__ __forceinline__ int plane_group(int plane, int span, int NG)
+{
+    if constexpr (BITS == 4) return (plane & 1) * 2 * NG + 2 * span + (plane >> 1);
+    else return plane * NG + span;
 }
 
 // Block top-KCAND of up to 4 (batch column, block) pairs at once.  Lane l holds rows l and
@@ -183,12 +206,13 @@ __device__ __forceinline__ void select_lane8(const float *vals0, const float *va
         }
 }
 
-template <int MP>
+template <int MP, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     coarse_tc8_kernel(const __grid_constant__ CUtensorMap tm_packed,
                       const __grid_constant__ CUtensorMap tm_x, const Tc8Params prm)
 {
-    using C = Cfg8<MP>;
+    using C = Cfg8<MP, BITS>;
+    constexpr int kBoxes = C::kPkBoxes;
     constexpr int N = C::N, T = C::T, K = C::kSlots, kU = C::kU, kPP = C::kPP;
     constexpr uint32_t kSlotCols = C::kSlotCols, kACols = C::kACols;
     constexpr int kRedHalf = MP * 2 * kRedPitch; // floats of one epilogue half's tile values
@@ -285,12 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t *const stage = stages + static_cast<size_t>(st) * C::kStage;
                     mbar_arrive_expect_tx(&full[st], C::kStage);
-                    tma_load_2d_hint(stage, &tm_packed, span * kSpanBytes, tile * kTileRows,
-                                     &full[st], policy);
+#pragma unroll
+                    for (int bx = 0; bx < kBoxes; ++bx)
+                        tma_load_2d_hint(stage + bx * kPkBytes, &tm_packed,
+                                         (kBoxes * span + bx) * kSpanBytes, tile * kTileRows,
+                                         &full[st], policy);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        tma_load_2d(stage + kPkBytes + q * (N * 128), &tm_x,
-                                    q * (prm.H / 4) + span * 128, 0, &full[st]);
+                        tma_load_2d(stage + kBoxes * kPkBytes + q * (N * 128), &tm_x,
+                                    plane_group<BITS>(q, span, NG) * kGroup, 0, &full[st]);
                 }
             }
         }
@@ -317,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         const uint32_t a_tmem = tmem + slot * kSlotCols;
                         const uint32_t d_tmem = a_tmem + kACols;
-                        const uint64_t xdesc = sw128_desc(
-                            smem_u32(stages + static_cast<size_t>(st) * C::kStage + kPkBytes));
+                        const uint64_t xdesc = sw128_desc(smem_u32(
+                            stages + static_cast<size_t>(st) * C::kStage + kBoxes * kPkBytes));
 #pragma unroll
                         for (int g = 0; g < kPP; ++g) {
                             const int plane = kPP * u + g;
@@ -354,16 +381,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t pk =
                     smem_u32(stages + static_cast<size_t>(st) * C::kStage) + row * kSpanBytes;
                 uint32_t w[32];
+                // this thread's row of packed box bx (128-byte swizzle)
+                auto load_box = [&](int bx) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t addr = pk + ((c ^ (row & 7)) << 4);
-                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]),
-                                   "=r"(w[4 * c + 3])
-                                 : "r"(addr));
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t addr = pk + bx * kPkBytes + ((c ^ (row & 7)) << 4);
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]),
+                                       "=r"(w[4 * c + 3])
+                                     : "r"(addr));
+                    }
+                };
+                if constexpr (BITS == 2) {
+                    // every plane of the span is in these 32 words: the stage goes back now
+                    load_box(0);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[st]);
                 // the span's units: their planes into the A buffer of slot q % K, free once that
                 // slot's previous unit (q - K) has been accumulated
 #pragma unroll
@@ -382,7 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int pp = 0; pp < kPP; pp += 2) {
                         const int plane = kPP * u + pp;
-                        if (plane == 0) {
+                        if constexpr (BITS == 4) {
+                            // planes 2 bx, 2 bx + 1 are the two nibbles of box bx
+                            load_box(plane >> 1);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                r0[i] = deq_nib_lo(w[i]);
+                                r1[i] = deq_nib_hi(w[i]);
+                            }
+                        } else if (plane == 0) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 r0[i] = deq4_e4m3<0>(w[i]);
@@ -404,6 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&a_full[slot]);
                 }
                 if (failed) break;
+                if constexpr (BITS == 4) {
+                    // both boxes have been read into registers
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
+                }
             }
         }
     } else if (warp >= 4 + kDqWarps) {
@@ -434,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s2[2], sz[2];
 #pragma unroll
                 for (int gl = 0; gl < 2; ++gl) {
-                    const int gi = (2 * h + gl) * NG + span;
+                    const int gi = plane_group<BITS>(2 * h + gl, span, NG);
                     uint16_t sb = 0, zb = 0;
                     if (full_tile) {
                         sb = sS[gi];
@@ -444,8 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         zb = __ldg(gZ + gi);
                     }
                     const float sv = bf16_bits_to_f32(sb), zv = bf16_bits_to_f32(zb);
-                    // odd planes carry 4 v 2^-9, even planes v 2^-9
-                    s2[gl] = (((2 * h + gl) & 1) ? 32.0f : 128.0f) * sv;
+                    // (S / B) sum x v with the MMA's sum of x v 2^-9 (2 bits, B = 4: odd planes
+                    // carry 4 v 2^-9, even planes v 2^-9; 4 bits, B = 16: v 2^-9)
+                    s2[gl] = (BITS == 4 ? 32.0f : (((2 * h + gl) & 1) ? 32.0f : 128.0f)) * sv;
                     sz[gl] = sv - zv;
                 }
                 // the unit holding this half's two groups (planes 2h, 2h+1) of the span
@@ -480,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < 2; ++u) {
                         const int k = 2 * wb + u, gl = k / CH, c = k % CH;
                         const float4 *xg = reinterpret_cast<const float4 *>(
-                            xs_s + ((2 * h + gl) * NG + span) * MP);
+                            xs_s + plane_group<BITS>(2 * h + gl, span, NG) * MP);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const float4 x4 = xg[c * 4 + j];
@@ -590,11 +638,11 @@ size_t tc8_fixed_smem(int MP, int H)
            MP * 4 + 64 * 8 + 32;
 }
 
-template <int MP>
+template <int MP, int BITS>
 cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
                        const Tc8Params &base, cudaStream_t stream)
 {
-    using C = Cfg8<MP>;
+    using C = Cfg8<MP, BITS>;
     CUtensorMap tm_x;
     CUresult r = encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                                       const_cast<uint8_t *>(xt8_chunk), base.H, C::N, base.H,
@@ -607,7 +655,7 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
     const size_t smem = fixed + static_cast<size_t>(nstage) * C::kStage;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(coarse_tc8_kernel<MP>,
+        cudaError_t e = cudaFuncSetAttribute(coarse_tc8_kernel<MP, BITS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemLimit8);
         if (e != cudaSuccess) return e;
@@ -616,20 +664,22 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
     Tc8Params prm = base;
     prm.nstage = nstage;
     const int grid = prm.ntiles < kNumSMs ? prm.ntiles : kNumSMs;
-    coarse_tc8_kernel<MP><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
+    coarse_tc8_kernel<MP, BITS><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
     return cudaGetLastError();
 }
 
 } // namespace
 
-bool tc8_supported(int M, int H)
+bool tc8_supported(int M, int H, int bits)
 {
     // the x staging keeps a row in registers: H <= 16384
     if (M < 1 || M > kMaxM || H % 512 != 0 || H > 16384) return false;
+    if (bits != 2 && bits != 4) return false;
     // at least two stages next to the fixed buffers, for every chunk size the batch uses
     for (int c = 0; c < tc8_chunks(M); ++c) {
         const int MP = tc8_chunk(M, c).MP;
-        const size_t stage = kPkBytes + static_cast<size_t>(MP) * 2 * 512;
+        const size_t stage = (bits / 2) * static_cast<size_t>(kPkBytes) +
+                             static_cast<size_t>(MP) * 2 * 512;
         if (tc8_fixed_smem(MP, H) + 2 * stage > static_cast<size_t>(kSmemLimit8)) return false;
     }
     return true;
@@ -653,11 +703,12 @@ int tc8_chunks(int M)
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream)
 {
     CUtensorMap tm_packed;
+    const int row_bytes = a.H * a.bits / 8; // packed bytes per row
     CUresult r = encode_tensor_map_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                                      const_cast<uint8_t *>(a.packed), a.H / 4, a.V, a.H / 4,
+                                      const_cast<uint8_t *>(a.packed), row_bytes, a.V, row_bytes,
                                       kSpanBytes, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (!tc8_supported(a.M, a.H)) return cudaErrorInvalidConfiguration;
+    if (!tc8_supported(a.M, a.H, a.bits)) return cudaErrorInvalidConfiguration;
     Tc8Params base;
     base.S = a.S;
     base.ZS = a.ZS;
@@ -680,8 +731,13 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
         base.inv_scale = w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows;
         const uint8_t *xt = w.xt8 + static_cast<size_t>(c) * w.chunk_bytes;
         cudaError_t e;
-        if (k.MP == 16) e = launch_cfg<16>(tm_packed, xt, base, stream);
-        else e = launch_cfg<32>(tm_packed, xt, base, stream);
+        if (a.bits == 4) {
+            if (k.MP == 16) e = launch_cfg<16, 4>(tm_packed, xt, base, stream);
+            else e = launch_cfg<32, 4>(tm_packed, xt, base, stream);
+        } else {
+            if (k.MP == 16) e = launch_cfg<16, 2>(tm_packed, xt, base, stream);
+            else e = launch_cfg<32, 2>(tm_packed, xt, base, stream);
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

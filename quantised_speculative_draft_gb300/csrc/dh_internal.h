@@ -25,9 +25,10 @@ constexpr int kRowDoneOffset = 128;
 constexpr int kSelDoneOffset = 256;
 
 // ---- launchers (each returns the launch status) ------------------------------------------
-// W: bf16 rows (wsc null) or e4m3 rows with per-row fp32 scales wsc.
-cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, uint8_t *packed,
-                            uint16_t *S, uint16_t *ZS, cudaStream_t stream);
+// W: bf16 rows (wsc null) or e4m3 rows with per-row fp32 scales wsc.  bits: 2 (quarter
+// split, packed [V, H/4]) or 4 (half split, packed [V, H/2]).
+cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits,
+                            uint8_t *packed, uint16_t *S, uint16_t *ZS, cudaStream_t stream);
 
 // x [M,H] bf16 -> group sums xs [Mpad, NGt] fp32 and the operand layouts of the coarse paths:
 //   xw (warp path): per 16-row batch chunk, B fragments in mma.sync register order
@@ -45,6 +46,8 @@ struct CoarseArgs {
     const uint16_t *xw; // warp path operand (per chunk)
     const uint16_t *xt; // tcgen05 path operand
     int M, H, V, kcand;
+    int bits = 2;       // 2: quarter-split packed [V, H/4]; 4: half-split [V, H/2] (tcgen05
+                        // 8-bit path only)
     float *cand_val;    // [M, nblk*kcand]
     int32_t *cand_idx;
     float *coarse;      // optional [M, V]
@@ -72,7 +75,7 @@ struct Tc8Workspace {
 cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
                             int *counters, int ncounters, cudaStream_t stream);
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream);
-bool tc8_supported(int M, int H); // shared memory of the 8-bit tcgen05 path fits
+bool tc8_supported(int M, int H, int bits = 2); // shared memory of the 8-bit tcgen05 path fits
 
 bool tc_supported(int M, int H);
 cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream);

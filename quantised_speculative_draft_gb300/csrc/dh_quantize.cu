@@ -1,14 +1,16 @@
-// dh_quantize.cu -- kernel (1): quantise and pack the bf16 head to 2 bits.
+// dh_quantize.cu -- kernel (1): quantise and pack the head to 2 (or 4) bits.
 //
-// radiance_drafthead.py, _quantize_head_now (BITS = 2, GROUP = 128): per (row, group of 128
-// consecutive k), in IEEE fp32,
-//     lo, hi = min, max;  sc = max((hi - lo) / 3, 1e-8);  zp = clamp(rne(-lo / sc), 0, 3)
-//     q_k = clamp(rne(w_k / sc + zp), 0, 3);  S = bf16(4 sc);  ZS = bf16(4 sc + zp sc)
-// and the quarter split: byte j of a row holds q[j] | q[Q+j] << 2 | q[2Q+j] << 4 | q[3Q+j] << 6.
+// radiance_drafthead.py, _quantize_head_now (GROUP = 128): per (row, group of 128 consecutive
+// k), in IEEE fp32, with L = 2^BITS - 1 levels and bias B = 2^BITS,
+//     lo, hi = min, max;  sc = max((hi - lo) / L, 1e-8);  zp = clamp(rne(-lo / sc), 0, L)
+//     q_k = clamp(rne(w_k / sc + zp), 0, L);  S = bf16(B sc);  ZS = bf16(B sc + zp sc)
+// BITS = 2 (the default head): quarter split, byte j of a row holds
+// q[j] | q[Q+j] << 2 | q[2Q+j] << 4 | q[3Q+j] << 6 (Q = H/4).  BITS = 4 (the page's 4-bit
+// variant): half split, byte j holds q[j] | q[H/2+j] << 4.
 //
 // Every arithmetic step uses the explicitly rounded intrinsics (no contraction into FMA),
 // division is correctly rounded, rintf rounds half to even: the result is bit-exact with the
-// definition.  The kernel is HBM-bound (2 bytes read per weight, 0.28 written).
+// definition.  The kernel is HBM-bound (2 bytes read per weight, BITS/8 + 1/32 written).
 //
 // An fp8 head (kernel (1) with the e4m3 input): row n's weights are the fp32 products
 // e4m3(b) * wsc[n] (radiance_drafthead.py, _quantize_head_now, the fp8 weight pre-scaled by its
@@ -16,9 +18,10 @@
 // those values.
 //
 // Work unit: one warp per (row n, span s), where span s is packed bytes [128 s, 128 s + 128)
-// of the row -- the four groups s, NG + s, 2 NG + s, 3 NG + s (NG = H / 512), one per plane.
-// Lane l owns packed bytes 4l .. 4l+3 of the span, i.e. four consecutive weights of each of
-// the four groups, so the packed word it writes needs nothing from other lanes.
+// of the row -- one group per plane p (P = 8 / BITS planes): group p NS + s, NS = H / (128 P)
+// spans per row.  Lane l owns packed bytes 4l .. 4l+3 of the span, i.e. four consecutive
+// weights of each of the span's groups, so the packed word it writes needs nothing from other
+// lanes.
 #include "dh_common.cuh"
 #include "dh_internal.h"
 
@@ -39,46 +42,49 @@ __device__ __forceinline__ float warp_max(float v)
 }
 
 // kFp8: W holds e4m3 bytes and wsc the per-row fp32 scales; otherwise W holds bf16.
-template <bool kFp8>
+template <bool kFp8, int BITS>
 __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ Wv,
                                                        const float *__restrict__ wsc,
                                                        uint8_t *__restrict__ packed,
                                                        uint16_t *__restrict__ S,
                                                        uint16_t *__restrict__ ZS, int V, int H)
 {
+    constexpr int P = 8 / BITS;                          // planes (codes per byte)
+    constexpr float L = static_cast<float>((1 << BITS) - 1);
+    constexpr float B = static_cast<float>(1 << BITS);
     const int lane = threadIdx.x & 31;
-    const int NG = H / 512;     // spans per row
+    const int PS = H / P;       // k stride between planes = packed bytes per row
+    const int NS = PS / 128;    // spans per row
     const int NGt = H / kGroup; // groups per row
-    const int Q = H / 4;
-    const long long total = static_cast<long long>(V) * NG;
+    const long long total = static_cast<long long>(V) * NS;
     const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
     for (long long item = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) +
                           (threadIdx.x >> 5);
          item < total; item += nwarps) {
-        const long long n = item / NG;
-        const int s = static_cast<int>(item - n * NG);
-        // four weights of each plane: k = p*Q + 128 s + 4 lane + i
-        float wv[4][4];
+        const long long n = item / NS;
+        const int s = static_cast<int>(item - n * NS);
+        // four weights of each plane: k = p*PS + 128 s + 4 lane + i
+        float wv[P][4];
         if constexpr (kFp8) {
             const uint8_t *row = static_cast<const uint8_t *>(Wv) + n * H;
             const float rs = __ldg(wsc + n);
-            uint32_t raw[4];
+            uint32_t raw[P];
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
-                raw[p] = __ldg(reinterpret_cast<const uint32_t *>(row + p * Q + 128 * s + 4 * lane));
+            for (int p = 0; p < P; ++p)
+                raw[p] = __ldg(reinterpret_cast<const uint32_t *>(row + p * PS + 128 * s + 4 * lane));
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
+            for (int p = 0; p < P; ++p)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     wv[p][i] = __fmul_rn(e4m3_to_f32(raw[p] >> (8 * i)), rs);
         } else {
             const uint16_t *row = static_cast<const uint16_t *>(Wv) + n * H;
-            uint2 raw[4];
+            uint2 raw[P];
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
-                raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * Q + 128 * s + 4 * lane));
+            for (int p = 0; p < P; ++p)
+                raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * PS + 128 * s + 4 * lane));
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
+            for (int p = 0; p < P; ++p) {
                 wv[p][0] = __uint_as_float(raw[p].x << 16);
                 wv[p][1] = __uint_as_float(raw[p].x & 0xFFFF0000u);
                 wv[p][2] = __uint_as_float(raw[p].y << 16);
@@ -87,47 +93,48 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
         }
         uint32_t word = 0;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
+        for (int p = 0; p < P; ++p) {
             const float *w = wv[p];
             float lo = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
             float hi = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
             lo = warp_min(lo);
             hi = warp_max(hi);
-            float sc = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+            float sc = __fdiv_rn(__fsub_rn(hi, lo), L);
             sc = fmaxf(sc, 1e-8f);
-            float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), 3.0f);
+            float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), L);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float r = rintf(__fadd_rn(__fdiv_rn(w[i], sc), zp));
-                uint32_t qv = static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 3.0f));
-                word |= qv << (8 * i + 2 * p);
+                uint32_t qv = static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), L));
+                word |= qv << (8 * i + BITS * p);
             }
             if (lane == p) {
-                const float s4 = __fmul_rn(4.0f, sc);
-                const long long gi = static_cast<long long>(p) * NG + s;
-                S[n * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(s4));
+                const float sb = __fmul_rn(B, sc);
+                const long long gi = static_cast<long long>(p) * NS + s;
+                S[n * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
                 ZS[n * NGt + gi] =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(s4, __fmul_rn(zp, sc))));
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(zp, sc))));
             }
         }
-        reinterpret_cast<uint32_t *>(packed + n * Q + 128 * s)[lane] = word;
+        reinterpret_cast<uint32_t *>(packed + n * PS + 128 * s)[lane] = word;
     }
 }
 
-cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, uint8_t *packed,
-                            uint16_t *S, uint16_t *ZS, cudaStream_t stream)
+cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits,
+                            uint8_t *packed, uint16_t *S, uint16_t *ZS, cudaStream_t stream)
 {
-    const long long total = static_cast<long long>(V) * (H / 512);
+    const long long total = static_cast<long long>(V) * (H / (bits == 4 ? 256 : 512));
     long long blocks = (total + 7) / 8;
     const long long cap = static_cast<long long>(kNumSMs) * 8;
     if (blocks > cap) blocks = cap;
-    if (wsc)
-        quantize_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, wsc, packed,
-                                                                                 S, ZS, V, H);
-    else
-        quantize_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, nullptr,
-                                                                                  packed, S, ZS,
-                                                                                  V, H);
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (bits == 4) {
+        if (wsc) quantize_kernel<true, 4><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
+        else quantize_kernel<false, 4><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
+    } else {
+        if (wsc) quantize_kernel<true, 2><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
+        else quantize_kernel<false, 2><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
+    }
     return cudaGetLastError();
 }
 

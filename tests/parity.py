@@ -30,8 +30,11 @@ def gpu_quantize(W: torch.Tensor):
     return packed, S, ZS
 
 
-def gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, debug=True, path=None):
-    """Run the CUDA path (dh_forward_debug) on device tensors; return numpy outputs."""
+def gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, debug=True, path=None, bits=2):
+    """Run the CUDA path (dh_forward_debug, or dh_forward4_debug for the 4-bit head) on device
+    tensors; return numpy outputs."""
+    fwd_dbg = dh.dh_forward4_debug if bits == 4 else dh.dh_forward_debug
+    fwd = dh.dh_forward4 if bits == 4 else dh.dh_forward
     M, H = x.shape
     V = W.shape[0]
     dev = x.device
@@ -51,15 +54,14 @@ def gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, debug=True, path=None)
             cidx = torch.full((M, nblk * kcand), -7, dtype=torch.int32, device=dev)
             sel = torch.full((M, rerank), -7, dtype=torch.int32, device=dev)
             sex = torch.full((M, rerank), float("nan"), dtype=torch.float32, device=dev)
-            dh.dh_forward_debug(x, packed, S, ZS, W, kcand, rerank, topk, idx, logit, ws,
-                                coarse=coarse, cand_val=cval, cand_idx=cidx, sel_idx=sel,
-                                sel_exact=sex)
+            fwd_dbg(x, packed, S, ZS, W, kcand, rerank, topk, idx, logit, ws, coarse=coarse,
+                    cand_val=cval, cand_idx=cidx, sel_idx=sel, sel_exact=sex)
             torch.cuda.synchronize()
             out.update(coarse=coarse.cpu().numpy(), cand_val=cval.cpu().numpy(),
                        cand_idx=cidx.cpu().numpy(), sel_idx=sel.cpu().numpy(),
                        sel_exact=sex.cpu().numpy())
         else:
-            dh.dh_forward(x, packed, S, ZS, W, kcand, rerank, topk, idx, logit, ws)
+            fwd(x, packed, S, ZS, W, kcand, rerank, topk, idx, logit, ws)
             torch.cuda.synchronize()
     finally:
         if prev is not None:
@@ -186,12 +188,12 @@ def check_result(gpu, ref, kcand, topk, x_bits, W_bits, rerank_fn=None):
     return ties
 
 
-def full_compare(x, W, packed, S, ZS, kcand, rerank, topk, path=None):
+def full_compare(x, W, packed, S, ZS, kcand, rerank, topk, path=None, bits=2):
     """Run GPU and oracle on the same tensors and apply every check.  Returns a report."""
-    gpu = gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, path=path)
+    gpu = gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, path=path, bits=bits)
     xb, Wb = host(x), host(W)
     pb, Sb, ZSb = host(packed), host(S), host(ZS)
-    ref = orc.forward(xb, pb, Sb, ZSb, Wb, kcand, rerank, topk)
+    ref = (orc.forward4 if bits == 4 else orc.forward)(xb, pb, Sb, ZSb, Wb, kcand, rerank, topk)
     rep = {}
     rep["coarse_worst"] = check_coarse(gpu["coarse"], ref["coarse"])
     tb = check_block_candidates(gpu, ref, kcand, W.shape[0])

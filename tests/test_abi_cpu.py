@@ -161,3 +161,22 @@ def test_fp8_head_entry_points_reject_bad_arguments(lib):
     bad = list(args)
     bad[15] = 16
     assert lib.dh_forward_fp8w(*bad) == -4
+
+
+def test_4bit_head_entry_points_reject_bad_arguments(lib):
+    assert lib.dh_quantize4(FAKE, 16, 1024, None, FAKE, FAKE, None) == -1
+    assert lib.dh_quantize4(FAKE, 16, 768, FAKE, FAKE, FAKE, None) == -2   # H % 512
+    assert lib.dh_quantize4(FAKE + 4, 16, 1024, FAKE, FAKE, FAKE, None) == -5
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1024, 8192, 1, 32, 1, FAKE, FAKE, FAKE, 1 << 40,
+            None]
+    bad = list(args)
+    bad[4] = None
+    assert lib.dh_forward4(*bad) == -1
+    bad = list(args)
+    bad[6] = 1000
+    assert lib.dh_forward4(*bad) == -2
+    bad = list(args)
+    bad[14] = 16
+    assert lib.dh_forward4(*bad) == -4
+    # the debug twin checks its optional outputs' alignment
+    assert lib.dh_forward4_debug(*args[:15], FAKE + 4, None, None, None, None, None) == -5
