@@ -30,6 +30,8 @@
  *   orc_quantize4      pinned: hand-worked golden group, on-grid rows recovered exactly,
  *                      half-split byte placement, error bound
  *   orc_coarse4        pinned: collapsed form == direct dequant-and-dot (exact scales)
+ *   orc_quantize_c4    pinned: hand-worked golden bytes; codes, S, ZS equal orc_quantize's
+ *   orc_coarse_c4      pinned: equals orc_coarse of the quarter-split packing of the same head
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -122,7 +124,8 @@ void orc_decode_e4m3(const uint8_t *b, int64_t n, float *out)
  * bits = 2: quarter split, byte j = q[j] | q[H/4+j] << 2 | q[H/2+j] << 4 | q[3H/4+j] << 6;
  * bits = 4: half split, byte j = q[j] | q[H/2+j] << 4. */
 static void quantize_row(const float *row, int64_t H, int bits, uint8_t *q, uint8_t *packed_row,
-                         uint16_t *S_row, uint16_t *ZS_row, float *sc_row, float *zp_row)
+                         uint16_t *S_row, uint16_t *ZS_row, float *sc_row, float *zp_row,
+                         int contiguous)
 {
     const int64_t NGt = H / GROUP, Q = H / 4;
     const float LEVELS = levels_of(bits), BIAS = bias_of(bits);
@@ -152,6 +155,12 @@ static void quantize_row(const float *row, int64_t H, int bits, uint8_t *q, uint
         for (int64_t j = 0; j < H / 2; ++j) packed_row[j] = (uint8_t)(q[j] | (q[H / 2 + j] << 4));
         return;
     }
+    if (contiguous) { /* the page's rejected layout: byte j holds k = 4j .. 4j+3 */
+        for (int64_t j = 0; j < Q; ++j)
+            packed_row[j] = (uint8_t)(q[4 * j] | (q[4 * j + 1] << 2) | (q[4 * j + 2] << 4) |
+                                      (q[4 * j + 3] << 6));
+        return;
+    }
     for (int64_t j = 0; j < Q; ++j)
         packed_row[j] = (uint8_t)(q[j] | (q[Q + j] << 2) | (q[2 * Q + j] << 4) | (q[3 * Q + j] << 6));
 }
@@ -171,7 +180,31 @@ int orc_quantize(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint1
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
         quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt,
-                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL);
+                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL, 0);
+    }
+    free(q);
+    free(row);
+    return 0;
+}
+
+/* The 2-bit head in the contiguous-4 layout the page measured against the quarter split
+ * (byte j = q[4j] | q[4j+1] << 2 | q[4j+2] << 4 | q[4j+3] << 6); codes, S and ZS are those of
+ * orc_quantize. */
+int orc_quantize_c4(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint16_t *S,
+                    uint16_t *ZS)
+{
+    if (H <= 0 || H % 512 != 0 || V <= 0) return -2;
+    const int64_t NGt = H / GROUP, Q = H / 4;
+    uint8_t *q = (uint8_t *)malloc((size_t)H);
+    float *row = (float *)malloc((size_t)H * sizeof(float));
+    if (!q || !row) {
+        free(q);
+        free(row);
+        return -1;
+    }
+    for (int64_t n = 0; n < V; ++n) {
+        for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
+        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL, 1);
     }
     free(q);
     free(row);
@@ -195,7 +228,7 @@ int orc_quantize4(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
         quantize_row(row, H, 4, q, packed + n * (H / 2), S + n * NGt, ZS + n * NGt,
-                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL);
+                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL, 0);
     }
     free(q);
     free(row);
@@ -218,7 +251,7 @@ int orc_quantize_fp8(const uint8_t *W8, const float *wsc, int64_t V, int64_t H, 
     }
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = e4m3_to_f32(W8[n * H + k]) * wsc[n];
-        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL);
+        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL, 0);
     }
     free(q);
     free(row);
@@ -246,7 +279,7 @@ typedef struct {
     const uint16_t *x;
     const uint8_t *packed;
     const uint16_t *S, *ZS;
-    int M, bits;
+    int M, bits, contiguous;
     int64_t H, V, n0, n1;
     double *c;
 } coarse_job;
@@ -262,8 +295,10 @@ static void *coarse_worker(void *arg)
     double *v = (double *)malloc((size_t)H * sizeof(double));
     for (int64_t n = jb->n0; n < jb->n1; ++n) {
         const uint8_t *prow = jb->packed + n * Q;
-        for (int64_t k = 0; k < H; ++k) /* v[n,k]: field k / Q of the packed byte k mod Q */
-            v[k] = (double)((prow[k % Q] >> (bits * (k / Q))) & mask);
+        if (jb->contiguous) /* v[n,k]: field k mod 4 of the packed byte k / 4 */
+            for (int64_t k = 0; k < H; ++k) v[k] = (double)((prow[k / 4] >> (2 * (k % 4))) & 3u);
+        else /* v[n,k]: field k / Q of the packed byte k mod Q */
+            for (int64_t k = 0; k < H; ++k) v[k] = (double)((prow[k % Q] >> (bits * (k / Q))) & mask);
         for (int m = 0; m < jb->M; ++m) {
             const uint16_t *xr = jb->x + (int64_t)m * H;
             double c = 0.0;
@@ -288,7 +323,7 @@ static void *coarse_worker(void *arg)
  * bias 4) or 4 (packed [V, H/2], bias 16). */
 static void coarse_bits(const uint16_t *x, const uint8_t *packed, const uint16_t *S,
                         const uint16_t *ZS, int M, int64_t H, int64_t V, double *c, int nthreads,
-                        int bits)
+                        int bits, int contiguous)
 {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
@@ -300,7 +335,7 @@ static void coarse_bits(const uint16_t *x, const uint8_t *packed, const uint16_t
         int64_t n0 = (int64_t)i * chunk, n1 = n0 + chunk;
         if (n1 > V) n1 = V;
         if (n0 >= n1) break;
-        jobs[i] = (coarse_job){x, packed, S, ZS, M, bits, H, V, n0, n1, c};
+        jobs[i] = (coarse_job){x, packed, S, ZS, M, bits, contiguous, H, V, n0, n1, c};
         if (nthreads == 1) {
             coarse_worker(&jobs[i]);
         } else {
@@ -314,14 +349,21 @@ static void coarse_bits(const uint16_t *x, const uint8_t *packed, const uint16_t
 void orc_coarse(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
                 int M, int64_t H, int64_t V, double *c, int nthreads)
 {
-    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2);
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2, 0);
+}
+
+/* The 2-bit head in the contiguous-4 layout (same group term). */
+void orc_coarse_c4(const uint16_t *x, const uint8_t *packed, const uint16_t *S,
+                   const uint16_t *ZS, int M, int64_t H, int64_t V, double *c, int nthreads)
+{
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2, 1);
 }
 
 /* The BITS = 4 head: group term S p - ZS xs with p = sum x (1 + v/16). */
 void orc_coarse4(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
                  int M, int64_t H, int64_t V, double *c, int nthreads)
 {
-    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 4);
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 4, 0);
 }
 
 /* ------------------------------------------------------------------------------------- */

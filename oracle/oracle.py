@@ -88,6 +88,10 @@ def _load():
         lib.orc_quantize4.restype = I
         lib.orc_coarse4.argtypes = [P, P, P, P, I, I64, I64, P, I]
         lib.orc_coarse4.restype = None
+        lib.orc_quantize_c4.argtypes = [P, I64, I64, P, P, P]
+        lib.orc_quantize_c4.restype = I
+        lib.orc_coarse_c4.argtypes = [P, P, P, P, I, I64, I64, P, I]
+        lib.orc_coarse_c4.restype = None
         _lib = lib
         return lib
 
@@ -155,6 +159,19 @@ def quantize4(W: np.ndarray, with_params: bool = False):
     return packed, S, ZS
 
 
+def quantize_c4(W: np.ndarray):
+    """The 2-bit head packed in the contiguous-4 layout: (packed u8 [V, H/4], S, ZS)."""
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    V, H = W.shape
+    packed = np.empty((V, H // 4), np.uint8)
+    S = np.empty((V, H // GROUP), np.uint16)
+    ZS = np.empty((V, H // GROUP), np.uint16)
+    rc = _load().orc_quantize_c4(_ptr(W), V, H, _ptr(packed), _ptr(S), _ptr(ZS))
+    if rc != 0:
+        raise ValueError(f"orc_quantize_c4: status {rc} (H must be a positive multiple of 512)")
+    return packed, S, ZS
+
+
 def unpack(packed: np.ndarray, H: int) -> np.ndarray:
     """Quarter-split packed bytes [V, H/4] -> 2-bit codes [V, H] (u8)."""
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
@@ -190,6 +207,20 @@ def coarse4(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
     c = np.empty((M, V), np.float64)
     _load().orc_coarse4(_ptr(x), _ptr(packed), _ptr(S), _ptr(ZS), M, H, V, _ptr(c),
                         nthreads or default_threads())
+    return c
+
+
+def coarse_c4(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
+    """Coarse values c [M, V] in fp64 from the contiguous-4 packed 2-bit head."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    S = np.ascontiguousarray(S, dtype=np.uint16)
+    ZS = np.ascontiguousarray(ZS, dtype=np.uint16)
+    M, H = x.shape
+    V = packed.shape[0]
+    c = np.empty((M, V), np.float64)
+    _load().orc_coarse_c4(_ptr(x), _ptr(packed), _ptr(S), _ptr(ZS), M, H, V, _ptr(c),
+                          nthreads or default_threads())
     return c
 
 
@@ -290,9 +321,10 @@ def forward_fp8(x, packed, S, ZS, W8, wsc, kcand: int, rerank_n: int, k: int,
 
 
 def forward4(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
-             nthreads: int | None = None) -> dict:
-    """The draft-head path on the 4-bit head (the rerank is the same bf16 one)."""
-    c = coarse4(x, packed, S, ZS, nthreads)
+             nthreads: int | None = None, coarse_fn=None) -> dict:
+    """The draft-head path on the 4-bit head (the rerank is the same bf16 one).  coarse_fn
+    replaces the coarse step (forward_c4 passes the contiguous-4 one)."""
+    c = (coarse_fn or coarse4)(x, packed, S, ZS, nthreads)
     cf = c.astype(np.float32)
     cval, cidx, nvalid = block_topk(cf, kcand)
     sel_idx, sel_val = select_topr(cval, cidx, rerank_n)
@@ -300,6 +332,12 @@ def forward4(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
     out_idx, out_val = topk(e, sel_idx, k)
     return dict(coarse=c, coarse_f32=cf, cand_val=cval, cand_idx=cidx, sel_idx=sel_idx,
                 sel_val=sel_val, exact=e, idx=out_idx, logit=out_val)
+
+
+def forward_c4(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
+               nthreads: int | None = None) -> dict:
+    """The draft-head path on the contiguous-4 packed 2-bit head."""
+    return forward4(x, packed, S, ZS, W, kcand, rerank_n, k, nthreads, coarse_fn=coarse_c4)
 
 
 def exact_head(x: np.ndarray, W: np.ndarray, nthreads: int | None = None) -> np.ndarray:

@@ -532,3 +532,37 @@ def test_forward4_with_full_candidate_pool_is_exact_topk():
     for m in range(M):
         o = _order(ex[m].astype(np.float32), np.arange(V))[:k]
         assert np.array_equal(res["idx"][m], o)
+
+
+# ------------------------------------------------------------------------------------------
+# the contiguous-4 layout (the page's packing ablation)
+# ------------------------------------------------------------------------------------------
+
+def test_packing_c4_golden_bytes():
+    spec = json.load(open(os.path.join(GOLD, "packing_c4.json")))
+    for row in spec["rows"]:
+        H = row["H"]
+        groups = [np.array([-0.75, 0.75] + [f] * 126) for f in row["group_fill"]]
+        W = f2bf_exact(np.concatenate(groups)[None, :])
+        packed, S, ZS = orc.quantize_c4(W)
+        want = np.zeros(H // 4, np.uint8)
+        for start, count, val in row["bytes"]:
+            want[start:start + count] = int(val, 16)
+        assert np.array_equal(packed[0], want), H
+        assert np.all(S == int(row["S"], 16)) and np.all(ZS == int(row["ZS"], 16))
+
+
+def test_c4_layout_holds_the_quarter_split_codes_and_coarse_values():
+    """Only the byte layout differs: unpacking either layout (test-side) gives the same codes,
+    S and ZS agree, and the coarse values of the two packings are identical."""
+    rng = np.random.default_rng(16)
+    V, H, M = 120, 1536, 3
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    pq, Sq, Zq = orc.quantize(W)
+    pc, Sc, Zc = orc.quantize_c4(W)
+    codes_c4 = np.stack([(pc >> (2 * f)) & 3 for f in range(4)], axis=2).reshape(V, H)
+    assert np.array_equal(codes_c4, my_unpack(pq, H))
+    assert np.array_equal(Sq, Sc) and np.array_equal(Zq, Zc)
+    assert np.array_equal(orc.coarse_c4(x, pc, Sc, Zc), orc.coarse(x, pq, Sq, Zq))
