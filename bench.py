@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--sets", type=int, default=2, help="resident input sets rotated per step")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8-head line")
     ap.add_argument("--no-int4", action="store_true", help="skip the 4-bit-head line")
+    ap.add_argument("--no-ablations", action="store_true", help="skip the layout ablations")
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2,
                     help="head width for --profile runs (4: the 4-bit head at KCAND=1)")
     ap.add_argument("--profile", action="store_true",
@@ -231,6 +232,25 @@ class Fp8Inputs:
         import quantised_speculative_draft_gb300 as dh
         dh.dh_forward_fp8w(self.x[:M], self.packed, self.S, self.ZS, self.W8, self.rs, KCAND,
                            RERANK, TOPK, idx, logit, ws)
+
+
+class C4Inputs(Inputs):
+    """The 2-bit head in the contiguous-4 layout (the page's packing ablation)."""
+
+    def __init__(self, seed, dev, max_m, V=V_FULL):
+        import quantised_speculative_draft_gb300 as dh
+        super().__init__(seed, dev, max_m, V)
+        dh.dh_quantize_c4(self.W, self.packed, self.S, self.ZS)
+
+    def call(self, M, ws, idx, logit):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_c4_debug(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND, RERANK,
+                               TOPK, idx, logit, ws)
+
+    def call_timed(self, M, ws, idx, logit, events):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_c4_debug(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND, RERANK,
+                               TOPK, idx, logit, ws, events=events)
 
 
 def make_outputs(M, dev, V=None):
@@ -525,6 +545,20 @@ def run_ours(args):
                                    "stages_us": {k: round(v, 2) for k, v in st4.items()}}
         del sets4
 
+    abl = None
+    if rank == 0 and not args.no_ablations:
+        nb = algorithmic_bytes(V_FULL, H_FULL)
+        setsc = [C4Inputs(seed, dev, M) for seed in range(args.sets)]
+        msc, _, _ = time_graph(setsc, M, args.sweep_steps, 5)
+        stc = time_stages(setsc, M, 20)
+        abl = {"contiguous4_packing": {
+            "workload": f"full-vocab 2-bit head M={M}, contiguous-4 layout (byte j = k 4j..4j+3)",
+            "us_per_call": round(msc * 1e3 / args.sweep_steps, 2),
+            "coarse_us": round(stc["coarse"], 2),
+            "coarse_frac_of_hbm": round(nb / stc["coarse"] / 1e3 / hbm, 4),
+            "quarter_split_coarse_us": round(stages["coarse"], 2)}}
+        del setsc
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xb, pb, Sb, ZSb, Wb = cpu_inputs
@@ -564,6 +598,7 @@ def run_ours(args):
             "pack": pack,
             "fp8_head": fp8,
             "int4_head": int4,
+            "ablations": abl,
             "sweep": sweep,
         }
         print(json.dumps(line), flush=True)

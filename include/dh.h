@@ -303,6 +303,26 @@ int dh_forward4_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *
                       int kcand, int rerank, int topk, int32_t *idx, float *logit,
                       void *workspace, size_t ws_bytes, void *const *events, void *stream);
 
+/*
+ * Contiguous-4 layout of the 2-bit head: the packing the page measured against the quarter
+ * split (radiance_drafthead.py, module docstring, 'Quarter-split packing' bullet).  Kept as an
+ * ablation: it gives the same coarse values and costs a byte transpose in the dequant.
+ *
+ * dh_quantize_c4 -- dh_quantize with packed [V, H/4] u8 holding k = 4j .. 4j+3 in byte j
+ *   (code of k = 4j + f in bits 2f .. 2f+1); scales and zeros as dh_quantize.  Bit-exact.
+ * dh_forward_c4_debug -- the forward on that packing (8-bit tcgen05 path only, DH_ERR_ARG
+ *   otherwise), with dh_forward_debug's optional outputs and, when `events` is not NULL,
+ *   dh_forward_timed's stage events.  Everything else as dh_forward.
+ */
+int dh_quantize_c4(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                   uint16_t *zeros, void *stream);
+int dh_forward_c4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                        const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                        int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                        void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                        int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
+                        void *const *events, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -164,7 +164,7 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
                  size_t ws_bytes, float *coarse, float *cand_val, int32_t *cand_idx,
                  int32_t *sel_idx, float *sel_exact, void *const *events, cudaStream_t stream,
                  float *sel_val = nullptr, int id_offset = 0, bool candidates_only = false,
-                 const float *w_scale = nullptr, int bits = 2)
+                 const float *w_scale = nullptr, int pack = kPackQuarter2)
 {
     // candidates_only: stop after the top-R selection (a vocabulary shard's local candidates,
     // indices offset by id_offset, values into sel_val); W, idx and logit are not used
@@ -186,9 +186,11 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
         return fail(DH_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
     const int path = choose_path(M, H);
     if (path < 0) return fail(DH_ERR_ARG, "the tcgen05 path does not support M=%d, H=%d", M, H);
-    if (bits == 4 && (path != DH_PATH_TC || !tc8_supported(M, H, 4)))
+    if (pack != kPackQuarter2 &&
+        (path != DH_PATH_TC || !tc8_supported(M, H, pack == kPackHalf4 ? 4 : 2)))
         return fail(DH_ERR_ARG,
-                    "the 4-bit head runs on the 8-bit tcgen05 path only (M=%d, H=%d: %s)", M, H,
+                    "the %s head runs on the 8-bit tcgen05 path only (M=%d, H=%d: %s)",
+                    pack == kPackHalf4 ? "4-bit" : "contiguous-4", M, H,
                     path != DH_PATH_TC ? "another coarse path is selected"
                                        : "its stages do not fit in shared memory");
     int *tflag = timeout_flag_ptr();
@@ -238,7 +240,7 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     a.H = H;
     a.V = V;
     a.kcand = kcand;
-    a.bits = bits;
+    a.pack = pack;
     a.cand_val = cval;
     a.cand_idx = cidx;
     a.coarse = coarse;
@@ -409,7 +411,7 @@ int dh_forward4(const uint16_t *x, const uint8_t *packed, const uint16_t *scales
     return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
                         logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
                         nullptr, static_cast<cudaStream_t>(stream), nullptr, 0, false, nullptr,
-                        4);
+                        kPackHalf4);
 }
 
 int dh_forward4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
@@ -424,7 +426,7 @@ int dh_forward4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *
     return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
                         logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
                         sel_exact, nullptr, static_cast<cudaStream_t>(stream), nullptr, 0, false,
-                        nullptr, 4);
+                        nullptr, kPackHalf4);
 }
 
 int dh_forward4_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
@@ -438,7 +440,43 @@ int dh_forward4_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *
     return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
                         logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
                         events, static_cast<cudaStream_t>(stream), nullptr, 0, false, nullptr,
-                        4);
+                        kPackHalf4);
+}
+
+int dh_quantize_c4(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                   uint16_t *zeros, void *stream)
+{
+    if (!W_bf16 || !packed || !scales || !zeros)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (V < 1) return fail(DH_ERR_SHAPE, "V=%d must be >= 1", V);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    const void *ptrs[] = {W_bf16, packed, scales, zeros};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    cudaError_t err = launch_quantize_c4(W_bf16, V, H, packed, scales, zeros,
+                                         static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
+    return ok();
+}
+
+int dh_forward_c4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                        const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                        int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                        void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                        int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
+                        void *const *events, void *stream)
+{
+    const void *opt[] = {coarse, cand_val, cand_idx, sel_idx, sel_exact};
+    for (const void *p : opt)
+        if (p && !aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    if (events)
+        for (int i = 0; i < DH_NUM_STAGE_EVENTS; ++i)
+            if (!events[i]) return fail(DH_ERR_NULL, "events[%d] is NULL", i);
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
+                        sel_exact, events, static_cast<cudaStream_t>(stream), nullptr, 0, false,
+                        nullptr, kPackContig2);
 }
 
 int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,

@@ -74,9 +74,9 @@ constexpr int kDqWarps = 4; // dequant warps (4-7); the epilogue is warps 8-15
 // q = kU span + u uses slot q % kSlots and is issued by that slot's own thread, so the issuers
 // of different slots run concurrently (a thread issuing tcgen05.mma is held ~57 cycles per
 // instruction; two threads overlap).  Both sizes give two slots.
-template <int MP, int BITS> struct Cfg8 {
+template <int MP, int PACK> struct Cfg8 {
     static constexpr int T = 2;
-    static constexpr int kPkBoxes = BITS == 4 ? 2 : 1;      // packed boxes per span
+    static constexpr int kPkBoxes = PACK == kPackHalf4 ? 2 : 1; // packed boxes per span
     static constexpr int N = MP * T;
     static constexpr int kU = MP == 16 ? 1 : 2;             // units per span
     static constexpr int kPP = 4 / kU;                      // planes per unit
@@ -123,14 +123,33 @@ __device__ __forceinline__ uint32_t deq4_e4m3(uint32_t w)
 __device__ __forceinline__ uint32_t deq_nib_lo(uint32_t w) { return w & 0x0F0F0F0Fu; }
 __device__ __forceinline__ uint32_t deq_nib_hi(uint32_t w) { return (w >> 4) & 0x0F0F0F0Fu; }
 
+// The contiguous-4 layout (the page's packing ablation): the eight words w[8p .. 8p+7] of a
+// span are group p's 128 codes, byte j holding k = 4j .. 4j+3.  The four fields of every byte
+// masked to the low bits (v 2^-9) and transposed 4 x 4 by byte permutes give four words of
+// e4m3 weights in k order: the price of the layout is this transpose (15 operations per
+// 16 weights against 4 for the quarter split).
+__device__ __forceinline__ void deq_c4(uint32_t w, uint32_t (&o)[4])
+{
+    const uint32_t p0 = w & 0x03030303u, p1 = (w >> 2) & 0x03030303u;
+    const uint32_t p2 = (w >> 4) & 0x03030303u, p3 = (w >> 6) & 0x03030303u;
+    const uint32_t t0 = __byte_perm(p0, p1, 0x5140), t1 = __byte_perm(p0, p1, 0x7362);
+    const uint32_t t2 = __byte_perm(p2, p3, 0x5140), t3 = __byte_perm(p2, p3, 0x7362);
+    o[0] = __byte_perm(t0, t2, 0x5410);
+    o[1] = __byte_perm(t0, t2, 0x7632);
+    o[2] = __byte_perm(t1, t3, 0x5410);
+    o[3] = __byte_perm(t1, t3, 0x7632);
+}
+
 // Weight group (index into a row's H/128 groups, = first k / 128) of plane `plane` of span
-// `span` (NG = H / 512 spans per row).  2 bits: one 128-byte box per span, plane p at
-// k = p H/4 + 128 span.  4 bits: two 128-byte boxes per span (packed bytes 256 span ..), plane
-// p = 2 box + half at k = half H/2 + 128 (2 span + box).
-template <int BITS>
+// `span` (NG = H / 512 spans per row).  Quarter split: one 128-byte box per span, plane p at
+// k = p H/4 + 128 span.  Half split (4 bits): two 128-byte boxes per span (packed bytes
+// 256 span ..), plane p = 2 box + half at k = half H/2 + 128 (2 span + box).  Contiguous-4:
+// the span's 512 consecutive k, plane p = group 4 span + p.
+template <int PACK>
 __device__ __forceinline__ int plane_group(int plane, int span, int NG)
 {
-    if constexpr (BITS == 4) return (plane & 1) * 2 * NG + 2 * span + (plane >> 1);
+    if constexpr (PACK == kPackHalf4) return (plane & 1) * 2 * NG + 2 * span + (plane >> 1);
+    else if constexpr (PACK == kPackContig2) return 4 * span + plane;
     else return plane * NG + span;
 }
 
@@ -206,12 +225,13 @@ __device__ __forceinline__ void select_lane8(const float *vals0, const float *va
         }
 }
 
-template <int MP, int BITS>
+template <int MP, int PACK>
 __global__ void __launch_bounds__(kThreads, 1)
     coarse_tc8_kernel(const __grid_constant__ CUtensorMap tm_packed,
                       const __grid_constant__ CUtensorMap tm_x, const Tc8Params prm)
 {
-    using C = Cfg8<MP, BITS>;
+    using C = Cfg8<MP, PACK>;
+    constexpr int BITS = PACK == kPackHalf4 ? 4 : 2;
     constexpr int kBoxes = C::kPkBoxes;
     constexpr int N = C::N, T = C::T, K = C::kSlots, kU = C::kU, kPP = C::kPP;
     constexpr uint32_t kSlotCols = C::kSlotCols, kACols = C::kACols;
@@ -317,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         tma_load_2d(stage + kBoxes * kPkBytes + q * (N * 128), &tm_x,
-                                    plane_group<BITS>(q, span, NG) * kGroup, 0, &full[st]);
+                                    plane_group<PACK>(q, span, NG) * kGroup, 0, &full[st]);
                 }
             }
         }
@@ -424,6 +444,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 r0[i] = deq_nib_lo(w[i]);
                                 r1[i] = deq_nib_hi(w[i]);
                             }
+                        } else if constexpr (PACK == kPackContig2) {
+                            // planes p, p + 1 are words 8p .. 8p + 15
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                uint32_t o0[4], o1[4];
+                                deq_c4(w[8 * plane + i], o0);
+                                deq_c4(w[8 * plane + 8 + i], o1);
+#pragma unroll
+                                for (int b = 0; b < 4; ++b) {
+                                    r0[4 * i + b] = o0[b];
+                                    r1[4 * i + b] = o1[b];
+                                }
+                            }
                         } else if (plane == 0) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
@@ -481,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s2[2], sz[2];
 #pragma unroll
                 for (int gl = 0; gl < 2; ++gl) {
-                    const int gi = plane_group<BITS>(2 * h + gl, span, NG);
+                    const int gi = plane_group<PACK>(2 * h + gl, span, NG);
                     uint16_t sb = 0, zb = 0;
                     if (full_tile) {
                         sb = sS[gi];
@@ -493,7 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float sv = bf16_bits_to_f32(sb), zv = bf16_bits_to_f32(zb);
                     // (S / B) sum x v with the MMA's sum of x v 2^-9 (2 bits, B = 4: odd planes
                     // carry 4 v 2^-9, even planes v 2^-9; 4 bits, B = 16: v 2^-9)
-                    s2[gl] = (BITS == 4 ? 32.0f : (((2 * h + gl) & 1) ? 32.0f : 128.0f)) * sv;
+                    // carry 4 v 2^-9, even planes v 2^-9; contiguous-4: every plane v 2^-9)
+                    s2[gl] = (BITS == 4 ? 32.0f
+                                        : (PACK == kPackQuarter2 && ((2 * h + gl) & 1) ? 32.0f
+                                                                                        : 128.0f)) *
+                             sv;
                     sz[gl] = sv - zv;
                 }
                 // the unit holding this half's two groups (planes 2h, 2h+1) of the span
@@ -528,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < 2; ++u) {
                         const int k = 2 * wb + u, gl = k / CH, c = k % CH;
                         const float4 *xg = reinterpret_cast<const float4 *>(
-                            xs_s + plane_group<BITS>(2 * h + gl, span, NG) * MP);
+                            xs_s + plane_group<PACK>(2 * h + gl, span, NG) * MP);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const float4 x4 = xg[c * 4 + j];
@@ -638,11 +675,11 @@ size_t tc8_fixed_smem(int MP, int H)
            MP * 4 + 64 * 8 + 32;
 }
 
-template <int MP, int BITS>
+template <int MP, int PACK>
 cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
                        const Tc8Params &base, cudaStream_t stream)
 {
-    using C = Cfg8<MP, BITS>;
+    using C = Cfg8<MP, PACK>;
     CUtensorMap tm_x;
     CUresult r = encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                                       const_cast<uint8_t *>(xt8_chunk), base.H, C::N, base.H,
@@ -655,7 +692,7 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
     const size_t smem = fixed + static_cast<size_t>(nstage) * C::kStage;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(coarse_tc8_kernel<MP, BITS>,
+        cudaError_t e = cudaFuncSetAttribute(coarse_tc8_kernel<MP, PACK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemLimit8);
         if (e != cudaSuccess) return e;
@@ -664,7 +701,7 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
     Tc8Params prm = base;
     prm.nstage = nstage;
     const int grid = prm.ntiles < kNumSMs ? prm.ntiles : kNumSMs;
-    coarse_tc8_kernel<MP, BITS><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
+    coarse_tc8_kernel<MP, PACK><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
     return cudaGetLastError();
 }
 
@@ -703,12 +740,13 @@ int tc8_chunks(int M)
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream)
 {
     CUtensorMap tm_packed;
-    const int row_bytes = a.H * a.bits / 8; // packed bytes per row
+    const int bits = a.pack == kPackHalf4 ? 4 : 2;
+    const int row_bytes = a.H * bits / 8; // packed bytes per row
     CUresult r = encode_tensor_map_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                                       const_cast<uint8_t *>(a.packed), row_bytes, a.V, row_bytes,
                                       kSpanBytes, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (!tc8_supported(a.M, a.H, a.bits)) return cudaErrorInvalidConfiguration;
+    if (!tc8_supported(a.M, a.H, bits)) return cudaErrorInvalidConfiguration;
     Tc8Params base;
     base.S = a.S;
     base.ZS = a.ZS;
@@ -731,12 +769,15 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
         base.inv_scale = w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows;
         const uint8_t *xt = w.xt8 + static_cast<size_t>(c) * w.chunk_bytes;
         cudaError_t e;
-        if (a.bits == 4) {
-            if (k.MP == 16) e = launch_cfg<16, 4>(tm_packed, xt, base, stream);
-            else e = launch_cfg<32, 4>(tm_packed, xt, base, stream);
+        if (a.pack == kPackHalf4) {
+            if (k.MP == 16) e = launch_cfg<16, kPackHalf4>(tm_packed, xt, base, stream);
+            else e = launch_cfg<32, kPackHalf4>(tm_packed, xt, base, stream);
+        } else if (a.pack == kPackContig2) {
+            if (k.MP == 16) e = launch_cfg<16, kPackContig2>(tm_packed, xt, base, stream);
+            else e = launch_cfg<32, kPackContig2>(tm_packed, xt, base, stream);
         } else {
-            if (k.MP == 16) e = launch_cfg<16, 2>(tm_packed, xt, base, stream);
-            else e = launch_cfg<32, 2>(tm_packed, xt, base, stream);
+            if (k.MP == 16) e = launch_cfg<16, kPackQuarter2>(tm_packed, xt, base, stream);
+            else e = launch_cfg<32, kPackQuarter2>(tm_packed, xt, base, stream);
         }
         if (e != cudaSuccess) return e;
     }

@@ -24,11 +24,20 @@ constexpr int kNumCounters = 384;   // [0, 64): work queues, [128, 256): per-row
 constexpr int kRowDoneOffset = 128;
 constexpr int kSelDoneOffset = 256;
 
+// Packed layouts of the head: the 2-bit quarter split (the default), the 4-bit half split and
+// the 2-bit contiguous-4 layout (the page's packing ablation).
+constexpr int kPackQuarter2 = 0;
+constexpr int kPackHalf4 = 1;
+constexpr int kPackContig2 = 2;
+
 // ---- launchers (each returns the launch status) ------------------------------------------
 // W: bf16 rows (wsc null) or e4m3 rows with per-row fp32 scales wsc.  bits: 2 (quarter
 // split, packed [V, H/4]) or 4 (half split, packed [V, H/2]).
 cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits,
                             uint8_t *packed, uint16_t *S, uint16_t *ZS, cudaStream_t stream);
+// The bf16 head in the contiguous-4 layout, packed [V, H/4].
+cudaError_t launch_quantize_c4(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
+                               uint16_t *ZS, cudaStream_t stream);
 
 // x [M,H] bf16 -> group sums xs [Mpad, NGt] fp32 and the operand layouts of the coarse paths:
 //   xw (warp path): per 16-row batch chunk, B fragments in mma.sync register order
@@ -46,8 +55,8 @@ struct CoarseArgs {
     const uint16_t *xw; // warp path operand (per chunk)
     const uint16_t *xt; // tcgen05 path operand
     int M, H, V, kcand;
-    int bits = 2;       // 2: quarter-split packed [V, H/4]; 4: half-split [V, H/2] (tcgen05
-                        // 8-bit path only)
+    int pack = 0;       // kPack*: the packed layout (all but the quarter split run on the
+                        // 8-bit tcgen05 path only)
     float *cand_val;    // [M, nblk*kcand]
     int32_t *cand_idx;
     float *coarse;      // optional [M, V]

@@ -120,6 +120,76 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
     }
 }
 
+// The contiguous-4 layout of the 2-bit head (the page's packing ablation: byte j holds
+// k = 4j .. 4j+3, code of k = 4j + f in bits 2f .. 2f+1).  Same group steps as above.  Work
+// unit: one warp per (row n, span s) of 128 packed bytes = k in [512 s, 512 s + 512) = groups
+// 4s .. 4s+3; lane l owns bytes 4l .. 4l+3 (k = 512 s + 16 l .. + 15), so each group is eight
+// lanes and its min / max reduce over those eight.
+__global__ void __launch_bounds__(256) quantize_c4_kernel(const uint16_t *__restrict__ W,
+                                                          uint8_t *__restrict__ packed,
+                                                          uint16_t *__restrict__ S,
+                                                          uint16_t *__restrict__ ZS, int V, int H)
+{
+    const int lane = threadIdx.x & 31;
+    const int Q = H / 4, NS = Q / 128, NGt = H / kGroup;
+    const long long total = static_cast<long long>(V) * NS;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long item = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) +
+                          (threadIdx.x >> 5);
+         item < total; item += nwarps) {
+        const long long n = item / NS;
+        const int s = static_cast<int>(item - n * NS);
+        const uint4 *src = reinterpret_cast<const uint4 *>(W + n * H + 512 * s + 16 * lane);
+        const uint4 a = __ldg(src), b = __ldg(src + 1);
+        const uint32_t raw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float w[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            w[2 * i] = __uint_as_float(raw[i] << 16);
+            w[2 * i + 1] = __uint_as_float(raw[i] & 0xFFFF0000u);
+        }
+        float lo = w[0], hi = w[0];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            lo = fminf(lo, w[i]);
+            hi = fmaxf(hi, w[i]);
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        float sc = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+        sc = fmaxf(sc, 1e-8f);
+        const float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), 3.0f);
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float r = rintf(__fadd_rn(__fdiv_rn(w[i], sc), zp));
+            word |= static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 3.0f)) << (2 * i);
+        }
+        if ((lane & 7) == 0) {
+            const float s4 = __fmul_rn(4.0f, sc);
+            const long long gi = 4LL * s + (lane >> 3);
+            S[n * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(s4));
+            ZS[n * NGt + gi] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(s4, __fmul_rn(zp, sc))));
+        }
+        reinterpret_cast<uint32_t *>(packed + n * Q + 128 * s)[lane] = word;
+    }
+}
+
+cudaError_t launch_quantize_c4(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
+                               uint16_t *ZS, cudaStream_t stream)
+{
+    const long long total = static_cast<long long>(V) * (H / 512);
+    long long blocks = (total + 7) / 8;
+    const long long cap = static_cast<long long>(kNumSMs) * 8;
+    if (blocks > cap) blocks = cap;
+    quantize_c4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, packed, S, ZS, V, H);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits,
                             uint8_t *packed, uint16_t *S, uint16_t *ZS, cudaStream_t stream)
 {

@@ -180,3 +180,15 @@ def test_4bit_head_entry_points_reject_bad_arguments(lib):
     assert lib.dh_forward4(*bad) == -4
     # the debug twin checks its optional outputs' alignment
     assert lib.dh_forward4_debug(*args[:15], FAKE + 4, None, None, None, None, None) == -5
+
+
+def test_c4_entry_points_reject_bad_arguments(lib):
+    assert lib.dh_quantize_c4(FAKE, 16, 1024, None, FAKE, FAKE, None) == -1
+    assert lib.dh_quantize_c4(FAKE, 16, 768, FAKE, FAKE, FAKE, None) == -2
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1024, 8192, 8, 32, 1, FAKE, FAKE, FAKE, 1 << 40]
+    assert lib.dh_forward_c4_debug(*args, FAKE + 4, None, None, None, None, None, None) == -5
+    events = (ctypes.c_void_p * 6)(FAKE, FAKE, None, FAKE, FAKE, FAKE)
+    assert lib.dh_forward_c4_debug(*args, None, None, None, None, None, events, None) == -1
+    bad = list(args)
+    bad[6] = 1000
+    assert lib.dh_forward_c4_debug(*bad, None, None, None, None, None, None, None) == -2
