@@ -32,6 +32,9 @@
  *   orc_coarse4        pinned: collapsed form == direct dequant-and-dot (exact scales)
  *   orc_quantize_c4    pinned: hand-worked golden bytes; codes, S, ZS equal orc_quantize's
  *   orc_coarse_c4      pinned: equals orc_coarse of the quarter-split packing of the same head
+ *   orc_quantize_g64   pinned: hand-worked golden groups at 64; each 64-group equals the
+ *                      128-group quantiser on that group's values doubled in place
+ *   orc_coarse_g64     pinned: collapsed form == direct dequant-and-dot over 64-groups
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -125,24 +128,24 @@ void orc_decode_e4m3(const uint8_t *b, int64_t n, float *out)
  * bits = 4: half split, byte j = q[j] | q[H/2+j] << 4. */
 static void quantize_row(const float *row, int64_t H, int bits, uint8_t *q, uint8_t *packed_row,
                          uint16_t *S_row, uint16_t *ZS_row, float *sc_row, float *zp_row,
-                         int contiguous)
+                         int contiguous, int G)
 {
-    const int64_t NGt = H / GROUP, Q = H / 4;
+    const int64_t NGt = H / G, Q = H / 4;
     const float LEVELS = levels_of(bits), BIAS = bias_of(bits);
     for (int64_t gi = 0; gi < NGt; ++gi) {
-        float lo = row[gi * GROUP], hi = lo;
-        for (int t = 1; t < GROUP; ++t) {
-            float w = row[gi * GROUP + t];
+        float lo = row[gi * G], hi = lo;
+        for (int t = 1; t < G; ++t) {
+            float w = row[gi * G + t];
             if (w < lo) lo = w;
             if (w > hi) hi = w;
         }
         float sc = (hi - lo) / LEVELS;
         if (sc < 1e-8f) sc = 1e-8f;
         float zp = clampf(round_half_even((-lo) / sc), 0.0f, LEVELS);
-        for (int t = 0; t < GROUP; ++t) {
-            float w = row[gi * GROUP + t];
+        for (int t = 0; t < G; ++t) {
+            float w = row[gi * G + t];
             float r = round_half_even(w / sc + zp);
-            q[gi * GROUP + t] = (uint8_t)clampf(r, 0.0f, LEVELS);
+            q[gi * G + t] = (uint8_t)clampf(r, 0.0f, LEVELS);
         }
         float s4 = BIAS * sc;
         float zsc = zp * sc;
@@ -180,7 +183,7 @@ int orc_quantize(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint1
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
         quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt,
-                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL, 0);
+                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL, 0, GROUP);
     }
     free(q);
     free(row);
@@ -204,7 +207,31 @@ int orc_quantize_c4(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, ui
     }
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
-        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL, 1);
+        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL, 1, GROUP);
+    }
+    free(q);
+    free(row);
+    return 0;
+}
+
+/* The group-size ablation the page measured (module docstring, 'Group 128, not 64'): the
+ * 2-bit head with groups of 64 consecutive k, S and ZS [V, H/64]; quarter-split packing. */
+int orc_quantize_g64(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint16_t *S,
+                     uint16_t *ZS)
+{
+    if (H <= 0 || H % 512 != 0 || V <= 0) return -2;
+    const int64_t NG64 = H / 64, Q = H / 4;
+    uint8_t *q = (uint8_t *)malloc((size_t)H);
+    float *row = (float *)malloc((size_t)H * sizeof(float));
+    if (!q || !row) {
+        free(q);
+        free(row);
+        return -1;
+    }
+    for (int64_t n = 0; n < V; ++n) {
+        for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
+        quantize_row(row, H, 2, q, packed + n * Q, S + n * NG64, ZS + n * NG64, NULL, NULL, 0,
+                     64);
     }
     free(q);
     free(row);
@@ -228,7 +255,7 @@ int orc_quantize4(const uint16_t *W, int64_t V, int64_t H, uint8_t *packed, uint
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = bf16_to_f32(W[n * H + k]);
         quantize_row(row, H, 4, q, packed + n * (H / 2), S + n * NGt, ZS + n * NGt,
-                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL, 0);
+                     sc_out ? sc_out + n * NGt : NULL, zp_out ? zp_out + n * NGt : NULL, 0, GROUP);
     }
     free(q);
     free(row);
@@ -251,7 +278,7 @@ int orc_quantize_fp8(const uint8_t *W8, const float *wsc, int64_t V, int64_t H, 
     }
     for (int64_t n = 0; n < V; ++n) {
         for (int64_t k = 0; k < H; ++k) row[k] = e4m3_to_f32(W8[n * H + k]) * wsc[n];
-        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL, 0);
+        quantize_row(row, H, 2, q, packed + n * Q, S + n * NGt, ZS + n * NGt, NULL, NULL, 0, GROUP);
     }
     free(q);
     free(row);
@@ -279,7 +306,7 @@ typedef struct {
     const uint16_t *x;
     const uint8_t *packed;
     const uint16_t *S, *ZS;
-    int M, bits, contiguous;
+    int M, bits, contiguous, group;
     int64_t H, V, n0, n1;
     double *c;
 } coarse_job;
@@ -288,7 +315,8 @@ static void *coarse_worker(void *arg)
 {
     coarse_job *jb = (coarse_job *)arg;
     const int bits = jb->bits;
-    const int64_t H = jb->H, NGt = H / GROUP;
+    const int G = jb->group;
+    const int64_t H = jb->H, NGt = H / G;
     const int64_t Q = H / (8 / bits); /* packed bytes per row: codes of k share byte k mod Q */
     const double bias = bits == 4 ? 16.0 : 4.0;
     const unsigned mask = (1u << bits) - 1u;
@@ -304,9 +332,9 @@ static void *coarse_worker(void *arg)
             double c = 0.0;
             for (int64_t gi = 0; gi < NGt; ++gi) {
                 double p = 0.0, xs = 0.0;
-                for (int t = 0; t < GROUP; ++t) {
-                    double xk = (double)bf16_to_f32(xr[gi * GROUP + t]);
-                    p += xk * (1.0 + v[gi * GROUP + t] / bias);
+                for (int t = 0; t < G; ++t) {
+                    double xk = (double)bf16_to_f32(xr[gi * G + t]);
+                    p += xk * (1.0 + v[gi * G + t] / bias);
                     xs += xk;
                 }
                 c += (double)bf16_to_f32(jb->S[n * NGt + gi]) * p -
@@ -323,7 +351,7 @@ static void *coarse_worker(void *arg)
  * bias 4) or 4 (packed [V, H/2], bias 16). */
 static void coarse_bits(const uint16_t *x, const uint8_t *packed, const uint16_t *S,
                         const uint16_t *ZS, int M, int64_t H, int64_t V, double *c, int nthreads,
-                        int bits, int contiguous)
+                        int bits, int contiguous, int group)
 {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
@@ -335,7 +363,7 @@ static void coarse_bits(const uint16_t *x, const uint8_t *packed, const uint16_t
         int64_t n0 = (int64_t)i * chunk, n1 = n0 + chunk;
         if (n1 > V) n1 = V;
         if (n0 >= n1) break;
-        jobs[i] = (coarse_job){x, packed, S, ZS, M, bits, contiguous, H, V, n0, n1, c};
+        jobs[i] = (coarse_job){x, packed, S, ZS, M, bits, contiguous, group, H, V, n0, n1, c};
         if (nthreads == 1) {
             coarse_worker(&jobs[i]);
         } else {
@@ -349,21 +377,28 @@ static void coarse_bits(const uint16_t *x, const uint8_t *packed, const uint16_t
 void orc_coarse(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
                 int M, int64_t H, int64_t V, double *c, int nthreads)
 {
-    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2, 0);
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2, 0, GROUP);
+}
+
+/* The 2-bit head with groups of 64 (S, ZS [V, H/64]): the same group term per 64-group. */
+void orc_coarse_g64(const uint16_t *x, const uint8_t *packed, const uint16_t *S,
+                    const uint16_t *ZS, int M, int64_t H, int64_t V, double *c, int nthreads)
+{
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2, 0, 64);
 }
 
 /* The 2-bit head in the contiguous-4 layout (same group term). */
 void orc_coarse_c4(const uint16_t *x, const uint8_t *packed, const uint16_t *S,
                    const uint16_t *ZS, int M, int64_t H, int64_t V, double *c, int nthreads)
 {
-    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2, 1);
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 2, 1, GROUP);
 }
 
 /* The BITS = 4 head: group term S p - ZS xs with p = sum x (1 + v/16). */
 void orc_coarse4(const uint16_t *x, const uint8_t *packed, const uint16_t *S, const uint16_t *ZS,
                  int M, int64_t H, int64_t V, double *c, int nthreads)
 {
-    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 4, 0);
+    coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 4, 0, GROUP);
 }
 
 /* ------------------------------------------------------------------------------------- */

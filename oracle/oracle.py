@@ -92,6 +92,10 @@ def _load():
         lib.orc_quantize_c4.restype = I
         lib.orc_coarse_c4.argtypes = [P, P, P, P, I, I64, I64, P, I]
         lib.orc_coarse_c4.restype = None
+        lib.orc_quantize_g64.argtypes = [P, I64, I64, P, P, P]
+        lib.orc_quantize_g64.restype = I
+        lib.orc_coarse_g64.argtypes = [P, P, P, P, I, I64, I64, P, I]
+        lib.orc_coarse_g64.restype = None
         _lib = lib
         return lib
 
@@ -172,6 +176,19 @@ def quantize_c4(W: np.ndarray):
     return packed, S, ZS
 
 
+def quantize_g64(W: np.ndarray):
+    """The 2-bit head with groups of 64: (packed u8 [V, H/4], S u16 [V, H/64], ZS)."""
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    V, H = W.shape
+    packed = np.empty((V, H // 4), np.uint8)
+    S = np.empty((V, H // 64), np.uint16)
+    ZS = np.empty((V, H // 64), np.uint16)
+    rc = _load().orc_quantize_g64(_ptr(W), V, H, _ptr(packed), _ptr(S), _ptr(ZS))
+    if rc != 0:
+        raise ValueError(f"orc_quantize_g64: status {rc} (H must be a positive multiple of 512)")
+    return packed, S, ZS
+
+
 def unpack(packed: np.ndarray, H: int) -> np.ndarray:
     """Quarter-split packed bytes [V, H/4] -> 2-bit codes [V, H] (u8)."""
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
@@ -221,6 +238,21 @@ def coarse_c4(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
     c = np.empty((M, V), np.float64)
     _load().orc_coarse_c4(_ptr(x), _ptr(packed), _ptr(S), _ptr(ZS), M, H, V, _ptr(c),
                           nthreads or default_threads())
+    return c
+
+
+def coarse_g64(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
+    """Coarse values c [M, V] in fp64 from the 2-bit head with 64-groups."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    S = np.ascontiguousarray(S, dtype=np.uint16)
+    ZS = np.ascontiguousarray(ZS, dtype=np.uint16)
+    M, H = x.shape
+    V = packed.shape[0]
+    assert S.shape[1] * 64 == H
+    c = np.empty((M, V), np.float64)
+    _load().orc_coarse_g64(_ptr(x), _ptr(packed), _ptr(S), _ptr(ZS), M, H, V, _ptr(c),
+                           nthreads or default_threads())
     return c
 
 
@@ -338,6 +370,12 @@ def forward_c4(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
                nthreads: int | None = None) -> dict:
     """The draft-head path on the contiguous-4 packed 2-bit head."""
     return forward4(x, packed, S, ZS, W, kcand, rerank_n, k, nthreads, coarse_fn=coarse_c4)
+
+
+def forward_g64(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
+                nthreads: int | None = None) -> dict:
+    """The draft-head path on the 64-group 2-bit head."""
+    return forward4(x, packed, S, ZS, W, kcand, rerank_n, k, nthreads, coarse_fn=coarse_g64)
 
 
 def exact_head(x: np.ndarray, W: np.ndarray, nthreads: int | None = None) -> np.ndarray:

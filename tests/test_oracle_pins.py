@@ -566,3 +566,47 @@ def test_c4_layout_holds_the_quarter_split_codes_and_coarse_values():
     assert np.array_equal(codes_c4, my_unpack(pq, H))
     assert np.array_equal(Sq, Sc) and np.array_equal(Zq, Zc)
     assert np.array_equal(orc.coarse_c4(x, pc, Sc, Zc), orc.coarse(x, pq, Sq, Zq))
+
+
+# ------------------------------------------------------------------------------------------
+# groups of 64 (the page's group-size ablation)
+# ------------------------------------------------------------------------------------------
+
+def test_quantize_g64_golden_groups():
+    """The hand-worked 128-groups of quantize_groups.json hold a 4-value pattern, so the same
+    pattern over 64 values has the same statistics, codes, S and ZS."""
+    spec = json.load(open(os.path.join(GOLD, "quantize_groups.json")))
+    for case in spec["cases"]:
+        group = np.tile(np.array(case["pattern"]), 16)          # 64 values
+        W = f2bf_exact(np.tile(group, 8)[None, :])              # H = 512: eight equal groups
+        packed, S, ZS = orc.quantize_g64(W)
+        assert np.array_equal(my_unpack(packed, 512)[0], np.tile(np.array(case["codes"]), 128))
+        assert np.all(S == int(case["S"], 16)) and np.all(ZS == int(case["ZS"], 16))
+
+
+def test_quantize_g64_equals_128_groups_of_doubled_values():
+    """Group g of 64 values quantises like a 128-group holding each of them twice (same min,
+    max and codes): the g64 quantiser against the pinned 128-group one."""
+    rng = np.random.default_rng(17)
+    V, H = 30, 1024
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    p64, S64, Z64 = orc.quantize_g64(W)
+    W2 = np.repeat(W, 2, axis=1)                                # [V, 2H]: 128-group g = 64-group g
+    p2, S2, Z2 = orc.quantize(W2)
+    assert np.array_equal(S64, S2) and np.array_equal(Z64, Z2)
+    assert np.array_equal(np.repeat(my_unpack(p64, H), 2, axis=1), my_unpack(p2, 2 * H))
+
+
+def test_coarse_g64_collapsed_form_equals_direct_dequant():
+    rng = np.random.default_rng(18)
+    V, H, M = 150, 1024, 4
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS = orc.quantize_g64(W)
+    v = my_unpack(packed, H).astype(np.float64)
+    s = np.repeat(bf2f(S), 64, axis=1)
+    zs = np.repeat(bf2f(ZS), 64, axis=1)
+    ref = bf2f(x) @ (s * (1.0 + v / 4.0) - zs).T
+    np.testing.assert_allclose(orc.coarse_g64(x, packed, S, ZS), ref, rtol=1e-11, atol=1e-11)
