@@ -253,6 +253,29 @@ class C4Inputs(Inputs):
                                TOPK, idx, logit, ws, events=events)
 
 
+class G64Inputs(Inputs):
+    """The 2-bit head with groups of 64 (the page's group-size ablation)."""
+
+    def __init__(self, seed, dev, max_m, V=V_FULL):
+        import torch
+        import quantised_speculative_draft_gb300 as dh
+        super().__init__(seed, dev, max_m, V)
+        V, H = self.W.shape
+        self.S = torch.empty(V, H // 64, dtype=torch.bfloat16, device=dev)
+        self.ZS = torch.empty(V, H // 64, dtype=torch.bfloat16, device=dev)
+        dh.dh_quantize_g64(self.W, self.packed, self.S, self.ZS)
+
+    def call(self, M, ws, idx, logit):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_g64_debug(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND, RERANK,
+                                TOPK, idx, logit, ws)
+
+    def call_timed(self, M, ws, idx, logit, events):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_g64_debug(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND, RERANK,
+                                TOPK, idx, logit, ws, events=events)
+
+
 def make_outputs(M, dev, V=None):
     import torch
     import quantised_speculative_draft_gb300 as dh
@@ -558,6 +581,19 @@ def run_ours(args):
             "coarse_frac_of_hbm": round(nb / stc["coarse"] / 1e3 / hbm, 4),
             "quarter_split_coarse_us": round(stages["coarse"], 2)}}
         del setsc
+        if M <= 16:
+            setsg = [G64Inputs(seed, dev, M) for seed in range(args.sets)]
+            nbg = V_FULL * H_FULL // 4 + 2 * V_FULL * (H_FULL // 64) * 2
+            msg, _, _ = time_graph(setsg, M, args.sweep_steps, 5)
+            stg = time_stages(setsg, M, 20)
+            abl["group64"] = {
+                "workload": f"full-vocab 2-bit head M={M}, groups of 64 (S, ZS [V, H/64])",
+                "us_per_call": round(msg * 1e3 / args.sweep_steps, 2),
+                "coarse_us": round(stg["coarse"], 2),
+                "coarse_bytes_per_launch": nbg,
+                "coarse_frac_of_hbm": round(nbg / stg["coarse"] / 1e3 / hbm, 4),
+                "group128_coarse_us": round(stages["coarse"], 2)}
+            del setsg
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

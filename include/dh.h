@@ -323,6 +323,25 @@ int dh_forward_c4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t
                         int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
                         void *const *events, void *stream);
 
+/*
+ * Groups of 64: the group size the page measured against 128 (radiance_drafthead.py, module
+ * docstring, 'Group 128, not 64').  Kept as an ablation: twice the scale/zero pairs and twice
+ * the per-group accumulator folds for the same packed bytes.
+ *
+ * dh_quantize_g64 -- dh_quantize with groups of 64 consecutive k: scales, zeros [V, H/64] bf16
+ *   (S = bf16(4 sc), ZS = bf16(4 sc + zp sc) per 64-group); packed [V, H/4] quarter split.
+ * dh_forward_g64_debug -- the forward on that head, M <= 16, 8-bit tcgen05 path only
+ *   (DH_ERR_ARG otherwise); optional debug outputs and stage events as dh_forward_c4_debug.
+ */
+int dh_quantize_g64(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                    uint16_t *zeros, void *stream);
+int dh_forward_g64_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                         const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                         int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                         void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                         int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
+                         void *const *events, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

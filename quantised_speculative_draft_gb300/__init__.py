@@ -24,7 +24,7 @@ __all__ = [
     "dh_last_error", "dh_version", "DraftHead", "dh_shard_candidates",
     "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_shard_topk", "dh_quantize_fp8",
     "dh_forward_fp8w", "dh_quantize4", "dh_forward4", "dh_forward4_debug", "dh_forward4_timed",
-    "dh_quantize_c4", "dh_forward_c4_debug",
+    "dh_quantize_c4", "dh_forward_c4_debug", "dh_quantize_g64", "dh_forward_g64_debug",
     "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16", "NUM_STAGE_EVENTS", "library_path",
 ]
 
@@ -112,6 +112,10 @@ def _load():
         lib.dh_quantize_c4.restype = I
         lib.dh_forward_c4_debug.argtypes = fwd + [P, P, P, P, P, P, P]
         lib.dh_forward_c4_debug.restype = I
+        lib.dh_quantize_g64.argtypes = [P, I, I, P, P, P, P]
+        lib.dh_quantize_g64.restype = I
+        lib.dh_forward_g64_debug.argtypes = fwd + [P, P, P, P, P, P, P]
+        lib.dh_forward_g64_debug.restype = I
         _lib = lib
         return lib
 
@@ -263,6 +267,25 @@ def dh_forward_c4_debug(x, packed, scales, zeros, W, kcand, rerank, topk, idx, l
         arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in events])
     _check(_load().dh_forward_c4_debug(*args, _p(coarse), _p(cand_val), _p(cand_idx),
                                        _p(sel_idx), _p(sel_exact), arr, _stream(stream)))
+
+
+def dh_quantize_g64(W, packed, scales, zeros, stream=None):
+    """The 2-bit head with groups of 64 (the group-size ablation): scales/zeros [V, H/64]."""
+    V, H = W.shape
+    _check(_load().dh_quantize_g64(_p(W), V, H, _p(packed), _p(scales), _p(zeros),
+                                   _stream(stream)))
+
+
+def dh_forward_g64_debug(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit,
+                         workspace, coarse=None, cand_val=None, cand_idx=None, sel_idx=None,
+                         sel_exact=None, events=None, stream=None):
+    """The forward on the 64-group head (M <= 16); optional debug outputs and stage events."""
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    arr = None
+    if events is not None:
+        arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in events])
+    _check(_load().dh_forward_g64_debug(*args, _p(coarse), _p(cand_val), _p(cand_idx),
+                                        _p(sel_idx), _p(sel_exact), arr, _stream(stream)))
 
 
 def dh_shard_candidates(x, packed, scales, zeros, vocab_offset, kcand, rerank, out_val, out_idx,

@@ -116,7 +116,7 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     const int chunks8 = tc8_chunks(M);
     L.xt8_chunk = align256(static_cast<size_t>(2 * kTc8MaxRows) * H); // T*MP <= 64 rows
     L.xt8 = take(L.xt8_chunk * chunks8);
-    L.xs8 = take(static_cast<size_t>(chunks8) * kTc8MaxRows * (H / kGroup) * 4);
+    L.xs8 = take(static_cast<size_t>(chunks8) * kTc8MaxRows * (H / 64) * 4); // room for 64-groups
     L.inv8 = take(static_cast<size_t>(chunks8) * kTc8MaxRows * 4);
     L.total = off;
     return L;
@@ -187,12 +187,15 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     const int path = choose_path(M, H);
     if (path < 0) return fail(DH_ERR_ARG, "the tcgen05 path does not support M=%d, H=%d", M, H);
     if (pack != kPackQuarter2 &&
-        (path != DH_PATH_TC || !tc8_supported(M, H, pack == kPackHalf4 ? 4 : 2)))
+        (path != DH_PATH_TC || !tc8_supported(M, H, pack == kPackHalf4 ? 4 : 2,
+                                              pack == kPackG64 ? 64 : 128)))
         return fail(DH_ERR_ARG,
                     "the %s head runs on the 8-bit tcgen05 path only (M=%d, H=%d: %s)",
-                    pack == kPackHalf4 ? "4-bit" : "contiguous-4", M, H,
+                    pack == kPackHalf4 ? "4-bit"
+                                       : (pack == kPackG64 ? "64-group" : "contiguous-4"),
+                    M, H,
                     path != DH_PATH_TC ? "another coarse path is selected"
-                                       : "its stages do not fit in shared memory");
+                                       : "the path does not take these sizes");
     int *tflag = timeout_flag_ptr();
     if (!tflag) return fail(DH_ERR_CUDA, "cannot resolve the device status flag");
 
@@ -218,6 +221,8 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     w8.xt8 = ws + L.xt8;
     w8.chunk_bytes = L.xt8_chunk;
     w8.xs = reinterpret_cast<float *>(ws + L.xs8);
+    w8.xs_chunk = static_cast<size_t>(kTc8MaxRows) * (H / 64);
+    w8.group = pack == kPackG64 ? 64 : 128;
     w8.inv_scale = reinterpret_cast<float *>(ws + L.inv8);
     if (path == DH_PATH_TC)
         err = launch_prep_fp8(x, M, H, w8, counters, kNumCounters, stream);
@@ -332,7 +337,7 @@ int dh_quantize(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t 
     const void *ptrs[] = {W_bf16, packed, scales, zeros};
     for (const void *p : ptrs)
         if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
-    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, 2, packed, scales, zeros,
+    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, 2, 128, packed, scales, zeros,
                                       static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
     return ok();
@@ -367,7 +372,7 @@ int dh_quantize_fp8(const uint8_t *W_e4m3, const float *row_scale, int V, int H,
         if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
     if (reinterpret_cast<uintptr_t>(row_scale) & 3u)
         return fail(DH_ERR_ALIGN, "row_scale %p is not 4-byte aligned", row_scale);
-    cudaError_t err = launch_quantize(W_e4m3, row_scale, V, H, 2, packed, scales, zeros,
+    cudaError_t err = launch_quantize(W_e4m3, row_scale, V, H, 2, 128, packed, scales, zeros,
                                       static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
     return ok();
@@ -397,7 +402,7 @@ int dh_quantize4(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t
     const void *ptrs[] = {W_bf16, packed, scales, zeros};
     for (const void *p : ptrs)
         if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
-    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, 4, packed, scales, zeros,
+    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, 4, 128, packed, scales, zeros,
                                       static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
     return ok();
@@ -477,6 +482,42 @@ int dh_forward_c4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t
                         logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
                         sel_exact, events, static_cast<cudaStream_t>(stream), nullptr, 0, false,
                         nullptr, kPackContig2);
+}
+
+int dh_quantize_g64(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
+                    uint16_t *zeros, void *stream)
+{
+    if (!W_bf16 || !packed || !scales || !zeros)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (V < 1) return fail(DH_ERR_SHAPE, "V=%d must be >= 1", V);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    const void *ptrs[] = {W_bf16, packed, scales, zeros};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    cudaError_t err = launch_quantize(W_bf16, nullptr, V, H, 2, 64, packed, scales, zeros,
+                                      static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(err));
+    return ok();
+}
+
+int dh_forward_g64_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                         const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                         int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                         void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                         int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
+                         void *const *events, void *stream)
+{
+    const void *opt[] = {coarse, cand_val, cand_idx, sel_idx, sel_exact};
+    for (const void *p : opt)
+        if (p && !aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    if (events)
+        for (int i = 0; i < DH_NUM_STAGE_EVENTS; ++i)
+            if (!events[i]) return fail(DH_ERR_NULL, "events[%d] is NULL", i);
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
+                        sel_exact, events, static_cast<cudaStream_t>(stream), nullptr, 0, false,
+                        nullptr, kPackG64);
 }
 
 int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,

@@ -78,10 +78,12 @@ template <int MP, int PACK> struct Cfg8 {
     static constexpr int T = 2;
     static constexpr int kPkBoxes = PACK == kPackHalf4 ? 2 : 1; // packed boxes per span
     static constexpr int N = MP * T;
-    static constexpr int kU = MP == 16 ? 1 : 2;             // units per span
+    static constexpr int G = PACK == kPackG64 ? 64 : 128;   // weight group size
+    static constexpr int kGPP = 128 / G;                    // groups per plane of a span
+    static constexpr int kU = MP == 16 && G == 128 ? 1 : 2; // units per span
     static constexpr int kPP = 4 / kU;                      // planes per unit
     static constexpr uint32_t kACols = 32 * kPP;
-    static constexpr uint32_t kSlotCols = kACols + kPP * N;
+    static constexpr uint32_t kSlotCols = kACols + kPP * kGPP * N; // one accumulator per group
     static constexpr int kSlotsFit = static_cast<int>(kTmemCols / kSlotCols);
     static constexpr int kSlots = kSlotsFit > 2 ? 2 : kSlotsFit; // one issuer warp per slot
     static constexpr uint32_t kXBytes = N * 512;            // 4 planes x 128 k x N rows
@@ -232,13 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using C = Cfg8<MP, PACK>;
     constexpr int BITS = PACK == kPackHalf4 ? 4 : 2;
+    constexpr int G = C::G, kGPP = C::kGPP;
+    constexpr int NGH = 2 * kGPP; // groups of an epilogue half in one span
     constexpr int kBoxes = C::kPkBoxes;
     constexpr int N = C::N, T = C::T, K = C::kSlots, kU = C::kU, kPP = C::kPP;
     constexpr uint32_t kSlotCols = C::kSlotCols, kACols = C::kACols;
     constexpr int kRedHalf = MP * 2 * kRedPitch; // floats of one epilogue half's tile values
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NG = prm.H / 512, NGt = prm.H / kGroup;
+    const int NG = prm.H / 512, NGt = prm.H / G;
     const int nstage = prm.nstage;
     const uint32_t sz_bytes = static_cast<uint32_t>(kTileRows) * NGt * 2; // S (or ZS) of a tile
 
@@ -371,11 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int plane = kPP * u + g;
                             // the descriptor's address field counts 16-byte units
                             const uint64_t qdesc = xdesc + static_cast<uint64_t>(plane * (N * 128) / 16);
-                            mma_ts_f8(d_tmem + g * N, a_tmem + g * 32, qdesc, idesc, 0u);
+                            // K = 32 per MMA: 128 / G groups of the plane, 4 / (128 / G) MMAs
+                            // each into the group's own accumulator
 #pragma unroll
-                            for (int i = 1; i < 4; ++i)
-                                mma_ts_f8(d_tmem + g * N, a_tmem + g * 32 + i * 8,
-                                          qdesc + static_cast<uint64_t>(i * 2), idesc, 1u);
+                            for (int i = 0; i < 4; ++i)
+                                mma_ts_f8(d_tmem + (g * kGPP + i / (4 / kGPP)) * N,
+                                          a_tmem + g * 32 + i * 8,
+                                          qdesc + static_cast<uint64_t>(i * 2), idesc,
+                                          (i % (4 / kGPP)) ? 1u : 0u);
                         }
                         // a commit takes an issue slot like an MMA: one per consumer
                         mma_commit(&d_full[slot]);
@@ -511,10 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int m = 0; m < MP; ++m) acc[m] = 0.f;
             for (int span = 0; span < NG; ++span, t += 4) {
-                float s2[2], sz[2];
+                // this half's groups: planes 2h, 2h+1, kGPP groups each
+                float s2[NGH], sz[NGH];
 #pragma unroll
-                for (int gl = 0; gl < 2; ++gl) {
-                    const int gi = plane_group<PACK>(2 * h + gl, span, NG);
+                for (int gl = 0; gl < NGH; ++gl) {
+                    const int plane = 2 * h + gl / kGPP;
+                    const int gi = plane_group<PACK>(plane, span, NG) * kGPP + gl % kGPP;
                     uint16_t sb = 0, zb = 0;
                     if (full_tile) {
                         sb = sS[gi];
@@ -524,13 +533,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         zb = __ldg(gZ + gi);
                     }
                     const float sv = bf16_bits_to_f32(sb), zv = bf16_bits_to_f32(zb);
-                    // (S / B) sum x v with the MMA's sum of x v 2^-9 (2 bits, B = 4: odd planes
-                    // carry 4 v 2^-9, even planes v 2^-9; 4 bits, B = 16: v 2^-9)
-                    // carry 4 v 2^-9, even planes v 2^-9; contiguous-4: every plane v 2^-9)
-                    s2[gl] = (BITS == 4 ? 32.0f
-                                        : (PACK == kPackQuarter2 && ((2 * h + gl) & 1) ? 32.0f
-                                                                                        : 128.0f)) *
-                             sv;
+                    // (S / B) sum x v with the MMA's sum of x v 2^-9 (quarter split, B = 4: odd
+                    // planes carry 4 v 2^-9, even planes v 2^-9; contiguous-4, B = 4: every
+                    // plane v 2^-9; 4 bits, B = 16: v 2^-9)
+                    const bool four_v = PACK != kPackHalf4 && PACK != kPackContig2 && (plane & 1);
+                    s2[gl] = (BITS == 4 ? 32.0f : (four_v ? 32.0f : 128.0f)) * sv;
                     sz[gl] = sv - zv;
                 }
                 // the unit holding this half's two groups (planes 2h, 2h+1) of the span
@@ -542,10 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // the half's first accumulator within the unit
                 const uint32_t dcol = tmem + lane_base + slot * kSlotCols + kACols +
-                                      (kU == 1 ? 2 * h : 0) * N;
-                // the unit's 2 * CH chunks, two per tcgen05 wait (64 registers)
+                                      (kU == 1 ? 2 * h * kGPP : 0) * N;
+                // the half's NGH * CH chunks, two per tcgen05 wait (64 registers)
 #pragma unroll
-                for (int wb = 0; wb < CH; ++wb) {
+                for (int wb = 0; wb < NGH * CH / 2; ++wb) {
                     float v[2][T][16];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
@@ -555,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_ld_x16(dcol + gl * N + tt * MP + c * 16, v[u][tt]);
                     }
                     tmem_wait_ld();
-                    if (wb == CH - 1) {
+                    if (wb == NGH * CH / 2 - 1) {
                         // every partial of the unit is in registers: the slot goes back
                         tc_fence_before();
                         __syncwarp();
@@ -564,8 +571,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int k = 2 * wb + u, gl = k / CH, c = k % CH;
-                        const float4 *xg = reinterpret_cast<const float4 *>(
-                            xs_s + plane_group<PACK>(2 * h + gl, span, NG) * MP);
+                        const int gi = plane_group<PACK>(2 * h + gl / kGPP, span, NG) * kGPP +
+                                       gl % kGPP;
+                        const float4 *xg = reinterpret_cast<const float4 *>(xs_s + gi * MP);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const float4 x4 = xg[c * 4 + j];
@@ -667,9 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Dynamic shared memory besides the stages: alignment slack, the double-buffered S/ZS tile
 // copies, the two epilogue halves' tile values, xs and 2^-e, barriers.
-size_t tc8_fixed_smem(int MP, int H)
+size_t tc8_fixed_smem(int MP, int H, int G)
 {
-    const int NGt = H / kGroup;
+    const int NGt = H / G;
     return 1024 + 4 * static_cast<size_t>(kTileRows) * NGt * 2 +
            2 * static_cast<size_t>(MP) * 2 * kRedPitch * 4 + static_cast<size_t>(NGt) * MP * 4 +
            MP * 4 + 64 * 8 + 32;
@@ -685,7 +693,7 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
                                       const_cast<uint8_t *>(xt8_chunk), base.H, C::N, base.H,
                                       128, C::N, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const size_t fixed = tc8_fixed_smem(MP, base.H);
+    const size_t fixed = tc8_fixed_smem(MP, base.H, C::G);
     int nstage = static_cast<int>((kSmemLimit8 - static_cast<long long>(fixed)) / C::kStage);
     if (nstage > 6) nstage = 6;
     if (nstage < 2) return cudaErrorInvalidConfiguration;
@@ -707,17 +715,20 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
 
 } // namespace
 
-bool tc8_supported(int M, int H, int bits)
+bool tc8_supported(int M, int H, int bits, int group)
 {
     // the x staging keeps a row in registers: H <= 16384
     if (M < 1 || M > kMaxM || H % 512 != 0 || H > 16384) return false;
     if (bits != 2 && bits != 4) return false;
+    // groups of 64 need two accumulators per plane: only the 16-row launch keeps two slots
+    if (group != 128 && (group != 64 || bits != 2 || M > 16)) return false;
     // at least two stages next to the fixed buffers, for every chunk size the batch uses
     for (int c = 0; c < tc8_chunks(M); ++c) {
         const int MP = tc8_chunk(M, c).MP;
         const size_t stage = (bits / 2) * static_cast<size_t>(kPkBytes) +
                              static_cast<size_t>(MP) * 2 * 512;
-        if (tc8_fixed_smem(MP, H) + 2 * stage > static_cast<size_t>(kSmemLimit8)) return false;
+        if (tc8_fixed_smem(MP, H, group) + 2 * stage > static_cast<size_t>(kSmemLimit8))
+            return false;
     }
     return true;
 }
@@ -746,7 +757,8 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
                                       const_cast<uint8_t *>(a.packed), row_bytes, a.V, row_bytes,
                                       kSpanBytes, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (!tc8_supported(a.M, a.H, bits)) return cudaErrorInvalidConfiguration;
+    if (!tc8_supported(a.M, a.H, bits, a.pack == kPackG64 ? 64 : 128))
+        return cudaErrorInvalidConfiguration;
     Tc8Params base;
     base.S = a.S;
     base.ZS = a.ZS;
@@ -760,18 +772,19 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
     base.coarse = a.coarse;
     base.timeout_flag = a.timeout_flag;
     base.nstage = 2;
-    const int NGt = a.H / kGroup;
     for (int c = 0; c < tc8_chunks(a.M); ++c) {
         const Tc8Chunk k = tc8_chunk(a.M, c);
         base.m0 = k.m0;
         base.mrows = k.rows;
-        base.xs = w.xs + static_cast<size_t>(c) * kTc8MaxRows * NGt;
+        base.xs = w.xs + static_cast<size_t>(c) * w.xs_chunk;
         base.inv_scale = w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows;
         const uint8_t *xt = w.xt8 + static_cast<size_t>(c) * w.chunk_bytes;
         cudaError_t e;
         if (a.pack == kPackHalf4) {
             if (k.MP == 16) e = launch_cfg<16, kPackHalf4>(tm_packed, xt, base, stream);
             else e = launch_cfg<32, kPackHalf4>(tm_packed, xt, base, stream);
+        } else if (a.pack == kPackG64) {
+            e = launch_cfg<16, kPackG64>(tm_packed, xt, base, stream); // M <= 16 (checked)
         } else if (a.pack == kPackContig2) {
             if (k.MP == 16) e = launch_cfg<16, kPackContig2>(tm_packed, xt, base, stream);
             else e = launch_cfg<32, kPackContig2>(tm_packed, xt, base, stream);

@@ -24,16 +24,19 @@ constexpr int kNumCounters = 384;   // [0, 64): work queues, [128, 256): per-row
 constexpr int kRowDoneOffset = 128;
 constexpr int kSelDoneOffset = 256;
 
-// Packed layouts of the head: the 2-bit quarter split (the default), the 4-bit half split and
-// the 2-bit contiguous-4 layout (the page's packing ablation).
+// Packed layouts of the head: the 2-bit quarter split (the default), the 4-bit half split, the
+// 2-bit contiguous-4 layout (the page's packing ablation) and the quarter split with groups of
+// 64 (the page's group-size ablation; S, ZS [V, H/64]).
 constexpr int kPackQuarter2 = 0;
 constexpr int kPackHalf4 = 1;
 constexpr int kPackContig2 = 2;
+constexpr int kPackG64 = 3;     // the quarter split with groups of 64 (group-size ablation)
 
 // ---- launchers (each returns the launch status) ------------------------------------------
 // W: bf16 rows (wsc null) or e4m3 rows with per-row fp32 scales wsc.  bits: 2 (quarter
-// split, packed [V, H/4]) or 4 (half split, packed [V, H/2]).
-cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits,
+// split, packed [V, H/4]) or 4 (half split, packed [V, H/2]).  group: 128, or 64 for the
+// 2-bit bf16 head of the group-size ablation (S, ZS [V, H/64]).
+cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits, int group,
                             uint8_t *packed, uint16_t *S, uint16_t *ZS, cudaStream_t stream);
 // The bf16 head in the contiguous-4 layout, packed [V, H/4].
 cudaError_t launch_quantize_c4(const uint16_t *W, int V, int H, uint8_t *packed, uint16_t *S,
@@ -78,13 +81,17 @@ int tc8_chunks(int M);
 struct Tc8Workspace {
     uint8_t *xt8;       // per launch [T*MP, H] e4m3 terms, chunk_bytes apart
     size_t chunk_bytes;
-    float *xs;          // per launch kTc8MaxRows x NGt scaled group sums of the represented x
+    float *xs;          // per launch kTc8MaxRows x (H / group) scaled group sums of the
+                        // represented x, xs_chunk floats apart
+    size_t xs_chunk;
     float *inv_scale;   // per launch kTc8MaxRows entries 2^-e
+    int group = 128;    // group size of xs (64: the group-size ablation)
 };
 cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
                             int *counters, int ncounters, cudaStream_t stream);
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream);
-bool tc8_supported(int M, int H, int bits = 2); // shared memory of the 8-bit tcgen05 path fits
+// the 8-bit tcgen05 path runs these sizes (shared memory and tensor memory fit)
+bool tc8_supported(int M, int H, int bits = 2, int group = 128);
 
 bool tc_supported(int M, int H);
 cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream);

@@ -123,6 +123,8 @@ __device__ __forceinline__ float e4m3_to_f32(__nv_fp8_storage_t v)
 
 constexpr int kPrepOcts = 8; // 16-byte slices of x per thread (H up to 16384)
 
+// G: the group size of the sums xs (128, or 64 for the group-size ablation).
+template <int G>
 __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restrict__ x, int H,
                                                        int m0, int rows, int MP, int T,
                                                        uint8_t *__restrict__ xt8,
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restric
     __shared__ float wmax[8];
     const int m = blockIdx.x;
     const bool valid = m < rows;
-    const int octs = H / 8, NGt = H / kGroup;
+    const int octs = H / 8, NGt = H / G;
     if (counters && m == 0)
         for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
     const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
@@ -197,21 +199,22 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restric
         for (int t = 0; t < T; ++t)
             *reinterpret_cast<uint2 *>(xt8 + (static_cast<long long>(t) * MP + m) * H + 8 * o) =
                 make_uint2(lo[t], hi[t]);
+        // the G / 8 octets of a group are consecutive lanes
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        if ((o & 15) == 0) xs[static_cast<long long>(m) * NGt + (o >> 4)] = sum;
+        for (int off = G / 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if ((o & (G / 8 - 1)) == 0) xs[static_cast<long long>(m) * NGt + o / (G / 8)] = sum;
     }
 }
 
 cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
                             int *counters, int ncounters, cudaStream_t stream)
 {
-    const int NGt = H / kGroup;
     for (int c = 0; c < tc8_chunks(M); ++c) {
         const Tc8Chunk k = tc8_chunk(M, c);
-        prep_fp8_kernel<<<k.MP, 256, 0, stream>>>(
+        auto kern = w.group == 64 ? prep_fp8_kernel<64> : prep_fp8_kernel<128>;
+        kern<<<k.MP, 256, 0, stream>>>(
             x, H, k.m0, k.rows, k.MP, k.T, w.xt8 + static_cast<size_t>(c) * w.chunk_bytes,
-            w.xs + static_cast<size_t>(c) * kTc8MaxRows * NGt,
+            w.xs + static_cast<size_t>(c) * w.xs_chunk,
             w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows, c == 0 ? counters : nullptr,
             ncounters);
         cudaError_t e = cudaGetLastError();

@@ -27,22 +27,27 @@
 
 namespace dh {
 
-__device__ __forceinline__ float warp_min(float v)
+// min / max over aligned groups of L lanes (L = 32: the warp)
+template <int L>
+__device__ __forceinline__ float lanes_min(float v)
 {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = L / 2; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
-__device__ __forceinline__ float warp_max(float v)
+template <int L>
+__device__ __forceinline__ float lanes_max(float v)
 {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = L / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
 // kFp8: W holds e4m3 bytes and wsc the per-row fp32 scales; otherwise W holds bf16.
-template <bool kFp8, int BITS>
+// G: the group size, 128 (the head) or 64 (the page's group-size ablation: each plane's 128 k
+// of a span are two groups, lanes 0-15 and 16-31).
+template <bool kFp8, int BITS, int G>
 __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ Wv,
                                                        const float *__restrict__ wsc,
                                                        uint8_t *__restrict__ packed,
@@ -55,7 +60,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
     const int lane = threadIdx.x & 31;
     const int PS = H / P;       // k stride between planes = packed bytes per row
     const int NS = PS / 128;    // spans per row
-    const int NGt = H / kGroup; // groups per row
+    const int NGt = H / G;      // groups per row
     const long long total = static_cast<long long>(V) * NS;
     const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
     for (long long item = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) +
@@ -97,8 +102,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
             const float *w = wv[p];
             float lo = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
             float hi = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-            lo = warp_min(lo);
-            hi = warp_max(hi);
+            lo = lanes_min<G / 4>(lo);
+            hi = lanes_max<G / 4>(hi);
             float sc = __fdiv_rn(__fsub_rn(hi, lo), L);
             sc = fmaxf(sc, 1e-8f);
             float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), L);
@@ -108,9 +113,10 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
                 uint32_t qv = static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), L));
                 word |= qv << (8 * i + BITS * p);
             }
-            if (lane == p) {
+            if ((lane & (G / 4 - 1)) == p) {
                 const float sb = __fmul_rn(B, sc);
-                const long long gi = static_cast<long long>(p) * NS + s;
+                const long long gi = (static_cast<long long>(p) * NS + s) * (128 / G) +
+                                     lane / (G / 4);
                 S[n * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
                 ZS[n * NGt + gi] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(zp, sc))));
@@ -190,7 +196,7 @@ cudaError_t launch_quantize_c4(const uint16_t *W, int V, int H, uint8_t *packed,
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits,
+cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits, int group,
                             uint8_t *packed, uint16_t *S, uint16_t *ZS, cudaStream_t stream)
 {
     const long long total = static_cast<long long>(V) * (H / (bits == 4 ? 256 : 512));
@@ -199,11 +205,13 @@ cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int b
     if (blocks > cap) blocks = cap;
     const unsigned g = static_cast<unsigned>(blocks);
     if (bits == 4) {
-        if (wsc) quantize_kernel<true, 4><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
-        else quantize_kernel<false, 4><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
+        if (wsc) quantize_kernel<true, 4, 128><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
+        else quantize_kernel<false, 4, 128><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
+    } else if (group == 64) { // the 2-bit bf16 head with groups of 64
+        quantize_kernel<false, 2, 64><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
     } else {
-        if (wsc) quantize_kernel<true, 2><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
-        else quantize_kernel<false, 2><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
+        if (wsc) quantize_kernel<true, 2, 128><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
+        else quantize_kernel<false, 2, 128><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
     }
     return cudaGetLastError();
 }

@@ -192,3 +192,13 @@ def test_c4_entry_points_reject_bad_arguments(lib):
     bad = list(args)
     bad[6] = 1000
     assert lib.dh_forward_c4_debug(*bad, None, None, None, None, None, None, None) == -2
+
+
+def test_g64_entry_points_reject_bad_arguments(lib):
+    assert lib.dh_quantize_g64(FAKE, 16, 1024, None, FAKE, FAKE, None) == -1
+    assert lib.dh_quantize_g64(FAKE, 16, 768, FAKE, FAKE, FAKE, None) == -2
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1024, 8192, 8, 32, 1, FAKE, FAKE, FAKE, 1 << 40]
+    assert lib.dh_forward_g64_debug(*args, FAKE + 4, None, None, None, None, None, None) == -5
+    bad = list(args)
+    bad[10] = 0
+    assert lib.dh_forward_g64_debug(*bad, None, None, None, None, None, None, None) == -3
