@@ -35,6 +35,8 @@
  *   orc_quantize_g64   pinned: hand-worked golden groups at 64; each 64-group equals the
  *                      128-group quantiser on that group's values doubled in place
  *   orc_coarse_g64     pinned: collapsed form == direct dequant-and-dot over 64-groups
+ *   orc_coarse_wside   pinned: equals orc_coarse where every dequantised weight is a bf16
+ *                      value (power-of-two scales); a dequant-and-dot with torch's bf16 rounding
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -399,6 +401,32 @@ void orc_coarse4(const uint16_t *x, const uint8_t *packed, const uint16_t *S, co
                  int M, int64_t H, int64_t V, double *c, int nthreads)
 {
     coarse_bits(x, packed, S, ZS, M, H, V, c, nthreads, 4, 0, GROUP);
+}
+
+/* The weight-side variant the page measured against (module docstring, 'The scale is applied
+ * to the accumulator, never to the weight tile'): every weight is dequantised on its own to
+ * the bf16 value bf16(S (1 + v/4) - ZS) and dotted with x.  S (1 + v/4) - ZS is exact in fp64
+ * (and in fp32) for stored bf16 S and ZS, so the only rounding is the bf16 one.
+ * c[m, n] = sum_k x[m, k] * w'[n, k], fp64. */
+void orc_coarse_wside(const uint16_t *x, const uint8_t *packed, const uint16_t *S,
+                      const uint16_t *ZS, int M, int64_t H, int64_t V, double *c)
+{
+    const int64_t Q = H / 4, NGt = H / GROUP;
+    double *w = (double *)malloc((size_t)H * sizeof(double));
+    for (int64_t n = 0; n < V; ++n) {
+        for (int64_t k = 0; k < H; ++k) {
+            const double v = (double)((packed[n * Q + k % Q] >> (2 * (k / Q))) & 3u);
+            const double s = (double)bf16_to_f32(S[n * NGt + k / GROUP]);
+            const double z = (double)bf16_to_f32(ZS[n * NGt + k / GROUP]);
+            w[k] = (double)bf16_to_f32(f32_to_bf16_rne((float)(s * (1.0 + v / 4.0) - z)));
+        }
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < H; ++k) acc += (double)bf16_to_f32(x[(int64_t)m * H + k]) * w[k];
+            c[(int64_t)m * V + n] = acc;
+        }
+    }
+    free(w);
 }
 
 /* ------------------------------------------------------------------------------------- */

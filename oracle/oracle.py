@@ -96,6 +96,8 @@ def _load():
         lib.orc_quantize_g64.restype = I
         lib.orc_coarse_g64.argtypes = [P, P, P, P, I, I64, I64, P, I]
         lib.orc_coarse_g64.restype = None
+        lib.orc_coarse_wside.argtypes = [P, P, P, P, I, I64, I64, P]
+        lib.orc_coarse_wside.restype = None
         _lib = lib
         return lib
 
@@ -256,6 +258,19 @@ def coarse_g64(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
     return c
 
 
+def coarse_wside(x, packed, S, ZS, nthreads: int | None = None) -> np.ndarray:
+    """Coarse values of the weight-side variant: sum_k x_k bf16(S (1 + v/4) - ZS), fp64."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    S = np.ascontiguousarray(S, dtype=np.uint16)
+    ZS = np.ascontiguousarray(ZS, dtype=np.uint16)
+    M, H = x.shape
+    V = packed.shape[0]
+    c = np.empty((M, V), np.float64)
+    _load().orc_coarse_wside(_ptr(x), _ptr(packed), _ptr(S), _ptr(ZS), M, H, V, _ptr(c))
+    return c
+
+
 def block_topk(cf: np.ndarray, kcand: int):
     """cf: fp32 coarse [M, V].  Returns (cval f32 [M, nblk*kcand], cidx i32, nvalid per row)."""
     cf = np.ascontiguousarray(cf, dtype=np.float32)
@@ -376,6 +391,12 @@ def forward_g64(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
                 nthreads: int | None = None) -> dict:
     """The draft-head path on the 64-group 2-bit head."""
     return forward4(x, packed, S, ZS, W, kcand, rerank_n, k, nthreads, coarse_fn=coarse_g64)
+
+
+def forward_wside(x, packed, S, ZS, W, kcand: int, rerank_n: int, k: int,
+                  nthreads: int | None = None) -> dict:
+    """The draft-head path with the weight-side coarse variant."""
+    return forward4(x, packed, S, ZS, W, kcand, rerank_n, k, nthreads, coarse_fn=coarse_wside)
 
 
 def exact_head(x: np.ndarray, W: np.ndarray, nthreads: int | None = None) -> np.ndarray:

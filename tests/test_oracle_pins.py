@@ -610,3 +610,37 @@ def test_coarse_g64_collapsed_form_equals_direct_dequant():
     zs = np.repeat(bf2f(ZS), 64, axis=1)
     ref = bf2f(x) @ (s * (1.0 + v / 4.0) - zs).T
     np.testing.assert_allclose(orc.coarse_g64(x, packed, S, ZS), ref, rtol=1e-11, atol=1e-11)
+
+
+# ------------------------------------------------------------------------------------------
+# weight-side dequant (the page's scale-placement ablation)
+# ------------------------------------------------------------------------------------------
+
+def test_coarse_wside_on_grid_weights_equals_the_activation_side_value():
+    """With power-of-two steps every dequantised weight sc (v - zp) is a bf16 value, so the
+    weight-side sum and the group form are the same number up to fp64 summation order."""
+    rng = np.random.default_rng(19)
+    V, H, M = 64, 1024, 3
+    W = f2bf_exact(_grid_weights(rng, V, H))
+    x = f2bf_exact(np.round(rng.standard_normal((M, H)) * 64) / 64)
+    packed, S, ZS = orc.quantize(W)
+    np.testing.assert_allclose(orc.coarse_wside(x, packed, S, ZS), orc.coarse(x, packed, S, ZS),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_coarse_wside_is_a_dot_with_bf16_rounded_weights():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(20)
+    V, H, M = 90, 1024, 4
+    W = (((rng.standard_normal((V, H)) * 0.02).astype(np.float32)).view(np.uint32) >> 16
+         ).astype(np.uint16)
+    x = ((rng.standard_normal((M, H)).astype(np.float32)).view(np.uint32) >> 16).astype(np.uint16)
+    packed, S, ZS = orc.quantize(W)
+    v = my_unpack(packed, H).astype(np.float64)
+    s = np.repeat(bf2f(S), 128, axis=1)
+    zs = np.repeat(bf2f(ZS), 128, axis=1)
+    wq = torch.from_numpy(s * (1.0 + v / 4.0) - zs).to(torch.bfloat16).double().numpy()
+    np.testing.assert_allclose(orc.coarse_wside(x, packed, S, ZS), bf2f(x) @ wq.T,
+                               rtol=1e-11, atol=1e-11)
+    # and it departs from the group form only by the bf16 rounding of the weights
+    assert np.abs(orc.coarse_wside(x, packed, S, ZS) - orc.coarse(x, packed, S, ZS)).max() < 0.05
