@@ -276,6 +276,34 @@ class G64Inputs(Inputs):
                                 TOPK, idx, logit, ws, events=events)
 
 
+class WsideInputs(Inputs):
+    """The head with the weight-side dequant coarse pass (the scale-placement ablation)."""
+
+    def call(self, M, ws, idx, logit):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_wside_debug(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND,
+                                  RERANK, TOPK, idx, logit, ws)
+
+    def call_timed(self, M, ws, idx, logit, events):
+        import quantised_speculative_draft_gb300 as dh
+        dh.dh_forward_wside_debug(self.x[:M], self.packed, self.S, self.ZS, self.W, KCAND,
+                                  RERANK, TOPK, idx, logit, ws, events=events)
+
+
+class AsPlain:
+    """An input set run through the plain dh_forward entry points."""
+
+    def __init__(self, inputs):
+        self.inputs = inputs
+        self.x = inputs.x
+
+    def call(self, M, ws, idx, logit):
+        Inputs.call(self.inputs, M, ws, idx, logit)
+
+    def call_timed(self, M, ws, idx, logit, events):
+        Inputs.call_timed(self.inputs, M, ws, idx, logit, events)
+
+
 def make_outputs(M, dev, V=None):
     import torch
     import quantised_speculative_draft_gb300 as dh
@@ -594,6 +622,25 @@ def run_ours(args):
                 "coarse_frac_of_hbm": round(nbg / stg["coarse"] / 1e3 / hbm, 4),
                 "group128_coarse_us": round(stages["coarse"], 2)}
             del setsg
+        setsw = [WsideInputs(seed, dev, M) for seed in range(args.sets)]
+        msw, _, _ = time_graph(setsw, M, args.sweep_steps, 5)
+        stw = time_stages(setsw, M, 20)
+        # the same head through the activation-side bf16 tcgen05 path, for the like-for-like
+        # comparison of the scale placement (same MMA kind and operands)
+        prev = dh.dh_set_coarse_path(dh.PATH_TC_BF16)
+        try:
+            stb = time_stages([AsPlain(sw) for sw in setsw], M, 20)
+        finally:
+            dh.dh_set_coarse_path(prev)
+        abl["weight_side_dequant"] = {
+            "workload": f"full-vocab 2-bit head M={M}, every weight dequantised to "
+                        "bf16(S (1 + v/4) - ZS), one bf16 tcgen05 accumulator per tile",
+            "us_per_call": round(msw * 1e3 / args.sweep_steps, 2),
+            "coarse_us": round(stw["coarse"], 2),
+            "coarse_frac_of_hbm": round(nb / stw["coarse"] / 1e3 / hbm, 4),
+            "activation_side_bf16_path_coarse_us": round(stb["coarse"], 2),
+            "activation_side_e4m3_path_coarse_us": round(stages["coarse"], 2)}
+        del setsw
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -342,6 +342,24 @@ int dh_forward_g64_debug(const uint16_t *x, const uint8_t *packed, const uint16_
                          int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
                          void *const *events, void *stream);
 
+/*
+ * Weight-side dequant: the scale placement the page measured against (radiance_drafthead.py,
+ * module docstring, 'The scale is applied to the accumulator, never to the weight tile').
+ * Kept as an ablation.
+ *
+ * dh_forward_wside_debug -- the forward on dh_quantize's head with the coarse value
+ *   c = sum_k x_k bf16(S_g (1 + v_k/4) - ZS_g): every weight dequantised with its group's
+ *   scale and zero and rounded to bf16, one bf16 tcgen05 accumulation per tile (no per-group
+ *   fold).  Runs on the bf16 tcgen05 path whatever dh_set_coarse_path selects; optional debug
+ *   outputs and stage events as dh_forward_c4_debug.
+ */
+int dh_forward_wside_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                           const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                           int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                           void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                           int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
+                           void *const *events, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

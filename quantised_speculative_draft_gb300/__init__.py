@@ -25,6 +25,7 @@ __all__ = [
     "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_shard_topk", "dh_quantize_fp8",
     "dh_forward_fp8w", "dh_quantize4", "dh_forward4", "dh_forward4_debug", "dh_forward4_timed",
     "dh_quantize_c4", "dh_forward_c4_debug", "dh_quantize_g64", "dh_forward_g64_debug",
+    "dh_forward_wside_debug",
     "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16", "NUM_STAGE_EVENTS", "library_path",
 ]
 
@@ -116,6 +117,8 @@ def _load():
         lib.dh_quantize_g64.restype = I
         lib.dh_forward_g64_debug.argtypes = fwd + [P, P, P, P, P, P, P]
         lib.dh_forward_g64_debug.restype = I
+        lib.dh_forward_wside_debug.argtypes = fwd + [P, P, P, P, P, P, P]
+        lib.dh_forward_wside_debug.restype = I
         _lib = lib
         return lib
 
@@ -286,6 +289,18 @@ def dh_forward_g64_debug(x, packed, scales, zeros, W, kcand, rerank, topk, idx, 
         arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in events])
     _check(_load().dh_forward_g64_debug(*args, _p(coarse), _p(cand_val), _p(cand_idx),
                                         _p(sel_idx), _p(sel_exact), arr, _stream(stream)))
+
+
+def dh_forward_wside_debug(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit,
+                           workspace, coarse=None, cand_val=None, cand_idx=None, sel_idx=None,
+                           sel_exact=None, events=None, stream=None):
+    """The forward with the weight-side dequant coarse pass (the scale-placement ablation)."""
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    arr = None
+    if events is not None:
+        arr = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in events])
+    _check(_load().dh_forward_wside_debug(*args, _p(coarse), _p(cand_val), _p(cand_idx),
+                                          _p(sel_idx), _p(sel_exact), arr, _stream(stream)))
 
 
 def dh_shard_candidates(x, packed, scales, zeros, vocab_offset, kcand, rerank, out_val, out_idx,

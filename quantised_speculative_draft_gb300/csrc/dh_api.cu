@@ -184,9 +184,11 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     const Layout L = layout_for(M, H, V, kcand, rerank);
     if (ws_bytes < L.total)
         return fail(DH_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
-    const int path = choose_path(M, H);
+    int path = choose_path(M, H);
+    if (pack == kPackWside) // the weight-side ablation runs on the bf16 tcgen05 path
+        path = tc_supported(M, H) ? DH_PATH_TC_BF16 : -1;
     if (path < 0) return fail(DH_ERR_ARG, "the tcgen05 path does not support M=%d, H=%d", M, H);
-    if (pack != kPackQuarter2 &&
+    if (pack != kPackQuarter2 && pack != kPackWside &&
         (path != DH_PATH_TC || !tc8_supported(M, H, pack == kPackHalf4 ? 4 : 2,
                                               pack == kPackG64 ? 64 : 128)))
         return fail(DH_ERR_ARG,
@@ -518,6 +520,25 @@ int dh_forward_g64_debug(const uint16_t *x, const uint8_t *packed, const uint16_
                         logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
                         sel_exact, events, static_cast<cudaStream_t>(stream), nullptr, 0, false,
                         nullptr, kPackG64);
+}
+
+int dh_forward_wside_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
+                           const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                           int kcand, int rerank, int topk, int32_t *idx, float *logit,
+                           void *workspace, size_t ws_bytes, float *coarse, float *cand_val,
+                           int32_t *cand_idx, int32_t *sel_idx, float *sel_exact,
+                           void *const *events, void *stream)
+{
+    const void *opt[] = {coarse, cand_val, cand_idx, sel_idx, sel_exact};
+    for (const void *p : opt)
+        if (p && !aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    if (events)
+        for (int i = 0; i < DH_NUM_STAGE_EVENTS; ++i)
+            if (!events[i]) return fail(DH_ERR_NULL, "events[%d] is NULL", i);
+    return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
+                        logit, workspace, ws_bytes, coarse, cand_val, cand_idx, sel_idx,
+                        sel_exact, events, static_cast<cudaStream_t>(stream), nullptr, 0, false,
+                        nullptr, kPackWside);
 }
 
 int dh_forward_debug(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,

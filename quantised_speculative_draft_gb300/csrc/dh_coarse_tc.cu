@@ -22,6 +22,11 @@
 //     accumulators in registers with the group's scale and zero, and at the end of the tile
 //     run the block top-KCAND selection;
 //   * every handoff is an mbarrier; every wait is bounded and gives up with a flag.
+//
+// kWS (the page's scale-placement ablation, module docstring: 'The scale is applied to the
+// accumulator, never to the weight tile'): the dequant warps instead write every weight as
+// bf16(S (1 + v/4) - ZS) -- the group's scale and zero applied to each element -- and all
+// MMAs of a tile accumulate into one buffer, so the epilogue has no per-group fold.
 #include "dh_common.cuh"
 #include "dh_internal.h"
 #include "dh_tcgen05.cuh"
@@ -72,7 +77,7 @@ __host__ __device__ constexpr uint32_t make_idesc(int N)
 
 // ---- the kernel -------------------------------------------------------------------------
 
-template <int N>
+template <int N, bool kWS>
 __global__ void __launch_bounds__(kThreads, 1)
     coarse_tc_kernel(const __grid_constant__ CUtensorMap tm_packed,
                      const __grid_constant__ CUtensorMap tm_x, const TcParams prm)
@@ -165,8 +170,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc(N);
-            uint32_t s = 0, t = 0;
-            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+            uint32_t s = 0, t = 0, it = 0;
+            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
+                // kWS: the tile's one accumulator, free once the epilogue read tile it - kD
+                const uint32_t dt = it % kD;
+                if (kWS && !mbar_wait_bounded(&d_empty[dt], ((it / kD) & 1u) ^ 1u,
+                                              prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
                 for (int span = 0; span < NG && !failed; ++span, ++s) {
                     const uint32_t st = s % nstage;
                     if (!mbar_wait_bounded(&full[st], (s / nstage) & 1u, prm.timeout_flag)) {
@@ -175,22 +187,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t xbase = smem_u32(stages + static_cast<size_t>(st) * kStage + kPkBytes);
                     for (int q = 0; q < 4; ++q, ++t) {
-                        const uint32_t a = t % kA, d = t % kD;
+                        const uint32_t a = t % kA, d = kWS ? dt : t % kD;
                         if (!mbar_wait_bounded(&a_full[a], (t / kA) & 1u, prm.timeout_flag) ||
-                            !mbar_wait_bounded(&d_empty[d], ((t / kD) & 1u) ^ 1u, prm.timeout_flag)) {
+                            (!kWS && !mbar_wait_bounded(&d_empty[d], ((t / kD) & 1u) ^ 1u,
+                                                        prm.timeout_flag))) {
                             failed = true;
                             break;
                         }
                         tc_fence_after();
                         const uint32_t d_tmem = tmem + Rings<N>::kDcol + d * N;
                         const uint32_t a_tmem = tmem + Rings<N>::kAcol + a * 64;
+                        // kWS: one accumulation over the whole tile
+                        const bool fresh = !kWS || (span == 0 && q == 0);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const uint32_t b_addr = xbase + (q * 2 + (i >> 2)) * (N * 128) + (i & 3) * 32;
-                            mma_ts(d_tmem, a_tmem + i * 8, sw128_desc(b_addr), idesc, i > 0 ? 1u : 0u);
+                            mma_ts(d_tmem, a_tmem + i * 8, sw128_desc(b_addr), idesc,
+                                   (i > 0 || !fresh) ? 1u : 0u);
                         }
                         mma_commit(&a_empty[a]);
-                        mma_commit(&d_full[d]);
+                        if (!kWS || (span == NG - 1 && q == 3)) mma_commit(&d_full[d]);
                     }
                     if (!failed) mma_commit(&empty[st]);
                 }
@@ -206,6 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
         uint32_t s = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+            const int grow = tile * kTileRows + row;
+            const bool row_ok = grow < prm.V;
+            const uint16_t *Srow = prm.S + static_cast<long long>(row_ok ? grow : 0) * NGt;
+            const uint16_t *Zrow = prm.ZS + static_cast<long long>(row_ok ? grow : 0) * NGt;
             for (int span = 0; span < NG; ++span, ++s) {
                 const uint32_t st = s % nstage;
                 if (!warp_wait(&full[st], (s / nstage) & 1u, prm.timeout_flag)) {
@@ -260,6 +280,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             r[2 * i + 1] = deq_pair_odd<3>(w[i]);
                         }
                     }
+                    if constexpr (kWS) {
+                        // the group's scale and zero on every weight: bf16(S (1 + v/4) - ZS),
+                        // the inner value exact, one rounding to bf16
+                        const int gi = q * NG + span;
+                        const float sv = row_ok ? bf16_bits_to_f32(__ldg(Srow + gi)) : 0.f;
+                        const float zv = row_ok ? bf16_bits_to_f32(__ldg(Zrow + gi)) : 0.f;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            const float lo = fmaf(sv, __uint_as_float(r[i] << 16), -zv);
+                            const float hi = fmaf(sv, __uint_as_float(r[i] & 0xFFFF0000u), -zv);
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                            r[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                        }
+                    }
                     tmem_st_x64(tmem + lane_base + Rings<N>::kAcol + a * 64, r);
                     tmem_wait_st();
                     tc_fence_before();
@@ -282,7 +316,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             float acc[N];
 #pragma unroll
             for (int m = 0; m < N; ++m) acc[m] = 0.f;
-            for (int span = 0; span < NG && !failed; ++span) {
+            if constexpr (kWS) {
+                // the tile's single accumulator holds the coarse values
+                const uint32_t dt = it % kD;
+                if (!warp_wait(&d_full[dt], (it / kD) & 1u, prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < N / 16; ++c) {
+                    float v[16];
+                    tmem_ld_x16(tmem + lane_base + Rings<N>::kDcol + dt * N + c * 16, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[c * 16 + j] = v[j];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&d_empty[dt]);
+            }
+            for (int span = 0; span < NG && !failed && !kWS; ++span) {
                 for (int q = 0; q < 4; ++q, ++t) {
                     const uint32_t d = t % kD;
                     if (!warp_wait(&d_full[d], (t / kD) & 1u, prm.timeout_flag)) {
@@ -394,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int N>
+template <int N, bool kWS>
 cudaError_t launch_n(const CUtensorMap &tm_packed, const uint16_t *xt_chunk, const TcParams &base,
                      cudaStream_t stream)
 {
@@ -414,7 +468,7 @@ cudaError_t launch_n(const CUtensorMap &tm_packed, const uint16_t *xt_chunk, con
     const size_t smem = fixed + static_cast<size_t>(nstage) * kStage;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(coarse_tc_kernel<N>,
+        cudaError_t e = cudaFuncSetAttribute(coarse_tc_kernel<N, kWS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemLimitTc);
         if (e != cudaSuccess) return e;
@@ -423,7 +477,7 @@ cudaError_t launch_n(const CUtensorMap &tm_packed, const uint16_t *xt_chunk, con
     TcParams prm = base;
     prm.nstage = nstage;
     const int grid = prm.ntiles < kNumSMs ? prm.ntiles : kNumSMs;
-    coarse_tc_kernel<N><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
+    coarse_tc_kernel<N, kWS><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
     return cudaGetLastError();
 }
 
@@ -473,11 +527,20 @@ cudaError_t launch_coarse_tc(const CoarseArgs &a, cudaStream_t stream)
         base.mrows = rows;
         const uint16_t *xt_chunk = a.xt + static_cast<size_t>(m0) * a.H;
         cudaError_t e;
-        switch (n) {
-        case 16: e = launch_n<16>(tm_packed, xt_chunk, base, stream); break;
-        case 32: e = launch_n<32>(tm_packed, xt_chunk, base, stream); break;
-        case 48: e = launch_n<48>(tm_packed, xt_chunk, base, stream); break;
-        default: e = launch_n<64>(tm_packed, xt_chunk, base, stream); break;
+        if (a.pack == kPackWside) {
+            switch (n) {
+            case 16: e = launch_n<16, true>(tm_packed, xt_chunk, base, stream); break;
+            case 32: e = launch_n<32, true>(tm_packed, xt_chunk, base, stream); break;
+            case 48: e = launch_n<48, true>(tm_packed, xt_chunk, base, stream); break;
+            default: e = launch_n<64, true>(tm_packed, xt_chunk, base, stream); break;
+            }
+        } else {
+            switch (n) {
+            case 16: e = launch_n<16, false>(tm_packed, xt_chunk, base, stream); break;
+            case 32: e = launch_n<32, false>(tm_packed, xt_chunk, base, stream); break;
+            case 48: e = launch_n<48, false>(tm_packed, xt_chunk, base, stream); break;
+            default: e = launch_n<64, false>(tm_packed, xt_chunk, base, stream); break;
+            }
         }
         if (e != cudaSuccess) return e;
     }

@@ -31,6 +31,8 @@ constexpr int kPackQuarter2 = 0;
 constexpr int kPackHalf4 = 1;
 constexpr int kPackContig2 = 2;
 constexpr int kPackG64 = 3;     // the quarter split with groups of 64 (group-size ablation)
+constexpr int kPackWside = 4;   // the quarter split, dequantised on the weight side (bf16
+                                // tcgen05 path; the scale-placement ablation)
 
 // ---- launchers (each returns the launch status) ------------------------------------------
 // W: bf16 rows (wsc null) or e4m3 rows with per-row fp32 scales wsc.  bits: 2 (quarter

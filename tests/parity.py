@@ -34,9 +34,10 @@ def gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, debug=True, path=None,
     """Run the CUDA path (dh_forward_debug, or dh_forward4_debug for the 4-bit head) on device
     tensors; return numpy outputs."""
     fwd_dbg = {4: dh.dh_forward4_debug, "c4": dh.dh_forward_c4_debug,
-               "g64": dh.dh_forward_g64_debug}.get(bits, dh.dh_forward_debug)
+               "g64": dh.dh_forward_g64_debug,
+               "wside": dh.dh_forward_wside_debug}.get(bits, dh.dh_forward_debug)
     fwd = dh.dh_forward4 if bits == 4 else dh.dh_forward
-    assert debug or bits not in ("c4", "g64")
+    assert debug or bits not in ("c4", "g64", "wside")
     M, H = x.shape
     V = W.shape[0]
     dev = x.device
@@ -195,8 +196,8 @@ def full_compare(x, W, packed, S, ZS, kcand, rerank, topk, path=None, bits=2):
     gpu = gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, path=path, bits=bits)
     xb, Wb = host(x), host(W)
     pb, Sb, ZSb = host(packed), host(S), host(ZS)
-    ref_fwd = {4: orc.forward4, "c4": orc.forward_c4, "g64": orc.forward_g64}.get(bits,
-                                                                                 orc.forward)
+    ref_fwd = {4: orc.forward4, "c4": orc.forward_c4, "g64": orc.forward_g64,
+               "wside": orc.forward_wside}.get(bits, orc.forward)
     ref = ref_fwd(xb, pb, Sb, ZSb, Wb, kcand, rerank, topk)
     rep = {}
     rep["coarse_worst"] = check_coarse(gpu["coarse"], ref["coarse"])

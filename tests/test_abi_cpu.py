@@ -202,3 +202,11 @@ def test_g64_entry_points_reject_bad_arguments(lib):
     bad = list(args)
     bad[10] = 0
     assert lib.dh_forward_g64_debug(*bad, None, None, None, None, None, None, None) == -3
+
+
+def test_wside_entry_point_rejects_bad_arguments(lib):
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1024, 8192, 8, 32, 1, FAKE, FAKE, FAKE, 1 << 40]
+    assert lib.dh_forward_wside_debug(*args, FAKE + 4, None, None, None, None, None, None) == -5
+    bad = list(args)
+    bad[3] = None
+    assert lib.dh_forward_wside_debug(*bad, None, None, None, None, None, None, None) == -1
