@@ -262,6 +262,16 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
                                        : (path == DH_PATH_TC_BF16 ? "tcgen05 bf16" : "warp"),
                     cudaGetErrorString(err));
     if (!rec(2)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+    if (!candidates_only && select_rerank_fits(rerank, kcand)) {
+        // one launch for the selection, the rerank and the top-k (the stage events 3 and 4
+        // then enclose nothing)
+        err = launch_select_rerank(cval, cidx, M, L.ncand, kcand, rerank, x, W, w_scale, H, V,
+                                   sel, ex, topk, idx, logit, stream);
+        if (err != cudaSuccess)
+            return fail(DH_ERR_CUDA, "select/rerank launch: %s", cudaGetErrorString(err));
+        if (!rec(3) || !rec(4) || !rec(5)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
+        return ok();
+    }
     err = launch_select(cval, cidx, M, L.ncand, kcand, rerank, sv, si, L.scratch_entries,
                         counters + kSelDoneOffset, true, sel, sel_val, id_offset, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
@@ -616,6 +626,7 @@ int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank)
     int prep = 1, coarse = (M + kWarpBatch - 1) / kWarpBatch;
     if (path == DH_PATH_TC) prep = coarse = tc8_chunks(M);
     else if (path == DH_PATH_TC_BF16) coarse = tc_launches(M);
+    if (select_rerank_fits(rerank, kcand)) return prep + coarse + 1; // fused select + rerank
     return prep + coarse + L.passes /*selection*/ + 1 /*rerank + top-k*/;
 }
 

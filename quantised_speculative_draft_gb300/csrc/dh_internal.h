@@ -122,6 +122,15 @@ cudaError_t launch_rerank_topk(const uint16_t *x, const void *W, const float *w_
                                const int32_t *sel_idx, int R, float *ex, int *row_done, int topk,
                                int32_t *out_idx, float *out_logit, int id_offset,
                                cudaStream_t stream);
+// Selection, rerank and top-k fused (R <= 32, any kcand <= 64): one 8-CTA cluster per batch
+// row on the coarse pass's block lists; writes sel_idx / ex [M, R] (the reranked ids in rank
+// order and their exact values) and the top-k, with the rerank kernel's arithmetic.
+bool select_rerank_fits(int R, int kcand);
+cudaError_t launch_select_rerank(const float *cand_val, const int32_t *cand_idx, int M,
+                                 long long ncand, int kcand, int R, const uint16_t *x,
+                                 const void *W, const float *w_scale, int H, int V,
+                                 int32_t *sel_idx, float *ex, int topk, int32_t *out_idx,
+                                 float *out_logit, cudaStream_t stream);
 // Per-rank partial exact values parts [P, M, R] merged by max, then the per-row top-k.
 cudaError_t launch_merge_topk(const float *parts, const int32_t *sel_idx, int P, int M, int R,
                               int topk, int32_t *out_idx, float *out_logit, cudaStream_t stream);

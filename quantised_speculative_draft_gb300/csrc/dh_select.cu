@@ -7,6 +7,8 @@
 #include "dh_common.cuh"
 #include "dh_internal.h"
 
+#include <cooperative_groups.h>
+
 namespace dh {
 
 namespace {
@@ -380,28 +382,21 @@ constexpr int kRerankThreads = 256;
 __device__ void sort_write_topk(unsigned long long *k, int n2, int topk, int32_t *oidx,
                                 float *ologit);
 
-// kFp8: W holds e4m3 rows and w_scale the per-row fp32 scales; each weight is the fp32
-// product e4m3(b) * w_scale[n], rounded once (radiance_drafthead.py, _rerank_exact, FP8 branch:
-// the selected fp8 rows are dequantised to fp32 before the dot product).  Otherwise W is bf16.
+// One thread's share of the exact logit x . W[n] (n < 0: none), the same arithmetic in every
+// caller so that every path reranks to the same bits: the thread takes the 8-weight slices
+// i = tid, tid + 256, ... of the row, sums their products in two fp32 partials (products of
+// bf16 values are exact in fp32; an fp8 weight is first rounded to fp32(e4m3 * scale)), and
+// returns their sum in fp64.  The caller reduces the 256 values: an xor-shuffle tree per warp,
+// then the eight warps in order.
 template <bool kFp8>
-__global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
-    const uint16_t *__restrict__ x, const void *__restrict__ Wv,
-    const float *__restrict__ w_scale, int H, int V, const int32_t *__restrict__ sel_idx, int R,
-    float *__restrict__ ex, int *__restrict__ row_done, int topk, int32_t *__restrict__ out_idx,
-    float *__restrict__ out_logit, int id_offset)
+__device__ __forceinline__ double rerank_partial(const uint16_t *__restrict__ xrow,
+                                                 const void *__restrict__ Wv,
+                                                 const float *__restrict__ w_scale, int n, int H,
+                                                 int tid)
 {
-    __shared__ double part[kRerankThreads / 32];
-    __shared__ unsigned long long k[kMaxRerank];
-    __shared__ int s_last;
-    const long long pair = blockIdx.x;
-    const int m = static_cast<int>(pair / R);
-    const int gid = sel_idx[pair];
-    const int n = gid >= 0 ? gid - id_offset : -1; // row of W (a shard starts at id_offset)
-    const int tid = threadIdx.x, lane = tid & 31;
-
     float a0 = 0.f, a1 = 0.f;
-    if (n >= 0 && n < V) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<long long>(m) * H);
+    if (n >= 0) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(xrow);
         const int nv = H / 8; // 8 weights per step
         if constexpr (kFp8) {
             const uint2 *wr = reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(Wv) +
@@ -438,7 +433,30 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
             }
         }
     }
-    double d = static_cast<double>(a0) + static_cast<double>(a1);
+    return static_cast<double>(a0) + static_cast<double>(a1);
+}
+
+// kFp8: W holds e4m3 rows and w_scale the per-row fp32 scales; each weight is the fp32
+// product e4m3(b) * w_scale[n], rounded once (radiance_drafthead.py, _rerank_exact, FP8 branch:
+// the selected fp8 rows are dequantised to fp32 before the dot product).  Otherwise W is bf16.
+template <bool kFp8>
+__global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
+    const uint16_t *__restrict__ x, const void *__restrict__ Wv,
+    const float *__restrict__ w_scale, int H, int V, const int32_t *__restrict__ sel_idx, int R,
+    float *__restrict__ ex, int *__restrict__ row_done, int topk, int32_t *__restrict__ out_idx,
+    float *__restrict__ out_logit, int id_offset)
+{
+    __shared__ double part[kRerankThreads / 32];
+    __shared__ unsigned long long k[kMaxRerank];
+    __shared__ int s_last;
+    const long long pair = blockIdx.x;
+    const int m = static_cast<int>(pair / R);
+    const int gid = sel_idx[pair];
+    const int n = gid >= 0 ? gid - id_offset : -1; // row of W (a shard starts at id_offset)
+    const int tid = threadIdx.x, lane = tid & 31;
+
+    double d = rerank_partial<kFp8>(x + static_cast<long long>(m) * H, Wv, w_scale,
+                                    (n >= 0 && n < V) ? n : -1, H, tid);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
     if (lane == 0) part[tid >> 5] = d;
@@ -470,6 +488,185 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
     __syncthreads();
     sort_write_topk(k, n2, topk, out_idx + static_cast<long long>(m) * topk,
                     out_logit + static_cast<long long>(m) * topk);
+}
+
+// ----------------------------------------------------------------------------------------
+// a5 + a6 + a7 fused for R <= 32: one cluster of kSrCtas CTAs per batch row, no hand-off
+// through global memory between the steps.
+//   1. CTA p keeps the 32 best block maxima of its slice of the row's blocks (warp sorts and a
+//      tree of warp merges), gathers those blocks' candidates and keeps their 32 best: list
+//      L_p in its shared memory.
+//   2. After a cluster barrier every CTA merges the kSrCtas lists, read from the other CTAs'
+//      shared memory, into the row's 32 best candidates G (rank order).  Exact: a candidate
+//      of the row's top 32 has a block among the 32 best maxima of the row, hence of its
+//      CTA's slice, and fewer than 32 candidates of that CTA's gathered set beat it.
+//   3. CTA p reranks G[p], G[p + kSrCtas], ... with the 256-thread dot product of the rerank
+//      kernel (same bits) and writes each exact value's rank key into CTA 0's shared memory.
+//   4. After a second cluster barrier CTA 0 sorts the R keys (one warp) and writes the top-k.
+// Every CTA finishes its reads of remote shared memory before the second barrier, so no CTA
+// exits while another still reads its memory.
+// ----------------------------------------------------------------------------------------
+constexpr int kSrCtas = 8;      // CTAs per row (a portable cluster)
+constexpr int kSrThreads = 256; // = kRerankThreads: the rerank's reduction shape
+constexpr int kSrRows = 4;      // reranked rows per CTA: R <= kSrCtas * kSrRows = 32
+
+// Descending bitonic sort of 32 keys, one per lane.
+__device__ __forceinline__ unsigned long long warp_sort32_desc(unsigned long long v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, stride);
+            v = keep_max ? kmax(v, o) : kmin(v, o);
+        }
+    }
+    return v;
+}
+
+// Tree merge of the eight warps' descending lists lists[0..7]; the result in lists[0].  Each
+// level's warps read their own slot and one above the level, which nobody writes in it.
+__device__ __forceinline__ void tree_merge8(unsigned long long (*lists)[32])
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int n = 4; n >= 1; n >>= 1) {
+        if (warp < n) lists[warp][lane] = warp_merge32_desc(lists[warp][lane], lists[warp + n][lane]);
+        __syncthreads();
+    }
+}
+
+template <bool kFp8>
+__global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
+    select_rerank_kernel(const float *__restrict__ cand_val, const int32_t *__restrict__ cand_idx,
+                         long long ncand, int nblk, int kcand, int R,
+                         const uint16_t *__restrict__ x, const void *__restrict__ Wv,
+                         const float *__restrict__ w_scale, int H, int V,
+                         int32_t *__restrict__ sel_idx, float *__restrict__ ex, int topk,
+                         int32_t *__restrict__ out_idx, float *__restrict__ out_logit)
+{
+    namespace cg = cooperative_groups;
+    __shared__ unsigned long long keys[kRowSelR * kBlockN]; // 2048: the largest gather
+    __shared__ unsigned long long lists[kSrThreads / 32][32];
+    __shared__ unsigned long long mylist[32];               // L_p, read by the cluster
+    __shared__ unsigned long long exk[32];                  // CTA 0: the R exact rank keys
+    __shared__ double part[kSrRows][kSrThreads / 32];
+    __shared__ int sblk[kRowSelR];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int p = static_cast<int>(cluster.block_rank());
+    const int m = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float *vrow = cand_val + static_cast<long long>(m) * ncand;
+    const int32_t *irow = cand_idx + static_cast<long long>(m) * ncand;
+
+    // 1a. the 32 best block maxima of this CTA's slice (a block's first entry is its best)
+    const int per = (nblk + kSrCtas - 1) / kSrCtas;
+    const int b0 = p * per, b1 = min(nblk, b0 + per);
+    constexpr int kRound = (kSrThreads / 32) * kRowSelChunk; // 1024 keys: a chunk per warp
+    unsigned long long acc = 0;
+    for (int base = b0; base < b1; base += kRound) {
+        for (int i = tid; i < kRound; i += kSrThreads) {
+            const int bk = base + i;
+            unsigned long long key = 0;
+            if (bk < b1) {
+                const long long e = static_cast<long long>(bk) * kcand;
+                const int id = irow[e];
+                if (id >= 0) key = rank_key(vrow[e], id);
+            }
+            keys[i] = key;
+        }
+        __syncthreads();
+        if (base + warp * kRowSelChunk < b1) // warp-uniform
+            acc = warp_merge32_desc(acc, warp_top32_of128(keys + warp * kRowSelChunk));
+        __syncthreads();
+    }
+    lists[warp][lane] = acc;
+    __syncthreads();
+    tree_merge8(lists);
+    if (tid < kRowSelR) {
+        const unsigned long long key = lists[0][tid];
+        sblk[tid] = key ? static_cast<int>(~static_cast<uint32_t>(key)) / kBlockN : -1;
+    }
+    __syncthreads();
+
+    // 1b. those blocks' candidates; their 32 best -> L_p
+    const int nc = kRowSelR * kcand;
+    const int nchunks = (nc + kRowSelChunk - 1) / kRowSelChunk;
+    for (int e = tid; e < nchunks * kRowSelChunk; e += kSrThreads) {
+        unsigned long long key = 0;
+        if (e < nc) {
+            const int bk = sblk[e / kcand];
+            if (bk >= 0) {
+                const long long c = static_cast<long long>(bk) * kcand + e % kcand;
+                const int id = irow[c];
+                if (id >= 0) key = rank_key(vrow[c], id);
+            }
+        }
+        keys[e] = key;
+    }
+    __syncthreads();
+    acc = 0;
+    for (int c = warp; c < nchunks; c += kSrThreads / 32)
+        acc = warp_merge32_desc(acc, warp_top32_of128(keys + c * kRowSelChunk));
+    lists[warp][lane] = acc;
+    __syncthreads();
+    tree_merge8(lists);
+    if (warp == 0) mylist[lane] = lists[0][lane];
+    cluster.sync();
+
+    // 2. every CTA merges the cluster's lists into G (lists[0], rank order)
+    {
+        const unsigned long long *rl = cluster.map_shared_rank(mylist, warp % kSrCtas);
+        lists[warp][lane] = warp < kSrCtas ? rl[lane] : 0ull;
+    }
+    __syncthreads();
+    tree_merge8(lists);
+
+    // 3. rerank G[p + kSrCtas r] (the four rows' loads in flight together)
+    int gid[kSrRows];
+    double d[kSrRows];
+#pragma unroll
+    for (int r = 0; r < kSrRows; ++r) {
+        const int j = p + kSrCtas * r;
+        const unsigned long long key = j < R ? lists[0][j] : 0ull;
+        gid[r] = key ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
+        const int n = (gid[r] >= 0 && gid[r] < V) ? gid[r] : -1;
+        d[r] = rerank_partial<kFp8>(x + static_cast<long long>(m) * H, Wv, w_scale, n, H, tid);
+    }
+#pragma unroll
+    for (int r = 0; r < kSrRows; ++r) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d[r] += __shfl_xor_sync(0xffffffffu, d[r], o);
+        if (lane == 0) part[r][warp] = d[r];
+    }
+    __syncthreads();
+    if (tid < kSrRows) {
+        const int r = tid, j = p + kSrCtas * r;
+        if (j < R) {
+            double t = 0.0;
+            for (int i = 0; i < kSrThreads / 32; ++i) t += part[r][i];
+            const bool ok = gid[r] >= 0 && gid[r] < V;
+            const float e = ok ? static_cast<float>(t) : -INFINITY;
+            sel_idx[static_cast<long long>(m) * R + j] = gid[r];
+            ex[static_cast<long long>(m) * R + j] = e;
+            unsigned long long *exk0 = cluster.map_shared_rank(exk, 0);
+            exk0[j] = ok ? rank_key(e, gid[r]) : 0ull;
+        }
+    }
+    cluster.sync();
+
+    // 4. CTA 0: the row's top-k of the R exact values
+    if (p == 0 && warp == 0) {
+        const unsigned long long key = warp_sort32_desc(lane < R ? exk[lane] : 0ull);
+        if (lane < topk) {
+            out_idx[static_cast<long long>(m) * topk + lane] =
+                key ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
+            out_logit[static_cast<long long>(m) * topk + lane] =
+                key ? f32_from_order_key(static_cast<uint32_t>(key >> 32)) : -INFINITY;
+        }
+    }
 }
 
 // ----------------------------------------------------------------------------------------
@@ -617,6 +814,30 @@ cudaError_t launch_rerank_topk(const uint16_t *x, const void *W, const float *w_
     else
         rerank_topk_kernel<false><<<blocks, kRerankThreads, 0, stream>>>(
             x, W, nullptr, H, V, sel_idx, R, ex, row_done, topk, out_idx, out_logit, id_offset);
+    return cudaGetLastError();
+}
+
+bool select_rerank_fits(int R, int kcand)
+{
+    return R >= 1 && R <= kSrCtas * kSrRows && R <= kRowSelR && kcand >= 1 && kcand <= kBlockN;
+}
+
+cudaError_t launch_select_rerank(const float *cand_val, const int32_t *cand_idx, int M,
+                                 long long ncand, int kcand, int R, const uint16_t *x,
+                                 const void *W, const float *w_scale, int H, int V,
+                                 int32_t *sel_idx, float *ex, int topk, int32_t *out_idx,
+                                 float *out_logit, cudaStream_t stream)
+{
+    const int nblk = static_cast<int>(ncand / kcand);
+    const dim3 grid(kSrCtas, static_cast<unsigned>(M));
+    if (w_scale)
+        select_rerank_kernel<true><<<grid, kSrThreads, 0, stream>>>(
+            cand_val, cand_idx, ncand, nblk, kcand, R, x, W, w_scale, H, V, sel_idx, ex, topk,
+            out_idx, out_logit);
+    else
+        select_rerank_kernel<false><<<grid, kSrThreads, 0, stream>>>(
+            cand_val, cand_idx, ncand, nblk, kcand, R, x, W, nullptr, H, V, sel_idx, ex, topk,
+            out_idx, out_logit);
     return cudaGetLastError();
 }
 
