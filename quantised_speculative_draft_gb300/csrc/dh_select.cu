@@ -8,6 +8,7 @@
 #include "dh_internal.h"
 
 #include <cooperative_groups.h>
+#include <type_traits>
 
 namespace dh {
 
@@ -301,15 +302,24 @@ __global__ void __launch_bounds__(kRowSelThreads) select_rows_kernel(
     const float *vrow = cand_val + static_cast<long long>(m) * ncand;
     const int32_t *irow = cand_idx + static_cast<long long>(m) * ncand;
 
-    for (int i = threadIdx.x; i < kRowSelCtaKeys; i += kRowSelThreads) {
-        const int bk = p * kRowSelCtaKeys + i;
-        unsigned long long key = 0;
-        if (bk < nblk) {
-            const long long e = static_cast<long long>(bk) * kcand;
-            const int id = irow[e];
-            if (id >= 0) key = rank_key(vrow[e], id);
+    {
+        // every load issued before any is used (value and index independently)
+        constexpr int kPer = kRowSelCtaKeys / kRowSelThreads;
+        int ids[kPer];
+        float vals[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int bk = p * kRowSelCtaKeys + threadIdx.x + u * kRowSelThreads;
+            const long long e = static_cast<long long>(bk < nblk ? bk : 0) * kcand;
+            ids[u] = __ldcg(irow + e);
+            vals[u] = __ldcg(vrow + e);
         }
-        keys[i] = key;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int bk = p * kRowSelCtaKeys + threadIdx.x + u * kRowSelThreads;
+            keys[threadIdx.x + u * kRowSelThreads] =
+                (bk < nblk && ids[u] >= 0) ? rank_key(vals[u], ids[u]) : 0ull;
+        }
     }
     __syncthreads();
     cta_top32(keys, kRowSelCtaKeys, lists);
@@ -434,6 +444,83 @@ __device__ __forceinline__ double rerank_partial(const uint16_t *__restrict__ xr
         }
     }
     return static_cast<double>(a0) + static_cast<double>(a1);
+}
+
+// rerank_partial for NR rows at once (rows n[r] < 0: none), with every row's FMA sequence
+// exactly rerank_partial's (slices in increasing i, the same two chains), so each d[r] has
+// the same bits.  The slices are taken kBatch at a time with all their loads issued before
+// the arithmetic, so the rows' HBM latencies overlap instead of following one another.
+template <bool kFp8, int NR>
+__device__ __forceinline__ void rerank_partial_rows(const uint16_t *__restrict__ xrow,
+                                                    const void *__restrict__ Wv,
+                                                    const float *__restrict__ w_scale,
+                                                    const int (&n)[NR], int H, int tid,
+                                                    double (&d)[NR])
+{
+    constexpr int kBatch = 3; // slices per thread in flight (H = 5120: all of them)
+    using WVec = typename std::conditional<kFp8, uint2, uint4>::type;
+    float a0[NR], a1[NR], rs[NR];
+    const WVec *wr[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        a0[r] = 0.f;
+        a1[r] = 0.f;
+        const long long row = n[r] >= 0 ? n[r] : 0;
+        if constexpr (kFp8) {
+            wr[r] = reinterpret_cast<const WVec *>(static_cast<const uint8_t *>(Wv) + row * H);
+            rs[r] = n[r] >= 0 ? __ldg(w_scale + row) : 0.f;
+        } else {
+            wr[r] = reinterpret_cast<const WVec *>(static_cast<const uint16_t *>(Wv) + row * H);
+            rs[r] = 0.f;
+        }
+    }
+    const uint4 *xr = reinterpret_cast<const uint4 *>(xrow);
+    const int nv = H / 8;
+    for (int i0 = tid; i0 < nv; i0 += kBatch * kRerankThreads) {
+        uint4 xv[kBatch];
+        WVec wv[kBatch][NR];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = i0 + b * kRerankThreads;
+            if (i < nv) {
+                xv[b] = __ldg(xr + i);
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    if (n[r] >= 0) wv[b][r] = __ldg(wr[r] + i);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = i0 + b * kRerankThreads;
+            if (i >= nv) break;
+            const uint32_t xs4[4] = {xv[b].x, xv[b].y, xv[b].z, xv[b].w};
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (n[r] < 0) continue;
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t wb = (q < 2 ? wv[b][r].x : wv[b][r].y) >> (16 * (q & 1));
+                        a0[r] = fmaf(__uint_as_float(xs4[q] << 16),
+                                     __fmul_rn(e4m3_to_f32(wb), rs[r]), a0[r]);
+                        a1[r] = fmaf(__uint_as_float(xs4[q] & 0xFFFF0000u),
+                                     __fmul_rn(e4m3_to_f32(wb >> 8), rs[r]), a1[r]);
+                    }
+                } else {
+                    const uint32_t ws4[4] = {wv[b][r].x, wv[b][r].y, wv[b][r].z, wv[b][r].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        a0[r] = fmaf(__uint_as_float(xs4[q] << 16), __uint_as_float(ws4[q] << 16),
+                                     a0[r]);
+                        a1[r] = fmaf(__uint_as_float(xs4[q] & 0xFFFF0000u),
+                                     __uint_as_float(ws4[q] & 0xFFFF0000u), a1[r]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) d[r] = static_cast<double>(a0[r]) + static_cast<double>(a1[r]);
 }
 
 // kFp8: W holds e4m3 rows and w_scale the per-row fp32 scales; each weight is the fp32
@@ -567,15 +654,22 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     constexpr int kRound = (kSrThreads / 32) * kRowSelChunk; // 1024 keys: a chunk per warp
     unsigned long long acc = 0;
     for (int base = b0; base < b1; base += kRound) {
-        for (int i = tid; i < kRound; i += kSrThreads) {
-            const int bk = base + i;
-            unsigned long long key = 0;
-            if (bk < b1) {
-                const long long e = static_cast<long long>(bk) * kcand;
-                const int id = irow[e];
-                if (id >= 0) key = rank_key(vrow[e], id);
-            }
-            keys[i] = key;
+        // every load of the round issued before any is used (value and index independently)
+        constexpr int kPer = kRound / kSrThreads;
+        int ids[kPer];
+        float vals[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int bk = base + tid + u * kSrThreads;
+            const long long e = static_cast<long long>(bk < b1 ? bk : b0) * kcand;
+            ids[u] = __ldcg(irow + e);
+            vals[u] = __ldcg(vrow + e);
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int bk = base + tid + u * kSrThreads;
+            keys[tid + u * kSrThreads] =
+                (bk < b1 && ids[u] >= 0) ? rank_key(vals[u], ids[u]) : 0ull;
         }
         __syncthreads();
         if (base + warp * kRowSelChunk < b1) // warp-uniform
@@ -594,17 +688,25 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     // 1b. those blocks' candidates; their 32 best -> L_p
     const int nc = kRowSelR * kcand;
     const int nchunks = (nc + kRowSelChunk - 1) / kRowSelChunk;
-    for (int e = tid; e < nchunks * kRowSelChunk; e += kSrThreads) {
-        unsigned long long key = 0;
-        if (e < nc) {
-            const int bk = sblk[e / kcand];
-            if (bk >= 0) {
-                const long long c = static_cast<long long>(bk) * kcand + e % kcand;
-                const int id = irow[c];
-                if (id >= 0) key = rank_key(vrow[c], id);
-            }
+    for (int e0 = 0; e0 < nchunks * kRowSelChunk; e0 += 2 * kSrThreads) {
+        int ids[2];
+        float vals[2];
+        bool live[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = e0 + tid + u * kSrThreads;
+            const int bk = e < nc ? sblk[e / kcand] : -1;
+            live[u] = bk >= 0;
+            const long long c = live[u] ? static_cast<long long>(bk) * kcand + e % kcand : 0;
+            ids[u] = __ldcg(irow + c);
+            vals[u] = __ldcg(vrow + c);
         }
-        keys[e] = key;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = e0 + tid + u * kSrThreads;
+            if (e < nchunks * kRowSelChunk)
+                keys[e] = (live[u] && ids[u] >= 0) ? rank_key(vals[u], ids[u]) : 0ull;
+        }
     }
     __syncthreads();
     acc = 0;
@@ -625,16 +727,17 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     tree_merge8(lists);
 
     // 3. rerank G[p + kSrCtas r] (the four rows' loads in flight together)
-    int gid[kSrRows];
+    int gid[kSrRows], nrow[kSrRows];
     double d[kSrRows];
 #pragma unroll
     for (int r = 0; r < kSrRows; ++r) {
         const int j = p + kSrCtas * r;
         const unsigned long long key = j < R ? lists[0][j] : 0ull;
         gid[r] = key ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
-        const int n = (gid[r] >= 0 && gid[r] < V) ? gid[r] : -1;
-        d[r] = rerank_partial<kFp8>(x + static_cast<long long>(m) * H, Wv, w_scale, n, H, tid);
+        nrow[r] = (gid[r] >= 0 && gid[r] < V) ? gid[r] : -1;
     }
+    rerank_partial_rows<kFp8, kSrRows>(x + static_cast<long long>(m) * H, Wv, w_scale, nrow, H,
+                                       tid, d);
 #pragma unroll
     for (int r = 0; r < kSrRows; ++r) {
 #pragma unroll
