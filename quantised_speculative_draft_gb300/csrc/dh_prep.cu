@@ -121,18 +121,21 @@ __device__ __forceinline__ float e4m3_to_f32(__nv_fp8_storage_t v)
     return __half2float(__half(h));
 }
 
-constexpr int kPrepOcts = 8; // 16-byte slices of x per thread (H up to 16384)
+constexpr int kPrepMaxThreads = 1024;
+constexpr int kPrepOcts = 2; // 16-byte slices of x per thread: one per thread up to H = 8192,
+                             // two up to H = 16384 (the CTA has min(H/8, 1024) threads)
 
 // G: the group size of the sums xs (128, or 64 for the group-size ablation).
 template <int G>
-__global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restrict__ x, int H,
+__global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_t *__restrict__ x,
+                                                                   int H,
                                                        int m0, int rows, int MP, int T,
                                                        uint8_t *__restrict__ xt8,
                                                        float *__restrict__ xs,
                                                        float *__restrict__ inv_scale,
                                                        int *__restrict__ counters, int ncounters)
 {
-    __shared__ float wmax[8];
+    __shared__ float wmax[kPrepMaxThreads / 32];
     const int m = blockIdx.x;
     const bool valid = m < rows;
     const int octs = H / 8, NGt = H / G;
@@ -140,12 +143,12 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restric
         for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
     const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
 
-    // the row stays in registers between the max and the split (H <= 256 * 8 * kPrepOcts)
+    // the row stays in registers between the max and the split (H <= 1024 * 8 * kPrepOcts)
     uint4 xv[kPrepOcts];
     float mx = 0.f;
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
-        const int o = threadIdx.x + j * 256;
+        const int o = threadIdx.x + j * blockDim.x;
         xv[j] = make_uint4(0, 0, 0, 0);
         if (valid && o < octs) xv[j] = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t *__restric
 
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
-        const int o = threadIdx.x + j * 256;
+        const int o = threadIdx.x + j * blockDim.x;
         if (o >= octs) break;
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
         uint32_t lo[3] = {0, 0, 0}, hi[3] = {0, 0, 0};
@@ -212,7 +215,10 @@ cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace 
     for (int c = 0; c < tc8_chunks(M); ++c) {
         const Tc8Chunk k = tc8_chunk(M, c);
         auto kern = w.group == 64 ? prep_fp8_kernel<64> : prep_fp8_kernel<128>;
-        kern<<<k.MP, 256, 0, stream>>>(
+        // one thread per 16-byte slice of the row (a multiple of 32 threads)
+        int threads = ((H / 8 + 31) / 32) * 32;
+        if (threads > kPrepMaxThreads) threads = kPrepMaxThreads;
+        kern<<<k.MP, threads, 0, stream>>>(
             x, H, k.m0, k.rows, k.MP, k.T, w.xt8 + static_cast<size_t>(c) * w.chunk_bytes,
             w.xs + static_cast<size_t>(c) * w.xs_chunk,
             w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows, c == 0 ? counters : nullptr,
