@@ -109,6 +109,21 @@ def test_forward_ragged(M, H, V, kcand, rerank, topk):
               "tie rows", len(rep["ties"]), "differing", sum(t[4] for t in rep["ties"]))
 
 
+@pytest.mark.parametrize("M, H, V, kcand, rerank, topk", [
+    (128, 512, 4096, 64, 32, 32),       # largest batch, whole blocks as candidates, top-k = R
+    (2, 1024, 100000 + 13, 8, 32, 32),  # 1563 blocks: ~196 per CTA of the row's cluster
+    (4, 512, 64 * 3 + 1, 1, 4, 2),      # four blocks, one candidate each: rerank all
+    (6, 1024, 8192, 2, 1, 1),           # RERANK 1
+])
+def test_forward_fused_selection_edges(M, H, V, kcand, rerank, topk):
+    """Sizes at the edges of the one-launch selection + rerank + top-k (RERANK <= 32)."""
+    x, W = _inputs(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    packed, S, ZS = gpu_quantize(W)
+    rep, gpu, ref = full_compare(x, W, packed, S, ZS, kcand, rerank, topk)
+    print((M, H, V, kcand, rerank, topk), rep["coarse_worst"], rep["exact_worst"],
+          "tie rows", len(rep["ties"]))
+
+
 def test_forward_full_pool_is_the_exact_head():
     """KCAND=64 and RERANK=V rerank every column: the result is the exact bf16 head's top-k."""
     M, H, V, k = 3, 512, 1000, 10
