@@ -47,6 +47,7 @@ def parse():
                     help="vocabulary rows (smaller heads are for profiling captures only)")
     ap.add_argument("--sets", type=int, default=2, help="resident input sets rotated per step")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8-head line")
+    ap.add_argument("--no-shard", action="store_true", help="skip the one-shard-head lines")
     ap.add_argument("--no-int4", action="store_true", help="skip the 4-bit-head line")
     ap.add_argument("--no-ablations", action="store_true", help="skip the layout ablations")
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2,
@@ -209,6 +210,24 @@ class Int4Inputs:
         import quantised_speculative_draft_gb300 as dh
         dh.dh_forward4_timed(self.x[:M], self.packed, self.S, self.ZS, self.W, self.kcand,
                              RERANK, TOPK, idx, logit, ws, events)
+
+
+class ShardInputs(Inputs):
+    """One resident input set of the one-shard head (V=124160: one rank's vocabulary slice at
+    two-way tensor parallelism), with that workload's distributions."""
+
+    def __init__(self, seed, dev, max_m):
+        import torch
+        import quantised_speculative_draft_gb300 as dh
+        from quantised_speculative_draft_gb300 import synth
+        wl = synth.shard(max_m)
+        self.x = synth.make_x(wl, seed, dev)
+        self.W = synth.make_w(wl, seed, dev)
+        V, H = self.W.shape
+        self.packed = torch.empty(V, H // 4, dtype=torch.uint8, device=dev)
+        self.S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        self.ZS = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        dh.dh_quantize(self.W, self.packed, self.S, self.ZS)
 
 
 class Fp8Inputs:
@@ -558,6 +577,22 @@ def run_ours(args):
         else None
     pack = time_quantize(dev) if rank == 0 else None
 
+    shard = None
+    if rank == 0 and not args.no_shard:
+        sets_sh = [ShardInputs(seed, dev, 64) for seed in range(args.sets)]
+        V_SH = sets_sh[0].W.shape[0]
+        shard = {"workload": f"one-shard head (V={V_SH}, H={H_FULL}, KCAND={KCAND}, "
+                             f"RERANK={RERANK}, argmax; RMS-normalised x, 512 hot rows)"}
+        for m in (16, 64):
+            msh, _, _ = time_graph(sets_sh, m, args.sweep_steps, 5)  # full-head workspace suffices
+            stsh = time_stages(sets_sh, m, 20)
+            nb_sh = algorithmic_bytes(V_SH, H_FULL)
+            shard[f"M{m}"] = {"us_per_call": round(msh * 1e3 / args.sweep_steps, 2),
+                              "coarse_us": round(stsh["coarse"], 2),
+                              "coarse_frac_of_hbm": round(nb_sh / stsh["coarse"] / 1e3 / hbm, 4),
+                              "stages_us": {k: round(v, 2) for k, v in stsh.items()}}
+        del sets_sh
+
     fp8 = None
     if rank == 0 and not args.no_fp8:
         del sets
@@ -679,6 +714,7 @@ def run_ours(args):
             "clocks": clocks,
             "stages_us": {k: round(v, 2) for k, v in stages.items()},
             "pack": pack,
+            "one_shard_head": shard,
             "fp8_head": fp8,
             "int4_head": int4,
             "ablations": abl,
