@@ -211,10 +211,13 @@ def test_forward_topk_caller_full_vocab(rerank):
     print(f"top-16 recall vs exact bf16 head at RERANK={rerank}: {rec:.3f}")
 
 
-def test_forward_full_vocab_m72_sampled():
-    """M=72, V=248320 (the largest point of the M sweep): sampled coarse values against the
-    oracle, the selection checked for consistency, exact values against the oracle."""
-    wl = synth.full(72)
+@pytest.mark.parametrize("wl", [synth.full(72), synth.shard(64)],
+                         ids=["full-vocab-M72", "one-shard-M64"])
+def test_forward_full_size_sampled(wl):
+    """The full-size workloads the oracle cannot run whole in seconds -- M=72 on the full head
+    (the largest point of the M sweep) and M=64 on the one-shard head (the compute-bound
+    regime): sampled coarse values against the oracle, the selection checked for consistency,
+    exact values against the oracle."""
     x, W = synth.make_x(wl, 0, DEV), synth.make_w(wl, 0, DEV)
     packed, S, ZS = gpu_quantize(W)
     gpu = gpu_forward(x, packed, S, ZS, W, 8, 32, 1)
@@ -226,7 +229,7 @@ def test_forward_full_vocab_m72_sampled():
     ref_c = orc.coarse(xb, host(packed[rows_t]), host(S[rows_t]), host(ZS[rows_t]))
     check_coarse(gpu["coarse"][:, rows], ref_c)
     # every candidate's value is its coarse value, and each block's list is its best kcand
-    M, V = 72, wl.V
+    M, V = wl.M, wl.V
     for m in range(0, M, 7):
         for b in rng.choice((V + 63) // 64, 20, replace=False):
             cols = np.arange(64 * b, 64 * b + 64)
