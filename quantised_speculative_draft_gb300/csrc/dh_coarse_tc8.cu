@@ -70,10 +70,12 @@ constexpr int kDqWarps = 4; // dequant warps (4-7); the epilogue is warps 8-15
 // Batch rows per launch MP in {16, 32}; x in T = 2 e4m3 terms; MMA N = T * MP.
 // The unit of MMA work is a whole span at N = 32 (kU = 1: 4 planes, 16 MMAs) and half a span
 // at N = 64 (kU = 2: planes 2u, 2u+1, 8 MMAs).  Tensor memory holds kSlots unit slots, each an
-// A buffer (32 columns of e4m3 per plane) and one N-column fp32 accumulator per plane; unit
-// q = kU span + u uses slot q % kSlots and is issued by that slot's own thread, so the issuers
-// of different slots run concurrently (a thread issuing tcgen05.mma is held ~57 cycles per
-// instruction; two threads overlap).  Both sizes give two slots.
+// A buffer (32 columns of e4m3 per plane) and one N-column fp32 accumulator per group of the
+// unit's planes; unit q = kU span + u uses slot q % kSlots and is issued by that slot's own
+// thread, so the issuers of different slots run concurrently (a thread issuing tcgen05.mma is
+// held ~57 cycles per instruction; two threads overlap).  Both sizes give two slots.  Groups
+// of 64 (kPackG64, MP = 16 only) put two accumulators on each plane and use half-span units
+// so that two slots still fit.
 template <int MP, int PACK> struct Cfg8 {
     static constexpr int T = 2;
     static constexpr int kPkBoxes = PACK == kPackHalf4 ? 2 : 1; // packed boxes per span
