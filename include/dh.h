@@ -198,7 +198,8 @@ int dh_device_status(int reset);
 /* Human-readable description of the last error on this thread ("" if none). */
 const char *dh_last_error(void);
 
-/* ABI version: (major << 16) | minor. */
+/* ABI version: (major << 16) | minor.  1.0: the head and its sharded calls; 1.2: the fp8
+ * head; 1.3: the 4-bit head and the design-choice ablations.  Minor versions only add calls. */
 int dh_version(void);
 
 /*

@@ -655,7 +655,7 @@ const char *dh_last_error(void)
 
 int dh_version(void)
 {
-    return (1 << 16) | 2;
+    return (1 << 16) | 3;
 }
 
 
