@@ -210,3 +210,16 @@ def test_wside_entry_point_rejects_bad_arguments(lib):
     bad = list(args)
     bad[3] = None
     assert lib.dh_forward_wside_debug(*bad, None, None, None, None, None, None, None) == -1
+
+
+def test_draft_head_rejects_bad_heads_on_the_host():
+    import torch
+    W = torch.zeros(64, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        dh.DraftHead(W, bits=3)                                   # no such width
+    with pytest.raises(ValueError):
+        dh.DraftHead(W.to(torch.uint8), bits=4, row_scale=torch.ones(64))  # 4-bit fp8 head
+    with pytest.raises(ValueError):
+        dh.DraftHead(W)                                           # not a CUDA tensor
+    with pytest.raises(ValueError):
+        dh.DraftHead(W.to(torch.uint8), row_scale=torch.ones(64))  # fp8 head off the device
