@@ -68,6 +68,26 @@ int *timeout_flag_ptr()
     return addr[dev];
 }
 
+} // namespace
+
+int device_sm_count()
+{
+    static std::mutex mu;
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kNumSMsFallback;
+    std::lock_guard<std::mutex> lk(mu);
+    if (count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            return kNumSMsFallback;
+        count[dev] = n;
+    }
+    return count[dev];
+}
+
+namespace {
+
 long long valid_candidates(int V, int kcand)
 {
     const long long nblk = (V + kBlockN - 1) / kBlockN;
@@ -81,8 +101,7 @@ struct Layout {
     long long nblk = 0, ncand = 0, scratch_entries = 0;
     int passes = 0;
     size_t xs = 0, xw = 0, xt = 0, cval = 0, cidx = 0, sval[2] = {0, 0}, sidx[2] = {0, 0},
-           sel = 0, ex = 0, counters = 0, xt8 = 0, xs8 = 0, inv8 = 0, total = 0;
-    size_t xt8_chunk = 0;
+           sel = 0, ex = 0, counters = 0, xt8 = 0, small8 = 0, total = 0;
 };
 
 
@@ -113,11 +132,11 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     L.sel = take(static_cast<size_t>(M) * rerank * 4);
     L.ex = take(static_cast<size_t>(M) * rerank * 4);
     L.counters = take(kNumCounters * 4);
-    const int chunks8 = tc8_chunks(M);
-    L.xt8_chunk = align256(static_cast<size_t>(2 * kTc8MaxRows) * H); // T*MP <= 64 rows
-    L.xt8 = take(L.xt8_chunk * chunks8);
-    L.xs8 = take(static_cast<size_t>(chunks8) * kTc8MaxRows * (H / 64) * 4); // room for 64-groups
-    L.inv8 = take(static_cast<size_t>(chunks8) * kTc8MaxRows * 4);
+    // the 8-bit path's staged x (the largest any packed layout needs) and, per launch, the
+    // small per-row data (group sums, 2^-e, term counts); the 4-bit and contiguous-4 layouts
+    // take the most launches (32 rows each)
+    L.xt8 = take(tc8_x_bytes(M, H));
+    L.small8 = take(static_cast<size_t>(tc8_chunks(M, kPackHalf4)) * tc8_small_floats(H) * 4);
     L.total = off;
     return L;
 }
@@ -221,13 +240,10 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     if (!rec(0)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     Tc8Workspace w8;
     w8.xt8 = ws + L.xt8;
-    w8.chunk_bytes = L.xt8_chunk;
-    w8.xs = reinterpret_cast<float *>(ws + L.xs8);
-    w8.xs_chunk = static_cast<size_t>(kTc8MaxRows) * (H / 64);
+    w8.small = reinterpret_cast<float *>(ws + L.small8);
     w8.group = pack == kPackG64 ? 64 : 128;
-    w8.inv_scale = reinterpret_cast<float *>(ws + L.inv8);
     if (path == DH_PATH_TC)
-        err = launch_prep_fp8(x, M, H, w8, counters, kNumCounters, stream);
+        err = launch_prep_fp8(x, M, H, pack, w8, counters, kNumCounters, stream);
     else
         err = launch_prep(x, M, H, path == DH_PATH_WARP ? L.Mpad_w : 0, xs,
                           path == DH_PATH_WARP ? xw : nullptr,
@@ -624,7 +640,7 @@ int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank)
     const int path = choose_path(M, H);
     if (path < 0) return 0;
     int prep = 1, coarse = (M + kWarpBatch - 1) / kWarpBatch;
-    if (path == DH_PATH_TC) prep = coarse = tc8_chunks(M);
+    if (path == DH_PATH_TC) prep = coarse = tc8_chunks(M, kPackQuarter2);
     else if (path == DH_PATH_TC_BF16) coarse = tc_launches(M);
     if (select_rerank_fits(rerank, kcand)) return prep + coarse + 1; // fused select + rerank
     return prep + coarse + L.passes /*selection*/ + 1 /*rerank + top-k*/;

@@ -466,17 +466,17 @@ cudaError_t launch_n(const CUtensorMap &tm_packed, const uint16_t *xt_chunk, con
     if (nstage > 4) nstage = 4;
     if (nstage < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = fixed + static_cast<size_t>(nstage) * kStage;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(coarse_tc_kernel<N, kWS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemLimitTc);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // the shared-memory limit is a per-device attribute: raised once on every device
+    static PerDeviceOnce attr;
+    cudaError_t e = attr.run([] {
+        return cudaFuncSetAttribute(coarse_tc_kernel<N, kWS>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimitTc);
+    });
+    if (e != cudaSuccess) return e;
     TcParams prm = base;
     prm.nstage = nstage;
-    const int grid = prm.ntiles < kNumSMs ? prm.ntiles : kNumSMs;
+    const int sms = device_sm_count();
+    const int grid = prm.ntiles < sms ? prm.ntiles : sms;
     coarse_tc_kernel<N, kWS><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
     return cudaGetLastError();
 }

@@ -352,17 +352,17 @@ cudaError_t launch_nt(const CoarseArgs &a, const CUtensorMap &tm, cudaStream_t s
     }
     if (nwarps < 1) return cudaErrorInvalidConfiguration;
     const size_t smem = fixed + static_cast<size_t>(nwarps) * use_stage * kStageBytes;
-    // raise the kernel's shared-memory cap once (per process) to the most any call needs
-    static int s_smem_set = 0;
-    cudaError_t err = cudaSuccess;
-    if (static_cast<int>(smem) > s_smem_set) {
-        err = cudaFuncSetAttribute(coarse_warp_kernel<NT>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-        if (err != cudaSuccess) return err;
-        s_smem_set = kSmemLimit;
-    }
+    // raise the kernel's shared-memory cap (a per-device attribute) once on every device to
+    // the most any call needs
+    static PerDeviceOnce attr;
+    cudaError_t err = attr.run([] {
+        return cudaFuncSetAttribute(coarse_warp_kernel<NT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    });
+    if (err != cudaSuccess) return err;
     const int chunks = (a.M + kWarpBatch - 1) / kWarpBatch;
-    const int grid = nblk < kNumSMs ? nblk : kNumSMs;
+    const int sms = device_sm_count();
+    const int grid = nblk < sms ? nblk : sms;
     for (int c = 0; c < chunks; ++c) {
         WarpParams prm;
         prm.xw = reinterpret_cast<const uint4 *>(a.xw) + static_cast<size_t>(c) * (xw_bytes / 16);

@@ -7,13 +7,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace dh {
 
 // ---- geometry shared by the host layer and the kernels ----------------------------------
 constexpr int kGroup = 128;             // quantisation group along H
 constexpr int kBlockN = 64;             // vocabulary columns per selection block
 constexpr int kSpanBytes = 128;         // packed bytes of a row covered by one pass over the planes
-constexpr int kNumSMs = 152;
+constexpr int kNumSMsFallback = 152; // GB300; used only if the device query fails
 constexpr int kWarpBatch = 16;          // batch rows per warp-path pass (two n8 tiles)
 constexpr int kWarpRowsPerWarp = 64;    // vocabulary rows per warp work item (one block)
 constexpr int kSelectChunk = 4096;      // candidates per CTA in one top-R selection pass
@@ -33,6 +35,34 @@ constexpr int kPackContig2 = 2;
 constexpr int kPackG64 = 3;     // the quarter split with groups of 64 (group-size ablation)
 constexpr int kPackWside = 4;   // the quarter split, dequantised on the weight side (bf16
                                 // tcgen05 path; the scale-placement ablation)
+
+// ---- per-device host state ---------------------------------------------------------------
+// Streaming multiprocessors of the current device (cudaDevAttrMultiProcessorCount), queried
+// once per device; the persistent grids are sized from it.
+int device_sm_count();
+
+// Host-side set-up that applies to the current device only (a kernel's shared-memory limit):
+// run(fn) calls fn once per device, with that device current, and remembers success.
+class PerDeviceOnce {
+  public:
+    template <class F> cudaError_t run(F fn)
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return fn(); // untracked: set it every time
+        std::lock_guard<std::mutex> lk(mu_);
+        if (done_[dev]) return cudaSuccess;
+        e = fn();
+        if (e == cudaSuccess) done_[dev] = true;
+        return e;
+    }
+
+  private:
+    static constexpr int kMaxDevices = 64;
+    std::mutex mu_;
+    bool done_[kMaxDevices] = {};
+};
 
 // ---- launchers (each returns the launch status) ------------------------------------------
 // W: bf16 rows (wsc null) or e4m3 rows with per-row fp32 scales wsc.  bits: 2 (quarter
@@ -72,24 +102,33 @@ struct CoarseArgs {
 cudaError_t launch_coarse_warp(const CoarseArgs &a, cudaStream_t stream);
 size_t warp_xw_elems(int M, int H); // bf16 elements of the warp-path operand
 
-// tcgen05 path with 8-bit operands: the batch is processed in launches of at most
-// kTc8MaxRows rows; launch c stages its rows as T e4m3 terms of MP (multiple of 16) rows.
-constexpr int kTc8MaxRows = 32;
+// tcgen05 path with 8-bit operands.  The batch runs in launches of at most tc8_max_rows(pack)
+// rows; launch c pads its rows to MP in {16, 32, 64} and stages them as kTc8Terms e4m3 terms
+// ([kTc8Terms * MP, H], term t in rows t * MP ..), of which it uses 2 or 3 (chosen on the
+// device from the staged rows' representation error).
+constexpr int kTc8Terms = 3;
+constexpr int kTc8MaxMP = 64;
+int tc8_max_rows(int pack);
 struct Tc8Chunk {
-    int m0, rows, MP, T;
+    int m0, rows, MP;
+    size_t x_off; // byte offset of the launch's staged x in Tc8Workspace::xt8
 };
-Tc8Chunk tc8_chunk(int M, int c);
-int tc8_chunks(int M);
+int tc8_chunks(int M, int pack);
+Tc8Chunk tc8_chunk(int M, int c, int pack, int H);
+size_t tc8_x_bytes(int M, int H); // staged-x bytes, enough for every pack
+// Per launch, tc8_small_floats(H) floats: xs of the 2-term and of the 3-term representation
+// ([kTc8MaxMP][H / 64] each, scaled units), per-row factors [3][kTc8MaxMP] (2^-e and the
+// weights of terms 2 and 3), terms per row [kTc8MaxMP] (int).
+inline size_t tc8_small_floats(int H)
+{
+    return 2 * static_cast<size_t>(kTc8MaxMP) * (H / 64) + 4 * kTc8MaxMP;
+}
 struct Tc8Workspace {
-    uint8_t *xt8;       // per launch [T*MP, H] e4m3 terms, chunk_bytes apart
-    size_t chunk_bytes;
-    float *xs;          // per launch kTc8MaxRows x (H / group) scaled group sums of the
-                        // represented x, xs_chunk floats apart
-    size_t xs_chunk;
-    float *inv_scale;   // per launch kTc8MaxRows entries 2^-e
-    int group = 128;    // group size of xs (64: the group-size ablation)
+    uint8_t *xt8;  // staged x of every launch
+    float *small;  // per launch tc8_small_floats(H) floats
+    int group = 128; // group size of xs (64: the group-size ablation)
 };
-cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
+cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, int pack, const Tc8Workspace &w,
                             int *counters, int ncounters, cudaStream_t stream);
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream);
 // the 8-bit tcgen05 path runs these sizes (shared memory and tensor memory fit)

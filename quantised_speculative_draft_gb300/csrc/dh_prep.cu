@@ -107,13 +107,21 @@ size_t warp_xw_elems(int M, int H)
 
 // ------------------------------------------------------------------------------------------
 // x staging for the 8-bit tcgen05 path.  Row m is scaled by 2^e (max |x 2^e| in [128, 256),
-// exact) and split into T e4m3 terms by successive round-to-nearest: x1 = e4m3(x 2^e),
-// x2 = e4m3(x 2^e - x1), x3 = e4m3(x 2^e - x1 - x2); every difference is exact in fp32.  A bf16
-// value (8 significant bits) is represented exactly by two terms unless it lies more than 10
-// binades below the row maximum; the third term shrinks that residual to below 2^-18 of the
-// maximum.  Term t of row m is row t*MP + m of the staged operand.  xs receives the group
-// sums of the represented values x1 + x2 + x3 (scaled units) and inv_scale the factor 2^-e.
-// One CTA per staged row.
+// exact) and written as three e4m3 terms, each the rounded residual of the ones before, scaled
+// by its own power of two so that its largest magnitude lies in [128, 256):
+//     r0 = x 2^e,  t1 = e4m3(r0),  r1 = r0 - t1,
+//     t2 = e4m3(2^s2 r1),  r2 = r1 - 2^-s2 t2,  t3 = e4m3(2^s3 r2),
+// so x 2^e ~ t1 + 2^-s2 t2 + 2^-s3 t3 (every difference is exact in fp32, no term saturates).
+// Each term carries four significant bits of what the terms before left over, at the scale of
+// the row's largest leftover: two terms represent every bf16 element of an ordinary row
+// exactly (the ones that are not lie more than ~14 binades below the row maximum), and the
+// third term covers rows whose elements span many more binades -- a few channels far above
+// the rest lose nothing, since the large channels are exact in t1 and the rest get t2 and t3 at
+// their own scale.  Term t of row m is row t MP + m of the staged operand.  The kernel also
+// writes the group sums of the two- and three-term representations (scaled units), 2^-e, the
+// term weights 2^-s2 and 2^-s3, and the number of terms the row needs: 3 when the two-term
+// residual sum_k |r2_k| exceeds 2^-20 sum_k |x_k 2^e|, else 2 (each coarse launch takes the
+// most any of its rows needs).  One CTA per staged row.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ float e4m3_to_f32(__nv_fp8_storage_t v)
 {
@@ -121,21 +129,81 @@ __device__ __forceinline__ float e4m3_to_f32(__nv_fp8_storage_t v)
     return __half2float(__half(h));
 }
 
+__device__ __forceinline__ __nv_fp8_storage_t to_e4m3(float v)
+{
+    return __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3); // round to nearest even
+}
+
+// The power of two 2^s that puts a largest magnitude mx > 0 in [128, 256) (s clamped to the
+// normal fp32 exponents); s = 0 for mx = 0.
+__device__ __forceinline__ int range_shift(float mx)
+{
+    if (!(mx > 0.f)) return 0;
+    int ex;
+    frexpf(mx, &ex); // mx = f 2^ex, f in [0.5, 1)
+    const int s = 8 - ex;
+    return s > 126 ? 126 : (s < -126 ? -126 : s);
+}
+
+__device__ __forceinline__ float pow2f(int s)
+{
+    return __int_as_float((s + 127) << 23);
+}
+
 constexpr int kPrepMaxThreads = 1024;
 constexpr int kPrepOcts = 2; // 16-byte slices of x per thread: one per thread up to H = 8192,
                              // two up to H = 16384 (the CTA has min(H/8, 1024) threads)
+constexpr float kTermsThreshold = 9.5367431640625e-7f; // 2^-20
 
-// G: the group size of the sums xs (128, or 64 for the group-size ablation).
+// Largest value of v over the CTA (v >= 0); every thread gets it.  red: kPrepMaxThreads / 32.
+__device__ __forceinline__ float cta_max(float v, float *red)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    __syncthreads(); // the previous use of red is over
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = 0.f;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) v = fmaxf(v, red[i]);
+    return v;
+}
+
+// The split of one scaled element r0 = x 2^e with term shifts s2, s3 (scales k2 = 2^s2 ...).
+struct Split3 {
+    __nv_fp8_storage_t b[3];
+    float t1, t2, t3, r1, r2; // term values in the scaled units and the residuals
+};
+
+__device__ __forceinline__ Split3 split3(float r0, float k2, float ik2, float k3, float ik3)
+{
+    Split3 o;
+    o.b[0] = to_e4m3(r0);
+    o.t1 = e4m3_to_f32(o.b[0]);
+    o.r1 = r0 - o.t1;
+    o.b[1] = to_e4m3(o.r1 * k2);
+    o.t2 = e4m3_to_f32(o.b[1]) * ik2;
+    o.r2 = o.r1 - o.t2;
+    o.b[2] = to_e4m3(o.r2 * k3);
+    o.t3 = e4m3_to_f32(o.b[2]) * ik3;
+    return o;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// G: the group size of the sums (128, or 64 for the group-size ablation).
 template <int G>
 __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_t *__restrict__ x,
-                                                                   int H,
-                                                       int m0, int rows, int MP, int T,
-                                                       uint8_t *__restrict__ xt8,
-                                                       float *__restrict__ xs,
-                                                       float *__restrict__ inv_scale,
-                                                       int *__restrict__ counters, int ncounters)
+                                                                   int H, int m0, int rows, int MP,
+                                                                   uint8_t *__restrict__ xt8,
+                                                                   float *__restrict__ xs2,
+                                                                   float *__restrict__ xs3,
+                                                                   float *__restrict__ row_f,
+                                                                   int *__restrict__ row_terms,
+                                                                   int *__restrict__ counters,
+                                                                   int ncounters)
 {
-    __shared__ float wmax[kPrepMaxThreads / 32];
+    __shared__ float wred[kPrepMaxThreads / 32];
     const int m = blockIdx.x;
     const bool valid = m < rows;
     const int octs = H / 8, NGt = H / G;
@@ -143,7 +211,7 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
         for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
     const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
 
-    // the row stays in registers between the max and the split (H <= 1024 * 8 * kPrepOcts)
+    // the row stays in registers between the passes (H <= 1024 * 8 * kPrepOcts)
     uint4 xv[kPrepOcts];
     float mx = 0.f;
 #pragma unroll
@@ -153,76 +221,121 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
         if (valid && o < octs) xv[j] = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
-                                 fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    mx = 0.f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mx = fmaxf(mx, wmax[i]);
-    int e = 0;
-    if (mx > 0.f) {
-        int ex;
-        frexpf(mx, &ex); // mx = f 2^ex, f in [0.5, 1)
-        e = 8 - ex;      // mx 2^e in [128, 256)
-        e = e > 126 ? 126 : (e < -126 ? -126 : e);
-    }
-    const float scale = __int_as_float((e + 127) << 23);
-    if (threadIdx.x == 0) inv_scale[m] = valid ? __int_as_float((127 - e) << 23) : 1.0f;
+    const int e = range_shift(cta_max(mx, wred));
+    const float scale = pow2f(e);
 
+    // pass 2: the largest first-term residual -> s2; pass 3: the largest second-term one -> s3
+    float m1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPrepOcts; ++j) {
+        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
+            m1 = fmaxf(m1, fabsf(r0 - e4m3_to_f32(to_e4m3(r0))));
+        }
+    }
+    const int s2 = range_shift(cta_max(m1, wred));
+    const float k2 = pow2f(s2), ik2 = pow2f(-s2);
+    float m2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPrepOcts; ++j) {
+        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
+            const Split3 sp = split3(r0, k2, ik2, 0.f, 0.f);
+            m2 = fmaxf(m2, fabsf(sp.r2));
+        }
+    }
+    const int s3 = range_shift(cta_max(m2, wred));
+    const float k3 = pow2f(s3), ik3 = pow2f(-s3);
+    if (threadIdx.x == 0) {
+        // per-row factors: 2^-e, then the weights of terms 2 and 3 (see the coarse kernel)
+        row_f[m] = valid ? pow2f(-e) : 1.0f;
+        row_f[kTc8MaxMP + m] = ik2;
+        row_f[2 * kTc8MaxMP + m] = ik3;
+    }
+
+    float l1 = 0.f, b2 = 0.f; // sum |x 2^e| and the two-term residual sum |r2|
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
         const int o = threadIdx.x + j * blockDim.x;
-        if (o >= octs) break;
+        // every lane of a warp takes part in the group shuffles: lanes past the row add 0
+        const bool live = o < octs;
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-        uint32_t lo[3] = {0, 0, 0}, hi[3] = {0, 0, 0};
-        float sum = 0.f;
+        uint32_t lo[kTc8Terms] = {0, 0, 0}, hi[kTc8Terms] = {0, 0, 0};
+        float sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float xe = (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u)
-                                     : __uint_as_float(w[i >> 1] << 16);
-            float r = xe * scale; // exact: a power of two
-            float rep = 0.f;
+            const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
+            const Split3 sp = split3(r0, k2, ik2, k3, ik3);
+            const float rep2 = sp.t1 + sp.t2;
+            sum2 += rep2;
+            sum3 += rep2 + sp.t3;
+            l1 += fabsf(r0);
+            b2 += fabsf(sp.r2);
 #pragma unroll
-            for (int t = 0; t < 3; ++t) {
-                if (t < T) {
-                    const __nv_fp8_storage_t b = __nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3);
-                    const float bf = e4m3_to_f32(b);
-                    r -= bf;
-                    rep += bf;
-                    if (i < 4) lo[t] |= static_cast<uint32_t>(b) << (8 * i);
-                    else hi[t] |= static_cast<uint32_t>(b) << (8 * (i - 4));
-                }
+            for (int t = 0; t < kTc8Terms; ++t) {
+                if (i < 4) lo[t] |= static_cast<uint32_t>(sp.b[t]) << (8 * i);
+                else hi[t] |= static_cast<uint32_t>(sp.b[t]) << (8 * (i - 4));
             }
-            sum += rep;
         }
-        for (int t = 0; t < T; ++t)
-            *reinterpret_cast<uint2 *>(xt8 + (static_cast<long long>(t) * MP + m) * H + 8 * o) =
-                make_uint2(lo[t], hi[t]);
+        if (live)
+#pragma unroll
+            for (int t = 0; t < kTc8Terms; ++t)
+                *reinterpret_cast<uint2 *>(xt8 + (static_cast<long long>(t) * MP + m) * H + 8 * o) =
+                    make_uint2(lo[t], hi[t]);
         // the G / 8 octets of a group are consecutive lanes
 #pragma unroll
-        for (int off = G / 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        if ((o & (G / 8 - 1)) == 0) xs[static_cast<long long>(m) * NGt + o / (G / 8)] = sum;
+        for (int off = G / 16; off > 0; off >>= 1) {
+            sum2 += __shfl_xor_sync(0xffffffffu, sum2, off);
+            sum3 += __shfl_xor_sync(0xffffffffu, sum3, off);
+        }
+        if (live && (o & (G / 8 - 1)) == 0) {
+            xs2[static_cast<long long>(m) * NGt + o / (G / 8)] = sum2;
+            xs3[static_cast<long long>(m) * NGt + o / (G / 8)] = sum3;
+        }
+    }
+    // the decision needs sums, not maxima: reduce (l1, b2) through the same buffer
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        b2 += __shfl_xor_sync(0xffffffffu, b2, off);
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) wred[threadIdx.x >> 5] = l1;
+    __syncthreads();
+    float L = 0.f;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) L += wred[i];
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) wred[threadIdx.x >> 5] = b2;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float B = 0.f;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) B += wred[i];
+        row_terms[m] = (valid && B > kTermsThreshold * L) ? 3 : 2;
     }
 }
 
-cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, const Tc8Workspace &w,
+cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, int pack, const Tc8Workspace &w,
                             int *counters, int ncounters, cudaStream_t stream)
 {
-    for (int c = 0; c < tc8_chunks(M); ++c) {
-        const Tc8Chunk k = tc8_chunk(M, c);
+    for (int c = 0; c < tc8_chunks(M, pack); ++c) {
+        const Tc8Chunk k = tc8_chunk(M, c, pack, H);
         auto kern = w.group == 64 ? prep_fp8_kernel<64> : prep_fp8_kernel<128>;
+        float *const small = w.small + static_cast<size_t>(c) * tc8_small_floats(H);
+        float *const xs2 = small;
+        float *const xs3 = small + static_cast<size_t>(kTc8MaxMP) * (H / 64);
+        float *const row_f = small + 2 * static_cast<size_t>(kTc8MaxMP) * (H / 64);
+        int *const terms = reinterpret_cast<int *>(row_f + 3 * kTc8MaxMP);
         // one thread per 16-byte slice of the row (a multiple of 32 threads)
         int threads = ((H / 8 + 31) / 32) * 32;
         if (threads > kPrepMaxThreads) threads = kPrepMaxThreads;
-        kern<<<k.MP, threads, 0, stream>>>(
-            x, H, k.m0, k.rows, k.MP, k.T, w.xt8 + static_cast<size_t>(c) * w.chunk_bytes,
-            w.xs + static_cast<size_t>(c) * w.xs_chunk,
-            w.inv_scale + static_cast<size_t>(c) * kTc8MaxRows, c == 0 ? counters : nullptr,
-            ncounters);
+        kern<<<k.MP, threads, 0, stream>>>(x, H, k.m0, k.rows, k.MP, w.xt8 + k.x_off, xs2, xs3,
+                                           row_f, terms, c == 0 ? counters : nullptr, ncounters);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -190,7 +190,7 @@ cudaError_t launch_quantize_c4(const uint16_t *W, int V, int H, uint8_t *packed,
 {
     const long long total = static_cast<long long>(V) * (H / 512);
     long long blocks = (total + 7) / 8;
-    const long long cap = static_cast<long long>(kNumSMs) * 8;
+    const long long cap = static_cast<long long>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     quantize_c4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, packed, S, ZS, V, H);
     return cudaGetLastError();
@@ -201,7 +201,7 @@ cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int b
 {
     const long long total = static_cast<long long>(V) * (H / (bits == 4 ? 256 : 512));
     long long blocks = (total + 7) / 8;
-    const long long cap = static_cast<long long>(kNumSMs) * 8;
+    const long long cap = static_cast<long long>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     const unsigned g = static_cast<unsigned>(blocks);
     if (bits == 4) {

@@ -85,8 +85,11 @@ def check_coarse(gpu_c, ref_c):
     err = np.abs(gpu_c.astype(np.float64) - ref_c)
     tol = COARSE_RTOL * (1.0 + np.abs(ref_c))
     bad = err > tol
-    assert not bad.any(), (f"{bad.sum()} coarse values off; worst ratio "
-                           f"{(err / tol).max():.3g}")
+    if bad.any():
+        r, c = np.unravel_index(np.argmax(err / tol), err.shape)
+        raise AssertionError(f"{bad.sum()} coarse values off (rows {sorted(set(np.nonzero(bad)[0].tolist()))[:10]}); "
+                             f"worst ratio {(err / tol).max():.3g} at row {r} column {c}: "
+                             f"GPU {gpu_c[r, c]!r} oracle {ref_c[r, c]!r}")
     return float((err / tol).max())
 
 

@@ -66,7 +66,7 @@ def test_forward4_matches_the_oracle(M, H, V, kcand, R, k):
 
 
 def test_forward4_rejects_sizes_and_paths_it_cannot_run():
-    M, H, V = 32, 8192, 4096                            # 64 blocks: 64 valid candidates
+    M, H, V = 32, 16384, 4096                           # 64 blocks: 64 valid candidates
     x = torch.zeros(M, H, dtype=torch.bfloat16, device=DEV)
     W = torch.zeros(V, H, dtype=torch.bfloat16, device=DEV)
     packed, S, ZS = _quantize4(W)
@@ -75,7 +75,7 @@ def test_forward4_rejects_sizes_and_paths_it_cannot_run():
     ws = torch.empty(nws, dtype=torch.uint8, device=DEV)
     idx = torch.empty(M, 1, dtype=torch.int32, device=DEV)
     logit = torch.empty(M, 1, dtype=torch.float32, device=DEV)
-    with pytest.raises(dh.DHError) as e:                 # MP = 32 stages do not fit at H = 8192
+    with pytest.raises(dh.DHError) as e:  # at H = 16384 the S / ZS tile copies alone need 128 KB
         dh.dh_forward4(x, packed, S, ZS, W, 1, 32, 1, idx, logit, ws)
     assert e.value.code == -8
     prev = dh.dh_set_coarse_path(dh.PATH_WARP)
