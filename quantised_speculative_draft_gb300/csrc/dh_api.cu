@@ -133,8 +133,8 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     L.ex = take(static_cast<size_t>(M) * rerank * 4);
     L.counters = take(kNumCounters * 4);
     // the 8-bit path's staged x (the largest any packed layout needs) and, per launch, the
-    // small per-row data (group sums, 2^-e, term counts); the 4-bit and contiguous-4 layouts
-    // take the most launches (32 rows each)
+    // small per-row data (group sums, 2^-e, term weights and counts); the 4-bit layout takes
+    // the most launches (16 rows each)
     L.xt8 = take(tc8_x_bytes(M, H));
     L.small8 = take(static_cast<size_t>(tc8_chunks(M, kPackHalf4)) * tc8_small_floats(H) * 4);
     L.total = off;

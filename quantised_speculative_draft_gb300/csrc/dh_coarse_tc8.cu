@@ -10,12 +10,12 @@
 //     for planes 1 and 3 (mask 0x0C), planes 2-3 after a 4-bit shift.  One AND (plus one
 //     shift) turns a 32-bit word of packed bytes into four weights of one plane, in k order;
 //   * x: every row is scaled by a power of two 2^e (max |x 2^e| in [128, 256)) and written as
-//     T e4m3 terms, x 2^e ~ t1 + w2 t2 + w3 t3, each term the rounded residual of the ones
-//     before at its own power-of-two scale (per row weights w2, w3; dh_prep.cu); the terms are
+//     T e4m3 terms, x 2^e ~ t1 + w2 t2 (+ w3 t3), each term the rounded residual of the ones
+//     before at its own power-of-two scale (per-row weights w2, w3; dh_prep.cu).  The terms are
 //     stacked along the MMA's N dimension (rows t MP + m) and recombined in fp32 in the
-//     epilogue.  Two terms represent every element of an ordinary row exactly, the third
-//     covers rows with a wide dynamic range; the staging kernel measures the two-term error of
-//     every row and a launch uses the third term when any row needs it;
+//     epilogue.  Two terms represent every element of an ordinary row exactly; a launch whose
+//     rows need the third term (the staging kernel measures each row's two-term error) runs the
+//     T = 3 instance of this kernel, the T = 2 instance returning at once, and vice versa;
 //   * per group g (128 consecutive k of one plane q), with p = sum_t w_t D_t the recombined
 //     partial, sum_k x_k v_k = 2^9 p / f (f = 1 for even q, 4 for odd q), and the page's
 //     group term S sum_k x_k (1 + v_k/4) - ZS xs = (S/4) sum_k x_k v_k + (S - ZS) xs, so
@@ -23,38 +23,37 @@
 //     with xs' the group sums of the represented x (in the scaled units): the scale and zero
 //     are applied to the fp32 partial of every group, never to the weight.
 //
-// The unit of MMA work is one plane of one span (128 k of 128 vocabulary rows: one weight
-// group, two for groups of 64): four tcgen05.mma of K = 32 into the unit's accumulator, then
-// one commit to the unit's tensor-memory slot (accumulator ready, A buffer free) and one to its
-// x stage.  A thread issuing tcgen05.mma is held for ~100 cycles per instruction whatever the
-// shape (~700 cycles per unit with its waits and commits), so the units are spread over I
-// issuer warps: unit q goes to issuer q mod I, tensor-memory slot q mod K and x stage q mod nx,
-// with K and nx multiples of I.  Every slot and x stage then belongs to one issuer, which
-// waits on the phases of its barriers strictly in order (a parity wait is only exact when the
-// phase before the awaited one has completed).
-//
-// Roles (28 warps, one CTA per SM, persistent over 128-row vocabulary tiles taken round-robin):
+// Roles (22 or 18 warps, one CTA per SM, persistent over 128-row vocabulary tiles).  The unit of
+// handoff is a span (N = 32: the four planes of 512 k) or half a span (larger N: planes 2u,
+// 2u+1); unit q uses tensor-memory slot q % 2 (an A buffer and one accumulator per group).  A
+// thread issuing tcgen05.mma is held ~100 cycles per instruction, so each plane has its own
+// issuer warp: the four issuers of a span work at once, and each of them takes every unit
+// that holds its plane, in order (every barrier's phases are awaited in order).  Writing a
+// span's A buffer takes a dequant warp ~1000 cycles, so with one unit per span two sets of
+// dequant warps take alternate spans (each set owns one slot).
 //   warp 0        TMA: per span one [128 rows x 128 B] box of packed codes (two for the 4-bit
-//                 head) into a ring of packed stages; per tile a bulk copy of the tile's S and
-//                 ZS rows (contiguous in memory) into a double-buffered shared copy
-//   warp 1        TMA: per unit the unit's 128 k of the staged x terms ([T MP rows x 128 B],
-//                 128-byte swizzle) into a ring of x stages
-//   warp 2        block top-KCAND of the previous tile (overlaps the current one)
-//   warps 3..3+I  MMA issuers (lane 0)
-//   warps 8-11    dequant: one TMEM lane (= one vocabulary row) per thread; reads the span's
-//                 packed bytes once, then writes each plane into its unit's A buffer
-//                 (tcgen05.st) as soon as that slot's previous unit has completed
-//   warps 12-27   epilogue, four sets of four warps (one per TMEM lane quarter): set cp folds
-//                 every unit for batch columns [cp MP/4, (cp + 1) MP/4) -- tcgen05.ld of the
-//                 terms, recombination, scale and zero fold into fp32 registers -- and at the
-//                 tile end writes those columns of the tile's coarse values
+//                 head) and four [128 k x N] boxes of the staged x terms (128-byte swizzle)
+//                 into a stage ring; per tile a bulk copy of the tile's S and ZS rows
+//                 (contiguous in memory) into a double-buffered shared copy for the epilogue
+//   warps 1, 3 and the last two   MMA issuers of planes 0..3: per unit 4 x tcgen05.mma kind::f8f6f4
+//                 (M = 128, K = 32) of their plane, one commit for the unit's accumulators and
+//                 one for the stage
+//   warp 2        block top-KCAND of the previous tile (overlaps the current one): one lane
+//                 per (batch column, block) pair keeps an insertion list of the best 8
+//   warps 4-11    dequant, two sets of four warps (one set where every launch body has two
+//                 units per span): one TMEM lane (= one vocabulary row) per thread, every plane
+//                 of the set's spans (tcgen05.st, one wait per unit)
+//   next 8 warps  epilogue, two halves of four warps (one per TMEM lane quarter): half h folds
+//                 planes 2h, 2h+1 of every span -- tcgen05.ld of the partials, recombination of
+//                 the terms, scale/zero fold into fp32 registers -- and at the tile end writes its
+//                 half of the coarse values; the selection warp adds the halves
 // Every handoff is an mbarrier; every wait is bounded.
 //
 // The 4-bit head (BITS = 4, half split, bias 16; _quantize_head_now's 4-bit variant) runs the
 // same pipeline: a nibble masked in place is the exact e4m3 weight v 2^-9 (v in 0..15), and two
 // 128-byte boxes of a row (packed bytes 256 span ..) carry four groups -- low and high nibbles
-// of each box -- so one span is again four planes of 128 k, with NG = H / 512 spans per row.
-// The fold becomes (2^9 / 16) S p = 32 S p for every plane.
+// of each box -- so one span is again four planes of 128 k, sixteen MMAs and four groups, with
+// NG = H / 512 spans per row.  The fold becomes (2^9 / 16) S p = 32 S p for every plane.
 #include "dh_common.cuh"
 #include "dh_internal.h"
 #include "dh_tcgen05.cuh"
@@ -66,51 +65,62 @@ namespace dh {
 namespace {
 
 constexpr int kTileRows = 128;
+
 constexpr int kTmemCols = 512;
 constexpr int kPkBytes = kTileRows * kSpanBytes; // 16 KB packed box per span
 constexpr int kSmemLimit8 = 232448;
-// The tile's coarse values for the selection warp: one 64-value block per (batch column,
+// The tile's coarse values for the selection warps: one 64-value block per (batch column,
 // block) pair, pairs kRedPitch floats apart (16-byte aligned, bank-conflict free per lane).
 constexpr int kRedPitch = 68;
+// Warp roles: 0 TMA, 2 selection, 4-7 the first dequant set (one warp per TMEM lane quarter),
+// then, for launches with one unit per span, the second dequant set (8-11); then the epilogue
+// (two halves of four warps) and the issuers of planes 2 and 3 (planes 0 and 1: warps 1, 3).
+// Launches that never use the second dequant set leave it out, for registers.
+constexpr int kWarpTma = 0, kWarpSel = 2, kWarpDq0 = 4;
+constexpr int kDqWarps = 4; // warps of one dequant set
+constexpr int kEpWarps = 8; // two halves of four
+constexpr int kIssuers = 4; // one MMA issuer warp per plane
+template <bool kTwoSets> struct Roles {
+    static constexpr int kEp0 = kTwoSets ? 12 : 8;           // first epilogue warp
+    static constexpr int kWarps = kEp0 + kEpWarps + 2;       // + the issuers of planes 2, 3
+    static constexpr int kThreads = 32 * kWarps;
+    __device__ static int issuer_plane(int warp)
+    {
+        return warp == 1 ? 0 : (warp == 3 ? 1 : (warp == kEp0 + 8 ? 2 : (warp == kEp0 + 9 ? 3 : -1)));
+    }
+};
 
-// warp roles
-constexpr int kWarpPk = 0, kWarpX = 1, kWarpSel = 2, kWarpIss0 = 3, kMaxIssuers = 5;
-constexpr int kWarpDq0 = 8, kDqWarps = 4;
-constexpr int kWarpEp0 = 12, kEpWarps = 16;
-constexpr int kWarps = kWarpEp0 + kEpWarps; // 28
-constexpr int kThreads = kWarps * 32;       // 896
-
-template <int MP, int PACK> struct Cfg8 {
-    static constexpr int kBoxes = PACK == kPackHalf4 ? 2 : 1; // packed boxes per span
-    static constexpr int G = PACK == kPackG64 ? 64 : 128;     // weight group size
-    static constexpr int GPU = 128 / G;                       // groups (accumulators) per unit
-    static constexpr int NT = kTc8Terms * MP;                 // accumulator columns, all terms
-    static constexpr uint32_t kSlotCols = 32 + GPU * NT;      // A buffer + accumulators
-    static constexpr int kSlotsFit = static_cast<int>(kTmemCols / kSlotCols);
-    // issuer warps, and tensor-memory slots: a multiple of them, so that each slot (and each x
-    // stage) belongs to one issuer, which waits on its barriers' phases in order
-    static constexpr int I = kSlotsFit < kMaxIssuers ? kSlotsFit : kMaxIssuers;
-    static constexpr int K = (kSlotsFit / I) * I;
-    static constexpr int CW = MP / 4;                         // columns per epilogue thread
-    // units read per tensor-memory round trip by one epilogue warp (register budget)
-    static constexpr int kPerUnit = GPU * kTc8Terms * CW;     // values loaded per unit
-    static constexpr int UPR = kPerUnit <= 24 ? 2 : 1;
-    static constexpr uint32_t kXTile = static_cast<uint32_t>(NT) * 128; // one x stage
-    static constexpr uint32_t kPkStage = kBoxes * kPkBytes;
-    static_assert(K >= 2 && K % I == 0, "tensor-memory slots: at least two, a multiple of I");
-    static_assert(MP % 16 == 0 && 2 * MP <= 256 && NT <= 256, "MMA N out of range");
-    static_assert(CW == 4 || CW == 8 || CW == 16, "epilogue column part of 4, 8 or 16");
-    static_assert(kXTile % 1024 == 0 && kPkStage % 1024 == 0, "stages keep 1024-byte alignment");
+// Batch rows per launch MP in {16, 32}; x in T in {2, 3} e4m3 terms; MMA N = T * MP.
+// The unit of handoff is a whole span at N = 32 (kU = 1: 4 planes, 16 MMAs) and half a span
+// otherwise (kU = 2: planes 2u, 2u+1, 8 MMAs).  Tensor memory holds two unit slots, each an A
+// buffer (32 columns of e4m3 per plane) and one N-column fp32 accumulator per group of the
+// unit's planes; unit q uses slot q % 2.  Groups of 64 (kPackG64, MP = 16 only) put two
+// accumulators on each plane.
+template <int MP, int PACK, int T_> struct Cfg8 {
+    static constexpr int T = T_;
+    static constexpr int kPkBoxes = PACK == kPackHalf4 ? 2 : 1; // packed boxes per span
+    static constexpr int N = MP * T;
+    static constexpr int G = PACK == kPackG64 ? 64 : 128;   // weight group size
+    static constexpr int kGPP = 128 / G;                    // groups per plane of a span
+    static constexpr int kU = (MP == 16 && G == 128 && T == 2) ? 1 : 2; // units per span
+    static constexpr int kPP = 4 / kU;                      // planes per unit
+    static constexpr uint32_t kACols = 32 * kPP;
+    static constexpr uint32_t kSlotCols = kACols + kPP * kGPP * N; // one accumulator per group
+    static constexpr int K = 2;                             // unit slots
+    static constexpr uint32_t kXBytes = N * 512;            // 4 planes x 128 k x N rows
+    static constexpr uint32_t kStage = kPkBoxes * kPkBytes + kXBytes; // multiple of 1024
+    static_assert(K * kSlotCols <= kTmemCols, "two unit slots must fit");
+    static_assert(N % 16 == 0 && N <= 256, "MMA N out of range");
 };
 
 struct Tc8Params {
     const uint16_t *S;
     const uint16_t *ZS;
-    const float *xs2;       // [MP][NGt] sums of the 2-term representation (scaled units)
-    const float *xs3;       // [MP][NGt] sums of the 3-term representation
-    const float *row_f;     // [3][kTc8MaxMP] per batch row: 2^-e, weights of terms 2 and 3
+    const float *xs2;       // [MP][NGt] group sums of the 2-term representation (scaled units)
+    const float *xs3;       // [MP][NGt] group sums of the 3-term representation
+    const float *row_f;     // [3][kTc8MaxMP] per batch row: 2^-e, weights w2 and w3
     const int *row_terms;   // [MP] terms each row needs (2 or 3)
-    int V, H, m0, mrows, kcand, ntiles, npk, nx;
+    int V, H, m0, mrows, kcand, ntiles, nstage2, nstage3; // stage counts of the two bodies
     long long ncand;
     float *cand_val;
     int32_t *cand_idx;
@@ -125,38 +135,9 @@ __host__ __device__ constexpr uint32_t make_idesc_f8(int N)
            (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
-__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8])
-{
-    uint32_t r[8];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                   "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr)
-                 : "memory");
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, float (&v)[4])
-{
-    uint32_t r[4];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr)
-                 : "memory");
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-template <int CW>
-__device__ __forceinline__ void tmem_ld_cw(uint32_t taddr, float (&v)[CW])
-{
-    if constexpr (CW == 4) tmem_ld_x4(taddr, v);
-    else if constexpr (CW == 8) tmem_ld_x8(taddr, v);
-    else tmem_ld_x16(taddr, v);
-}
-
-__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t *r)
+// e4m3 weights of plane P from a word of four packed bytes (four consecutive k): the codes
+// masked in place, v 2^-9 (even P) or 4 v 2^-9 (odd P), exact e4m3 values
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16])
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {"
                  "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::
@@ -167,19 +148,16 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t *r)
                  : "memory");
 }
 
-// e4m3 weights of plane P from a word of four packed bytes (four consecutive k): the codes
-// masked in place, v 2^-9 (even P) or 4 v 2^-9 (odd P), exact e4m3 values
-__device__ __forceinline__ uint32_t deq4_e4m3(uint32_t w, int P)
+template <int P>
+__device__ __forceinline__ uint32_t deq4_e4m3(uint32_t w)
 {
     return (P >= 2 ? (w >> 4) : w) & ((P & 1) ? 0x0C0C0C0Cu : 0x03030303u);
 }
 
 // The 4-bit head: the low / high nibble of each byte, v 2^-9 with v in 0..15 (e4m3 bytes 0..15
 // are exactly p 2^-9: subnormals up to 7, then 2^-6 (1 + m/8) = (8 + m) 2^-9).
-__device__ __forceinline__ uint32_t deq_nib(uint32_t w, int hi)
-{
-    return (hi ? (w >> 4) : w) & 0x0F0F0F0Fu;
-}
+__device__ __forceinline__ uint32_t deq_nib_lo(uint32_t w) { return w & 0x0F0F0F0Fu; }
+__device__ __forceinline__ uint32_t deq_nib_hi(uint32_t w) { return (w >> 4) & 0x0F0F0F0Fu; }
 
 // The contiguous-4 layout (the page's packing ablation): the eight words w[8p .. 8p+7] of a
 // span are group p's 128 codes, byte j holding k = 4j .. 4j+3.  The four fields of every byte
@@ -237,12 +215,13 @@ __device__ __forceinline__ void select_pairs(uint32_t (&k0)[NB], uint32_t (&k1)[
 }
 
 // Block top-KCAND for KCAND <= 8, one lane per (batch column, block) pair: the lane walks the
-// block's 64 values in row order and keeps the 8 best in a descending list.  A value enters
-// only where it is strictly greater, so equal values keep the lower row first; rows past the
-// head hold -inf and never enter, leaving (-inf, -1) in unfilled slots.  With `coarse` set it
-// also writes the block's coarse values (rows below V).
-__device__ __forceinline__ void select_lane8(const float *pair, int base_row, int V, int kcand,
-                                             float *oval, int32_t *oidx, float *coarse)
+// block's 64 values (the sums of the two epilogue halves) in row order and keeps the 8 best in a
+// descending list.  A value enters only where it is strictly greater, so equal values keep the
+// lower row first; rows past the head hold -inf and never enter, leaving (-inf, -1) in unfilled
+// slots.  With `coarse` set it also writes the block's coarse values (rows below V).
+__device__ __forceinline__ void select_lane8(const float *vals0, const float *vals1, int base_row,
+                                             int V, int kcand, float *oval, int32_t *oidx,
+                                             float *coarse)
 {
     float v[8];
     int r[8];
@@ -253,8 +232,9 @@ __device__ __forceinline__ void select_lane8(const float *pair, int base_row, in
     }
 #pragma unroll 2
     for (int j4 = 0; j4 < kBlockN / 4; ++j4) {
-        const float4 u = reinterpret_cast<const float4 *>(pair)[j4];
-        const float uu[4] = {u.x, u.y, u.z, u.w};
+        const float4 u0 = reinterpret_cast<const float4 *>(vals0)[j4];
+        const float4 u1 = reinterpret_cast<const float4 *>(vals1)[j4];
+        const float uu[4] = {u0.x + u1.x, u0.y + u1.y, u0.z + u1.z, u0.w + u1.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float xv = uu[e];
@@ -281,115 +261,74 @@ __device__ __forceinline__ void select_lane8(const float *pair, int base_row, in
         }
 }
 
-// Shared-memory plan of one launch configuration.
-struct Smem8 {
-    uint32_t pk, x, sz, red, xs, inv, bars, total;
-    int npk, nx;
-};
+// Two dequant sets exactly when the two-term body has one unit per span.
+template <int MP, int PACK> constexpr bool two_sets() { return Cfg8<MP, PACK, 2>::kU == 1; }
 
-__host__ __device__ inline uint32_t sz_tile_bytes(int H, int G)
+// The kernel body for a launch whose rows take TT x terms (see Cfg8).
+template <int MP, int PACK, int TT>
+__device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, const CUtensorMap &tm_x,
+                                                const Tc8Params &prm, int nstage,
+                                                uint8_t *smem_raw)
 {
-    return static_cast<uint32_t>(kTileRows) * (H / G) * 2; // S (or ZS) of one tile
-}
-
-template <int MP, int PACK>
-__host__ __device__ inline Smem8 smem_plan(int H, int npk, int nx)
-{
-    using C = Cfg8<MP, PACK>;
-    Smem8 p;
-    p.npk = npk;
-    p.nx = nx;
-    p.pk = 0; // offsets from the 1024-aligned base
-    p.x = p.pk + static_cast<uint32_t>(npk) * C::kPkStage;
-    p.sz = p.x + static_cast<uint32_t>(nx) * C::kXTile;
-    p.red = p.sz + 4 * sz_tile_bytes(H, C::G);
-    p.xs = p.red + static_cast<uint32_t>(MP) * 2 * kRedPitch * 4;
-    p.inv = p.xs + static_cast<uint32_t>(H / C::G) * MP * 4;
-    p.bars = (p.inv + 3 * MP * 4 + 4 + 7u) & ~7u; // 2^-e, term weights, the launch's term count
-    const uint32_t nbars = 2 * npk + 2 * nx + 3 * C::K + 4 + 2 + C::I;
-    // + the tensor-memory address word, + slack for the 1024-byte alignment of the base (no
-    // static shared memory: the dynamic size may then take the whole per-block limit)
-    p.total = p.bars + nbars * 8 + 8 + 1024;
-    return p;
-}
-
-template <int MP, int PACK>
-__global__ void __launch_bounds__(kThreads, 1)
-    coarse_tc8_kernel(const __grid_constant__ CUtensorMap tm_packed,
-                      const __grid_constant__ CUtensorMap tm_x, const Tc8Params prm)
-{
-    using C = Cfg8<MP, PACK>;
+    using C = Cfg8<MP, PACK, TT>;
     constexpr int BITS = PACK == kPackHalf4 ? 4 : 2;
-    constexpr int G = C::G, GPU = C::GPU, NT = C::NT, K = C::K, I = C::I;
-    constexpr int CW = C::CW, UPR = C::UPR, kBoxes = C::kBoxes;
-    constexpr uint32_t kSlotCols = C::kSlotCols;
-    extern __shared__ uint8_t smem_raw[];
+    constexpr int G = C::G, kGPP = C::kGPP;
+    constexpr int kBoxes = C::kPkBoxes;
+    constexpr int N = C::N, T = C::T, K = C::K, kU = C::kU, kPP = C::kPP;
+    constexpr int kGU = kPP * kGPP;         // weight groups (accumulators) of a unit
+    using R = Roles<two_sets<MP, PACK>()>;
+    constexpr int kDqSets = kU == 1 ? 2 : 1; // dequant warp sets (alternate spans)
+    static_assert(kDqSets == 1 || two_sets<MP, PACK>(), "a second dequant set needs its warps");
+    constexpr int kWarpEp0 = R::kEp0;
+    constexpr uint32_t kSlotCols = C::kSlotCols, kACols = C::kACols;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = prm.H / 512, NGt = prm.H / G;
-    const int npk = prm.npk, nx = prm.nx;
-    const Smem8 L = smem_plan<MP, PACK>(prm.H, npk, nx);
-    const uint32_t sz_bytes = sz_tile_bytes(prm.H, G);
+    const uint32_t sz_bytes = static_cast<uint32_t>(kTileRows) * NGt * 2; // S (or ZS) of a tile
 
     // ---- shared memory ------------------------------------------------------------------
     const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *const base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t *const pkring = base + L.pk;
-    uint8_t *const xring = base + L.x;
-    uint8_t *const szbuf = base + L.sz;
-    float *const red = reinterpret_cast<float *>(base + L.red);
-    float *const xs_s = reinterpret_cast<float *>(base + L.xs); // [NGt][MP]
-    float *const inv_s = reinterpret_cast<float *>(base + L.inv); // [MP] 2^-e
-    float *const tw_s = inv_s + MP;                               // [2][MP] term weights
-    int *const nterms_s = reinterpret_cast<int *>(tw_s + 2 * MP);
-    uint64_t *const bars = reinterpret_cast<uint64_t *>(base + L.bars);
-    uint64_t *const pk_full = bars;              // [npk] TMA -> dequant
-    uint64_t *const pk_empty = pk_full + npk;    // [npk] dequant (4 warps) -> TMA
-    uint64_t *const x_full = pk_empty + npk;     // [nx]  TMA -> issuer
-    uint64_t *const x_empty = x_full + nx;       // [nx]  MMA commit -> TMA
-    uint64_t *const a_full = x_empty + nx;       // [K]   dequant (4 warps) -> issuer
-    uint64_t *const d_full = a_full + K;         // [K]   MMA commit -> epilogue, dequant
-    uint64_t *const d_empty = d_full + K;        // [K]   epilogue (16 warps) -> issuer
-    uint64_t *const sz_full = d_empty + K;       // [2]   bulk copy -> epilogue
-    uint64_t *const sz_empty = sz_full + 2;      // [2]   epilogue (16 warps) -> bulk copy
-    uint64_t *const red_full = sz_empty + 2;     // [1]   epilogue (16 warps) -> selection
-    uint64_t *const red_free = red_full + 1;     // [1]   selection -> epilogue
-    uint64_t *const fin = red_free + 1;          // [I]   issuer drain before teardown
-    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(fin + I);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    uint8_t *const stages = smem_raw + pad;                                   // nstage x kStage
+    uint8_t *const szbuf = stages + static_cast<size_t>(nstage) * C::kStage; // [2][S, ZS] tiles
+    float *const red = reinterpret_cast<float *>(szbuf + 4 * static_cast<size_t>(sz_bytes));
+    constexpr int kRedHalf = MP * 2 * kRedPitch; // floats of one epilogue half's tile values
+    float *const xs_s = red + 2 * kRedHalf;                                   // [NGt][MP]
+    float *const inv_s = xs_s + NGt * MP;                                     // [MP] 2^-e
+    float *const tw_s = inv_s + MP;                                           // [2][MP] w2, w3
+    uint64_t *const bars = reinterpret_cast<uint64_t *>(tw_s + 2 * MP);
+    uint64_t *const full = bars;              // [nstage] TMA -> dequant, MMA
+    uint64_t *const empty = full + nstage;    // [nstage] dequant (4 warps) + issuers -> TMA
+    uint64_t *const a_full = empty + nstage;  // [K]      dequant (4 warps) -> MMA, per unit
+    uint64_t *const d_full = a_full + K;      // [K]      MMA -> epilogue + dequant, per unit
+    uint64_t *const d_empty = d_full + K;     // [K]      epilogue -> MMA, per unit
+    uint64_t *const fin = d_empty + K;        // [4]      MMA drain before teardown
+    uint64_t *const red_full = fin + kIssuers; // [1]     epilogue (8 warps) -> selection
+    uint64_t *const red_free = red_full + 1;  // [1]      selection -> epilogue: `red` free
+    uint64_t *const sz_full = red_free + 1;   // [2]      bulk copy -> epilogue: S, ZS of a tile
+    uint64_t *const sz_empty = sz_full + 2;   // [2]      epilogue (8 warps) -> bulk copy
+    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(sz_empty + 2);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_packed);
         prefetch_tensormap(&tm_x);
-        for (int i = 0; i < npk; ++i) {
-            mbar_init(&pk_full[i], 1);
-            mbar_init(&pk_empty[i], kDqWarps);
-        }
-        for (int i = 0; i < nx; ++i) {
-            mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], 1);
+        for (int i = 0; i < nstage; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kDqWarps + kIssuers); // one dequant set, each plane's issuer
         }
         for (int i = 0; i < K; ++i) {
             mbar_init(&a_full[i], kDqWarps);
-            mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], kEpWarps); // every epilogue warp reads every unit
+            mbar_init(&d_full[i], kPP);     // one commit per plane of the unit
+            mbar_init(&d_empty[i], kU == 1 ? 8 : 4); // the epilogue warps reading the unit
         }
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&fin[i], 1);
+        mbar_init(red_full, kEpWarps);
+        mbar_init(red_free, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sz_full[i], 1);
             mbar_init(&sz_empty[i], kEpWarps);
         }
-        mbar_init(red_full, kEpWarps);
-        mbar_init(red_free, 1);
-        for (int i = 0; i < I; ++i) mbar_init(&fin[i], 1);
         fence_barrier_init();
     }
-    // the launch's term count: the most any of its rows needs
-    if (warp == 0) {
-        int t = 2;
-        for (int m = lane; m < MP; m += 32) t = max(t, prm.row_terms[m]);
-        t = __reduce_max_sync(0xffffffffu, t);
-        if (lane == 0) *nterms_s = t > 2 ? 3 : 2;
-    }
-    __syncthreads();
-    const int T = *nterms_s;
     const float *const xsrc = T == 3 ? prm.xs3 : prm.xs2;
     for (int i = threadIdx.x; i < NGt * MP; i += blockDim.x) {
         const int g = i / MP, m = i - g * MP;
@@ -400,24 +339,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tw_s[i] = prm.row_f[kTc8MaxMP + i];
         tw_s[MP + i] = prm.row_f[2 * kTc8MaxMP + i];
     }
-    if (warp == kWarpPk) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kWarpTma) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     const int first_tile = blockIdx.x, tile_step = gridDim.x;
-    const int my_tiles = first_tile < prm.ntiles ? (prm.ntiles - 1 - first_tile) / tile_step + 1 : 0;
-    const int units = my_tiles * NG * 4; // this CTA's units, in order
     bool failed = false;
 
-    if (warp == kWarpPk) {
-        // ---------------- TMA: packed codes and S / ZS ----------------
+    if (warp == kWarpTma) {
+        // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            uint32_t s = 0;
-            for (int it = 0; it < my_tiles && !failed; ++it) {
-                const int tile = first_tile + it * tile_step;
+            uint32_t s = 0, it = 0;
+            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
                 // the tile's S and ZS rows (contiguous in memory) into buffer it % 2, free once
                 // the epilogue finished tile it - 2; a partial last tile is read from global
                 // memory by the epilogue instead (an arrival without data keeps the phases)
@@ -436,152 +372,182 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&sz_full[b]);
                 }
                 for (int span = 0; span < NG; ++span, ++s) {
-                    const uint32_t st = s % npk;
-                    if (!mbar_wait_bounded(&pk_empty[st], ((s / npk) & 1u) ^ 1u, prm.timeout_flag)) {
+                    const uint32_t st = s % nstage;
+                    if (!mbar_wait_bounded(&empty[st], ((s / nstage) & 1u) ^ 1u, prm.timeout_flag)) {
                         failed = true;
                         break;
                     }
-                    uint8_t *const stage = pkring + static_cast<size_t>(st) * C::kPkStage;
-                    mbar_arrive_expect_tx(&pk_full[st], C::kPkStage);
+                    uint8_t *const stage = stages + static_cast<size_t>(st) * C::kStage;
+                    mbar_arrive_expect_tx(&full[st], C::kStage);
 #pragma unroll
                     for (int bx = 0; bx < kBoxes; ++bx)
                         tma_load_2d_hint(stage + bx * kPkBytes, &tm_packed,
                                          (kBoxes * span + bx) * kSpanBytes, tile * kTileRows,
-                                         &pk_full[st], policy);
+                                         &full[st], policy);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tma_load_2d(stage + kBoxes * kPkBytes + q * (N * 128), &tm_x,
+                                    plane_group<PACK>(q, span, NG) * kGroup, 0, &full[st]);
                 }
             }
         }
-    } else if (warp == kWarpX) {
-        // ---------------- TMA: the staged x terms of every unit ----------------
+    } else if (R::issuer_plane(warp) >= 0) {
+        // ---------------- MMA issuers: one warp per plane, every unit holding that plane ------
         if (lane == 0) {
-            const uint32_t xbytes = static_cast<uint32_t>(T) * MP * 128;
-            for (int q = 0; q < units && !failed; ++q) {
-                const int span = (q >> 2) % NG, plane = q & 3;
-                const uint32_t st = q % nx;
-                if (!mbar_wait_bounded(&x_empty[st], ((q / nx) & 1u) ^ 1u, prm.timeout_flag)) {
-                    failed = true;
-                    break;
-                }
-                uint8_t *const stage = xring + static_cast<size_t>(st) * C::kXTile;
-                const int k0 = plane_group<PACK>(plane, span, NG) * kGroup;
-                mbar_arrive_expect_tx(&x_full[st], xbytes);
-                for (int t = 0; t < T; ++t)
-                    tma_load_2d(stage + t * (MP * 128), &tm_x, k0, t * MP, &x_full[st]);
-            }
-        }
-    } else if (warp >= kWarpIss0 && warp < kWarpIss0 + I) {
-        // ---------------- MMA issuers: unit q goes to issuer q % I, slot q % K ----------------
-        if (lane == 0) {
-            const int me = warp - kWarpIss0;
-            const uint32_t idesc = make_idesc_f8(T * MP);
-            for (int q = me; q < units && !failed; q += I) {
-                const uint32_t slot = q % K, use = q / K, st = q % nx;
-                if (!mbar_wait_bounded(&x_full[st], (q / nx) & 1u, prm.timeout_flag) ||
-                    !mbar_wait_bounded(&a_full[slot], use & 1u, prm.timeout_flag) ||
-                    !mbar_wait_bounded(&d_empty[slot], (use & 1u) ^ 1u, prm.timeout_flag)) {
-                    failed = true;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a_tmem = tmem + slot * kSlotCols;
-                const uint32_t d_tmem = a_tmem + 32;
-                const uint64_t xdesc =
-                    sw128_desc(smem_u32(xring + static_cast<size_t>(st) * C::kXTile));
-                // K = 32 per MMA (32 bytes of the swizzled rows: +2 in the descriptor's 16-byte
-                // address units); groups of 64 put MMAs 0-1 and 2-3 in their own accumulators
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    mma_ts_f8(d_tmem + (i / (4 / GPU)) * NT, a_tmem + i * 8,
-                              xdesc + static_cast<uint64_t>(i * 2), idesc,
-                              (i % (4 / GPU)) ? 1u : 0u);
-                mma_commit(&d_full[slot]);
-                mma_commit(&x_empty[st]);
-            }
-            mma_commit(&fin[me]);
-            mbar_wait_bounded(&fin[me], 0, prm.timeout_flag);
-        }
-    } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kDqWarps) {
-        // ---------------- dequant: one TMEM lane (= tile row) per thread ----------------
-        const int row = ((warp & 3) << 5) | lane;
-        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
-        int q = 0;
-        for (int sidx = 0; sidx < my_tiles * NG && !failed; ++sidx) {
-            const uint32_t st = sidx % npk;
-            if (!warp_wait(&pk_full[st], (sidx / npk) & 1u, prm.timeout_flag)) {
-                failed = true;
-                break;
-            }
-            const uint32_t pk = smem_u32(pkring + static_cast<size_t>(st) * C::kPkStage) +
-                                row * kSpanBytes;
-            uint32_t w[32];
-            // this thread's row of packed box bx (128-byte swizzle)
-            auto load_box = [&](int bx) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t addr = pk + bx * kPkBytes + ((c ^ (row & 7)) << 4);
-                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]),
-                                   "=r"(w[4 * c + 3])
-                                 : "r"(addr));
-                }
-            };
-            load_box(0);
-            if constexpr (BITS == 2) {
-                // every plane of the span is in these 32 words: the stage goes back now
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&pk_empty[st]);
-            }
-#pragma unroll 1
-            for (int plane = 0; plane < 4; ++plane, ++q) {
-                if (BITS == 4 && plane == 2) {
-                    // planes 2 bx, 2 bx + 1 are the two nibbles of box bx
-                    load_box(1);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&pk_empty[st]);
-                }
-                const uint32_t slot = q % K, use = q / K;
-                // the slot's A buffer is free once its previous unit's MMAs have completed
-                if (use > 0 && !warp_wait(&d_full[slot], (use - 1) & 1u, prm.timeout_flag)) {
-                    failed = true;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t abuf = tmem + lane_base + slot * kSlotCols;
-                // two halves of 16 columns (64 k) each
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t r[16];
-                    if constexpr (BITS == 4) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) r[i] = deq_nib(w[16 * hf + i], plane & 1);
-                    } else if constexpr (PACK == kPackContig2) {
-                        // plane p is words 8p .. 8p + 7; half hf is words 8p + 4 hf ..
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t o[4];
-                            deq_c4(w[8 * plane + 4 * hf + i], o);
-#pragma unroll
-                            for (int b = 0; b < 4; ++b) r[4 * i + b] = o[b];
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) r[i] = deq4_e4m3(w[16 * hf + i], plane);
+            constexpr uint32_t idesc = make_idesc_f8(N);
+            const int plane = R::issuer_plane(warp);
+            const int u = plane / kPP, g = plane % kPP; // the plane's unit in a span, and its place
+            uint32_t s = 0;
+            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+                for (int span = 0; span < NG && !failed; ++span, ++s) {
+                    const uint32_t st = s % nstage;
+                    const uint32_t q = kU * s + u, slot = q % K, use = q / K;
+                    if (!mbar_wait_bounded(&full[st], (s / nstage) & 1u, prm.timeout_flag) ||
+                        !mbar_wait_bounded(&a_full[slot], use & 1u, prm.timeout_flag) ||
+                        !mbar_wait_bounded(&d_empty[slot], (use & 1u) ^ 1u, prm.timeout_flag)) {
+                        failed = true;
+                        break;
                     }
-                    tmem_st_x16(abuf + 16 * hf, r);
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem + slot * kSlotCols;
+                    const uint32_t d_tmem = a_tmem + kACols;
+                    // the descriptor's address field counts 16-byte units
+                    const uint64_t qdesc =
+                        sw128_desc(smem_u32(stages + static_cast<size_t>(st) * C::kStage +
+                                            kBoxes * kPkBytes)) +
+                        static_cast<uint64_t>(plane * (N * 128) / 16);
+                    // K = 32 per MMA: 128 / G groups of the plane, 4 / (128 / G) MMAs each into
+                    // the group's own accumulator
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        mma_ts_f8(d_tmem + (g * kGPP + i / (4 / kGPP)) * N, a_tmem + g * 32 + i * 8,
+                                  qdesc + static_cast<uint64_t>(i * 2), idesc,
+                                  (i % (4 / kGPP)) ? 1u : 0u);
+                    mma_commit(&d_full[slot]);
+                    mma_commit(&empty[st]);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[slot]);
             }
+            mma_commit(&fin[plane]);
+            mbar_wait_bounded(&fin[plane], 0, prm.timeout_flag);
         }
-    } else if (warp >= kWarpEp0) {
-        // ---------------- epilogue: set cp = batch columns [cp CW, cp CW + CW) ----------------
-        const int cp = (warp - kWarpEp0) >> 2;
+    } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kDqWarps * kDqSets) {
+        // ---------------- dequant: one TMEM lane (= tile row) per thread, all four planes ------
+        // With one unit per span the two sets of four warps take alternate spans (span s uses
+        // slot s % 2, so each set owns one slot and stage parity); otherwise set 0 takes them all.
+        const int set = (warp - kWarpDq0) >> 2;
         const int row = ((warp & 3) << 5) | lane;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
-        for (int it = 0; it < my_tiles && !failed; ++it) {
-            const int tile = first_tile + it * tile_step;
+        uint32_t s = 0;
+        for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+            for (int span = 0; span < NG; ++span, ++s) {
+                if (kDqSets == 2 && static_cast<int>(s & 1u) != set) continue;
+                const uint32_t st = s % nstage;
+                if (!warp_wait(&full[st], (s / nstage) & 1u, prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
+                const uint32_t pk =
+                    smem_u32(stages + static_cast<size_t>(st) * C::kStage) + row * kSpanBytes;
+                uint32_t w[32];
+                // this thread's row of packed box bx (128-byte swizzle)
+                auto load_box = [&](int bx) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t addr = pk + bx * kPkBytes + ((c ^ (row & 7)) << 4);
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]),
+                                       "=r"(w[4 * c + 3])
+                                     : "r"(addr));
+                    }
+                };
+                if constexpr (BITS == 2) {
+                    // every plane of the span is in these 32 words: the stage goes back now
+                    load_box(0);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
+                }
+                // the span's units: their planes into the A buffer of slot q % K, free once that
+                // slot's previous unit (q - K) has been accumulated
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const uint32_t q = kU * s + u, slot = q % K, use = q / K;
+                    if (use > 0 &&
+                        !warp_wait(&d_full[slot], (use - 1) & 1u, prm.timeout_flag)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t abuf = tmem + lane_base + slot * kSlotCols;
+                    // planes kPP u .. kPP u + kPP - 1, two at a time, in halves of 16 columns
+                    // (64 k; a tcgen05.st reads its registers at issue: r0 and r1 are free
+                    // again after it)
+#pragma unroll
+                    for (int pp = 0; pp < kPP; pp += 2) {
+                        const int plane = kPP * u + pp;
+                        // planes 2 bx, 2 bx + 1 of the 4-bit head are the two nibbles of box bx
+                        if constexpr (BITS == 4) load_box(plane >> 1);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            uint32_t r0[16], r1[16];
+                            if constexpr (BITS == 4) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    r0[i] = deq_nib_lo(w[16 * hf + i]);
+                                    r1[i] = deq_nib_hi(w[16 * hf + i]);
+                                }
+                            } else if constexpr (PACK == kPackContig2) {
+                                // planes p, p + 1 are words 8p .. 8p + 15; half hf of plane p is
+                                // words 8p + 4 hf ..
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    uint32_t o0[4], o1[4];
+                                    deq_c4(w[8 * plane + 4 * hf + i], o0);
+                                    deq_c4(w[8 * plane + 8 + 4 * hf + i], o1);
+#pragma unroll
+                                    for (int b = 0; b < 4; ++b) {
+                                        r0[4 * i + b] = o0[b];
+                                        r1[4 * i + b] = o1[b];
+                                    }
+                                }
+                            } else if (plane == 0) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    r0[i] = deq4_e4m3<0>(w[16 * hf + i]);
+                                    r1[i] = deq4_e4m3<1>(w[16 * hf + i]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    r0[i] = deq4_e4m3<2>(w[16 * hf + i]);
+                                    r1[i] = deq4_e4m3<3>(w[16 * hf + i]);
+                                }
+                            }
+                            tmem_st_x16(abuf + pp * 32 + 16 * hf, r0);
+                            tmem_st_x16(abuf + pp * 32 + 32 + 16 * hf, r1);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[slot]);
+                }
+                if (failed) break;
+                if constexpr (BITS == 4) {
+                    // both boxes have been read into registers
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
+                }
+            }
+        }
+    } else if (warp >= kWarpEp0 && warp < kWarpEp0 + kEpWarps) {
+        // ---------------- epilogue: two halves of four warps, each two groups of every span ---
+        const int h = (warp - kWarpEp0) >> 2; // planes 2h, 2h + 1
+        const int row = ((warp & 3) << 5) | lane;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        constexpr int NGH = 2 * kGPP; // groups of a half in one span
+        constexpr int CH = MP / 16;   // 16-column chunks of one term of one group
+        uint32_t t = 0, it = 0;
+        for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
             const int grow = tile * kTileRows + row;
             const bool row_ok = grow < prm.V;
             const bool full_tile = (tile + 1) * kTileRows <= prm.V;
@@ -595,70 +561,80 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint16_t *const sZ = sS + sz_bytes / 2;
             const uint16_t *const gS = prm.S + static_cast<long long>(row_ok ? grow : 0) * NGt;
             const uint16_t *const gZ = prm.ZS + static_cast<long long>(row_ok ? grow : 0) * NGt;
-            float acc[CW];
+            float acc[MP];
 #pragma unroll
-            for (int j = 0; j < CW; ++j) acc[j] = 0.f;
-            for (int span = 0; span < NG && !failed; ++span) {
-#pragma unroll 1
-                for (int p0 = 0; p0 < 4; p0 += UPR) {
-                    // the units of planes p0 .. p0 + UPR - 1 of the span
-                    float v[UPR][GPU][kTc8Terms][CW];
-                    const int q0 = (it * NG + span) * 4 + p0;
+            for (int m = 0; m < MP; ++m) acc[m] = 0.f;
+            for (int span = 0; span < NG; ++span, t += 4) {
+                // this half's groups: planes 2h, 2h+1, kGPP groups each
+                float s2[NGH], sz[NGH];
 #pragma unroll
-                    for (int u = 0; u < UPR; ++u) {
-                        const uint32_t slot = (q0 + u) % K, use = (q0 + u) / K;
-                        if (!warp_wait(&d_full[slot], use & 1u, prm.timeout_flag)) {
-                            failed = true;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t dcol = tmem + lane_base + slot * kSlotCols + 32 + cp * CW;
-#pragma unroll
-                        for (int a = 0; a < GPU; ++a)
-#pragma unroll
-                            for (int t = 0; t < kTc8Terms; ++t)
-                                if (t < T) tmem_ld_cw<CW>(dcol + a * NT + t * MP, v[u][a][t]);
+                for (int gl = 0; gl < NGH; ++gl) {
+                    const int plane = 2 * h + gl / kGPP;
+                    const int gi = plane_group<PACK>(plane, span, NG) * kGPP + gl % kGPP;
+                    uint16_t sb = 0, zb = 0;
+                    if (full_tile) {
+                        sb = sS[gi];
+                        zb = sZ[gi];
+                    } else if (row_ok) {
+                        sb = __ldg(gS + gi);
+                        zb = __ldg(gZ + gi);
                     }
-                    if (failed) break;
+                    const float sv = bf16_bits_to_f32(sb), zv = bf16_bits_to_f32(zb);
+                    // (S / B) sum x v with the MMA's sum of x v 2^-9 (quarter split, B = 4: odd
+                    // planes carry 4 v 2^-9, even planes v 2^-9; contiguous-4, B = 4: every
+                    // plane v 2^-9; 4 bits, B = 16: v 2^-9)
+                    const bool four_v = PACK != kPackHalf4 && PACK != kPackContig2 && (plane & 1);
+                    s2[gl] = (BITS == 4 ? 32.0f : (four_v ? 32.0f : 128.0f)) * sv;
+                    sz[gl] = sv - zv;
+                }
+                // the unit holding this half's two groups (planes 2h, 2h+1) of the span
+                const uint32_t q = kU * (t / 4) + (kU == 1 ? 0 : h), slot = q % K, use = q / K;
+                if (!warp_wait(&d_full[slot], use & 1u, prm.timeout_flag)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                // the half's first accumulator within the unit
+                const uint32_t dcol = tmem + lane_base + slot * kSlotCols + kACols +
+                                      (kU == 1 ? 2 * h * kGPP : 0) * N;
+                // the half's NGH * CH chunks, one per tcgen05 wait (T * 16 registers)
+#pragma unroll
+                for (int k = 0; k < NGH * CH; ++k) {
+                    const int gl = k / CH, c = k % CH;
+                    float v[T][16];
+#pragma unroll
+                    for (int tt = 0; tt < T; ++tt)
+                        tmem_ld_x16(dcol + gl * N + tt * MP + c * 16, v[tt]);
                     tmem_wait_ld();
-                    // every partial of these units is in registers: their slots go back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
+                    if (k == NGH * CH - 1) {
+                        // every partial of the unit is in registers: the slot goes back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&d_empty[slot]);
+                    }
+                    const int gi = plane_group<PACK>(2 * h + gl / kGPP, span, NG) * kGPP + gl % kGPP;
+                    const float4 *xg = reinterpret_cast<const float4 *>(xs_s + gi * MP);
 #pragma unroll
-                        for (int u = 0; u < UPR; ++u) mbar_arrive(&d_empty[(q0 + u) % K]);
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 x4 = xg[c * 4 + j];
+                        const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+                        const float4 a4 = reinterpret_cast<const float4 *>(tw_s)[c * 4 + j];
+                        const float w2[4] = {a4.x, a4.y, a4.z, a4.w};
+                        float w3[4] = {0.f, 0.f, 0.f, 0.f};
+                        if constexpr (T == 3) {
+                            const float4 b4 = reinterpret_cast<const float4 *>(tw_s + MP)[c * 4 + j];
+                            w3[0] = b4.x;
+                            w3[1] = b4.y;
+                            w3[2] = b4.z;
+                            w3[3] = b4.w;
+                        }
 #pragma unroll
-                    for (int u = 0; u < UPR; ++u) {
-                        const int plane = p0 + u;
-#pragma unroll
-                        for (int a = 0; a < GPU; ++a) {
-                            const int gi = plane_group<PACK>(plane, span, NG) * GPU + a;
-                            uint16_t sb = 0, zb = 0;
-                            if (full_tile) {
-                                sb = sS[gi];
-                                zb = sZ[gi];
-                            } else if (row_ok) {
-                                sb = __ldg(gS + gi);
-                                zb = __ldg(gZ + gi);
-                            }
-                            const float sv = bf16_bits_to_f32(sb), zv = bf16_bits_to_f32(zb);
-                            // (S / B) sum x v with the MMA's sum of x v 2^-9 (quarter split,
-                            // B = 4: odd planes carry 4 v 2^-9, even planes v 2^-9;
-                            // contiguous-4, B = 4: every plane v 2^-9; 4 bits, B = 16: v 2^-9)
-                            const bool four_v = PACK != kPackHalf4 && PACK != kPackContig2 && (plane & 1);
-                            const float s2 = (BITS == 4 ? 32.0f : (four_v ? 32.0f : 128.0f)) * sv;
-                            const float sz = sv - zv;
-                            const float *const xg = xs_s + gi * MP + cp * CW;
-                            const float *const w2 = tw_s + cp * CW, *const w3 = w2 + MP;
-#pragma unroll
-                            for (int j = 0; j < CW; ++j) {
-                                // the row's terms, weighted by their powers of two (exact)
-                                float r = fmaf(sz, xg[j], acc[j]);
-                                r = fmaf(s2, v[u][a][0][j], r);
-                                r = fmaf(s2 * w2[j], v[u][a][1][j], r);
-                                if (T == 3) r = fmaf(s2 * w3[j], v[u][a][2][j], r);
-                                acc[j] = r;
-                            }
+                        for (int i = 0; i < 4; ++i) {
+                            // the row's terms weighted by their powers of two (exact)
+                            float p = fmaf(w2[i], v[1][4 * j + i], v[0][4 * j + i]);
+                            if constexpr (T == 3) p = fmaf(w3[i], v[2][4 * j + i], p);
+                            const int m = c * 16 + 4 * j + i;
+                            acc[m] = fmaf(s2[gl], p, fmaf(sz[gl], xv[i], acc[m]));
                         }
                     }
                 }
@@ -672,20 +648,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 failed = true;
                 break;
             }
-            float *const rh = red + (row >> 6) * kRedPitch + (row & 63);
+            float *const rh = red + h * kRedHalf + (row >> 6) * kRedPitch + (row & 63);
 #pragma unroll
-            for (int j = 0; j < CW; ++j) {
-                const int m = cp * CW + j;
-                rh[2 * m * kRedPitch] = row_ok ? acc[j] * inv_s[m] : -INFINITY;
-            }
+            for (int m = 0; m < MP; ++m) rh[2 * m * kRedPitch] = row_ok ? acc[m] * inv_s[m] : -INFINITY;
             __syncwarp();
             if (lane == 0) mbar_arrive(red_full);
         }
     } else if (warp == kWarpSel) {
         // ---------------- block top-KCAND: pair = (batch column m, block b of the tile) ------
+        // the tile's coarse values are the sums of the two epilogue halves (both -inf past V)
         const int npairs = 2 * prm.mrows;
-        for (int it = 0; it < my_tiles && !failed; ++it) {
-            const int tile = first_tile + it * tile_step;
+        uint32_t it = 0;
+        for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
             if (!warp_wait(red_full, it & 1u, prm.timeout_flag)) {
                 failed = true;
                 break;
@@ -700,8 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float *const cdbg =
                             prm.coarse ? prm.coarse + static_cast<long long>(prm.m0 + m) * prm.V
                                        : nullptr;
-                        select_lane8(red + pidx * kRedPitch, blk * kBlockN, prm.V, prm.kcand,
-                                     prm.cand_val + off, prm.cand_idx + off, cdbg);
+                        select_lane8(red + pidx * kRedPitch, red + kRedHalf + pidx * kRedPitch,
+                                     blk * kBlockN, prm.V, prm.kcand, prm.cand_val + off,
+                                     prm.cand_idx + off, cdbg);
                     }
                 }
             } else {
@@ -719,8 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           static_cast<long long>(blk) * kBlockN < prm.V;
                         const int g0 = blk * kBlockN + lane;
                         const float *pv = red + (live ? pidx : 0) * kRedPitch;
-                        const float c0 = pv[lane];
-                        const float c1 = pv[lane + 32];
+                        const float c0 = pv[lane] + pv[kRedHalf + lane];
+                        const float c1 = pv[lane + 32] + pv[kRedHalf + lane + 32];
                         k0[bb] = (live && g0 < prm.V) ? f32_order_key(c0) : 0u;
                         k1[bb] = (live && g0 + 32 < prm.V) ? f32_order_key(c1) : 0u;
                         if (prm.coarse && live) {
@@ -746,43 +721,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kWarpPk) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kWarpTma) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Stage counts for a launch configuration: x stages a multiple of the issuer count (each
-// issuer owns nx / I of them, two where they fit, so that an issuer's next x tile is in flight
-// while it works), then as many packed stages as fit (two to eight); false if nothing fits.
+// One launch covers both term counts: the launch's count is the most any of its rows needs.
 template <int MP, int PACK>
-bool pick_stages(int H, int *npk, int *nx)
+__global__ void __launch_bounds__(Roles<two_sets<MP, PACK>()>::kThreads, 1)
+    coarse_tc8_kernel(const __grid_constant__ CUtensorMap tm_packed,
+                      const __grid_constant__ CUtensorMap tm_x2,
+                      const __grid_constant__ CUtensorMap tm_x3, const Tc8Params prm)
 {
-    using C = Cfg8<MP, PACK>;
-    for (int per = 2; per >= 1; --per) {
-        const int x = per * C::I;
-        for (int p = 8; p >= 2; --p) {
-            if (smem_plan<MP, PACK>(H, p, x).total <= static_cast<uint32_t>(kSmemLimit8)) {
-                *npk = p;
-                *nx = x;
-                return true;
-            }
-        }
-    }
-    return false;
+    extern __shared__ uint8_t smem_raw[];
+    int need = 2;
+    for (int m = 0; m < MP; ++m) need = max(need, prm.row_terms[m]);
+    if (need == 3) coarse_tc8_body<MP, PACK, 3>(tm_packed, tm_x3, prm, prm.nstage3, smem_raw);
+    else coarse_tc8_body<MP, PACK, 2>(tm_packed, tm_x2, prm, prm.nstage2, smem_raw);
+}
+
+// Dynamic shared memory besides the stages: alignment slack, the double-buffered S/ZS tile
+// copies, the two epilogue halves' tile values, xs, 2^-e and the term weights, barriers.
+size_t tc8_fixed_smem(int MP, int H, int G)
+{
+    const int NGt = H / G;
+    return 1024 + 4 * static_cast<size_t>(kTileRows) * NGt * 2 +
+           2 * static_cast<size_t>(MP) * 2 * kRedPitch * 4 + static_cast<size_t>(NGt) * MP * 4 +
+           3 * MP * 4 + 64 * 8 + 32;
+}
+
+// Stage count of a body: as many as fit (at most 6); even when two dequant sets alternate
+// spans, so that each stage's barriers always serve the same set.
+template <int MP, int PACK, int TT>
+int tc8_stages(int H)
+{
+    using C = Cfg8<MP, PACK, TT>;
+    const size_t fixed = tc8_fixed_smem(MP, H, C::G);
+    long long n = (kSmemLimit8 - static_cast<long long>(fixed)) / C::kStage;
+    if (n > 6) n = 6;
+    if (C::kU == 1) n &= ~1LL;
+    return static_cast<int>(n);
 }
 
 template <int MP, int PACK>
 cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
                        const Tc8Params &base, cudaStream_t stream)
 {
-    CUtensorMap tm_x;
-    // the staged x of the launch: [3 MP rows, H] bytes; a box is one term's MP rows x 128 k
-    CUresult r = encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                                      const_cast<uint8_t *>(xt8_chunk), base.H,
-                                      static_cast<uint64_t>(kTc8Terms) * MP, base.H, 128, MP,
-                                      CU_TENSOR_MAP_SWIZZLE_128B);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    int npk = 0, nx = 0;
-    if (!pick_stages<MP, PACK>(base.H, &npk, &nx)) return cudaErrorInvalidConfiguration;
-    const uint32_t smem = smem_plan<MP, PACK>(base.H, npk, nx).total;
+    // the staged x of the launch: [3 MP rows, H] bytes; a box is a plane's 128 k of the
+    // first T terms (T MP rows)
+    CUtensorMap tm_x[2];
+    for (int t = 0; t < 2; ++t) {
+        CUresult r = encode_tensor_map_2d(&tm_x[t], CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                          const_cast<uint8_t *>(xt8_chunk), base.H,
+                                          static_cast<uint64_t>(kTc8Terms) * MP, base.H, 128,
+                                          (2 + t) * MP, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    const int n2 = tc8_stages<MP, PACK, 2>(base.H), n3 = tc8_stages<MP, PACK, 3>(base.H);
+    if (n2 < 2 || n3 < 2) return cudaErrorInvalidConfiguration;
+    const size_t s2 = tc8_fixed_smem(MP, base.H, Cfg8<MP, PACK, 2>::G) +
+                      static_cast<size_t>(n2) * Cfg8<MP, PACK, 2>::kStage;
+    const size_t s3 = tc8_fixed_smem(MP, base.H, Cfg8<MP, PACK, 3>::G) +
+                      static_cast<size_t>(n3) * Cfg8<MP, PACK, 3>::kStage;
+    const size_t smem = s2 > s3 ? s2 : s3;
     // the shared-memory limit is a per-device attribute: raised once on every device
     static PerDeviceOnce attr;
     cudaError_t e = attr.run([] {
@@ -791,32 +790,30 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
     });
     if (e != cudaSuccess) return e;
     Tc8Params prm = base;
-    prm.npk = npk;
-    prm.nx = nx;
+    prm.nstage2 = n2;
+    prm.nstage3 = n3;
     const int sms = device_sm_count();
     const int grid = prm.ntiles < sms ? prm.ntiles : sms;
-    coarse_tc8_kernel<MP, PACK><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x, prm);
+    constexpr int kThreads = Roles<two_sets<MP, PACK>()>::kThreads;
+    coarse_tc8_kernel<MP, PACK><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x[0], tm_x[1], prm);
     return cudaGetLastError();
 }
 
 template <int PACK>
-bool fits_all(int H)
+bool fits(int MP, int H)
 {
-    int p, x;
-    if constexpr (PACK == kPackG64) return pick_stages<16, PACK>(H, &p, &x);
-    else if constexpr (PACK == kPackQuarter2)
-        return pick_stages<16, PACK>(H, &p, &x) && pick_stages<32, PACK>(H, &p, &x) &&
-               pick_stages<64, PACK>(H, &p, &x);
-    else return pick_stages<16, PACK>(H, &p, &x) && pick_stages<32, PACK>(H, &p, &x);
+    if (MP == 16) return tc8_stages<16, PACK, 2>(H) >= 2 && tc8_stages<16, PACK, 3>(H) >= 2;
+    if constexpr (PACK == kPackG64) return false; // groups of 64: 16-row launches only
+    else return tc8_stages<32, PACK, 2>(H) >= 2 && tc8_stages<32, PACK, 3>(H) >= 2;
 }
 
 } // namespace
 
 int tc8_max_rows(int pack)
 {
-    if (pack == kPackG64) return 16;
-    if (pack == kPackQuarter2) return 64;
-    return 32; // the 4-bit head and the contiguous-4 layout
+    // groups of 64 need two accumulators per plane; the 4-bit head's 32 KB packed boxes leave
+    // no room for two stages of 32 rows in three terms
+    return (pack == kPackG64 || pack == kPackHalf4) ? 16 : 32;
 }
 
 int tc8_chunks(int M, int pack)
@@ -831,7 +828,7 @@ Tc8Chunk tc8_chunk(int M, int c, int pack, int H)
     Tc8Chunk k;
     k.m0 = c * r;
     k.rows = M - k.m0 < r ? M - k.m0 : r;
-    k.MP = k.rows <= 16 ? 16 : (k.rows <= 32 ? 32 : 64);
+    k.MP = k.rows <= 16 ? 16 : 32;
     // launches before c are full (r rows, MP = r)
     k.x_off = static_cast<size_t>(c) * kTc8Terms * r * H;
     return k;
@@ -840,7 +837,7 @@ Tc8Chunk tc8_chunk(int M, int c, int pack, int H)
 size_t tc8_x_bytes(int M, int H)
 {
     size_t most = 0;
-    const int packs[3] = {kPackQuarter2, kPackHalf4, kPackG64};
+    const int packs[2] = {kPackQuarter2, kPackHalf4};
     for (int pack : packs) {
         const int n = tc8_chunks(M, pack);
         const Tc8Chunk last = tc8_chunk(M, n - 1, pack, H);
@@ -855,10 +852,18 @@ bool tc8_supported(int M, int H, int bits, int group)
     // the x staging keeps a row in registers: H <= 16384
     if (M < 1 || M > kMaxM || H % 512 != 0 || H > 16384) return false;
     if (bits != 2 && bits != 4) return false;
-    if (bits == 4) return group == 128 && fits_all<kPackHalf4>(H);
-    if (group == 64) return M <= 16 && fits_all<kPackG64>(H);
-    if (group != 128) return false;
-    return fits_all<kPackQuarter2>(H) && fits_all<kPackContig2>(H);
+    // groups of 64 need two accumulators per plane: only the 16-row launch
+    if (group != 128 && (group != 64 || bits != 2 || M > 16)) return false;
+    const int pack = bits == 4 ? kPackHalf4 : (group == 64 ? kPackG64 : kPackQuarter2);
+    for (int c = 0; c < tc8_chunks(M, pack); ++c) {
+        const int MP = tc8_chunk(M, c, pack, H).MP;
+        bool ok;
+        if (pack == kPackHalf4) ok = fits<kPackHalf4>(MP, H);
+        else if (pack == kPackG64) ok = fits<kPackG64>(MP, H);
+        else ok = fits<kPackQuarter2>(MP, H) && fits<kPackContig2>(MP, H);
+        if (!ok) return false;
+    }
+    return true;
 }
 
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream)
@@ -872,8 +877,6 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (!tc8_supported(a.M, a.H, bits, a.pack == kPackG64 ? 64 : 128))
         return cudaErrorInvalidConfiguration;
-    const int G = a.pack == kPackG64 ? 64 : 128;
-    const int NGt = a.H / G;
     Tc8Params base;
     base.S = a.S;
     base.ZS = a.ZS;
@@ -886,17 +889,16 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
     base.cand_idx = a.cand_idx;
     base.coarse = a.coarse;
     base.timeout_flag = a.timeout_flag;
-    base.npk = base.nx = 2;
+    base.nstage2 = base.nstage3 = 2;
     for (int c = 0; c < tc8_chunks(a.M, a.pack); ++c) {
         const Tc8Chunk k = tc8_chunk(a.M, c, a.pack, a.H);
-        float *const small = w.small + static_cast<size_t>(c) * tc8_small_floats(a.H);
+        const float *const small = w.small + static_cast<size_t>(c) * tc8_small_floats(a.H);
         base.m0 = k.m0;
         base.mrows = k.rows;
         base.xs2 = small;
         base.xs3 = small + static_cast<size_t>(kTc8MaxMP) * (a.H / 64);
         base.row_f = small + 2 * static_cast<size_t>(kTc8MaxMP) * (a.H / 64);
         base.row_terms = reinterpret_cast<const int *>(base.row_f + 3 * kTc8MaxMP);
-        (void)NGt;
         const uint8_t *xt = w.xt8 + k.x_off;
         cudaError_t e;
         if (a.pack == kPackHalf4) {
@@ -909,8 +911,7 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
             else e = launch_cfg<32, kPackContig2>(tm_packed, xt, base, stream);
         } else {
             if (k.MP == 16) e = launch_cfg<16, kPackQuarter2>(tm_packed, xt, base, stream);
-            else if (k.MP == 32) e = launch_cfg<32, kPackQuarter2>(tm_packed, xt, base, stream);
-            else e = launch_cfg<64, kPackQuarter2>(tm_packed, xt, base, stream);
+            else e = launch_cfg<32, kPackQuarter2>(tm_packed, xt, base, stream);
         }
         if (e != cudaSuccess) return e;
     }

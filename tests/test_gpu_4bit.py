@@ -52,8 +52,8 @@ def test_quantize4_bit_exact(V, H):
     (5, 1024, 8192 + 37, 1, 32, 4),       # ragged tail block
     (16, 5120, 12288 + 64 * 3 + 5, 1, 32, 1),
     (16, 2048, 16384, 8, 32, 1),          # KCAND = 8 on the 4-bit head
-    (32, 5120, 4096, 1, 32, 1),           # MP = 32, half-span units
-    (33, 1536, 6144, 4, 24, 5),           # two batch chunks (32 + 16 rows)
+    (32, 5120, 4096, 1, 32, 1),           # two launches of 16 rows
+    (33, 1536, 6144, 4, 24, 5),           # three batch chunks (16 + 16 + 1 rows)
     (64, 1024, 4096, 8, 64, 16),          # RERANK 64, top-16
 ])
 def test_forward4_matches_the_oracle(M, H, V, kcand, R, k):
