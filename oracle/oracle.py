@@ -434,6 +434,11 @@ def decision_gaps(res: dict, kcand: int, k: int) -> np.ndarray:
       3. the gaps between consecutive exact values among the top-k and the (k+1)-th.
     Coarse margins are divided by (1 + |value|), exact margins are absolute.  A row whose
     minimum is <= 1e-3 is a tie row.  Returns that minimum per row (inf when none applies).
+
+    Margins 1 and 2 are the two selections the page makes on coarse values (radiance_drafthead.py:
+    ``_emit``, the per-block top KCAND by successive max-and-mask, and the top-RERANK gather
+    over the block candidates in ``_apply_head_int2``); margin 3 is the final ordering on exact
+    values.  Pinned on hand-worked rows, with planted mistakes that must be caught.
     """
     cf = res["coarse_f32"].astype(np.float64)
     M, V = cf.shape

@@ -343,6 +343,117 @@ def test_decision_gap_flags_a_planted_tie():
     assert orc.decision_gaps(res2, 8, 1)[0] == 0.0
 
 
+def _res_from_coarse(rows, exact, kcand, R):
+    """A forward() result built from hand-set coarse rows (fp32 [M, V]) through the oracle's
+    brute-force-pinned block_topk / select_topr, with the given exact values of the selected
+    entries (one list of R per row)."""
+    cf = np.asarray(rows, dtype=np.float32)
+    cval, cidx, _ = orc.block_topk(cf, kcand)
+    sel, selv = orc.select_topr(cval, cidx, R)
+    return dict(coarse_f32=cf, cand_val=cval, cand_idx=cidx, sel_idx=sel, sel_val=selv,
+                exact=np.asarray(exact, dtype=np.float64))
+
+
+def _row(V, entries, fill=-8.0):
+    r = np.full(V, fill, np.float32)
+    for c, v in entries.items():
+        r[c] = v
+    return r
+
+
+def _check_margin_pins(gaps_fn):
+    """The decision margins on hand-built coarse rows, each worked out by hand.
+
+    Page: radiance_drafthead.py, _emit (each block of 64 emits its top KC by successive
+    max-and-mask) and the top-RERANK gather over the block candidates in _apply_head_int2.
+    A coarse value that moves by its rounding error can change the returned indices only at
+    those two boundaries (a block's KC-th / (KC+1)-th entry, when the latter could have made
+    the reranked set; the R-th / (R+1)-th candidate) or in the final exact top-k.
+    """
+    d = 2.0 ** -10
+    # (a) KC boundary inside a block whose (KC+1)-th value reaches the R-th selected value:
+    #     block 0 = {10, 9, 9 - d}, block 1 = {3, 2}; KC = 2, R = 2 -> selected {10, 9},
+    #     R-th = 9, block 0's 3rd value 9 - d reaches it.  margin 1 = d / (1 + 9).
+    a = _row(128, {3: 10.0, 5: 9.0, 9: 9.0 - d, 70: 3.0, 71: 2.0})
+    # (b) the same near-tie (5 | 5 - d) in a block that cannot reach the R-th value 9:
+    #     block 0 = {10, 5, 5 - d}, block 1 = {9, 8} -> selected {10, 9}; only margin 2 applies,
+    #     (9 - 8) / (1 + 9) = 0.1.
+    b = _row(128, {3: 10.0, 5: 5.0, 9: 5.0 - d, 70: 9.0, 71: 8.0})
+    # (c) R boundary: block 0 = {10, 9}, block 1 = {9 - d, 2} -> candidates 10, 9, 9 - d, 2;
+    #     margin 2 = d / (1 + 9).  No block's 3rd value reaches 9.
+    c = _row(128, {3: 10.0, 5: 9.0, 70: 9.0 - d, 71: 2.0})
+    res = _res_from_coarse([a, b, c], [[5.0, 1.0]] * 3, 2, 2)
+    assert res["sel_idx"].tolist() == [[3, 5], [3, 70], [3, 5]]
+    g = gaps_fn(res, 2, 1)
+    assert g[0] == d / 10.0 and g[0] <= 1e-3          # flagged
+    assert g[1] == 0.1                                 # not flagged: the near-tie cannot reach
+    assert g[2] == d / 10.0 and g[2] <= 1e-3          # flagged
+
+    # (d) clear rows, KC = 1, R = 2, three blocks.
+    #     row 0: block 0 = {10, 9.75}, block 1 = {9.5}, block 2 = {3}; selected {10, 9.5}; block
+    #     0's 2nd value 9.75 is above the R-th (9.5), so margin 1 = (10 - 9.75) / (1 + 10);
+    #     margin 2 = (9.5 - 3) / (1 + 9.5); exact gap 5 - 1 = 4.
+    #     row 1: block 0 = {4}, block 1 = {-5, -5.5}, block 2 = {-2}; selected {4, -2}, R-th -2;
+    #     block 1's 2nd value -5.5 does not reach it; margin 2 = (-2 - -5) / (1 + 2) = 1;
+    #     exact gap 0.5 (absolute, unscaled) is the minimum.
+    r0 = _row(192, {3: 10.0, 4: 9.75, 70: 9.5, 130: 3.0})
+    r1 = _row(192, {10: 4.0, 80: -5.0, 81: -5.5, 150: -2.0})
+    res = _res_from_coarse([r0, r1], [[5.0, 1.0], [7.0, 6.5]], 1, 2)
+    assert res["sel_idx"].tolist() == [[3, 70], [10, 150]]
+    g = gaps_fn(res, 1, 1)
+    assert g[0] == 0.25 / 11.0
+    assert g[1] == 0.5
+    # the same rows judged at k = 2 (both reranked entries returned): no (k+1)-th exact value
+    # exists, so the exact margin is the gap between the two
+    g2 = gaps_fn(res, 1, 2)
+    assert g2[0] == 0.25 / 11.0 and g2[1] == 0.5
+
+    # (e) fewer than R + 1 candidates: no R boundary; a ragged last block (V = 129) whose only
+    #     column cannot have a (KC+1)-th value.  KC = 1, R = 3: blocks {10, 9.9}, {8}, {7}.
+    #     Block 0's 2nd value 9.9 reaches the R-th (7): margin 1 = 0.1 / 11 in fp32 values.
+    e = _row(129, {0: 10.0, 1: 9.9, 64: 8.0, 128: 7.0})
+    res = _res_from_coarse([e], [[3.0, 2.0, 1.0]], 1, 3)
+    assert res["sel_idx"].tolist() == [[0, 64, 128]]
+    g = gaps_fn(res, 1, 1)
+    assert g[0] == (10.0 - float(np.float32(9.9))) / 11.0
+
+
+def test_decision_gap_margins_on_hand_built_rows():
+    _check_margin_pins(orc.decision_gaps)
+
+
+_GAP_MUTANTS = {
+    "drop the reach condition": (
+        "reach = np.isfinite(k1) & (k1 >= r_th - 1e-3 * (1.0 + abs(r_th)))",
+        "reach = np.isfinite(k1)"),
+    "drop the (1 + |v|) scaling of margin 1": (
+        "/ (1.0 + np.abs(kth[reach]))", "/ 1.0"),
+    "drop the (1 + |v|) scaling of margin 2": (
+        "/ (1.0 + abs(cv[R - 1]))", "/ 1.0"),
+    "R boundary one place early": (
+        "(cv[R - 1] - cv[R])", "(cv[R - 2] - cv[R - 1])"),
+    "KC boundary one place late": (
+        "blocks[:, kcand - 1], blocks[:, kcand]", "blocks[:, kcand], blocks[:, kcand + 1]"),
+    "reach measured against the top candidate": (
+        "r_th = cv[R - 1]", "r_th = cv[0]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(_GAP_MUTANTS))
+def test_decision_gap_pins_catch_planted_mistakes(name):
+    """Each mutant is the oracle's decision_gaps with one plausible mistake planted in its
+    source (on the CPU); the hand-worked margins must reject every one."""
+    import inspect
+    import textwrap
+    old, new = _GAP_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(orc.decision_gaps))
+    assert src.count(old) == 1, f"mutation site for {name!r} not found"
+    ns = dict(vars(orc))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    with pytest.raises(AssertionError):
+        _check_margin_pins(ns["decision_gaps"])
+
+
 # ------------------------------------------------------------------------------------------
 # fp8 head (e4m3 rows, per-row fp32 scale): decode, quantise, rerank
 # ------------------------------------------------------------------------------------------
