@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--no-shard", action="store_true", help="skip the one-shard-head lines")
     ap.add_argument("--no-int4", action="store_true", help="skip the 4-bit-head line")
     ap.add_argument("--no-ablations", action="store_true", help="skip the layout ablations")
+    ap.add_argument("--no-topk", action="store_true", help="skip the top-k caller lines")
+    ap.add_argument("--no-tiny", action="store_true", help="skip the tiny-head line")
+    ap.add_argument("--no-recall", action="store_true",
+                    help="skip the recall measurements against the exact bf16 head")
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2,
                     help="head width for --profile runs (4: the 4-bit head at KCAND=1)")
     ap.add_argument("--profile", action="store_true",
@@ -230,6 +234,36 @@ class ShardInputs(Inputs):
         dh.dh_quantize(self.W, self.packed, self.S, self.ZS)
 
 
+class WlInputs:
+    """One resident input set of a named workload, run with that workload's own KCAND,
+    RERANK and top-k (the tiny head, the top-k caller)."""
+
+    def __init__(self, wl, seed, dev):
+        import torch
+        import quantised_speculative_draft_gb300 as dh
+        from quantised_speculative_draft_gb300 import synth
+        self.wl = wl
+        self.x = synth.make_x(wl, seed, dev)
+        self.W = synth.make_w(wl, seed, dev)
+        V, H = self.W.shape
+        self.packed = torch.empty(V, H // 4, dtype=torch.uint8, device=dev)
+        self.S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        self.ZS = torch.empty(V, H // 128, dtype=torch.bfloat16, device=dev)
+        dh.dh_quantize(self.W, self.packed, self.S, self.ZS)
+
+    def call(self, M, ws, idx, logit):
+        import quantised_speculative_draft_gb300 as dh
+        w = self.wl
+        dh.dh_forward(self.x[:M], self.packed, self.S, self.ZS, self.W, w.kcand, w.rerank, w.topk,
+                      idx, logit, ws)
+
+    def call_timed(self, M, ws, idx, logit, events):
+        import quantised_speculative_draft_gb300 as dh
+        w = self.wl
+        dh.dh_forward_timed(self.x[:M], self.packed, self.S, self.ZS, self.W, w.kcand, w.rerank,
+                            w.topk, idx, logit, ws, events)
+
+
 class Fp8Inputs:
     """One resident input set of the fp8 head: e4m3 rows with per-row scales and their int2
     packing (dh_quantize_fp8); the rerank reads the e4m3 rows."""
@@ -323,13 +357,17 @@ class AsPlain:
         Inputs.call_timed(self.inputs, M, ws, idx, logit, events)
 
 
-def make_outputs(M, dev, V=None):
+def make_outputs(M, dev, V=None, s=None):
+    """Workspace and outputs for M rows of the input set s (its workload's sizes and selection
+    parameters; the full head's by default)."""
     import torch
     import quantised_speculative_draft_gb300 as dh
-    ws = torch.empty(dh.dh_workspace_bytes(M, H_FULL, V or V_FULL, KCAND, RERANK),
-                     dtype=torch.uint8, device=dev)
-    idx = torch.empty(M, TOPK, dtype=torch.int32, device=dev)
-    logit = torch.empty(M, TOPK, dtype=torch.float32, device=dev)
+    wl = getattr(s, "wl", None)
+    V_, H, kc, R, k = ((wl.V, wl.H, wl.kcand, wl.rerank, wl.topk) if wl is not None
+                       else (V or V_FULL, H_FULL, KCAND, RERANK, TOPK))
+    ws = torch.empty(dh.dh_workspace_bytes(M, H, V_, kc, R), dtype=torch.uint8, device=dev)
+    idx = torch.empty(M, k, dtype=torch.int32, device=dev)
+    logit = torch.empty(M, k, dtype=torch.float32, device=dev)
     return ws, idx, logit
 
 
@@ -340,7 +378,7 @@ def fwd(sets, i, M, ws, idx, logit):
 def time_graph(sets, M, steps, warmup, dist=None):
     """Mean device time per forward: one CUDA graph per input set, replayed alternately."""
     import torch
-    ws, idx, logit = make_outputs(M, sets[0].x.device)
+    ws, idx, logit = make_outputs(M, sets[0].x.device, s=sets[0])
     for i in range(warmup):
         fwd(sets, i, M, ws, idx, logit)
     torch.cuda.synchronize()
@@ -376,7 +414,7 @@ def time_stages(sets, M, steps):
     """Per-stage device time (CUDA events at the stage boundaries, on the launch stream)."""
     import torch
     import quantised_speculative_draft_gb300 as dh
-    ws, idx, logit = make_outputs(M, sets[0].x.device)
+    ws, idx, logit = make_outputs(M, sets[0].x.device, s=sets[0])
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(dh.NUM_STAGE_EVENTS)]
            for _ in range(steps)]
     for row in evs:          # torch creates the CUDA event on its first record
@@ -426,6 +464,38 @@ def time_e2e(sets, M, steps):
     return e0.elapsed_time(e1) * 1e3 / steps, M * H_FULL * 2, M * TOPK * 8
 
 
+def exact_topk_ids(x, W, k):
+    """The stock bf16 head's top-k ids per row (value descending, ties to the lower id), from
+    dh_rerank over every vocabulary row: the exact logits x . W[n] for all n.  Not timed."""
+    import numpy as np
+    import torch
+    import quantised_speculative_draft_gb300 as dh
+    M, V = x.shape[0], W.shape[0]
+    ids = torch.arange(V, dtype=torch.int32, device=x.device).repeat(M, 1).contiguous()
+    ex = torch.empty(M, V, dtype=torch.float32, device=x.device)
+    dh.dh_rerank(x, W, ids, ex)
+    e = ex.cpu().numpy()
+    del ids, ex
+    return np.stack([np.argsort(-e[m], kind="stable")[:k] for m in range(M)])
+
+
+def recall(s, M):
+    """Recall of dh_forward on the first M rows of input set s against the exact bf16 head:
+    the fraction of rows whose argmax matches (top-k = 1), else the mean |returned ∩ exact
+    top-k| / k."""
+    import torch
+    import quantised_speculative_draft_gb300 as dh
+    ws, idx, logit = make_outputs(M, s.x.device, s=s)
+    s.call(M, ws, idx, logit)
+    torch.cuda.synchronize()
+    assert dh.dh_device_status(reset=True) == 0, "a device-side wait timed out"
+    got = idx.cpu().numpy()
+    k = got.shape[1]
+    ref = exact_topk_ids(s.x[:M], s.W, k)
+    hits = [len(set(got[m].tolist()) & set(ref[m].tolist())) / k for m in range(M)]
+    return round(sum(hits) / M, 4)
+
+
 def time_quantize(dev):
     """dh_quantize on the one-shard head (124160 x 5120 bf16) and on the full head."""
     import torch
@@ -455,23 +525,24 @@ def time_quantize(dev):
     return out
 
 
-def roofline_entry(M, coarse_us, hbm, tflops, src):
-    """Roofline of the coarse kernel: the bound is whichever of the weight stream (bytes at the
-    measured copy bandwidth) and the contraction (2 M H V flops at the e4m3 tensor peak, taken
-    as the measured bf16 peak x 2, the nominal fp8/bf16 ratio) takes longer."""
-    nbytes = algorithmic_bytes(V_FULL, H_FULL)
-    flops = 2 * M * H_FULL * V_FULL
-    fp8_peak = 2.0 * tflops
+def roofline_entry(M, coarse_us, hbm, tflops, src, V=V_FULL, H=H_FULL):
+    """Roofline of the coarse kernel.  The bound is whichever of the weight stream (the
+    algorithmic bytes at the measured copy bandwidth) and the contraction (2 M H V flops at the
+    measured dense bf16 tensor peak, the head's own operand type) takes longer: the weight
+    stream up to M = 32 on the full head, the contraction from M = 64."""
+    nbytes = algorithmic_bytes(V, H)
+    flops = 2 * M * H * V
     gbs = nbytes / coarse_us / 1e3
     tfs = flops / coarse_us / 1e6
     t_hbm = nbytes / (hbm * 1e3)          # us
-    t_tc = flops / (fp8_peak * 1e6)       # us
+    t_tc = flops / (tflops * 1e6)         # us
     if t_hbm >= t_tc:
         return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(gbs / hbm, 4), "peak_source": src, "bytes_per_launch": nbytes}
-    return {"bound": "tensor", "achieved": round(tfs, 1), "peak": round(fp8_peak, 1),
-            "unit": "TFLOP/s", "frac": round(tfs / fp8_peak, 4),
-            "peak_source": src + " bf16 x 2 (e4m3)", "flops_per_launch": flops}
+                "frac": round(gbs / hbm, 4), "peak_source": src + " HBM copy",
+                "bytes_per_launch": nbytes}
+    return {"bound": "tensor", "achieved": round(tfs, 1), "peak": round(tflops, 1),
+            "unit": "TFLOP/s", "frac": round(tfs / tflops, 4),
+            "peak_source": src + " dense bf16 (burst)", "flops_per_launch": flops}
 
 
 def traffic_from_profile(M):
@@ -489,6 +560,14 @@ def traffic_from_profile(M):
     if h.hexdigest() != rec.get("sha256"):
         return None
     return rec.get("traffic_per_launch", {}).get(str(M))
+
+
+def workload_config(M, world):
+    """The `config` object of both arms' JSON lines (identical for the same run)."""
+    return {"workload": f"full-vocab head M={M} (V={V_FULL}, H={H_FULL}, KCAND={KCAND}, "
+                        f"RERANK={RERANK}, argmax)",
+            "M": M, "H": H_FULL, "V": V_FULL, "kcand": KCAND, "rerank": RERANK, "topk": TOPK,
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def cpu_oracle_sample(xb, packed, S, ZS, Wb, M, frac_den):
@@ -573,6 +652,11 @@ def run_ours(args):
                           "roofline": {"bound": r["bound"], "frac": r["frac"]},
                           "stages_us": {k: round(v, 2) for k, v in st.items()}})
 
+    rec = {}
+    if rank == 0 and not args.no_recall:
+        rec["full_head_M%d_argmax" % M] = recall(sets[0], M)
+        rec["full_head_M72_argmax"] = recall(sets[0], 72)
+
     cpu_inputs = host_copies(sets) if rank == 0 and world == 1 and not args.no_cpu_baseline \
         else None
     pack = time_quantize(dev) if rank == 0 else None
@@ -587,11 +671,49 @@ def run_ours(args):
             msh, _, _ = time_graph(sets_sh, m, args.sweep_steps, 5)  # full-head workspace suffices
             stsh = time_stages(sets_sh, m, 20)
             nb_sh = algorithmic_bytes(V_SH, H_FULL)
+            rsh = roofline_entry(m, stsh["coarse"], hbm, tfl, src, V=V_SH)
             shard[f"M{m}"] = {"us_per_call": round(msh * 1e3 / args.sweep_steps, 2),
                               "coarse_us": round(stsh["coarse"], 2),
                               "coarse_frac_of_hbm": round(nb_sh / stsh["coarse"] / 1e3 / hbm, 4),
+                              "roofline": {"bound": rsh["bound"], "frac": rsh["frac"]},
                               "stages_us": {k: round(v, 2) for k, v in stsh.items()}}
+            if not args.no_recall:
+                rec[f"one_shard_head_M{m}_argmax"] = recall(sets_sh[0], m)
         del sets_sh
+
+    topk_caller = None
+    if rank == 0 and not args.no_topk:
+        from quantised_speculative_draft_gb300 import synth
+        topk_caller = {}
+        for R in (32, 64):
+            wl = synth.topk_caller(R)
+            sets_tk = [WlInputs(wl, seed, dev) for seed in range(args.sets)]
+            mtk, _, _ = time_graph(sets_tk, wl.M, args.sweep_steps, 5)
+            sttk = time_stages(sets_tk, wl.M, 20)
+            topk_caller[f"R{R}"] = {
+                "workload": f"top-k caller: M={wl.M}, V={wl.V}, H={wl.H}, top-{wl.topk}, "
+                            f"RERANK={R}, KCAND={wl.kcand}; {wl.hot_rows} rows at "
+                            f"{wl.hot_scale}x norm",
+                "us_per_call": round(mtk * 1e3 / args.sweep_steps, 2),
+                "coarse_us": round(sttk["coarse"], 2),
+                "stages_us": {k: round(v, 2) for k, v in sttk.items()}}
+            if not args.no_recall:
+                rec[f"topk_caller_R{R}_top{wl.topk}"] = recall(sets_tk[0], wl.M)
+            del sets_tk
+        torch.cuda.empty_cache()
+
+    tiny = None
+    if rank == 0 and not args.no_tiny:
+        from quantised_speculative_draft_gb300 import synth
+        wl = synth.tiny(1)
+        sets_t = [WlInputs(wl, seed, dev) for seed in range(args.sets)]
+        mt, _, _ = time_graph(sets_t, 1, args.sweep_steps, 5)
+        stt = time_stages(sets_t, 1, 20)
+        tiny = {"workload": f"tiny head: M=1, H={wl.H}, V={wl.V}, KCAND={wl.kcand}, "
+                            f"RERANK={wl.rerank}, argmax (its 2.4 MB of weights stay in L2)",
+                "us_per_call": round(mt * 1e3 / args.sweep_steps, 2),
+                "stages_us": {k: round(v, 2) for k, v in stt.items()}}
+        del sets_t
 
     fp8 = None
     if rank == 0 and not args.no_fp8:
@@ -694,18 +816,20 @@ def run_ours(args):
             "metric": METRIC, "value": round(us_per_call / (world if world > 1 else 1), 3),
             "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms / args.steps, 6), "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-            "dtype_detail": "coarse pass: e4m3 tensor-core operands (exact 2-bit codes and an "
-                            "exact two-term split of the bf16 x), fp32 accumulation; rerank: "
-                            "bf16 x and W, fp32 products summed in fp64",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 x e4m3 -> fp32 (coarse); bf16 -> fp32/fp64 (rerank)",
+            "dtype_detail": "coarse pass: tcgen05 kind::f8f6f4 MMAs with fp32 accumulation; "
+                            "each 2-bit code masked in place is an exact e4m3 weight, and each "
+                            "bf16 x row is staged as 2 or 3 e4m3 terms (row scale 2^e, per-row "
+                            "term shifts), the third only for rows whose two-term residual "
+                            "sum |r2| exceeds 2^-20 sum |x|; ordinary rows are represented "
+                            "exactly except elements ~14+ binades below the row maximum. "
+                            "Rerank: bf16 x and W, exact fp32 products summed in fp64",
             "data": "synthetic (seeded normal x and W with hot rows; no trained weights)",
-            "config": {"workload": f"full-vocab head M={M} (V={V_FULL}, H={H_FULL}, "
-                                   f"KCAND={KCAND}, RERANK={RERANK}, argmax)",
-                       "M": M, "H": H_FULL, "V": V_FULL, "kcand": KCAND, "rerank": RERANK,
-                       "topk": TOPK, "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": "two resident input sets of 2.9 GB alternate between steps "
+            "config": workload_config(M, world),
+            "timing": {"l2": "two resident input sets of 2.9 GB alternate between steps "
                              "(inputs larger than L2, no flush)",
-                       "timing": "CUDA graph per input set, replayed back to back; CUDA events"},
+                       "method": "CUDA graph per input set, replayed back to back; CUDA events"},
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -714,7 +838,10 @@ def run_ours(args):
             "clocks": clocks,
             "stages_us": {k: round(v, 2) for k, v in stages.items()},
             "pack": pack,
+            "recall_vs_exact_bf16": rec or None,
             "one_shard_head": shard,
+            "topk_caller": topk_caller,
+            "tiny_head": tiny,
             "fp8_head": fp8,
             "int4_head": int4,
             "ablations": abl,
@@ -765,10 +892,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"full-vocab head M={M} (V={V_FULL}, H={H_FULL}, KCAND={KCAND}, "
-                               f"RERANK={RERANK}, argmax)",
-                   "M": M, "H": H_FULL, "V": V_FULL, "kcand": KCAND, "rerank": RERANK,
-                   "topk": TOPK},
+        "config": workload_config(M, world),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": orc.default_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,

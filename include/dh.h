@@ -203,6 +203,22 @@ const char *dh_last_error(void);
 int dh_version(void);
 
 /*
+ * dh_rerank -- the exact step alone: exact[m, j] = sum_k x[m, k] W[idx[m, j], k] for arbitrary
+ * index lists, the same dot product (and bits) as the rerank inside dh_forward.
+ * Page: radiance_drafthead.py, _rerank_exact (bf16 branch).  With idx[m, :] = 0 .. V-1 it is
+ * the stock bf16 head over the whole vocabulary (for recall measurements).
+ *   x      [M, H]  bf16, 16-byte aligned                                      (input)
+ *   W_bf16 [V, H]  bf16 head rows, 16-byte aligned                            (input)
+ *   idx    [M, n]  int32 row ids; an id outside [0, V) gives -inf                (input)
+ *   exact  [M, n]  fp32 exact logits                                         (output)
+ * 1 <= M <= 128, H a positive multiple of 512, V >= 1, n >= 1, M n < 2^31.  Stream-ordered on
+ * `stream`, no allocation, no synchronisation.  DH_ERR_NULL / DH_ERR_SHAPE / DH_ERR_ALIGN /
+ * DH_ERR_CUDA as dh_forward.
+ */
+int dh_rerank(const uint16_t *x, const uint16_t *W_bf16, int M, int H, int V, const int32_t *idx,
+              long long n, float *exact, void *stream);
+
+/*
  * Vocabulary-parallel head: each rank holds rows [vocab_offset, vocab_offset + Vs) of the
  * head (its own packed/S/ZS and bf16 rows) and the result equals the unsharded dh_forward bit
  * for bit.  The pages deploy the head as per-rank vocabulary shards

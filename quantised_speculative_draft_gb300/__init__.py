@@ -22,7 +22,7 @@ __all__ = [
     "dh_forward_timed", "dh_set_coarse_path", "dh_coarse_path_for", "dh_device_status",
     "dh_forward_launch_count", "dh_forward_noalloc", "NOALLOC_WORKSPACE_BYTES",
     "dh_last_error", "dh_version", "DraftHead", "dh_shard_candidates",
-    "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_shard_topk", "dh_quantize_fp8",
+    "dh_shard_rerank_workspace_bytes", "dh_shard_rerank", "dh_rerank", "dh_shard_topk", "dh_quantize_fp8",
     "dh_forward_fp8w", "dh_quantize4", "dh_forward4", "dh_forward4_debug", "dh_forward4_timed",
     "dh_quantize_c4", "dh_forward_c4_debug", "dh_quantize_g64", "dh_forward_g64_debug",
     "dh_forward_wside_debug",
@@ -96,6 +96,8 @@ def _load():
         lib.dh_shard_rerank.argtypes = [P, P, I, I, I, L, P, P, L, I, P, P, P, S, P]
         lib.dh_shard_rerank.restype = I
         lib.dh_shard_topk.argtypes = [P, P, I, I, I, I, P, P, P]
+        lib.dh_rerank.restype = I
+        lib.dh_rerank.argtypes = [P, P, I, I, I, P, L, P, P]
         lib.dh_shard_topk.restype = I
         lib.dh_quantize_fp8.argtypes = [P, P, I, I, P, P, P, P]
         lib.dh_quantize_fp8.restype = I
@@ -327,6 +329,13 @@ def dh_shard_rerank(x, W_shard, vocab_offset, all_val, all_idx, rerank, sel_idx,
     _check(_load().dh_shard_rerank(_p(x), _p(W_shard), M, H, Vs, int(vocab_offset), _p(all_val),
                                    _p(all_idx), all_val.shape[1], rerank, _p(sel_idx), _p(exact),
                                    _p(workspace), nbytes, _stream(stream)))
+
+
+def dh_rerank(x, W, idx, exact, stream=None):
+    """Exact logits exact[m, j] = x[m] . W[idx[m, j]] (int32 ids; outside [0, V) -> -inf)."""
+    M, H = x.shape
+    _check(_load().dh_rerank(_p(x), _p(W), M, H, W.shape[0], _p(idx), idx.shape[1], _p(exact),
+                             _stream(stream)))
 
 
 def dh_shard_topk(exact_parts, sel_idx, topk, idx, logit, stream=None):

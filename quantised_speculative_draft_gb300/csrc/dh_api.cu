@@ -705,6 +705,26 @@ size_t dh_shard_rerank_workspace_bytes(int M, long long ncand_all, int rerank)
     return 4 * align256(static_cast<size_t>(entries) * 4) + align256(kNumCounters * 4);
 }
 
+int dh_rerank(const uint16_t *x, const uint16_t *W_bf16, int M, int H, int V, const int32_t *idx,
+              long long n, float *exact, void *stream)
+{
+    if (!x || !W_bf16 || !idx || !exact) return fail(DH_ERR_NULL, "a required pointer is NULL");
+    if (M < 1 || M > kMaxM) return fail(DH_ERR_SHAPE, "M=%d outside [1, %d]", M, kMaxM);
+    if (H <= 0 || H % 512 != 0)
+        return fail(DH_ERR_SHAPE, "H=%d is not a positive multiple of 512", H);
+    if (V < 1) return fail(DH_ERR_SHAPE, "V=%d must be >= 1", V);
+    if (n < 1 || n * M > 0x7FFFFFFFLL)
+        return fail(DH_ERR_SHAPE, "n=%lld: need 1 <= n and M n < 2^31", n);
+    const void *ptrs[] = {x, W_bf16};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(DH_ERR_ALIGN, "pointer %p is not 16-byte aligned", p);
+    cudaError_t err = launch_rerank_topk(x, W_bf16, nullptr, M, H, V, idx, static_cast<int>(n),
+                                         exact, nullptr, 0, nullptr, nullptr, 0,
+                                         static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));
+    return ok();
+}
+
 int dh_shard_rerank(const uint16_t *x, const uint16_t *W_shard, int M, int H, int Vs,
                     long long vocab_offset, const float *all_val, const int32_t *all_idx,
                     long long ncand_all, int rerank, int32_t *sel_idx, float *exact,

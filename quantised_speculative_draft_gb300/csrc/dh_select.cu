@@ -552,11 +552,14 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
         double t = 0.0;
         for (int i = 0; i < kRerankThreads / 32; ++i) t += part[i];
         ex[pair] = (n >= 0 && n < V) ? static_cast<float>(t) : -INFINITY;
-        __threadfence();
-        s_last = atomicAdd(&row_done[m], 1) == R - 1;
+        s_last = 0;
+        if (topk > 0) { // only a top-k that follows needs to know which CTA finished last
+            __threadfence();
+            s_last = atomicAdd(&row_done[m], 1) == R - 1;
+        }
     }
     __syncthreads();
-    if (!s_last || topk == 0) return;
+    if (!s_last) return;
     __threadfence();
 
     // this CTA finished row m last: top-k of its R reranked entries (bitonic, descending)

@@ -194,19 +194,40 @@ def check_result(gpu, ref, kcand, topk, x_bits, W_bits, rerank_fn=None):
     return ties
 
 
+_ORACLE_FWD = {4: orc.forward4, "c4": orc.forward_c4, "g64": orc.forward_g64,
+               "wside": orc.forward_wside}
+
+
+def _apply_checks(gpu, ref, xb, Wb, kcand, rerank, topk, V):
+    rep = {}
+    rep["coarse_worst"] = check_coarse(gpu["coarse"], ref["coarse"])
+    tb = check_block_candidates(gpu, ref, kcand, V)
+    rep["tie_blocks"] = len(tb)
+    rep["tie_sel_rows"] = check_selection(gpu, ref, rerank, tb)
+    rep["exact_worst"] = check_exact_values(gpu, xb, Wb)
+    rep["ties"] = check_result(gpu, ref, kcand, topk, xb, Wb)
+    return rep
+
+
 def full_compare(x, W, packed, S, ZS, kcand, rerank, topk, path=None, bits=2):
     """Run GPU and oracle on the same tensors and apply every check.  Returns a report."""
     gpu = gpu_forward(x, packed, S, ZS, W, kcand, rerank, topk, path=path, bits=bits)
     xb, Wb = host(x), host(W)
     pb, Sb, ZSb = host(packed), host(S), host(ZS)
-    ref_fwd = {4: orc.forward4, "c4": orc.forward_c4, "g64": orc.forward_g64,
-               "wside": orc.forward_wside}.get(bits, orc.forward)
-    ref = ref_fwd(xb, pb, Sb, ZSb, Wb, kcand, rerank, topk)
-    rep = {}
-    rep["coarse_worst"] = check_coarse(gpu["coarse"], ref["coarse"])
-    tb = check_block_candidates(gpu, ref, kcand, W.shape[0])
-    rep["tie_blocks"] = len(tb)
-    rep["tie_sel_rows"] = check_selection(gpu, ref, rerank, tb)
-    rep["exact_worst"] = check_exact_values(gpu, xb, Wb)
-    rep["ties"] = check_result(gpu, ref, kcand, topk, xb, Wb)
+    ref = _ORACLE_FWD.get(bits, orc.forward)(xb, pb, Sb, ZSb, Wb, kcand, rerank, topk)
+    rep = _apply_checks(gpu, ref, xb, Wb, kcand, rerank, topk, W.shape[0])
     return rep, gpu, ref
+
+
+def rows_compare(gpu, rows, x, W, packed, S, ZS, kcand, rerank, topk, bits=2):
+    """Every check of full_compare on a subset of the batch rows: the oracle runs the whole
+    path (all V coarse values, both selections, the rerank) for x[rows] only, and the GPU's
+    outputs for those rows -- taken from a launch over the whole batch -- are judged against
+    it.  For workloads too large for the oracle to run on every row in seconds."""
+    rows = np.asarray(rows)
+    sub = {k: v[rows] for k, v in gpu.items()}
+    xb, Wb = host(x)[rows], host(W)
+    pb, Sb, ZSb = host(packed), host(S), host(ZS)
+    ref = _ORACLE_FWD.get(bits, orc.forward)(xb, pb, Sb, ZSb, Wb, kcand, rerank, topk)
+    rep = _apply_checks(sub, ref, xb, Wb, kcand, rerank, topk, W.shape[0])
+    return rep, ref

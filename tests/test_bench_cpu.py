@@ -17,14 +17,21 @@ def test_algorithmic_bytes_of_the_full_and_shard_heads():
 
 
 def test_roofline_entry_picks_the_longer_bound():
-    # M=16: the weight stream (357.6 MB at 6780 GB/s = 52.7 us) dwarfs 41 GFLOP at e4m3 rates
-    r = bench.roofline_entry(16, 110.8, 6780.0, 2000.0, "measured")
+    # M=16: the weight stream (357.6 MB at 6780 GB/s = 52.7 us) dwarfs 40.7 GFLOP at the bf16 peak
+    r = bench.roofline_entry(16, 110.8, 6780.0, 1928.0, "measured")
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert abs(r["achieved"] - 357_580_800 / 110.8 / 1e3) < 0.1
     assert abs(r["frac"] - r["achieved"] / 6780.0) < 1e-4
-    # with a tensor peak 100x lower the contraction becomes the bound
-    r = bench.roofline_entry(72, 430.0, 6780.0, 20.0, "measured")
-    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 40.0
+    # M=32 is still the weight stream's (81.4 GFLOP / 1928 TF/s = 42.2 us < 52.7 us) ...
+    assert bench.roofline_entry(32, 160.0, 6780.0, 1928.0, "measured")["bound"] == "hbm"
+    # ... and M=64 the contraction's, against the bf16 peak itself (162.7 GFLOP -> 84.4 us)
+    r = bench.roofline_entry(64, 320.0, 6780.0, 1928.0, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1928.0
+    assert abs(r["achieved"] - 2 * 64 * 5120 * 248320 / 320.0 / 1e6) < 0.1
+    assert abs(r["frac"] - r["achieved"] / 1928.0) < 1e-4
+    # the one-shard head: half the bytes and flops
+    r = bench.roofline_entry(16, 60.0, 6780.0, 1928.0, "measured", V=124160)
+    assert r["bytes_per_launch"] == 178_790_400
 
 
 def test_recorded_traffic_is_dropped_once_a_source_changes(tmp_path, monkeypatch):

@@ -10,7 +10,7 @@ import quantised_speculative_draft_gb300 as dh
 from quantised_speculative_draft_gb300 import synth
 from oracle import oracle as orc
 
-from parity import full_compare, host
+from parity import full_compare, gpu_forward, host, check_coarse, rows_compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -55,6 +55,7 @@ def test_quantize4_bit_exact(V, H):
     (32, 5120, 4096, 1, 32, 1),           # two launches of 16 rows
     (33, 1536, 6144, 4, 24, 5),           # three batch chunks (16 + 16 + 1 rows)
     (64, 1024, 4096, 8, 64, 16),          # RERANK 64, top-16
+    (16, 5120, 40000 + 37, 1, 32, 1),     # 313 tiles of 128 rows: every CTA runs two or more
 ])
 def test_forward4_matches_the_oracle(M, H, V, kcand, R, k):
     wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
@@ -103,3 +104,22 @@ def test_draft_head_class_builds_the_4bit_head():
     torch.cuda.synchronize()
     assert torch.equal(head.packed, packed)
     assert torch.equal(idx, i2) and torch.equal(logit, l2)
+
+
+def test_forward4_full_head_sampled():
+    """The 4-bit head at full size (M=16, H=5120, V=248320, KCAND 1): coarse values of 2000
+    sampled vocabulary rows (plus every reranked one and the last) for the whole batch against
+    the oracle's 4-bit coarse value, then three whole batch rows through the oracle's path."""
+    wl = synth.full(16)
+    x, W = synth.make_x(wl, 0, DEV), synth.make_w(wl, 0, DEV)
+    packed, S, ZS = _quantize4(W)
+    gpu = gpu_forward(x, packed, S, ZS, W, 1, 32, 1, bits=4)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([rng.choice(wl.V, 2000, replace=False),
+                                     gpu["sel_idx"].ravel(), [wl.V - 1]]))
+    rows_t = torch.from_numpy(rows).to(DEV)
+    ref_c = orc.coarse4(host(x), host(packed[rows_t]), host(S[rows_t]), host(ZS[rows_t]))
+    worst = check_coarse(gpu["coarse"][:, rows], ref_c)
+    rep, _ = rows_compare(gpu, [0, 7, 15], x, W, packed, S, ZS, 1, 32, 1, bits=4)
+    print("4-bit full head: sampled coarse worst", worst, "rows", rep["coarse_worst"],
+          "tie rows", len(rep["ties"]))

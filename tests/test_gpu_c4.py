@@ -48,6 +48,7 @@ def test_quantize_c4_bit_exact(V, H):
     (1, 1024, 8192, 8, 32, 1),
     (16, 5120, 12288 + 37, 8, 32, 4),     # ragged tail block
     (33, 1536, 6144, 4, 24, 5),           # two batch chunks (32 + 16 rows)
+    (16, 5120, 40000 + 37, 8, 32, 1),     # 313 tiles of 128 rows: every CTA runs two or more
 ])
 def test_forward_c4_matches_the_oracle_and_the_quarter_split(M, H, V, kcand, R, k):
     wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)

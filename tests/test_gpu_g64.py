@@ -47,6 +47,7 @@ def test_quantize_g64_bit_exact(V, H):
     (1, 1024, 8192, 8, 32, 1),
     (5, 1024, 8192 + 37, 8, 32, 4),       # ragged tail block
     (16, 5120, 12288, 8, 32, 1),
+    (16, 5120, 40000 + 37, 8, 32, 1),     # 313 tiles of 128 rows: every CTA runs two or more
 ])
 def test_forward_g64_matches_the_oracle(M, H, V, kcand, R, k):
     wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)

@@ -9,7 +9,7 @@ import quantised_speculative_draft_gb300 as dh
 from quantised_speculative_draft_gb300 import synth
 from oracle import oracle as orc
 
-from parity import full_compare, gpu_forward, gpu_quantize, host, check_coarse
+from parity import full_compare, gpu_forward, gpu_quantize, host, check_coarse, rows_compare
 
 pytestmark = pytest.mark.gpu
 
@@ -211,6 +211,18 @@ def test_forward_topk_caller_full_vocab(rerank):
     print(f"top-16 recall vs exact bf16 head at RERANK={rerank}: {rec:.3f}")
 
 
+def test_forward_full_head_m16_full_compare():
+    """The headline workload whole: M=16, H=5120, V=248320, KCAND 8, RERANK 32, argmax, on the
+    default coarse path; every coarse value, both selections and the result against the
+    oracle."""
+    wl = synth.full(16)
+    x, W = synth.make_x(wl, 0, DEV), synth.make_w(wl, 0, DEV)
+    packed, S, ZS = gpu_quantize(W)
+    rep, gpu, ref = full_compare(x, W, packed, S, ZS, 8, 32, 1)
+    print("full M=16", rep["coarse_worst"], rep["exact_worst"], "tie rows", len(rep["ties"]),
+          "differing", sum(t[4] for t in rep["ties"]))
+
+
 @pytest.mark.parametrize("wl", [synth.full(72), synth.shard(64)],
                          ids=["full-vocab-M72", "one-shard-M64"])
 def test_forward_full_size_sampled(wl):
@@ -247,3 +259,42 @@ def test_forward_full_size_sampled(wl):
     for m in range(M):
         e, i = gpu["sel_exact"][m], gpu["sel_idx"][m]
         assert gpu["idx"][m, 0] == i[np.lexsort((i, -e))][0]
+    # four whole batch rows against the oracle's own path: all V coarse values, its block
+    # candidates and top-R selection (not the GPU's), the rerank and the argmax
+    sample = np.unique(np.linspace(0, M - 1, 4).astype(int))
+    rep, _ = rows_compare(gpu, sample, x, W, packed, S, ZS, 8, 32, 1)
+    print(wl.name, "rows", sample.tolist(), rep["coarse_worst"],
+          "tie rows", len(rep["ties"]))
+
+
+def test_rerank_entry_on_arbitrary_lists_and_the_whole_vocabulary():
+    """dh_rerank: exact logits of arbitrary id lists (repeats, out-of-range ids -> -inf), and
+    with every id of a ragged head it is the stock bf16 head, against the oracle."""
+    M, H, V = 5, 1536, 3000 + 17
+    x, W = _inputs(M, H, V, hot_rows=60, hot_scale=4.0)
+    xb, Wb = host(x), host(W)
+    rng = np.random.default_rng(3)
+    n = 77
+    ids = rng.integers(0, V, (M, n)).astype(np.int32)
+    ids[:, 5] = ids[:, 4]                       # a repeated id
+    ids[0, 10], ids[1, 11], ids[2, 12] = -1, V, 2 ** 31 - 1
+    idx = torch.from_numpy(ids).to(DEV)
+    ex = torch.full((M, n), float("nan"), dtype=torch.float32, device=DEV)
+    dh.dh_rerank(x, W, idx, ex)
+    torch.cuda.synchronize()
+    g = ex.cpu().numpy()
+    bad = (ids < 0) | (ids >= V)
+    assert np.isneginf(g[bad]).all()
+    e = orc.rerank(xb, Wb, np.where(bad, 0, ids))
+    tol = 1e-5 * np.maximum(np.abs(e), 1.0)
+    assert (np.abs(g - e)[~bad] <= tol[~bad]).all()
+    assert g[0, 5] == g[0, 4]
+    # the whole vocabulary: the exact bf16 head
+    full = torch.arange(V, dtype=torch.int32, device=DEV).repeat(M, 1).contiguous()
+    exf = torch.empty(M, V, dtype=torch.float32, device=DEV)
+    dh.dh_rerank(x, W, full, exf)
+    torch.cuda.synchronize()
+    ref = orc.exact_head(xb, Wb)
+    assert (np.abs(exf.cpu().numpy() - ref) <= 1e-5 * np.maximum(np.abs(ref), 1.0)).all()
+    with pytest.raises(dh.DHError):
+        dh.dh_rerank(x, W, full[:, :0], exf[:, :0])

@@ -1,13 +1,17 @@
 """Vocabulary-parallel head on one GPU: the head split into shards run one after another
 through the sharded entry points (dh_shard_candidates / dh_shard_rerank / dh_shard_topk), the
-exchanges done by stacking, must return exactly what the unsharded dh_forward returns."""
+exchanges done by stacking, must return exactly what the unsharded dh_forward returns, and
+that result is judged against the oracle by the rules in parity.py."""
 import pytest
 import torch
 
 import quantised_speculative_draft_gb300 as dh
 from quantised_speculative_draft_gb300 import synth
+from oracle import oracle as orc
 from quantised_speculative_draft_gb300.sharded import (DeviceShard, sharded_forward_sequential,
                                                        split_rows)
+
+from parity import check_result, host
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -49,6 +53,11 @@ def test_sequential_shards_equal_the_unsharded_forward(P, M, H, V, kcand, R, k):
     assert dh.dh_device_status(reset=True) == 0
     assert torch.equal(sidx, idx)
     assert torch.equal(slogit, logit)
+    xb, Wb = host(x), host(W)
+    ref = orc.forward(xb, host(packed), host(S), host(ZS), Wb, kcand, R, k)
+    ties = check_result({"idx": sidx.cpu().numpy(), "logit": slogit.cpu().numpy()}, ref,
+                        kcand, k, xb, Wb)
+    print("sharded", P, M, V, "tie rows", len(ties), "differing", sum(t[4] for t in ties))
 
 
 def test_shard_candidates_are_the_shard_slice_of_the_coarse_pass():

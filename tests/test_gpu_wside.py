@@ -26,6 +26,7 @@ def _build():
     (5, 1024, 8192 + 37, 8, 32, 4),       # ragged tail block
     (16, 5120, 12288, 8, 32, 1),
     (40, 1536, 6144, 4, 24, 5),           # N = 48 launch
+    (16, 5120, 40000 + 37, 8, 32, 1),     # 313 tiles of 128 rows: every CTA runs two or more
 ])
 def test_forward_wside_matches_the_oracle(M, H, V, kcand, R, k):
     wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)

@@ -7,7 +7,6 @@ already run every other test.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 import quantised_speculative_draft_gb300 as dh
@@ -65,7 +64,6 @@ def test_noalloc_matches_the_workspace_forward_on_two_calls():
         assert rc == 0, dh.dh_last_error()
         torch.cuda.synchronize()
         assert dh.dh_device_status(reset=True) == 0
+        # the same kernels on the same inputs: bit for bit, indices and logits
         assert torch.equal(idx, ridx)
-        r = rlogit.cpu().numpy()
-        g = logit.cpu().numpy()
-        assert (np.abs(g - r) <= 1e-5 * np.maximum(np.abs(r), 1.0)).all()
+        assert torch.equal(logit, rlogit)
