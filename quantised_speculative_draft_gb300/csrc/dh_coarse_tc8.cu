@@ -23,30 +23,33 @@
 //     with xs' the group sums of the represented x (in the scaled units): the scale and zero
 //     are applied to the fp32 partial of every group, never to the weight.
 //
-// Roles (22 or 18 warps, one CTA per SM, persistent over 128-row vocabulary tiles).  The unit of
+// Roles (23 or 19 warps, one CTA per SM, persistent over 128-row vocabulary tiles).  The unit of
 // handoff is a span (N = 32: the four planes of 512 k) or half a span (larger N: planes 2u,
-// 2u+1); unit q uses tensor-memory slot q % 2 (an A buffer and one accumulator per group).  A
-// thread issuing tcgen05.mma is held ~100 cycles per instruction, so each plane has its own
-// issuer warp: the four issuers of a span work at once, and each of them takes every unit
-// that holds its plane, in order (every barrier's phases are awaited in order).  Writing a
-// span's A buffer takes a dequant warp ~1000 cycles, so with one unit per span two sets of
-// dequant warps take alternate spans (each set owns one slot).
+// 2u+1); unit q uses tensor-memory slot q % 2 (an A buffer and one accumulator per group).
+// Issuing a tcgen05.mma holds the issuing warp for many cycles, so each plane has its own issuer
+// warp: the four issuers of a span work at once, each on its own SM sub-partition, and each of
+// them takes every unit that holds its plane, in order (every barrier's phases are awaited in
+// order).  With one unit per span two sets of dequant warps share each span's A buffer, which
+// halves the time a slot waits for its weights.
 //   warp 0        TMA: per span one [128 rows x 128 B] box of packed codes (two for the 4-bit
 //                 head) and four [128 k x N] boxes of the staged x terms (128-byte swizzle)
 //                 into a stage ring; per tile a bulk copy of the tile's S and ZS rows
 //                 (contiguous in memory) into a double-buffered shared copy for the epilogue
-//   warps 1, 3 and the last two   MMA issuers of planes 0..3: per unit 4 x tcgen05.mma kind::f8f6f4
-//                 (M = 128, K = 32) of their plane, one commit for the unit's accumulators and
-//                 one for the stage
-//   warp 2        block top-KCAND of the previous tile (overlaps the current one): one lane
-//                 per (batch column, block) pair keeps an insertion list of the best 8
+//   warps 1-3 and the one after the epilogue   MMA issuers of planes 0..3, a whole warp each
+//                 (one elected lane issues): per unit 4 x tcgen05.mma kind::f8f6f4 (M = 128,
+//                 K = 32) of their plane, one commit for the unit's accumulators and one for
+//                 the stage
 //   warps 4-11    dequant, two sets of four warps (one set where every launch body has two
-//                 units per span): one TMEM lane (= one vocabulary row) per thread, every plane
-//                 of the set's spans (tcgen05.st, one wait per unit)
+//                 units per span): one TMEM lane (= one vocabulary row) per thread; with two
+//                 sets, set c writes k half c of every plane (2-bit layouts) or planes 2c,
+//                 2c + 1 (4-bit head); a single set every plane (tcgen05.st, one wait per unit)
 //   next 8 warps  epilogue, two halves of four warps (one per TMEM lane quarter): half h folds
 //                 planes 2h, 2h+1 of every span -- tcgen05.ld of the partials, recombination of
 //                 the terms, scale/zero fold into fp32 registers -- and at the tile end writes its
 //                 half of the coarse values; the selection warp adds the halves
+//   last 2 warps  block top-KCAND of the previous tile (overlaps the current one): two lanes
+//                 per (batch column, block) pair each keep an insertion list of the best 8 of
+//                 their 32 rows, then merge
 // Every handoff is an mbarrier; every wait is bounded.
 //
 // The 4-bit head (BITS = 4, half split, bias 16; _quantize_head_now's 4-bit variant) runs the
@@ -59,6 +62,7 @@
 #include "dh_tcgen05.cuh"
 
 #include <climits>
+#include <type_traits>
 
 namespace dh {
 
@@ -72,21 +76,25 @@ constexpr int kSmemLimit8 = 232448;
 // The tile's coarse values for the selection warps: one 64-value block per (batch column,
 // block) pair, pairs kRedPitch floats apart (16-byte aligned, bank-conflict free per lane).
 constexpr int kRedPitch = 68;
-// Warp roles: 0 TMA, 2 selection, 4-7 the first dequant set (one warp per TMEM lane quarter),
-// then, for launches with one unit per span, the second dequant set (8-11); then the epilogue
-// (two halves of four warps) and the issuers of planes 2 and 3 (planes 0 and 1: warps 1, 3).
-// Launches that never use the second dequant set leave it out, for registers.
-constexpr int kWarpTma = 0, kWarpSel = 2, kWarpDq0 = 4;
+// Warp roles: 0 TMA, 1-3 the MMA issuers of planes 0-2, 4-7 the first dequant set (one warp per
+// TMEM lane quarter), then, for launches with one unit per span, the second dequant set (8-11);
+// then the epilogue (two halves of four warps), the issuer of plane 3 and the two selection
+// warps.
+// The four issuers sit on the four SM sub-partitions (warp % 4).  Launches that never use the
+// second dequant set leave it out, for registers.
+constexpr int kWarpTma = 0, kWarpDq0 = 4;
 constexpr int kDqWarps = 4; // warps of one dequant set
 constexpr int kEpWarps = 8; // two halves of four
 constexpr int kIssuers = 4; // one MMA issuer warp per plane
 template <bool kTwoSets> struct Roles {
     static constexpr int kEp0 = kTwoSets ? 12 : 8;           // first epilogue warp
-    static constexpr int kWarps = kEp0 + kEpWarps + 2;       // + the issuers of planes 2, 3
+    static constexpr int kSel0 = kEp0 + kEpWarps + 1;        // the two selection warps
+    static constexpr int kSel1 = kEp0 + kEpWarps + 2;
+    static constexpr int kWarps = kEp0 + kEpWarps + 3;       // + the plane-3 issuer, selection
     static constexpr int kThreads = 32 * kWarps;
     __device__ static int issuer_plane(int warp)
     {
-        return warp == 1 ? 0 : (warp == 3 ? 1 : (warp == kEp0 + 8 ? 2 : (warp == kEp0 + 9 ? 3 : -1)));
+        return (warp >= 1 && warp <= 3) ? warp - 1 : (warp == kEp0 + kEpWarps ? 3 : -1);
     }
 };
 
@@ -214,15 +222,34 @@ __device__ __forceinline__ void select_pairs(uint32_t (&k0)[NB], uint32_t (&k1)[
     }
 }
 
-// Block top-KCAND for KCAND <= 8, one lane per (batch column, block) pair: the lane walks the
-// block's 64 values (the sums of the two epilogue halves) in row order and keeps the 8 best in a
-// descending list.  A value enters only where it is strictly greater, so equal values keep the
-// lower row first; rows past the head hold -inf and never enter, leaving (-inf, -1) in unfilled
-// slots.  With `coarse` set it also writes the block's coarse values (rows below V).
-__device__ __forceinline__ void select_lane8(const float *vals0, const float *vals1, int base_row,
-                                             int V, int kcand, float *oval, int32_t *oidx,
-                                             float *coarse)
+// (va, ra) ranks above (vb, rb): larger value, equal values to the lower row (an empty slot,
+// row -1, loses every tie).
+__device__ __forceinline__ bool ranks_above(float va, int ra, float vb, int rb)
 {
+    return va > vb || (va == vb && static_cast<uint32_t>(ra) < static_cast<uint32_t>(rb));
+}
+
+__device__ __forceinline__ void cmp_swap(float (&v)[8], int (&r)[8], int a, int b)
+{
+    const bool sw = ranks_above(v[b], r[b], v[a], r[a]);
+    const float va = v[a], vb = v[b];
+    const int ra = r[a], rb = r[b];
+    v[a] = sw ? vb : va;
+    v[b] = sw ? va : vb;
+    r[a] = sw ? rb : ra;
+    r[b] = sw ? ra : rb;
+}
+
+// Block top-KCAND for KCAND <= 8, two lanes per (batch column, block) pair: lane 2i + h keeps the
+// best 8 of rows 32h .. 32h + 31 of its pair's block (insertion, as select_lane8), then lane 2i
+// merges the two lists: the best 8 of the 16 are the better of list[k] and partner[7 - k]
+// (a bitonic sequence), sorted by a bitonic merge.  Every lane of the warp takes part (shuffles);
+// `live` is false for lanes whose pair is past the batch or the head.
+__device__ __forceinline__ void select_pair2(bool live, const float *vals0, const float *vals1,
+                                             int base_row, int V, int kcand, float *oval,
+                                             int32_t *oidx, float *coarse, int lane)
+{
+    const int h = lane & 1;
     float v[8];
     int r[8];
 #pragma unroll
@@ -230,28 +257,50 @@ __device__ __forceinline__ void select_lane8(const float *vals0, const float *va
         v[k] = -INFINITY;
         r[k] = -1;
     }
+    if (live) {
 #pragma unroll 2
-    for (int j4 = 0; j4 < kBlockN / 4; ++j4) {
-        const float4 u0 = reinterpret_cast<const float4 *>(vals0)[j4];
-        const float4 u1 = reinterpret_cast<const float4 *>(vals1)[j4];
-        const float uu[4] = {u0.x + u1.x, u0.y + u1.y, u0.z + u1.z, u0.w + u1.w};
+        for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 u0 = reinterpret_cast<const float4 *>(vals0 + 32 * h)[j4];
+            const float4 u1 = reinterpret_cast<const float4 *>(vals1 + 32 * h)[j4];
+            const float uu[4] = {u0.x + u1.x, u0.y + u1.y, u0.z + u1.z, u0.w + u1.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float xv = uu[e];
-            const int row = base_row + 4 * j4 + e;
-            if (coarse && row < V) coarse[row] = xv;
-            bool c[8];
+            for (int e = 0; e < 4; ++e) {
+                const float xv = uu[e];
+                const int row = base_row + 32 * h + 4 * j4 + e;
+                if (coarse && row < V) coarse[row] = xv;
+                bool c[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) c[k] = xv > v[k];
-            // the list is descending, so c is false up to the insertion point, true after it
+                for (int k = 0; k < 8; ++k) c[k] = xv > v[k];
 #pragma unroll
-            for (int k = 7; k > 0; --k) {
-                v[k] = c[k] ? (c[k - 1] ? v[k - 1] : xv) : v[k];
-                r[k] = c[k] ? (c[k - 1] ? r[k - 1] : row) : r[k];
+                for (int k = 7; k > 0; --k) {
+                    v[k] = c[k] ? (c[k - 1] ? v[k - 1] : xv) : v[k];
+                    r[k] = c[k] ? (c[k - 1] ? r[k - 1] : row) : r[k];
+                }
+                v[0] = c[0] ? xv : v[0];
+                r[0] = c[0] ? row : r[0];
             }
-            v[0] = c[0] ? xv : v[0];
-            r[0] = c[0] ? row : r[0];
         }
+    }
+    float pv[8];
+    int pr[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        pv[k] = __shfl_xor_sync(0xffffffffu, v[k], 1);
+        pr[k] = __shfl_xor_sync(0xffffffffu, r[k], 1);
+    }
+    if (!live || h != 0) return;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (ranks_above(pv[7 - k], pr[7 - k], v[k], r[k])) {
+            v[k] = pv[7 - k];
+            r[k] = pr[7 - k];
+        }
+    }
+#pragma unroll
+    for (int s = 4; s > 0; s >>= 1) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if ((k & s) == 0) cmp_swap(v, r, k, k + s);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -277,7 +326,7 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
     constexpr int N = C::N, T = C::T, K = C::K, kU = C::kU, kPP = C::kPP;
     constexpr int kGU = kPP * kGPP;         // weight groups (accumulators) of a unit
     using R = Roles<two_sets<MP, PACK>()>;
-    constexpr int kDqSets = kU == 1 ? 2 : 1; // dequant warp sets (alternate spans)
+    constexpr int kDqSets = kU == 1 ? 2 : 1; // dequant warp sets (split each span's planes)
     static_assert(kDqSets == 1 || two_sets<MP, PACK>(), "a second dequant set needs its warps");
     constexpr int kWarpEp0 = R::kEp0;
     constexpr uint32_t kSlotCols = C::kSlotCols, kACols = C::kACols;
@@ -313,16 +362,16 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
         prefetch_tensormap(&tm_x);
         for (int i = 0; i < nstage; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kDqWarps + kIssuers); // one dequant set, each plane's issuer
+            mbar_init(&empty[i], kDqSets * kDqWarps + kIssuers); // dequant warps, issuers
         }
         for (int i = 0; i < K; ++i) {
-            mbar_init(&a_full[i], kDqWarps);
+            mbar_init(&a_full[i], kDqSets * kDqWarps);
             mbar_init(&d_full[i], kPP);     // one commit per plane of the unit
             mbar_init(&d_empty[i], kU == 1 ? 8 : 4); // the epilogue warps reading the unit
         }
         for (int i = 0; i < kIssuers; ++i) mbar_init(&fin[i], 1);
         mbar_init(red_full, kEpWarps);
-        mbar_init(red_free, 1);
+        mbar_init(red_free, 2); // both selection warps
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sz_full[i], 1);
             mbar_init(&sz_empty[i], kEpWarps);
@@ -352,7 +401,7 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            uint32_t s = 0, it = 0;
+            uint32_t st = 0, ph = 0, it = 0; // stage ring position and its phase parity
             for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
                 // the tile's S and ZS rows (contiguous in memory) into buffer it % 2, free once
                 // the epilogue finished tile it - 2; a partial last tile is read from global
@@ -371,9 +420,8 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
                 } else {
                     mbar_arrive(&sz_full[b]);
                 }
-                for (int span = 0; span < NG; ++span, ++s) {
-                    const uint32_t st = s % nstage;
-                    if (!mbar_wait_bounded(&empty[st], ((s / nstage) & 1u) ^ 1u, prm.timeout_flag)) {
+                for (int span = 0; span < NG; ++span) {
+                    if (!mbar_wait_bounded(&empty[st], ph ^ 1u, prm.timeout_flag)) {
                         failed = true;
                         break;
                     }
@@ -388,156 +436,181 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
                     for (int q = 0; q < 4; ++q)
                         tma_load_2d(stage + kBoxes * kPkBytes + q * (N * 128), &tm_x,
                                     plane_group<PACK>(q, span, NG) * kGroup, 0, &full[st]);
+                    if (++st == static_cast<uint32_t>(nstage)) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
         }
     } else if (R::issuer_plane(warp) >= 0) {
         // ---------------- MMA issuers: one warp per plane, every unit holding that plane ------
-        if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc_f8(N);
-            const int plane = R::issuer_plane(warp);
-            const int u = plane / kPP, g = plane % kPP; // the plane's unit in a span, and its place
-            uint32_t s = 0;
-            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
-                for (int span = 0; span < NG && !failed; ++span, ++s) {
-                    const uint32_t st = s % nstage;
-                    const uint32_t q = kU * s + u, slot = q % K, use = q / K;
-                    if (!mbar_wait_bounded(&full[st], (s / nstage) & 1u, prm.timeout_flag) ||
-                        !mbar_wait_bounded(&a_full[slot], use & 1u, prm.timeout_flag) ||
-                        !mbar_wait_bounded(&d_empty[slot], (use & 1u) ^ 1u, prm.timeout_flag)) {
-                        failed = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_tmem = tmem + slot * kSlotCols;
-                    const uint32_t d_tmem = a_tmem + kACols;
-                    // the descriptor's address field counts 16-byte units
-                    const uint64_t qdesc =
-                        sw128_desc(smem_u32(stages + static_cast<size_t>(st) * C::kStage +
-                                            kBoxes * kPkBytes)) +
-                        static_cast<uint64_t>(plane * (N * 128) / 16);
-                    // K = 32 per MMA: 128 / G groups of the plane, 4 / (128 / G) MMAs each into
-                    // the group's own accumulator
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        mma_ts_f8(d_tmem + (g * kGPP + i / (4 / kGPP)) * N, a_tmem + g * 32 + i * 8,
-                                  qdesc + static_cast<uint64_t>(i * 2), idesc,
-                                  (i % (4 / kGPP)) ? 1u : 0u);
-                    mma_commit(&d_full[slot]);
-                    mma_commit(&empty[st]);
-                }
-            }
-            mma_commit(&fin[plane]);
-            mbar_wait_bounded(&fin[plane], 0, prm.timeout_flag);
-        }
-    } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kDqWarps * kDqSets) {
-        // ---------------- dequant: one TMEM lane (= tile row) per thread, all four planes ------
-        // With one unit per span the two sets of four warps take alternate spans (span s uses
-        // slot s % 2, so each set owns one slot and stage parity); otherwise set 0 takes them all.
-        const int set = (warp - kWarpDq0) >> 2;
-        const int row = ((warp & 3) << 5) | lane;
-        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
-        uint32_t s = 0;
+        // The whole warp runs the loop (warp-uniform operands); one elected lane issues.
+        constexpr uint32_t idesc = make_idesc_f8(N);
+        const int plane = R::issuer_plane(warp);
+        const int u = plane / kPP, g = plane % kPP; // the plane's unit in a span, and its place
+        uint32_t st = 0, ph = 0, q = u;             // stage ring position, parity; unit index
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
-            for (int span = 0; span < NG; ++span, ++s) {
-                if (kDqSets == 2 && static_cast<int>(s & 1u) != set) continue;
-                const uint32_t st = s % nstage;
-                if (!warp_wait(&full[st], (s / nstage) & 1u, prm.timeout_flag)) {
+            for (int span = 0; span < NG && !failed; ++span, q += kU) {
+                const uint32_t slot = q % K, use = q / K;
+                if (!warp_wait(&full[st], ph, prm.timeout_flag) ||
+                    !warp_wait(&a_full[slot], use & 1u, prm.timeout_flag) ||
+                    !warp_wait(&d_empty[slot], (use & 1u) ^ 1u, prm.timeout_flag)) {
                     failed = true;
                     break;
                 }
-                const uint32_t pk =
-                    smem_u32(stages + static_cast<size_t>(st) * C::kStage) + row * kSpanBytes;
-                uint32_t w[32];
-                // this thread's row of packed box bx (128-byte swizzle)
-                auto load_box = [&](int bx) {
+                tc_fence_after();
+                const uint32_t a_tmem = tmem + slot * kSlotCols;
+                const uint32_t d_tmem = a_tmem + kACols;
+                // the descriptor's address field counts 16-byte units
+                const uint64_t qdesc =
+                    sw128_desc(smem_u32(stages + static_cast<size_t>(st) * C::kStage +
+                                        kBoxes * kPkBytes)) +
+                    static_cast<uint64_t>(plane * (N * 128) / 16);
+                // K = 32 per MMA: 128 / G groups of the plane, 4 / (128 / G) MMAs each into
+                // the group's own accumulator
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t addr = pk + bx * kPkBytes + ((c ^ (row & 7)) << 4);
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]),
-                                       "=r"(w[4 * c + 3])
-                                     : "r"(addr));
-                    }
-                };
-                if constexpr (BITS == 2) {
-                    // every plane of the span is in these 32 words: the stage goes back now
-                    load_box(0);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[st]);
+                for (int i = 0; i < 4; ++i)
+                    mma_ts_f8_elect(d_tmem + (g * kGPP + i / (4 / kGPP)) * N, a_tmem + g * 32 + i * 8,
+                                    qdesc + static_cast<uint64_t>(i * 2), idesc,
+                                    (i % (4 / kGPP)) ? 1u : 0u);
+                mma_commit_elect(&d_full[slot]);
+                mma_commit_elect(&empty[st]);
+                if (++st == static_cast<uint32_t>(nstage)) {
+                    st = 0;
+                    ph ^= 1u;
                 }
-                // the span's units: their planes into the A buffer of slot q % K, free once that
-                // slot's previous unit (q - K) has been accumulated
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const uint32_t q = kU * s + u, slot = q % K, use = q / K;
-                    if (use > 0 &&
-                        !warp_wait(&d_full[slot], (use - 1) & 1u, prm.timeout_flag)) {
+            }
+        }
+        mma_commit_elect(&fin[plane]);
+        warp_wait(&fin[plane], 0, prm.timeout_flag);
+    } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kDqWarps * kDqSets) {
+        // ---------------- dequant: one TMEM lane (= tile row) per thread ------------------------
+        // With one unit per span two sets of four warps share every span.  2-bit layouts: set c
+        // writes k half c (64 k) of every plane and reads only that half of the packed row; the
+        // 4-bit head: set c writes planes 2c, 2c + 1, the two nibbles of packed box c.  A single
+        // set writes every plane.
+        const int row = ((warp & 3) << 5) | lane;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        auto run = [&](auto set_c) {
+            constexpr int SET = decltype(set_c)::value;
+            constexpr bool kSplitK = kDqSets == 2 && BITS == 2;
+            constexpr bool kSplitP = kDqSets == 2 && BITS == 4;
+            constexpr int hf0 = kSplitK ? SET : 0, hf1 = kSplitK ? SET + 1 : 2;
+            constexpr int pp0 = kSplitP ? 2 * SET : 0, pp1 = kSplitP ? 2 * SET + 2 : kPP;
+            uint32_t s = 0, st = 0, ph = 0; // span count, stage ring position and parity
+            for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step) {
+                for (int span = 0; span < NG; ++span, ++s) {
+                    if (!warp_wait(&full[st], ph, prm.timeout_flag)) {
                         failed = true;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t abuf = tmem + lane_base + slot * kSlotCols;
-                    // planes kPP u .. kPP u + kPP - 1, two at a time, in halves of 16 columns
-                    // (64 k; a tcgen05.st reads its registers at issue: r0 and r1 are free
-                    // again after it)
+                    const uint32_t pk =
+                        smem_u32(stages + static_cast<size_t>(st) * C::kStage) + row * kSpanBytes;
+                    uint32_t w[32];
+                    // this thread's row of packed box bx (128-byte swizzle): the 16-byte chunks
+                    // holding this warp's k halves (chunk c is words 4c .. 4c + 3)
+                    auto load_box = [&](int bx) {
 #pragma unroll
-                    for (int pp = 0; pp < kPP; pp += 2) {
-                        const int plane = kPP * u + pp;
-                        // planes 2 bx, 2 bx + 1 of the 4-bit head are the two nibbles of box bx
-                        if constexpr (BITS == 4) load_box(plane >> 1);
+                        for (int c = 0; c < 8; ++c) {
+                            const int hc = PACK == kPackContig2 ? (c & 1) : (c >> 2);
+                            if (hc < hf0 || hc >= hf1) continue;
+                            const uint32_t addr = pk + bx * kPkBytes + ((c ^ (row & 7)) << 4);
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]),
+                                           "=r"(w[4 * c + 3])
+                                         : "r"(addr));
+                        }
+                    };
+                    if constexpr (BITS == 2) {
+                        // every plane of this warp's share is in these words: the stage goes back
+                        load_box(0);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[st]);
+                    }
+                    // the span's units: their planes into the A buffer of slot q % K, free once
+                    // that slot's previous unit (q - K) has been accumulated
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            uint32_t r0[16], r1[16];
-                            if constexpr (BITS == 4) {
+                    for (int u = 0; u < kU; ++u) {
+                        const uint32_t q = kU * s + u, slot = q % K, use = q / K;
+                        if (use > 0 &&
+                            !warp_wait(&d_full[slot], (use - 1) & 1u, prm.timeout_flag)) {
+                            failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t abuf = tmem + lane_base + slot * kSlotCols;
+                        // this warp's planes of the unit, two at a time, in halves of 16 columns
+                        // (64 k; a tcgen05.st reads its registers at issue: r0 and r1 are free
+                        // again after it)
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    r0[i] = deq_nib_lo(w[16 * hf + i]);
-                                    r1[i] = deq_nib_hi(w[16 * hf + i]);
-                                }
-                            } else if constexpr (PACK == kPackContig2) {
-                                // planes p, p + 1 are words 8p .. 8p + 15; half hf of plane p is
-                                // words 8p + 4 hf ..
+                        for (int pp = pp0; pp < pp1; pp += 2) {
+                            const int plane = kPP * u + pp;
+                            // planes 2 bx, 2 bx + 1 of the 4-bit head: the nibbles of box bx
+                            if constexpr (BITS == 4) load_box(plane >> 1);
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    uint32_t o0[4], o1[4];
-                                    deq_c4(w[8 * plane + 4 * hf + i], o0);
-                                    deq_c4(w[8 * plane + 8 + 4 * hf + i], o1);
+                            for (int hf = hf0; hf < hf1; ++hf) {
+                                uint32_t r0[16], r1[16];
+                                if constexpr (BITS == 4) {
 #pragma unroll
-                                    for (int b = 0; b < 4; ++b) {
-                                        r0[4 * i + b] = o0[b];
-                                        r1[4 * i + b] = o1[b];
+                                    for (int i = 0; i < 16; ++i) {
+                                        r0[i] = deq_nib_lo(w[16 * hf + i]);
+                                        r1[i] = deq_nib_hi(w[16 * hf + i]);
+                                    }
+                                } else if constexpr (PACK == kPackContig2) {
+                                    // planes p, p + 1 are words 8p .. 8p + 15; half hf of plane
+                                    // p is words 8p + 4 hf ..
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        uint32_t o0[4], o1[4];
+                                        deq_c4(w[8 * plane + 4 * hf + i], o0);
+                                        deq_c4(w[8 * plane + 8 + 4 * hf + i], o1);
+#pragma unroll
+                                        for (int b = 0; b < 4; ++b) {
+                                            r0[4 * i + b] = o0[b];
+                                            r1[4 * i + b] = o1[b];
+                                        }
+                                    }
+                                } else if (plane == 0) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) {
+                                        r0[i] = deq4_e4m3<0>(w[16 * hf + i]);
+                                        r1[i] = deq4_e4m3<1>(w[16 * hf + i]);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) {
+                                        r0[i] = deq4_e4m3<2>(w[16 * hf + i]);
+                                        r1[i] = deq4_e4m3<3>(w[16 * hf + i]);
                                     }
                                 }
-                            } else if (plane == 0) {
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    r0[i] = deq4_e4m3<0>(w[16 * hf + i]);
-                                    r1[i] = deq4_e4m3<1>(w[16 * hf + i]);
-                                }
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    r0[i] = deq4_e4m3<2>(w[16 * hf + i]);
-                                    r1[i] = deq4_e4m3<3>(w[16 * hf + i]);
-                                }
+                                tmem_st_x16(abuf + pp * 32 + 16 * hf, r0);
+                                tmem_st_x16(abuf + pp * 32 + 32 + 16 * hf, r1);
                             }
-                            tmem_st_x16(abuf + pp * 32 + 16 * hf, r0);
-                            tmem_st_x16(abuf + pp * 32 + 32 + 16 * hf, r1);
                         }
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&a_full[slot]);
                     }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_full[slot]);
-                }
-                if (failed) break;
-                if constexpr (BITS == 4) {
-                    // both boxes have been read into registers
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[st]);
+                    if (failed) break;
+                    if constexpr (BITS == 4) {
+                        // this warp's boxes have been read into registers
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[st]);
+                    }
+                    if (++st == static_cast<uint32_t>(nstage)) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
+        };
+        if constexpr (kDqSets == 2) {
+            if ((warp - kWarpDq0) >> 2) run(std::integral_constant<int, 1>{});
+            else run(std::integral_constant<int, 0>{});
+        } else {
+            run(std::integral_constant<int, 0>{});
         }
     } else if (warp >= kWarpEp0 && warp < kWarpEp0 + kEpWarps) {
         // ---------------- epilogue: two halves of four warps, each two groups of every span ---
@@ -561,9 +634,11 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
             const uint16_t *const sZ = sS + sz_bytes / 2;
             const uint16_t *const gS = prm.S + static_cast<long long>(row_ok ? grow : 0) * NGt;
             const uint16_t *const gZ = prm.ZS + static_cast<long long>(row_ok ? grow : 0) * NGt;
-            float acc[MP];
+            // the row's coarse values for batch rows 2i, 2i + 1 (packed fp32 pairs: one FFMA2
+            // folds two rows)
+            float2 acc2[MP / 2];
 #pragma unroll
-            for (int m = 0; m < MP; ++m) acc[m] = 0.f;
+            for (int i = 0; i < MP / 2; ++i) acc2[i] = make_float2(0.f, 0.f);
             for (int span = 0; span < NG; ++span, t += 4) {
                 // this half's groups: planes 2h, 2h+1, kGPP groups each
                 float s2[NGH], sz[NGH];
@@ -597,15 +672,14 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
                 // the half's first accumulator within the unit
                 const uint32_t dcol = tmem + lane_base + slot * kSlotCols + kACols +
                                       (kU == 1 ? 2 * h * kGPP : 0) * N;
-                // the half's NGH * CH chunks, one per tcgen05 wait (T * 16 registers)
+                // the half's NGH * CH chunks, one per tcgen05 wait (T * 16 registers, as packed
+                // pairs of batch rows)
 #pragma unroll
                 for (int k = 0; k < NGH * CH; ++k) {
                     const int gl = k / CH, c = k % CH;
-                    float v[T][16];
-#pragma unroll
-                    for (int tt = 0; tt < T; ++tt)
-                        tmem_ld_x16(dcol + gl * N + tt * MP + c * 16, v[tt]);
-                    tmem_wait_ld();
+                    uint64_t u[T][8];
+                    if constexpr (T == 3) tmem_ld_terms3(dcol + gl * N + c * 16, MP, u);
+                    else tmem_ld_terms2(dcol + gl * N + c * 16, MP, u);
                     if (k == NGH * CH - 1) {
                         // every partial of the unit is in registers: the slot goes back
                         tc_fence_before();
@@ -614,27 +688,28 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
                     }
                     const int gi = plane_group<PACK>(2 * h + gl / kGPP, span, NG) * kGPP + gl % kGPP;
                     const float4 *xg = reinterpret_cast<const float4 *>(xs_s + gi * MP);
+                    const float2 s2v = make_float2(s2[gl], s2[gl]), szv = make_float2(sz[gl], sz[gl]);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float4 x4 = xg[c * 4 + j];
-                        const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
                         const float4 a4 = reinterpret_cast<const float4 *>(tw_s)[c * 4 + j];
-                        const float w2[4] = {a4.x, a4.y, a4.z, a4.w};
-                        float w3[4] = {0.f, 0.f, 0.f, 0.f};
+                        const float2 xv[2] = {make_float2(x4.x, x4.y), make_float2(x4.z, x4.w)};
+                        const float2 w2[2] = {make_float2(a4.x, a4.y), make_float2(a4.z, a4.w)};
+                        float2 w3[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                         if constexpr (T == 3) {
                             const float4 b4 = reinterpret_cast<const float4 *>(tw_s + MP)[c * 4 + j];
-                            w3[0] = b4.x;
-                            w3[1] = b4.y;
-                            w3[2] = b4.z;
-                            w3[3] = b4.w;
+                            w3[0] = make_float2(b4.x, b4.y);
+                            w3[1] = make_float2(b4.z, b4.w);
                         }
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // the row's terms weighted by their powers of two (exact)
-                            float p = fmaf(w2[i], v[1][4 * j + i], v[0][4 * j + i]);
-                            if constexpr (T == 3) p = fmaf(w3[i], v[2][4 * j + i], p);
-                            const int m = c * 16 + 4 * j + i;
-                            acc[m] = fmaf(s2[gl], p, fmaf(sz[gl], xv[i], acc[m]));
+                        for (int i = 0; i < 2; ++i) {
+                            // batch rows m, m + 1: the terms weighted by their powers of two
+                            // (exact), then the scale and zero fold, two rows per instruction
+                            const int e = 2 * j + i; // pair within the chunk
+                            float2 p = __ffma2_rn(w2[i], pair_f2(u[1][e]), pair_f2(u[0][e]));
+                            if constexpr (T == 3) p = __ffma2_rn(w3[i], pair_f2(u[2][e]), p);
+                            const int mp = c * 8 + e;
+                            acc2[mp] = __ffma2_rn(s2v, p, __ffma2_rn(szv, xv[i], acc2[mp]));
                         }
                     }
                 }
@@ -650,14 +725,18 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
             }
             float *const rh = red + h * kRedHalf + (row >> 6) * kRedPitch + (row & 63);
 #pragma unroll
-            for (int m = 0; m < MP; ++m) rh[2 * m * kRedPitch] = row_ok ? acc[m] * inv_s[m] : -INFINITY;
+            for (int i = 0; i < MP / 2; ++i) {
+                rh[4 * i * kRedPitch] = row_ok ? acc2[i].x * inv_s[2 * i] : -INFINITY;
+                rh[(4 * i + 2) * kRedPitch] = row_ok ? acc2[i].y * inv_s[2 * i + 1] : -INFINITY;
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(red_full);
         }
-    } else if (warp == kWarpSel) {
+    } else if (warp == R::kSel0 || warp == R::kSel1) {
         // ---------------- block top-KCAND: pair = (batch column m, block b of the tile) ------
         // the tile's coarse values are the sums of the two epilogue halves (both -inf past V)
         const int npairs = 2 * prm.mrows;
+        const int sw = warp == R::kSel0 ? 0 : 1;
         uint32_t it = 0;
         for (int tile = first_tile; tile < prm.ntiles && !failed; tile += tile_step, ++it) {
             if (!warp_wait(red_full, it & 1u, prm.timeout_flag)) {
@@ -665,21 +744,23 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
                 break;
             }
             if (prm.kcand <= 8) {
-                // one lane per pair
-                for (int pidx = lane; pidx < npairs; pidx += 32) {
+                // two lanes per pair: selection warp sw takes pairs 16 sw .. 16 sw + 15 of
+                // every 32
+                for (int p0 = 0; p0 < npairs; p0 += 32) {
+                    const int pidx = p0 + 16 * sw + (lane >> 1);
                     const int m = pidx >> 1, blk = tile * 2 + (pidx & 1);
-                    if (static_cast<long long>(blk) * kBlockN < prm.V) {
-                        const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
-                                              static_cast<long long>(blk) * prm.kcand;
-                        float *const cdbg =
-                            prm.coarse ? prm.coarse + static_cast<long long>(prm.m0 + m) * prm.V
-                                       : nullptr;
-                        select_lane8(red + pidx * kRedPitch, red + kRedHalf + pidx * kRedPitch,
-                                     blk * kBlockN, prm.V, prm.kcand, prm.cand_val + off,
-                                     prm.cand_idx + off, cdbg);
-                    }
+                    const bool live = pidx < npairs && static_cast<long long>(blk) * kBlockN < prm.V;
+                    const long long off = static_cast<long long>(prm.m0 + m) * prm.ncand +
+                                          static_cast<long long>(blk) * prm.kcand;
+                    float *const cdbg = (prm.coarse && live)
+                                            ? prm.coarse + static_cast<long long>(prm.m0 + m) * prm.V
+                                            : nullptr;
+                    const int pp = live ? pidx : 0;
+                    select_pair2(live, red + pp * kRedPitch, red + kRedHalf + pp * kRedPitch,
+                                 blk * kBlockN, prm.V, prm.kcand, live ? prm.cand_val + off : nullptr,
+                                 live ? prm.cand_idx + off : nullptr, cdbg, lane);
                 }
-            } else {
+            } else if (sw == 0) {
                 // larger KCAND: four pairs at a time, one warp-wide round per entry
                 for (int p0 = 0; p0 < npairs; p0 += 4) {
                     uint32_t k0[4], k1[4];
@@ -748,8 +829,7 @@ size_t tc8_fixed_smem(int MP, int H, int G)
            3 * MP * 4 + 64 * 8 + 32;
 }
 
-// Stage count of a body: as many as fit (at most 6); even when two dequant sets alternate
-// spans, so that each stage's barriers always serve the same set.
+// Stage count of a body: as many as fit (at most 6).
 template <int MP, int PACK, int TT>
 int tc8_stages(int H)
 {
@@ -757,7 +837,6 @@ int tc8_stages(int H)
     const size_t fixed = tc8_fixed_smem(MP, H, C::G);
     long long n = (kSmemLimit8 - static_cast<long long>(fixed)) / C::kStage;
     if (n > 6) n = 6;
-    if (C::kU == 1) n &= ~1LL;
     return static_cast<int>(n);
 }
 

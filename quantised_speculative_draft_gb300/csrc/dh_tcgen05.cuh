@@ -50,6 +50,29 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
         : "memory");
 }
 
+// The same two instructions issued by one elected lane of a warp that runs the loop around them
+// together: the operands are warp-uniform, so the loop's arithmetic stays on the uniform
+// datapath and the instruction stream per MMA is short.
+__device__ __forceinline__ void mma_ts_f8_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_elect(uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_x64(uint32_t taddr, const uint32_t (&r)[64])
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"
@@ -91,6 +114,87 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// One 16-column chunk of each of T terms (term t at columns taddr + t * stride ..), read with T
+// tcgen05.ld and one wait in a single asm block, returned as packed pairs: u[t][i] holds
+// columns 2i, 2i + 1 of term t, ready as FFMA2 operands.
+__device__ __forceinline__ float2 pair_f2(uint64_t u)
+{
+    return make_float2(__uint_as_float(static_cast<uint32_t>(u)),
+                       __uint_as_float(static_cast<uint32_t>(u >> 32)));
+}
+
+__device__ __forceinline__ void tmem_ld_terms2(uint32_t taddr, uint32_t stride, uint64_t (&u)[2][8])
+{
+    asm volatile("{\n\t.reg .b32 a<16>, b<16>;\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {a0, a1, a2, a3, a4, a5, a6, a7, a8, a9, a10, a11, a12, a13, a14, a15}, [%16];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {b0, b1, b2, b3, b4, b5, b6, b7, b8, b9, b10, b11, b12, b13, b14, b15}, [%17];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;\n\t"
+                 "mov.b64 %0, {a0, a1};\n\t"
+                 "mov.b64 %1, {a2, a3};\n\t"
+                 "mov.b64 %2, {a4, a5};\n\t"
+                 "mov.b64 %3, {a6, a7};\n\t"
+                 "mov.b64 %4, {a8, a9};\n\t"
+                 "mov.b64 %5, {a10, a11};\n\t"
+                 "mov.b64 %6, {a12, a13};\n\t"
+                 "mov.b64 %7, {a14, a15};\n\t"
+                 "mov.b64 %8, {b0, b1};\n\t"
+                 "mov.b64 %9, {b2, b3};\n\t"
+                 "mov.b64 %10, {b4, b5};\n\t"
+                 "mov.b64 %11, {b6, b7};\n\t"
+                 "mov.b64 %12, {b8, b9};\n\t"
+                 "mov.b64 %13, {b10, b11};\n\t"
+                 "mov.b64 %14, {b12, b13};\n\t"
+                 "mov.b64 %15, {b14, b15};\n\t"
+                 "}"
+                 : "=l"(u[0][0]), "=l"(u[0][1]), "=l"(u[0][2]), "=l"(u[0][3]), "=l"(u[0][4]),
+                   "=l"(u[0][5]), "=l"(u[0][6]), "=l"(u[0][7]), "=l"(u[1][0]), "=l"(u[1][1]),
+                   "=l"(u[1][2]), "=l"(u[1][3]), "=l"(u[1][4]), "=l"(u[1][5]), "=l"(u[1][6]),
+                   "=l"(u[1][7])
+                 : "r"(taddr), "r"(taddr + stride)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_terms3(uint32_t taddr, uint32_t stride, uint64_t (&u)[3][8])
+{
+    asm volatile("{\n\t.reg .b32 a<16>, b<16>, c<16>;\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {a0, a1, a2, a3, a4, a5, a6, a7, a8, a9, a10, a11, a12, a13, a14, a15}, [%24];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {b0, b1, b2, b3, b4, b5, b6, b7, b8, b9, b10, b11, b12, b13, b14, b15}, [%25];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {c0, c1, c2, c3, c4, c5, c6, c7, c8, c9, c10, c11, c12, c13, c14, c15}, [%26];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;\n\t"
+                 "mov.b64 %0, {a0, a1};\n\t"
+                 "mov.b64 %1, {a2, a3};\n\t"
+                 "mov.b64 %2, {a4, a5};\n\t"
+                 "mov.b64 %3, {a6, a7};\n\t"
+                 "mov.b64 %4, {a8, a9};\n\t"
+                 "mov.b64 %5, {a10, a11};\n\t"
+                 "mov.b64 %6, {a12, a13};\n\t"
+                 "mov.b64 %7, {a14, a15};\n\t"
+                 "mov.b64 %8, {b0, b1};\n\t"
+                 "mov.b64 %9, {b2, b3};\n\t"
+                 "mov.b64 %10, {b4, b5};\n\t"
+                 "mov.b64 %11, {b6, b7};\n\t"
+                 "mov.b64 %12, {b8, b9};\n\t"
+                 "mov.b64 %13, {b10, b11};\n\t"
+                 "mov.b64 %14, {b12, b13};\n\t"
+                 "mov.b64 %15, {b14, b15};\n\t"
+                 "mov.b64 %16, {c0, c1};\n\t"
+                 "mov.b64 %17, {c2, c3};\n\t"
+                 "mov.b64 %18, {c4, c5};\n\t"
+                 "mov.b64 %19, {c6, c7};\n\t"
+                 "mov.b64 %20, {c8, c9};\n\t"
+                 "mov.b64 %21, {c10, c11};\n\t"
+                 "mov.b64 %22, {c12, c13};\n\t"
+                 "mov.b64 %23, {c14, c15};\n\t"
+                 "}"
+                 : "=l"(u[0][0]), "=l"(u[0][1]), "=l"(u[0][2]), "=l"(u[0][3]), "=l"(u[0][4]),
+                   "=l"(u[0][5]), "=l"(u[0][6]), "=l"(u[0][7]), "=l"(u[1][0]), "=l"(u[1][1]),
+                   "=l"(u[1][2]), "=l"(u[1][3]), "=l"(u[1][4]), "=l"(u[1][5]), "=l"(u[1][6]),
+                   "=l"(u[1][7]), "=l"(u[2][0]), "=l"(u[2][1]), "=l"(u[2][2]), "=l"(u[2][3]),
+                   "=l"(u[2][4]), "=l"(u[2][5]), "=l"(u[2][6]), "=l"(u[2][7])
+                 : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -100,6 +204,16 @@ __device__ __forceinline__ void tmem_wait_ld()
 // .sync.aligned tcgen05 instructions after it are never reached by part of a warp.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *flag)
 {
+    // the common case, a phase that has already completed: one probe and one vote
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "vote.sync.all.pred p, p, 0xffffffff;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    if (done) return true;
     const bool ok = mbar_wait_bounded(bar, parity, flag);
     return __all_sync(0xffffffffu, ok);
 }
