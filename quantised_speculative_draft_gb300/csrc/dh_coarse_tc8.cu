@@ -802,6 +802,8 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the selection may be scheduled (it waits for this grid before it reads the candidates)
+    pdl_trigger();
     if (warp == kWarpTma) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -813,6 +815,8 @@ __global__ void __launch_bounds__(Roles<two_sets<MP, PACK>()>::kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_x3, const Tc8Params prm)
 {
     extern __shared__ uint8_t smem_raw[];
+    // launched while the x staging may still run: everything below reads its output
+    pdl_wait();
     int need = 2;
     for (int m = 0; m < MP; ++m) need = max(need, prm.row_terms[m]);
     if (need == 3) coarse_tc8_body<MP, PACK, 3>(tm_packed, tm_x3, prm, prm.nstage3, smem_raw);
@@ -874,8 +878,8 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
     const int sms = device_sm_count();
     const int grid = prm.ntiles < sms ? prm.ntiles : sms;
     constexpr int kThreads = Roles<two_sets<MP, PACK>()>::kThreads;
-    coarse_tc8_kernel<MP, PACK><<<grid, kThreads, smem, stream>>>(tm_packed, tm_x[0], tm_x[1], prm);
-    return cudaGetLastError();
+    return launch_pdl(coarse_tc8_kernel<MP, PACK>, dim3(grid), dim3(kThreads), smem, stream,
+                      tm_packed, tm_x[0], tm_x[1], prm);
 }
 
 template <int PACK>

@@ -76,6 +76,16 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
                  : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start while its predecessor in the stream still runs; pdl_wait() blocks until that predecessor
+// has completed and its memory is visible, pdl_trigger() lets this kernel's own dependents start.
+// Both are no-ops for a kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

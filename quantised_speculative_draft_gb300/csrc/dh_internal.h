@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <utility>
 
 namespace dh {
 
@@ -40,6 +41,26 @@ constexpr int kPackWside = 4;   // the quarter split, dequantised on the weight 
 // Streaming multiprocessors of the current device (cudaDevAttrMultiProcessorCount), queried
 // once per device; the persistent grids are sized from it.
 int device_sm_count();
+
+// Launch with programmatic stream serialization: the kernel may be scheduled before its
+// predecessor in the stream has finished; it must call pdl_wait() before it reads anything
+// the predecessor writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Host-side set-up that applies to the current device only (a kernel's shared-memory limit):
 // run(fn) calls fn once per device, with that device current, and remembers success.

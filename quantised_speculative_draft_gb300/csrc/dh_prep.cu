@@ -204,6 +204,8 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
                                                                    int ncounters)
 {
     __shared__ float wred[kPrepMaxThreads / 32];
+    // the coarse pass may be scheduled now: it waits for this grid before it reads x
+    pdl_trigger();
     const int m = blockIdx.x;
     const bool valid = m < rows;
     const int octs = H / 8, NGt = H / G;

@@ -645,6 +645,8 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     __shared__ double part[kSrRows][kSrThreads / 32];
     __shared__ int sblk[kRowSelR];
     cg::cluster_group cluster = cg::this_cluster();
+    // launched while the coarse pass may still run: the candidates are its output
+    pdl_wait();
     const int p = static_cast<int>(cluster.block_rank());
     const int m = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -937,14 +939,12 @@ cudaError_t launch_select_rerank(const float *cand_val, const int32_t *cand_idx,
     const int nblk = static_cast<int>(ncand / kcand);
     const dim3 grid(kSrCtas, static_cast<unsigned>(M));
     if (w_scale)
-        select_rerank_kernel<true><<<grid, kSrThreads, 0, stream>>>(
-            cand_val, cand_idx, ncand, nblk, kcand, R, x, W, w_scale, H, V, sel_idx, ex, topk,
-            out_idx, out_logit);
-    else
-        select_rerank_kernel<false><<<grid, kSrThreads, 0, stream>>>(
-            cand_val, cand_idx, ncand, nblk, kcand, R, x, W, nullptr, H, V, sel_idx, ex, topk,
-            out_idx, out_logit);
-    return cudaGetLastError();
+        return launch_pdl(select_rerank_kernel<true>, grid, dim3(kSrThreads), 0, stream, cand_val,
+                          cand_idx, ncand, nblk, kcand, R, x, W, w_scale, H, V, sel_idx, ex, topk,
+                          out_idx, out_logit);
+    return launch_pdl(select_rerank_kernel<false>, grid, dim3(kSrThreads), 0, stream, cand_val,
+                      cand_idx, ncand, nblk, kcand, R, x, W, static_cast<const float *>(nullptr),
+                      H, V, sel_idx, ex, topk, out_idx, out_logit);
 }
 
 } // namespace dh
