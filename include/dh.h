@@ -167,12 +167,20 @@ int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t 
  *   DH_PATH_WARP     warp-level mma.sync on bf16 operands (the page's 1 + v/4 bit pattern),
  *                    batch handled 16 rows at a time
  *   DH_PATH_TC       tcgen05 with 8-bit operands: each 2-bit code masked in place is an exact
- *                    e4m3 subnormal weight, x split into two e4m3 terms stacked along N, batch
- *                    in launches of 32 rows
+ *                    e4m3 weight; each bf16 x row is scaled by a power of two and written as
+ *                    two e4m3 terms (three when the row's two-term residual is not negligible),
+ *                    each at its own power-of-two scale, stacked along N; batch in launches of
+ *                    16 or 32 rows
  *   DH_PATH_TC_BF16  tcgen05 on bf16 operands (the page's 1 + v/4 bit pattern)
- * All paths compute the same coarse values up to fp32 rounding.  dh_set_coarse_path returns
- * the previous setting, or DH_ERR_ARG for an unknown value.  dh_coarse_path_for(M) reports
- * which path a forward with M rows would take.
+ * The bf16 paths compute the coarse values from the exact bf16 x, up to fp32 rounding order.
+ * DH_PATH_TC computes them from its e4m3 representation of x: exact for every element within
+ * ~13 binades of its row's maximum with two terms, and with a third term for rows whose
+ * elements span more; the remaining difference is below the coarse tolerance the tests apply
+ * (1e-3 (1 + |value|)) for rows with outliers up to 2^12 times the rest.  Every path evaluates
+ * the group term S p - ZS xs in fp32, so rows with far larger outliers lose precision to
+ * cancellation on every path.  dh_set_coarse_path returns the previous setting, or DH_ERR_ARG
+ * for an unknown value.  dh_coarse_path_for(M) reports which path a forward with M rows would
+ * take.
  */
 #define DH_PATH_AUTO 0
 #define DH_PATH_WARP 1
