@@ -25,6 +25,8 @@
 #include "dh_common.cuh"
 #include "dh_internal.h"
 
+#include <type_traits>
+
 namespace dh {
 
 // min / max over aligned groups of L lanes (L = 32: the warp)
@@ -61,33 +63,45 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
     const int PS = H / P;       // k stride between planes = packed bytes per row
     const int NS = PS / 128;    // spans per row
     const int NGt = H / G;      // groups per row
-    const long long total = static_cast<long long>(V) * NS;
-    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    for (long long item = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) +
-                          (threadIdx.x >> 5);
-         item < total; item += nwarps) {
-        const long long n = item / NS;
-        const int s = static_cast<int>(item - n * NS);
+    // work items (n, s) = warp w, w + nwarps, ...: the position advances by (dn, ds) with no
+    // division in the loop, and the next item's weights are loaded before this one is quantised
+    const int nwarps = gridDim.x * (blockDim.x >> 5);
+    const int dn = nwarps / NS, ds = nwarps - dn * NS;
+    const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    int n = w0 / NS, s = w0 - (w0 / NS) * NS;
+    using Raw = typename std::conditional<kFp8, uint32_t, uint2>::type;
+    auto load = [&](int rn, int rs, Raw (&raw)[P]) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            if constexpr (kFp8) {
+                const uint8_t *row = static_cast<const uint8_t *>(Wv) + static_cast<long long>(rn) * H;
+                raw[p] = __ldg(reinterpret_cast<const uint32_t *>(row + p * PS + 128 * rs + 4 * lane));
+            } else {
+                const uint16_t *row = static_cast<const uint16_t *>(Wv) + static_cast<long long>(rn) * H;
+                raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * PS + 128 * rs + 4 * lane));
+            }
+        }
+    };
+    Raw raw[P];
+    if (n < V) load(n, s, raw);
+    while (n < V) {
+        int nn = n + dn, ns = s + ds;
+        if (ns >= NS) {
+            ns -= NS;
+            ++nn;
+        }
+        Raw next[P];
+        if (nn < V) load(nn, ns, next);
         // four weights of each plane: k = p*PS + 128 s + 4 lane + i
         float wv[P][4];
         if constexpr (kFp8) {
-            const uint8_t *row = static_cast<const uint8_t *>(Wv) + n * H;
             const float rs = __ldg(wsc + n);
-            uint32_t raw[P];
-#pragma unroll
-            for (int p = 0; p < P; ++p)
-                raw[p] = __ldg(reinterpret_cast<const uint32_t *>(row + p * PS + 128 * s + 4 * lane));
 #pragma unroll
             for (int p = 0; p < P; ++p)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     wv[p][i] = __fmul_rn(e4m3_to_f32(raw[p] >> (8 * i)), rs);
         } else {
-            const uint16_t *row = static_cast<const uint16_t *>(Wv) + n * H;
-            uint2 raw[P];
-#pragma unroll
-            for (int p = 0; p < P; ++p)
-                raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * PS + 128 * s + 4 * lane));
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 wv[p][0] = __uint_as_float(raw[p].x << 16);
@@ -117,12 +131,16 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
                 const float sb = __fmul_rn(B, sc);
                 const long long gi = (static_cast<long long>(p) * NS + s) * (128 / G) +
                                      lane / (G / 4);
-                S[n * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
-                ZS[n * NGt + gi] =
+                S[static_cast<long long>(n) * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
+                ZS[static_cast<long long>(n) * NGt + gi] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(zp, sc))));
             }
         }
-        reinterpret_cast<uint32_t *>(packed + n * PS + 128 * s)[lane] = word;
+        reinterpret_cast<uint32_t *>(packed + static_cast<long long>(n) * PS + 128 * s)[lane] = word;
+#pragma unroll
+        for (int p = 0; p < P; ++p) raw[p] = next[p];
+        n = nn;
+        s = ns;
     }
 }
 
@@ -196,24 +214,37 @@ cudaError_t launch_quantize_c4(const uint16_t *W, int V, int H, uint8_t *packed,
     return cudaGetLastError();
 }
 
+// One resident wave: as many blocks as fit on every SM at once (the work loop strides over the
+// items), so that no block waits for a second round while others have finished.
+template <bool kFp8, int BITS, int G>
+cudaError_t launch_quantize_cfg(const void *W, const float *wsc, int V, int H, uint8_t *packed,
+                                uint16_t *S, uint16_t *ZS, cudaStream_t stream)
+{
+    const long long total = static_cast<long long>(V) * (H / (128 * (8 / BITS)));
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, quantize_kernel<kFp8, BITS, G>, 256, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    long long blocks = (total + 7) / 8;
+    const long long cap = static_cast<long long>(device_sm_count()) * per_sm;
+    if (blocks > cap) blocks = cap;
+    quantize_kernel<kFp8, BITS, G><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        W, wsc, packed, S, ZS, V, H);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize(const void *W, const float *wsc, int V, int H, int bits, int group,
                             uint8_t *packed, uint16_t *S, uint16_t *ZS, cudaStream_t stream)
 {
-    const long long total = static_cast<long long>(V) * (H / (bits == 4 ? 256 : 512));
-    long long blocks = (total + 7) / 8;
-    const long long cap = static_cast<long long>(device_sm_count()) * 8;
-    if (blocks > cap) blocks = cap;
-    const unsigned g = static_cast<unsigned>(blocks);
     if (bits == 4) {
-        if (wsc) quantize_kernel<true, 4, 128><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
-        else quantize_kernel<false, 4, 128><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
-    } else if (group == 64) { // the 2-bit bf16 head with groups of 64
-        quantize_kernel<false, 2, 64><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
-    } else {
-        if (wsc) quantize_kernel<true, 2, 128><<<g, 256, 0, stream>>>(W, wsc, packed, S, ZS, V, H);
-        else quantize_kernel<false, 2, 128><<<g, 256, 0, stream>>>(W, nullptr, packed, S, ZS, V, H);
+        if (wsc) return launch_quantize_cfg<true, 4, 128>(W, wsc, V, H, packed, S, ZS, stream);
+        return launch_quantize_cfg<false, 4, 128>(W, nullptr, V, H, packed, S, ZS, stream);
     }
-    return cudaGetLastError();
+    if (group == 64) // the 2-bit bf16 head with groups of 64
+        return launch_quantize_cfg<false, 2, 64>(W, nullptr, V, H, packed, S, ZS, stream);
+    if (wsc) return launch_quantize_cfg<true, 2, 128>(W, wsc, V, H, packed, S, ZS, stream);
+    return launch_quantize_cfg<false, 2, 128>(W, nullptr, V, H, packed, S, ZS, stream);
 }
 
 } // namespace dh
