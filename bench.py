@@ -64,7 +64,7 @@ def parse():
 def path_name(p):
     import quantised_speculative_draft_gb300 as dh
     return {dh.PATH_TC: "tcgen05 8-bit", dh.PATH_TC_BF16: "tcgen05 bf16",
-            dh.PATH_WARP: "warp mma.sync bf16"}.get(p, str(p))
+            dh.PATH_WARP: "warp mma.sync bf16", dh.PATH_CORE: "CUDA-core fp32"}.get(p, str(p))
 
 
 def algorithmic_bytes4(V, H):
@@ -434,6 +434,30 @@ def time_stages(sets, M, steps):
     return out
 
 
+def compare_paths(sets, M, steps, hbm, tfl, src):
+    """µs/call and coarse-pass time of every coarse path that runs M rows (small batches: the
+    CUDA-core path and the 8-bit tcgen05 path)."""
+    import quantised_speculative_draft_gb300 as dh
+    out = {}
+    for p in (dh.PATH_CORE, dh.PATH_TC):
+        prev = dh.dh_set_coarse_path(p)
+        try:
+            try:
+                if dh.dh_coarse_path_for(M) != p:
+                    continue
+            except dh.DHError:
+                continue
+            ms, _, _ = time_graph(sets, M, steps, 5)
+            st = time_stages(sets, M, 20)
+            r = roofline_entry(M, st["coarse"], hbm, tfl, src)
+            out[path_name(p)] = {"us_per_call": round(ms * 1e3 / steps, 2),
+                                 "coarse_us": round(st["coarse"], 2),
+                                 "roofline": {"bound": r["bound"], "frac": r["frac"]}}
+        finally:
+            dh.dh_set_coarse_path(prev)
+    return out
+
+
 def time_e2e(sets, M, steps):
     """The same call end to end with host buffers: pinned x in, dh_forward, idx/logit out."""
     import torch
@@ -651,6 +675,10 @@ def run_ours(args):
                           "coarse_TF/s": round(2 * m * H_FULL * V_FULL / st["coarse"] / 1e6, 1),
                           "roofline": {"bound": r["bound"], "frac": r["frac"]},
                           "stages_us": {k: round(v, 2) for k, v in st.items()}})
+            if m <= 4:
+                # the small-batch regime choice: both coarse paths that take this M, timed
+                # the same way; the automatic choice above is the faster one
+                sweep[-1]["paths"] = compare_paths(sets, m, args.sweep_steps, hbm, tfl, src)
 
     rec = {}
     if rank == 0 and not args.no_recall:

@@ -172,7 +172,12 @@ int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t 
  *                    each at its own power-of-two scale, stacked along N; batch in launches of
  *                    16 or 32 rows
  *   DH_PATH_TC_BF16  tcgen05 on bf16 operands (the page's 1 + v/4 bit pattern)
- * The bf16 paths compute the coarse values from the exact bf16 x, up to fp32 rounding order.
+ *   DH_PATH_CORE     CUDA cores, M <= 4 and H a multiple of 512: fp32 FMAs on weights made from
+ *                    the packed bits (1 + v 2^(2p-8) by a shift and an and-or, minus 1.0
+ *                    exactly), x as fp32 in shared memory; the small-batch alternative to the
+ *                    tensor paths, never chosen by DH_PATH_AUTO (slower at every M it takes)
+ * The bf16 paths and DH_PATH_CORE compute the coarse values from the exact bf16 x, up to fp32
+ * rounding order.
  * DH_PATH_TC computes them from its e4m3 representation of x: exact for every element within
  * ~13 binades of its row's maximum with two terms, and with a third term for rows whose
  * elements span more; the remaining difference is below the coarse tolerance the tests apply
@@ -186,6 +191,7 @@ int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t 
 #define DH_PATH_WARP 1
 #define DH_PATH_TC 2
 #define DH_PATH_TC_BF16 3
+#define DH_PATH_CORE 4
 int dh_set_coarse_path(int path);
 int dh_coarse_path_for(int M);
 

@@ -26,10 +26,10 @@ __all__ = [
     "dh_forward_fp8w", "dh_quantize4", "dh_forward4", "dh_forward4_debug", "dh_forward4_timed",
     "dh_quantize_c4", "dh_forward_c4_debug", "dh_quantize_g64", "dh_forward_g64_debug",
     "dh_forward_wside_debug",
-    "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16", "NUM_STAGE_EVENTS", "library_path",
+    "PATH_AUTO", "PATH_WARP", "PATH_TC", "PATH_TC_BF16", "PATH_CORE", "NUM_STAGE_EVENTS", "library_path",
 ]
 
-PATH_AUTO, PATH_WARP, PATH_TC, PATH_TC_BF16 = 0, 1, 2, 3
+PATH_AUTO, PATH_WARP, PATH_TC, PATH_TC_BF16, PATH_CORE = 0, 1, 2, 3, 4
 NUM_STAGE_EVENTS = 6
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 GROUP = 128

@@ -171,6 +171,7 @@ int choose_path(int M, int H)
     if (p == DH_PATH_TC) return tc8_supported(M, H) ? p : -1;
     if (p == DH_PATH_TC_BF16) return tc_supported(M, H) ? p : -1;
     if (p == DH_PATH_WARP) return DH_PATH_WARP;
+    if (p == DH_PATH_CORE) return core_supported(M, H) ? p : -1;
     // automatic: the 8-bit tcgen05 path where it is available, else the warp path
     if (tc8_supported(M, H)) return DH_PATH_TC;
     return DH_PATH_WARP;
@@ -244,6 +245,9 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     w8.group = pack == kPackG64 ? 64 : 128;
     if (path == DH_PATH_TC)
         err = launch_prep_fp8(x, M, H, pack, w8, counters, kNumCounters, stream);
+    else if (path == DH_PATH_CORE)
+        err = launch_prep(x, M, H, core_mpad(M), xs, nullptr, nullptr, 0, counters,
+                          kNumCounters, stream);
     else
         err = launch_prep(x, M, H, path == DH_PATH_WARP ? L.Mpad_w : 0, xs,
                           path == DH_PATH_WARP ? xw : nullptr,
@@ -253,6 +257,7 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     if (!rec(1)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
 
     CoarseArgs a;
+    a.x = x;
     a.packed = packed;
     a.S = scales;
     a.ZS = zeros;
@@ -271,11 +276,14 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     a.timeout_flag = tflag;
     if (path == DH_PATH_TC) err = launch_coarse_tc8(a, w8, stream);
     else if (path == DH_PATH_TC_BF16) err = launch_coarse_tc(a, stream);
+    else if (path == DH_PATH_CORE) err = launch_coarse_core(a, stream);
     else err = launch_coarse_warp(a, stream);
     if (err != cudaSuccess)
         return fail(DH_ERR_CUDA, "coarse launch (%s path): %s",
-                    path == DH_PATH_TC ? "tcgen05 8-bit"
-                                       : (path == DH_PATH_TC_BF16 ? "tcgen05 bf16" : "warp"),
+                    path == DH_PATH_TC
+                        ? "tcgen05 8-bit"
+                        : (path == DH_PATH_TC_BF16 ? "tcgen05 bf16"
+                                                   : (path == DH_PATH_CORE ? "CUDA-core" : "warp")),
                     cudaGetErrorString(err));
     if (!rec(2)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     if (!candidates_only && select_rerank_fits(rerank, kcand)) {
@@ -619,7 +627,7 @@ int dh_forward_noalloc(const uint16_t *x, const uint8_t *packed, const uint16_t 
 int dh_set_coarse_path(int path)
 {
     if (path != DH_PATH_AUTO && path != DH_PATH_WARP && path != DH_PATH_TC &&
-        path != DH_PATH_TC_BF16)
+        path != DH_PATH_TC_BF16 && path != DH_PATH_CORE)
         return fail(DH_ERR_ARG, "unknown coarse path %d", path);
     std::lock_guard<std::mutex> lk(g_path_mu);
     const int prev = g_path;
@@ -642,6 +650,7 @@ int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank)
     int prep = 1, coarse = (M + kWarpBatch - 1) / kWarpBatch;
     if (path == DH_PATH_TC) prep = coarse = tc8_chunks(M, kPackQuarter2);
     else if (path == DH_PATH_TC_BF16) coarse = tc_launches(M);
+    else if (path == DH_PATH_CORE) coarse = 1;
     if (select_rerank_fits(rerank, kcand)) return prep + coarse + 1; // fused select + rerank
     return prep + coarse + L.passes /*selection*/ + 1 /*rerank + top-k*/;
 }

@@ -104,6 +104,7 @@ cudaError_t launch_prep(const uint16_t *x, int M, int H, int Mpad, float *xs, ui
                         cudaStream_t stream);
 
 struct CoarseArgs {
+    const uint16_t *x;  // [M, H] bf16 (the CUDA-core path reads it directly)
     const uint8_t *packed;
     const uint16_t *S;
     const uint16_t *ZS;
@@ -121,6 +122,12 @@ struct CoarseArgs {
 };
 
 cudaError_t launch_coarse_warp(const CoarseArgs &a, cudaStream_t stream);
+
+// CUDA-core path for M <= 4 (H a multiple of 512): fp32 FMAs on weights made from the packed
+// bits, x read from CoarseArgs::x, group sums from xs (core_mpad(M) rows).
+bool core_supported(int M, int H);
+int core_mpad(int M);
+cudaError_t launch_coarse_core(const CoarseArgs &a, cudaStream_t stream);
 size_t warp_xw_elems(int M, int H); // bf16 elements of the warp-path operand
 
 // tcgen05 path with 8-bit operands.  The batch runs in launches of at most tc8_max_rows(pack)
