@@ -384,10 +384,60 @@ bool row_select_fits(long long ncand, int kcand, int R)
 // a6 + a7: exact rerank, then the top-k of the row.  One CTA of 256 threads per (row m,
 // candidate j): every thread takes H/2048 16-byte slices of x and of the candidate's bf16 row
 // (products of bf16 values are exact in fp32), sums them in two fp32 partials, and the CTA
-// combines the 512 partials in fp64.  The last CTA to finish a row (an atomic count per row,
+// combines the 512 partials in float-float arithmetic (an unevaluated sum hi + lo of two
+// fp32 values, about 44 significant bits: the CUDA cores' fp32 pipes instead of GB300's few
+// fp64 units), rounded once to fp32 at the end.  The last CTA to finish a row (an atomic count per row,
 // zeroed by the staging kernel) sorts that row's R exact values and writes its top-k.
 // ----------------------------------------------------------------------------------------
 constexpr int kRerankThreads = 256;
+
+// Float-float value hi + lo (|lo| <= ulp(hi) / 2 after normalisation).  Explicitly rounded
+// operations keep the compiler from contracting or reassociating them.
+struct FF {
+    float hi, lo;
+};
+
+// hi + lo = a + b exactly (Knuth's TwoSum, any magnitudes).
+__device__ __forceinline__ FF two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return FF{s, e};
+}
+
+// a + b for float-float values: the exact sum of the high parts plus both low parts, then
+// renormalised (Dekker's FastTwoSum, |s.hi| >= |t| up to the low parts' rounding).
+__device__ __forceinline__ FF ff_add(FF a, FF b)
+{
+    const FF s = two_sum(a.hi, b.hi);
+    const float t = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+    const float hi = __fadd_rn(s.hi, t);
+    return FF{hi, __fsub_rn(t, __fsub_rn(hi, s.hi))};
+}
+
+__device__ __forceinline__ FF ff_shfl_xor(FF v, int o)
+{
+    return FF{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+
+// The CTA-wide sum of the 256 threads' values, the same order in every caller: an xor-shuffle
+// tree per warp, then the eight warps in order (part: eight slots of shared memory).  The
+// result reaches thread 0 only, rounded to fp32.
+__device__ __forceinline__ FF ff_warp_sum(FF v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+    return v;
+}
+
+__device__ __forceinline__ float ff_sum8(const FF *part)
+{
+    FF t = part[0];
+#pragma unroll
+    for (int i = 1; i < kRerankThreads / 32; ++i) t = ff_add(t, part[i]);
+    return __fadd_rn(t.hi, t.lo);
+}
 
 __device__ void sort_write_topk(unsigned long long *k, int n2, int topk, int32_t *oidx,
                                 float *ologit);
@@ -396,10 +446,10 @@ __device__ void sort_write_topk(unsigned long long *k, int n2, int topk, int32_t
 // caller so that every path reranks to the same bits: the thread takes the 8-weight slices
 // i = tid, tid + 256, ... of the row, sums their products in two fp32 partials (products of
 // bf16 values are exact in fp32; an fp8 weight is first rounded to fp32(e4m3 * scale)), and
-// returns their sum in fp64.  The caller reduces the 256 values: an xor-shuffle tree per warp,
-// then the eight warps in order.
+// returns their exact sum as a float-float value.  The caller reduces the 256 values with
+// ff_warp_sum and ff_sum8.
 template <bool kFp8>
-__device__ __forceinline__ double rerank_partial(const uint16_t *__restrict__ xrow,
+__device__ __forceinline__ FF rerank_partial(const uint16_t *__restrict__ xrow,
                                                  const void *__restrict__ Wv,
                                                  const float *__restrict__ w_scale, int n, int H,
                                                  int tid)
@@ -443,7 +493,7 @@ __device__ __forceinline__ double rerank_partial(const uint16_t *__restrict__ xr
             }
         }
     }
-    return static_cast<double>(a0) + static_cast<double>(a1);
+    return two_sum(a0, a1);
 }
 
 // rerank_partial for NR rows at once (rows n[r] < 0: none), with every row's FMA sequence
@@ -455,7 +505,7 @@ __device__ __forceinline__ void rerank_partial_rows(const uint16_t *__restrict__
                                                     const void *__restrict__ Wv,
                                                     const float *__restrict__ w_scale,
                                                     const int (&n)[NR], int H, int tid,
-                                                    double (&d)[NR])
+                                                    FF (&d)[NR])
 {
     constexpr int kBatch = 3; // slices per thread in flight (H = 5120: all of them)
     using WVec = typename std::conditional<kFp8, uint2, uint4>::type;
@@ -520,7 +570,7 @@ __device__ __forceinline__ void rerank_partial_rows(const uint16_t *__restrict__
         }
     }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) d[r] = static_cast<double>(a0[r]) + static_cast<double>(a1[r]);
+    for (int r = 0; r < NR; ++r) d[r] = two_sum(a0[r], a1[r]);
 }
 
 // kFp8: W holds e4m3 rows and w_scale the per-row fp32 scales; each weight is the fp32
@@ -533,7 +583,7 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
     float *__restrict__ ex, int *__restrict__ row_done, int topk, int32_t *__restrict__ out_idx,
     float *__restrict__ out_logit, int id_offset)
 {
-    __shared__ double part[kRerankThreads / 32];
+    __shared__ FF part[kRerankThreads / 32];
     __shared__ unsigned long long k[kMaxRerank];
     __shared__ int s_last;
     const long long pair = blockIdx.x;
@@ -542,16 +592,13 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
     const int n = gid >= 0 ? gid - id_offset : -1; // row of W (a shard starts at id_offset)
     const int tid = threadIdx.x, lane = tid & 31;
 
-    double d = rerank_partial<kFp8>(x + static_cast<long long>(m) * H, Wv, w_scale,
-                                    (n >= 0 && n < V) ? n : -1, H, tid);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    const FF d = ff_warp_sum(rerank_partial<kFp8>(x + static_cast<long long>(m) * H, Wv, w_scale,
+                                                  (n >= 0 && n < V) ? n : -1, H, tid));
     if (lane == 0) part[tid >> 5] = d;
     __syncthreads();
     if (tid == 0) {
-        double t = 0.0;
-        for (int i = 0; i < kRerankThreads / 32; ++i) t += part[i];
-        ex[pair] = (n >= 0 && n < V) ? static_cast<float>(t) : -INFINITY;
+        const float t = ff_sum8(part);
+        ex[pair] = (n >= 0 && n < V) ? t : -INFINITY;
         s_last = 0;
         if (topk > 0) { // only a top-k that follows needs to know which CTA finished last
             __threadfence();
@@ -599,6 +646,13 @@ __global__ void __launch_bounds__(kRerankThreads) rerank_topk_kernel(
 constexpr int kSrCtas = 8;      // CTAs per row (a portable cluster)
 constexpr int kSrThreads = 256; // = kRerankThreads: the rerank's reduction shape
 constexpr int kSrRows = 4;      // reranked rows per CTA: R <= kSrCtas * kSrRows = 32
+constexpr int kSrPrefetch = 8;  // weight rows of L_p's best candidates prefetched into L2
+
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Descending bitonic sort of 32 keys, one per lane.
 __device__ __forceinline__ unsigned long long warp_sort32_desc(unsigned long long v)
@@ -642,14 +696,18 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     __shared__ unsigned long long lists[kSrThreads / 32][32];
     __shared__ unsigned long long mylist[32];               // L_p, read by the cluster
     __shared__ unsigned long long exk[32];                  // CTA 0: the R exact rank keys
-    __shared__ double part[kSrRows][kSrThreads / 32];
+    __shared__ FF part[kSrRows][kSrThreads / 32];
     __shared__ int sblk[kRowSelR];
     cg::cluster_group cluster = cg::this_cluster();
-    // launched while the coarse pass may still run: the candidates are its output
-    pdl_wait();
     const int p = static_cast<int>(cluster.block_rank());
     const int m = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t wrow_bytes = static_cast<uint32_t>(H) * (kFp8 ? 1u : 2u);
+    // x is the caller's input (complete before the staging kernel ran): its row goes to L2 for
+    // the rerank while the selection runs
+    if (tid == 0) prefetch_l2_bulk(x + static_cast<long long>(m) * H, static_cast<uint32_t>(H) * 2u);
+    // launched while the coarse pass may still run: the candidates are its output
+    pdl_wait();
     const float *vrow = cand_val + static_cast<long long>(m) * ncand;
     const int32_t *irow = cand_idx + static_cast<long long>(m) * ncand;
 
@@ -721,6 +779,15 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     __syncthreads();
     tree_merge8(lists);
     if (warp == 0) mylist[lane] = lists[0][lane];
+    // the weight rows of this CTA's best candidates start on their way to L2: the rows the
+    // cluster reranks are the 32 best of the eight lists, mostly near the top of each
+    if (tid < kSrPrefetch) {
+        const unsigned long long key = lists[0][tid];
+        const int id = key ? static_cast<int>(~static_cast<uint32_t>(key)) : -1;
+        if (id >= 0 && id < V)
+            prefetch_l2_bulk(static_cast<const uint8_t *>(Wv) + static_cast<long long>(id) * wrow_bytes,
+                             wrow_bytes);
+    }
     cluster.sync();
 
     // 2. every CTA merges the cluster's lists into G (lists[0], rank order)
@@ -733,7 +800,7 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
 
     // 3. rerank G[p + kSrCtas r] (the four rows' loads in flight together)
     int gid[kSrRows], nrow[kSrRows];
-    double d[kSrRows];
+    FF d[kSrRows];
 #pragma unroll
     for (int r = 0; r < kSrRows; ++r) {
         const int j = p + kSrCtas * r;
@@ -745,18 +812,16 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
                                        tid, d);
 #pragma unroll
     for (int r = 0; r < kSrRows; ++r) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) d[r] += __shfl_xor_sync(0xffffffffu, d[r], o);
+        d[r] = ff_warp_sum(d[r]);
         if (lane == 0) part[r][warp] = d[r];
     }
     __syncthreads();
     if (tid < kSrRows) {
         const int r = tid, j = p + kSrCtas * r;
         if (j < R) {
-            double t = 0.0;
-            for (int i = 0; i < kSrThreads / 32; ++i) t += part[r][i];
+            const float t = ff_sum8(part[r]);
             const bool ok = gid[r] >= 0 && gid[r] < V;
-            const float e = ok ? static_cast<float>(t) : -INFINITY;
+            const float e = ok ? t : -INFINITY;
             sel_idx[static_cast<long long>(m) * R + j] = gid[r];
             ex[static_cast<long long>(m) * R + j] = e;
             unsigned long long *exk0 = cluster.map_shared_rank(exk, 0);
