@@ -156,15 +156,18 @@ constexpr int kPrepOcts = 2; // 16-byte slices of x per thread: one per thread u
 constexpr float kTermsThreshold = 9.5367431640625e-7f; // 2^-20
 
 // Largest value of v over the CTA (v >= 0); every thread gets it.  red: kPrepMaxThreads / 32.
+// Every warp combines the warps' maxima with shuffles (one shared-memory read per lane).
 __device__ __forceinline__ float cta_max(float v, float *red)
 {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
     __syncthreads(); // the previous use of red is over
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    if (lane == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    v = 0.f;
-    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) v = fmaxf(v, red[i]);
+    v = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
 }
 

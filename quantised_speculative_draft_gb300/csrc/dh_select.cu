@@ -222,8 +222,9 @@ __device__ __forceinline__ unsigned long long kmin(unsigned long long a, unsigne
     return a < b ? a : b;
 }
 
-// Sorts four warp lists (one key per lane each) descending, in lockstep (bitonic, 15 stages).
-__device__ __forceinline__ void warp_sort32x4_desc(unsigned long long (&v)[4])
+// Sorts N warp lists (one key per lane each) descending, in lockstep (bitonic, 15 stages).
+template <int N>
+__device__ __forceinline__ void warp_sort32xN_desc(unsigned long long (&v)[N])
 {
     const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -232,7 +233,7 @@ __device__ __forceinline__ void warp_sort32x4_desc(unsigned long long (&v)[4])
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
+            for (int r = 0; r < N; ++r) {
                 const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], stride);
                 v[r] = keep_max ? kmax(v[r], o) : kmin(v[r], o);
             }
@@ -262,8 +263,17 @@ __device__ __forceinline__ unsigned long long warp_top32_of128(const unsigned lo
     unsigned long long v[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) v[r] = k[r * 32 + lane];
-    warp_sort32x4_desc(v);
+    warp_sort32xN_desc<4>(v);
     return warp_merge32_desc(warp_merge32_desc(v[0], v[1]), warp_merge32_desc(v[2], v[3]));
+}
+
+// The 32 best (descending, one per lane) of the 64 keys k[0..63] (0 = empty).
+__device__ __forceinline__ unsigned long long warp_top32_of64(const unsigned long long *k)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned long long v[2] = {k[lane], k[32 + lane]};
+    warp_sort32xN_desc<2>(v);
+    return warp_merge32_desc(v[0], v[1]);
 }
 
 // The 32 best of n keys in shared memory (n a multiple of 128, keys beyond the data 0), by the
@@ -711,11 +721,14 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     const float *vrow = cand_val + static_cast<long long>(m) * ncand;
     const int32_t *irow = cand_idx + static_cast<long long>(m) * ncand;
 
-    // 1a. the 32 best block maxima of this CTA's slice (a block's first entry is its best)
+    // 1a. the 32 best block maxima of this CTA's slice (a block's first entry is its best);
+    // 64 keys per warp and round, so that all eight warps sort
     const int per = (nblk + kSrCtas - 1) / kSrCtas;
     const int b0 = p * per, b1 = min(nblk, b0 + per);
-    constexpr int kRound = (kSrThreads / 32) * kRowSelChunk; // 1024 keys: a chunk per warp
+    constexpr int kWarpKeys = 64;
+    constexpr int kRound = (kSrThreads / 32) * kWarpKeys; // 512 keys
     unsigned long long acc = 0;
+    bool have = false; // warp-uniform: acc holds a list
     for (int base = b0; base < b1; base += kRound) {
         // every load of the round issued before any is used (value and index independently)
         constexpr int kPer = kRound / kSrThreads;
@@ -735,8 +748,11 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
                 (bk < b1 && ids[u] >= 0) ? rank_key(vals[u], ids[u]) : 0ull;
         }
         __syncthreads();
-        if (base + warp * kRowSelChunk < b1) // warp-uniform
-            acc = warp_merge32_desc(acc, warp_top32_of128(keys + warp * kRowSelChunk));
+        if (base + warp * kWarpKeys < b1) { // warp-uniform
+            const unsigned long long top = warp_top32_of64(keys + warp * kWarpKeys);
+            acc = have ? warp_merge32_desc(acc, top) : top;
+            have = true;
+        }
         __syncthreads();
     }
     lists[warp][lane] = acc;
@@ -773,8 +789,16 @@ __global__ void __cluster_dims__(kSrCtas, 1, 1) __launch_bounds__(kSrThreads, 1)
     }
     __syncthreads();
     acc = 0;
-    for (int c = warp; c < nchunks; c += kSrThreads / 32)
-        acc = warp_merge32_desc(acc, warp_top32_of128(keys + c * kRowSelChunk));
+    if (nc <= (kSrThreads / 32) * 32) {
+        // one 32-key list per warp (entries past nc empty: the gather wrote whole 128-key
+        // chunks only, and the rest of keys[] still holds phase 1a's keys): a single sort,
+        // then the tree merge
+        const int e = warp * 32 + lane;
+        acc = warp_sort32_desc(e < nc ? keys[e] : 0ull);
+    } else {
+        for (int c = warp; c < nchunks; c += kSrThreads / 32)
+            acc = warp_merge32_desc(acc, warp_top32_of128(keys + c * kRowSelChunk));
+    }
     lists[warp][lane] = acc;
     __syncthreads();
     tree_merge8(lists);
