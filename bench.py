@@ -58,6 +58,8 @@ def parse():
                     help="head width for --profile runs (4: the 4-bit head at KCAND=1)")
     ap.add_argument("--profile", action="store_true",
                     help="only run warmup + steps forwards (no timing, no JSON): for ncu")
+    ap.add_argument("--coarse-path", choices=["auto", "tc8", "core", "tc_bf16", "warp"],
+                    default="auto", help="coarse path of --profile runs")
     return ap.parse_args()
 
 
@@ -627,6 +629,8 @@ def run_ours(args):
     dev = f"cuda:{local}"
     dh.build()
     if args.profile:
+        dh.dh_set_coarse_path({"auto": dh.PATH_AUTO, "tc8": dh.PATH_TC, "core": dh.PATH_CORE,
+                               "tc_bf16": dh.PATH_TC_BF16, "warp": dh.PATH_WARP}[args.coarse_path])
         if args.bits == 4:
             sets = [Int4Inputs(seed, dev, args.M, 1, args.V) for seed in range(args.sets)]
         else:
@@ -845,14 +849,15 @@ def run_ours(args):
             "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms / args.steps, 6), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 x e4m3 -> fp32 (coarse); bf16 -> fp32/fp64 (rerank)",
+            "dtype": "e4m3 x e4m3 -> fp32 (coarse); bf16 -> fp32, float-float sums (rerank)",
             "dtype_detail": "coarse pass: tcgen05 kind::f8f6f4 MMAs with fp32 accumulation; "
                             "each 2-bit code masked in place is an exact e4m3 weight, and each "
                             "bf16 x row is staged as 2 or 3 e4m3 terms (row scale 2^e, per-row "
                             "term shifts), the third only for rows whose two-term residual "
                             "sum |r2| exceeds 2^-20 sum |x|; ordinary rows are represented "
                             "exactly except elements ~14+ binades below the row maximum. "
-                            "Rerank: bf16 x and W, exact fp32 products summed in fp64",
+                            "Rerank: bf16 x and W, exact fp32 products summed in two fp32 chains per "
+                            "thread, then combined as float-float (hi + lo) pairs and rounded once",
             "data": "synthetic (seeded normal x and W with hot rows; no trained weights)",
             "config": workload_config(M, world),
             "timing": {"l2": "two resident input sets of 2.9 GB alternate between steps "
