@@ -15,8 +15,6 @@
 #include "dh_common.cuh"
 #include "dh_internal.h"
 
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 namespace dh {
 
@@ -123,15 +121,27 @@ size_t warp_xw_elems(int M, int H)
 // residual sum_k |r2_k| exceeds 2^-20 sum_k |x_k 2^e|, else 2 (each coarse launch takes the
 // most any of its rows needs).  One CTA per staged row.
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ float e4m3_to_f32(__nv_fp8_storage_t v)
+// Round to nearest even onto the e4m3 grid (three mantissa bits; normal exponents from -6, the
+// subnormal spacing 2^-9 below 2^-6), for |r| < 448, in fp32 arithmetic: with 2^k <= |r| <
+// 2^(k+1) (k at least -6), c = 1.5 2^(k+20) puts r + c in [2^(k+20), 2^(k+21)), whose spacing is
+// e4m3's 2^(k-3) at r; the add rounds to nearest even on that grid (c is an even multiple of
+// the spacing, 3 2^22 of them), and subtracting c again is exact.  The conversion units of an
+// SM are few; these four operations run on the integer and fp32 pipes.
+__device__ __forceinline__ float round_e4m3(float r)
 {
-    const __half_raw h = __nv_cvt_fp8_to_halfraw(v, __NV_E4M3);
-    return __half2float(__half(h));
+    int ex = static_cast<int>((__float_as_uint(r) >> 23) & 0xFFu);
+    ex = ex < 121 ? 121 : ex; // 121 = 127 - 6
+    const float c = __uint_as_float((static_cast<uint32_t>(ex + 20) << 23) | 0x400000u);
+    return __fsub_rn(__fadd_rn(r, c), c);
 }
 
-__device__ __forceinline__ __nv_fp8_storage_t to_e4m3(float v)
+// The e4m3 bytes of two values already on the e4m3 grid (exact, no rounding): lo in bits 0-7,
+// hi in bits 8-15.
+__device__ __forceinline__ uint32_t e4m3x2_bits(float lo, float hi)
 {
-    return __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3); // round to nearest even
+    uint16_t v;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(hi), "f"(lo));
+    return v;
 }
 
 // The power of two 2^s that puts a largest magnitude mx > 0 in [128, 256) (s clamped to the
@@ -173,21 +183,28 @@ __device__ __forceinline__ float cta_max(float v, float *red)
 
 // The split of one scaled element r0 = x 2^e with term shifts s2, s3 (scales k2 = 2^s2 ...).
 struct Split3 {
-    __nv_fp8_storage_t b[3];
+    float u[3];               // the terms as stored (e4m3 values, each at its own scale)
     float t1, t2, t3, r1, r2; // term values in the scaled units and the residuals
 };
 
+// The first two terms only (NT = 2) or all three; k2, k3 and their inverses are powers of two.
+template <int NT>
 __device__ __forceinline__ Split3 split3(float r0, float k2, float ik2, float k3, float ik3)
 {
     Split3 o;
-    o.b[0] = to_e4m3(r0);
-    o.t1 = e4m3_to_f32(o.b[0]);
+    o.u[0] = round_e4m3(r0);
+    o.t1 = o.u[0];
     o.r1 = r0 - o.t1;
-    o.b[1] = to_e4m3(o.r1 * k2);
-    o.t2 = e4m3_to_f32(o.b[1]) * ik2;
+    o.u[1] = round_e4m3(o.r1 * k2);
+    o.t2 = o.u[1] * ik2;
     o.r2 = o.r1 - o.t2;
-    o.b[2] = to_e4m3(o.r2 * k3);
-    o.t3 = e4m3_to_f32(o.b[2]) * ik3;
+    if constexpr (NT == 3) {
+        o.u[2] = round_e4m3(o.r2 * k3);
+        o.t3 = o.u[2] * ik3;
+    } else {
+        o.u[2] = 0.f;
+        o.t3 = 0.f;
+    }
     return o;
 }
 
@@ -207,6 +224,7 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
                                                                    int ncounters)
 {
     __shared__ float wred[kPrepMaxThreads / 32];
+    __shared__ float wred2[kPrepMaxThreads / 32];
     // the coarse pass may be scheduled now: it waits for this grid before it reads x
     pdl_trigger();
     const int m = blockIdx.x;
@@ -216,7 +234,10 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
         for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
     const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
 
-    // the row stays in registers between the passes (H <= 1024 * 8 * kPrepOcts)
+    // the row stays in registers between the passes (H <= 1024 * 8 * kPrepOcts); the second
+    // slice of every thread exists only when the row has more slices than the CTA has threads
+    // (CTA-uniform)
+    const int nj = octs > static_cast<int>(blockDim.x) ? 2 : 1;
     uint4 xv[kPrepOcts];
     float mx = 0.f;
 #pragma unroll
@@ -235,11 +256,12 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
     float m1 = 0.f;
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
+        if (j >= nj) break;
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
-            m1 = fmaxf(m1, fabsf(r0 - e4m3_to_f32(to_e4m3(r0))));
+            m1 = fmaxf(m1, fabsf(r0 - round_e4m3(r0)));
         }
     }
     const int s2 = range_shift(cta_max(m1, wred));
@@ -247,11 +269,12 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
     float m2 = 0.f;
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
+        if (j >= nj) break;
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
-            const Split3 sp = split3(r0, k2, ik2, 0.f, 0.f);
+            const Split3 sp = split3<2>(r0, k2, ik2, 0.f, 0.f);
             m2 = fmaxf(m2, fabsf(sp.r2));
         }
     }
@@ -267,26 +290,31 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
     float l1 = 0.f, b2 = 0.f; // sum |x 2^e| and the two-term residual sum |r2|
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
+        if (j >= nj) break; // CTA-uniform
         const int o = threadIdx.x + j * blockDim.x;
         // every lane of a warp takes part in the group shuffles: lanes past the row add 0
         const bool live = o < octs;
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-        uint32_t lo[kTc8Terms] = {0, 0, 0}, hi[kTc8Terms] = {0, 0, 0};
+        float u[kTc8Terms][8];
         float sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
-            const Split3 sp = split3(r0, k2, ik2, k3, ik3);
+            const Split3 sp = split3<3>(r0, k2, ik2, k3, ik3);
             const float rep2 = sp.t1 + sp.t2;
             sum2 += rep2;
             sum3 += rep2 + sp.t3;
             l1 += fabsf(r0);
             b2 += fabsf(sp.r2);
 #pragma unroll
-            for (int t = 0; t < kTc8Terms; ++t) {
-                if (i < 4) lo[t] |= static_cast<uint32_t>(sp.b[t]) << (8 * i);
-                else hi[t] |= static_cast<uint32_t>(sp.b[t]) << (8 * (i - 4));
-            }
+            for (int t = 0; t < kTc8Terms; ++t) u[t][i] = sp.u[t];
+        }
+        // the terms' bytes, element i in byte i of the 8-byte slice
+        uint32_t lo[kTc8Terms], hi[kTc8Terms];
+#pragma unroll
+        for (int t = 0; t < kTc8Terms; ++t) {
+            lo[t] = e4m3x2_bits(u[t][0], u[t][1]) | (e4m3x2_bits(u[t][2], u[t][3]) << 16);
+            hi[t] = e4m3x2_bits(u[t][4], u[t][5]) | (e4m3x2_bits(u[t][6], u[t][7]) << 16);
         }
         if (live)
 #pragma unroll
@@ -310,17 +338,19 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         b2 += __shfl_xor_sync(0xffffffffu, b2, off);
     }
+    // (wred's last use, the third maximum, ended at a barrier; wred2 is fresh)
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) wred[threadIdx.x >> 5] = l1;
-    __syncthreads();
-    float L = 0.f;
-    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) L += wred[i];
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) wred[threadIdx.x >> 5] = b2;
+    if ((threadIdx.x & 31) == 0) {
+        wred[threadIdx.x >> 5] = l1;
+        wred2[threadIdx.x >> 5] = b2;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        float B = 0.f;
-        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) B += wred[i];
+        float L = 0.f, B = 0.f;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) {
+            L += wred[i];
+            B += wred2[i];
+        }
         row_terms[m] = (valid && B > kTermsThreshold * L) ? 3 : 2;
     }
 }
