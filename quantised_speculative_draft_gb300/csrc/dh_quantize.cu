@@ -10,7 +10,11 @@
 //
 // Every arithmetic step uses the explicitly rounded intrinsics (no contraction into FMA),
 // division is correctly rounded, rintf rounds half to even: the result is bit-exact with the
-// definition.  The kernel is HBM-bound (2 bytes read per weight, BITS/8 + 1/32 written).
+// definition.  The per-weight division is replaced by a product with the group's reciprocal
+// wherever that provably gives the same code (quant_code), because a correctly rounded
+// division per weight -- a reciprocal on the SM's few special-function units, a rounding and a
+// float-to-int conversion -- bound the kernel far below the HBM rate (2 bytes read per weight,
+// BITS/8 + 1/32 written).
 //
 // An fp8 head (kernel (1) with the e4m3 input): row n's weights are the fp32 products
 // e4m3(b) * wsc[n] (radiance_drafthead.py, _quantize_head_now, the fp8 weight pre-scaled by its
@@ -46,6 +50,47 @@ __device__ __forceinline__ float lanes_max(float v)
     return v;
 }
 
+// The code q = clamp(rne(fl32(fl32(w / sc) + zp)), 0, L) of one weight, without a division in the
+// common case.  With rcp = fl32(1 / sc), t = fma(w, rcp, zp) (one rounding) differs from the
+// defining t* = fl32(fl32(w / sc) + zp) by less than 2^-24 (4 |t| + 4 L + 4) (the reciprocal's
+// and the quotient's roundings of |w / sc| <= |t| + L, the sums' of |t|), below the margin
+// 2^-21 (|t| + 16) for L <= 15; so where t lies farther than the margin from every
+// half-integer, rne(t) = rne(t*) and the cheap code is the exact one.  t is clamped to [0, L]
+// first (the code's own clamp: no boundary is left at the ends, and a clamped t sits half a
+// unit from the nearest one), then rounded to an integer by adding 1.5 2^23 (round to nearest
+// even on the unit grid), whose bits give the code.  Within the margin the defining division
+// decides (a few weights in ten thousand).
+__device__ __forceinline__ uint32_t quant_code(float w, float sc, float rcp, float zp, float L)
+{
+    constexpr float kMagic = 12582912.0f; // 1.5 2^23
+    const float tc = fminf(fmaxf(__fmaf_rn(w, rcp, zp), 0.0f), L);
+    const float sm = __fadd_rn(tc, kMagic);
+    const float r = __fsub_rn(sm, kMagic);
+    uint32_t q = static_cast<uint32_t>(__float_as_int(sm) - __float_as_int(kMagic));
+    // distance to the nearest half-integer: | |tc - r| - 1/2 |
+    if (fabsf(__fsub_rn(fabsf(__fsub_rn(tc, r)), 0.5f)) <= __fmaf_rn(tc, 0x1p-21f, 0x1p-17f)) {
+        const float re = rintf(__fadd_rn(__fdiv_rn(w, sc), zp));
+        q = static_cast<uint32_t>(fminf(fmaxf(re, 0.0f), L));
+    }
+    return q;
+}
+
+// min / max over the whole warp in one instruction each (groups of 128: every lane holds four
+// weights of each group of the span)
+__device__ __forceinline__ float warp_min_f32(float v)
+{
+    float r;
+    asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ float warp_max_f32(float v)
+{
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // kFp8: W holds e4m3 bytes and wsc the per-row fp32 scales; otherwise W holds bf16.
 // G: the group size, 128 (the head) or 64 (the page's group-size ablation: each plane's 128 k
 // of a span are two groups, lanes 0-15 and 16-31).
@@ -64,7 +109,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
     const int NS = PS / 128;    // spans per row
     const int NGt = H / G;      // groups per row
     // work items (n, s) = warp w, w + nwarps, ...: the position advances by (dn, ds) with no
-    // division in the loop, and the next item's weights are loaded before this one is quantised
+    // division in the loop, and the next two items' weights are in flight while this one is
+    // quantised (2 KB per warp: enough loads outstanding to cover the HBM latency)
     const int nwarps = gridDim.x * (blockDim.x >> 5);
     const int dn = nwarps / NS, ds = nwarps - dn * NS;
     const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -82,16 +128,24 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
             }
         }
     };
-    Raw raw[P];
-    if (n < V) load(n, s, raw);
-    while (n < V) {
-        int nn = n + dn, ns = s + ds;
-        if (ns >= NS) {
-            ns -= NS;
-            ++nn;
+    auto advance = [&](int &an, int &as) {
+        an += dn;
+        as += ds;
+        if (as >= NS) {
+            as -= NS;
+            ++an;
         }
-        Raw next[P];
-        if (nn < V) load(nn, ns, next);
+    };
+    Raw raw[P], next[P];
+    if (n < V) load(n, s, raw);
+    int nn = n, ns = s;
+    advance(nn, ns);
+    if (nn < V) load(nn, ns, next);
+    while (n < V) {
+        int n2 = nn, s2 = ns;
+        advance(n2, s2);
+        Raw next2[P];
+        if (n2 < V) load(n2, s2, next2);
         // four weights of each plane: k = p*PS + 128 s + 4 lane + i
         float wv[P][4];
         if constexpr (kFp8) {
@@ -111,36 +165,78 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
             }
         }
         uint32_t word = 0;
+        if constexpr (G == 128) {
+            // the span's P groups each cover the whole warp: one reduction instruction per
+            // extremum, then lane l computes the scale, zero point and reciprocal of group
+            // l % P once (not every lane every group) and the others fetch them
+            float lo[P], hi[P];
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const float *w = wv[p];
-            float lo = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
-            float hi = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-            lo = lanes_min<G / 4>(lo);
-            hi = lanes_max<G / 4>(hi);
-            float sc = __fdiv_rn(__fsub_rn(hi, lo), L);
-            sc = fmaxf(sc, 1e-8f);
-            float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), L);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float r = rintf(__fadd_rn(__fdiv_rn(w[i], sc), zp));
-                uint32_t qv = static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), L));
-                word |= qv << (8 * i + BITS * p);
+            for (int p = 0; p < P; ++p) {
+                const float *w = wv[p];
+                lo[p] = warp_min_f32(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
+                hi[p] = warp_max_f32(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
             }
-            if ((lane & (G / 4 - 1)) == p) {
-                const float sb = __fmul_rn(B, sc);
-                const long long gi = (static_cast<long long>(p) * NS + s) * (128 / G) +
-                                     lane / (G / 4);
+            const int gp = lane & (P - 1);
+            float glo = lo[0], ghi = hi[0];
+#pragma unroll
+            for (int p = 1; p < P; ++p)
+                if (gp == p) {
+                    glo = lo[p];
+                    ghi = hi[p];
+                }
+            const float gsc = fmaxf(__fdiv_rn(__fsub_rn(ghi, glo), L), 1e-8f);
+            const float gzp = fminf(fmaxf(rintf(__fdiv_rn(-glo, gsc)), 0.0f), L);
+            const float grcp = __frcp_rn(gsc);
+            if (lane < P) {
+                const float sb = __fmul_rn(B, gsc);
+                const long long gi = static_cast<long long>(lane) * NS + s;
                 S[static_cast<long long>(n) * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
                 ZS[static_cast<long long>(n) * NGt + gi] =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(zp, sc))));
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(gzp, gsc))));
+            }
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const float sc = __shfl_sync(0xffffffffu, gsc, p);
+                const float zp = __shfl_sync(0xffffffffu, gzp, p);
+                const float rcp = __shfl_sync(0xffffffffu, grcp, p);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    word |= quant_code(wv[p][i], sc, rcp, zp, L) << (8 * i + BITS * p);
+            }
+        } else {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const float *w = wv[p];
+                float lo = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
+                float hi = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+                lo = lanes_min<G / 4>(lo);
+                hi = lanes_max<G / 4>(hi);
+                float sc = __fdiv_rn(__fsub_rn(hi, lo), L);
+                sc = fmaxf(sc, 1e-8f);
+                float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), L);
+                const float rcp = __frcp_rn(sc);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) word |= quant_code(w[i], sc, rcp, zp, L) << (8 * i + BITS * p);
+                if ((lane & (G / 4 - 1)) == p) {
+                    const float sb = __fmul_rn(B, sc);
+                    const long long gi = (static_cast<long long>(p) * NS + s) * (128 / G) +
+                                         lane / (G / 4);
+                    S[static_cast<long long>(n) * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
+                    ZS[static_cast<long long>(n) * NGt + gi] =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(zp, sc))));
+                }
             }
         }
         reinterpret_cast<uint32_t *>(packed + static_cast<long long>(n) * PS + 128 * s)[lane] = word;
 #pragma unroll
-        for (int p = 0; p < P; ++p) raw[p] = next[p];
+        for (int p = 0; p < P; ++p) {
+            raw[p] = next[p];
+            next[p] = next2[p];
+        }
         n = nn;
         s = ns;
+        nn = n2;
+        ns = s2;
     }
 }
 
@@ -186,12 +282,10 @@ __global__ void __launch_bounds__(256) quantize_c4_kernel(const uint16_t *__rest
         float sc = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
         sc = fmaxf(sc, 1e-8f);
         const float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), 3.0f);
+        const float rcp = __frcp_rn(sc);
         uint32_t word = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float r = rintf(__fadd_rn(__fdiv_rn(w[i], sc), zp));
-            word |= static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 3.0f)) << (2 * i);
-        }
+        for (int i = 0; i < 16; ++i) word |= quant_code(w[i], sc, rcp, zp, 3.0f) << (2 * i);
         if ((lane & 7) == 0) {
             const float s4 = __fmul_rn(4.0f, sc);
             const long long gi = 4LL * s + (lane >> 3);
