@@ -648,7 +648,7 @@ int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank)
     const int path = choose_path(M, H);
     if (path < 0) return 0;
     int prep = 1, coarse = (M + kWarpBatch - 1) / kWarpBatch;
-    if (path == DH_PATH_TC) prep = coarse = tc8_chunks(M, kPackQuarter2);
+    if (path == DH_PATH_TC) coarse = tc8_chunks(M, kPackQuarter2); // one staging launch
     else if (path == DH_PATH_TC_BF16) coarse = tc_launches(M);
     else if (path == DH_PATH_CORE) coarse = 1;
     if (select_rerank_fits(rerank, kcand)) return prep + coarse + 1; // fused select + rerank

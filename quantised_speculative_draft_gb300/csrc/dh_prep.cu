@@ -211,15 +211,21 @@ __device__ __forceinline__ Split3 split3(float r0, float k2, float ik2, float k3
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// The coarse launches of one forward (batch chunks of up to 32 rows, padded to MP): one
+// staging launch covers them all, block b staging row b - first[c] of chunk c.
+constexpr int kMaxPrepChunks = 8; // 128 rows in chunks of 16
+struct PrepChunks {
+    int n;
+    int first[kMaxPrepChunks + 1]; // first block of each chunk; first[n] = the grid
+    int m0[kMaxPrepChunks], rows[kMaxPrepChunks], MP[kMaxPrepChunks];
+    uint8_t *xt8[kMaxPrepChunks];  // the chunk's staged x
+    float *small[kMaxPrepChunks];  // the chunk's group sums, row factors and term counts
+};
+
 // G: the group size of the sums (128, or 64 for the group-size ablation).
 template <int G>
 __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_t *__restrict__ x,
-                                                                   int H, int m0, int rows, int MP,
-                                                                   uint8_t *__restrict__ xt8,
-                                                                   float *__restrict__ xs2,
-                                                                   float *__restrict__ xs3,
-                                                                   float *__restrict__ row_f,
-                                                                   int *__restrict__ row_terms,
+                                                                   int H, const PrepChunks ch,
                                                                    int *__restrict__ counters,
                                                                    int ncounters)
 {
@@ -227,10 +233,18 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
     __shared__ float wred2[kPrepMaxThreads / 32];
     // the coarse pass may be scheduled now: it waits for this grid before it reads x
     pdl_trigger();
-    const int m = blockIdx.x;
+    int c = 0;
+    while (c + 1 < ch.n && static_cast<int>(blockIdx.x) >= ch.first[c + 1]) ++c;
+    const int m = static_cast<int>(blockIdx.x) - ch.first[c];
+    const int m0 = ch.m0[c], rows = ch.rows[c], MP = ch.MP[c];
+    uint8_t *const xt8 = ch.xt8[c];
+    float *const xs2 = ch.small[c];
+    float *const xs3 = xs2 + static_cast<size_t>(kTc8MaxMP) * (H / 64);
+    float *const row_f = xs2 + 2 * static_cast<size_t>(kTc8MaxMP) * (H / 64);
+    int *const row_terms = reinterpret_cast<int *>(row_f + 3 * kTc8MaxMP);
     const bool valid = m < rows;
     const int octs = H / 8, NGt = H / G;
-    if (counters && m == 0)
+    if (counters && blockIdx.x == 0)
         for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
     const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
 
@@ -358,23 +372,27 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
 cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, int pack, const Tc8Workspace &w,
                             int *counters, int ncounters, cudaStream_t stream)
 {
-    for (int c = 0; c < tc8_chunks(M, pack); ++c) {
+    PrepChunks ch;
+    ch.n = tc8_chunks(M, pack);
+    if (ch.n > kMaxPrepChunks) return cudaErrorInvalidValue;
+    int blocks = 0;
+    for (int c = 0; c < ch.n; ++c) {
         const Tc8Chunk k = tc8_chunk(M, c, pack, H);
-        auto kern = w.group == 64 ? prep_fp8_kernel<64> : prep_fp8_kernel<128>;
-        float *const small = w.small + static_cast<size_t>(c) * tc8_small_floats(H);
-        float *const xs2 = small;
-        float *const xs3 = small + static_cast<size_t>(kTc8MaxMP) * (H / 64);
-        float *const row_f = small + 2 * static_cast<size_t>(kTc8MaxMP) * (H / 64);
-        int *const terms = reinterpret_cast<int *>(row_f + 3 * kTc8MaxMP);
-        // one thread per 16-byte slice of the row (a multiple of 32 threads)
-        int threads = ((H / 8 + 31) / 32) * 32;
-        if (threads > kPrepMaxThreads) threads = kPrepMaxThreads;
-        kern<<<k.MP, threads, 0, stream>>>(x, H, k.m0, k.rows, k.MP, w.xt8 + k.x_off, xs2, xs3,
-                                           row_f, terms, c == 0 ? counters : nullptr, ncounters);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        ch.first[c] = blocks;
+        ch.m0[c] = k.m0;
+        ch.rows[c] = k.rows;
+        ch.MP[c] = k.MP;
+        ch.xt8[c] = w.xt8 + k.x_off;
+        ch.small[c] = w.small + static_cast<size_t>(c) * tc8_small_floats(H);
+        blocks += k.MP;
     }
-    return cudaSuccess;
+    ch.first[ch.n] = blocks;
+    auto kern = w.group == 64 ? prep_fp8_kernel<64> : prep_fp8_kernel<128>;
+    // one thread per 16-byte slice of the row (a multiple of 32 threads)
+    int threads = ((H / 8 + 31) / 32) * 32;
+    if (threads > kPrepMaxThreads) threads = kPrepMaxThreads;
+    kern<<<blocks, threads, 0, stream>>>(x, H, ch, counters, ncounters);
+    return cudaGetLastError();
 }
 
 } // namespace dh
