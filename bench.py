@@ -915,7 +915,7 @@ def run_reference(args):
     orc.forward(xb, pc, Sc, ZSc, Wb, KCAND, RERANK, TOPK)
     t_full = (time.perf_counter() - t0) * (V_FULL / Vc)
     budget = min(t_full, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
-    Vs = int(V_FULL * budget / t_full) // 64 * 64
+    Vs = V_FULL if budget >= t_full else int(V_FULL * budget / t_full) // 64 * 64
     Vs = max(Vc, min(V_FULL, Vs))
     packed, S, ZS = orc.quantize(Wb[:Vs])
     times = []
