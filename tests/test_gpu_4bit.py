@@ -56,6 +56,8 @@ def test_quantize4_bit_exact(V, H):
     (33, 1536, 6144, 4, 24, 5),           # three batch chunks (16 + 16 + 1 rows)
     (64, 1024, 4096, 8, 64, 16),          # RERANK 64, top-16
     (16, 5120, 40000 + 37, 1, 32, 1),     # 313 tiles of 128 rows: every CTA runs two or more
+    (128, 1024, 4096 + 64 * 2 + 9, 1, 32, 1),  # eight 16-row chunks: one staging launch for all
+    (113, 512, 3000, 4, 32, 3),           # eight chunks, the last of one row
 ])
 def test_forward4_matches_the_oracle(M, H, V, kcand, R, k):
     wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
