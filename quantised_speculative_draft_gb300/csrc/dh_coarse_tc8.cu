@@ -90,8 +90,21 @@ template <bool kTwoSets> struct Roles {
     static constexpr int kEp0 = kTwoSets ? 12 : 8;           // first epilogue warp
     static constexpr int kSel0 = kEp0 + kEpWarps + 1;        // the two selection warps
     static constexpr int kSel1 = kEp0 + kEpWarps + 2;
-    static constexpr int kWarps = kEp0 + kEpWarps + 3;       // + the plane-3 issuer, selection
+    // + the plane-3 issuer, the selection warps and one idle warp: whole warpgroups, so that
+    // every warpgroup can set its own register budget
+    static constexpr int kWarps = kEp0 + kEpWarps + 4;
     static constexpr int kThreads = 32 * kWarps;
+    // registers a thread: at launch (the kernel's count, checked on the host), then per
+    // warpgroup -- the TMA / issuer and the issuer / selection warpgroups give registers to
+    // the epilogue's; the budgets add up to the launch's exactly
+    static constexpr int kRegsLaunch = kTwoSets ? 80 : 96;
+    static constexpr int kRegsLight = 64;
+    static constexpr int kRegsDq = kTwoSets ? 80 : 96;
+    static constexpr int kRegsEp = (kRegsLaunch * (kWarps / 4) - 2 * kRegsLight -
+                                    (kTwoSets ? 2 : 1) * kRegsDq) / 2;
+    static_assert(kWarps % 4 == 0, "whole warpgroups");
+    static_assert(2 * kRegsLight + (kTwoSets ? 2 : 1) * kRegsDq + 2 * kRegsEp ==
+                      kRegsLaunch * (kWarps / 4), "register budgets must add up");
     __device__ static int issuer_plane(int warp)
     {
         return (warp >= 1 && warp <= 3) ? warp - 1 : (warp == kEp0 + kEpWarps ? 3 : -1);
@@ -397,7 +410,11 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
     const int first_tile = blockIdx.x, tile_step = gridDim.x;
     bool failed = false;
 
+    // Register budgets per warpgroup, set at the top of each role's branch (every warp of a
+    // warpgroup sets the same value): the TMA / issuer and the issuer / selection / idle
+    // warpgroups drop to kRegsLight, the epilogue's two rise to kRegsEp.
     if (warp == kWarpTma) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R::kRegsLight));
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
@@ -444,6 +461,7 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
             }
         }
     } else if (R::issuer_plane(warp) >= 0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R::kRegsLight));
         // ---------------- MMA issuers: one warp per plane, every unit holding that plane ------
         // The whole warp runs the loop (warp-uniform operands); one elected lane issues.
         constexpr uint32_t idesc = make_idesc_f8(N);
@@ -613,6 +631,7 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
             run(std::integral_constant<int, 0>{});
         }
     } else if (warp >= kWarpEp0 && warp < kWarpEp0 + kEpWarps) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R::kRegsEp));
         // ---------------- epilogue: two halves of four warps, each two groups of every span ---
         const int h = (warp - kWarpEp0) >> 2; // planes 2h, 2h + 1
         const int row = ((warp & 3) << 5) | lane;
@@ -733,6 +752,7 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
             if (lane == 0) mbar_arrive(red_full);
         }
     } else if (warp == R::kSel0 || warp == R::kSel1) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R::kRegsLight));
         // ---------------- block top-KCAND: pair = (batch column m, block b of the tile) ------
         // the tile's coarse values are the sums of the two epilogue halves (both -inf past V)
         const int npairs = 2 * prm.mrows;
@@ -796,6 +816,9 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
             __syncwarp();
             if (lane == 0) mbar_arrive(red_free);
         }
+    } else if (warp == R::kWarps - 1) {
+        // the idle warp that completes the last warpgroup gives its registers up too
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R::kRegsLight));
     }
 
     // ---- teardown: every role is done (or gave up); release tensor memory ----
@@ -868,6 +891,14 @@ cudaError_t launch_cfg(const CUtensorMap &tm_packed, const uint8_t *xt8_chunk,
     // the shared-memory limit is a per-device attribute: raised once on every device
     static PerDeviceOnce attr;
     cudaError_t e = attr.run([] {
+        // the warpgroups' register budgets (setmaxnreg) add up to the launch's registers a
+        // thread times its threads: a kernel built with another count could wait forever for
+        // registers in setmaxnreg.inc, so it is not launched
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, coarse_tc8_kernel<MP, PACK>);
+        if (err != cudaSuccess) return err;
+        if (fa.numRegs != Roles<two_sets<MP, PACK>()>::kRegsLaunch)
+            return cudaErrorInvalidConfiguration;
         return cudaFuncSetAttribute(coarse_tc8_kernel<MP, PACK>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit8);
     });
