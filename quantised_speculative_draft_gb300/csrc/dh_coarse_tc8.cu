@@ -98,7 +98,8 @@ template <bool kTwoSets> struct Roles {
     // warpgroup -- the TMA / issuer and the issuer / selection warpgroups give registers to
     // the epilogue's; the budgets add up to the launch's exactly
     static constexpr int kRegsLaunch = kTwoSets ? 80 : 96;
-    static constexpr int kRegsLight = 64;
+    // light warpgroups: 48 in 24-warp launches, 64 in 20-warp ones (each measured faster)
+    static constexpr int kRegsLight = kTwoSets ? 48 : 64;
     static constexpr int kRegsDq = kTwoSets ? 80 : 96;
     static constexpr int kRegsEp = (kRegsLaunch * (kWarps / 4) - 2 * kRegsLight -
                                     (kTwoSets ? 2 : 1) * kRegsDq) / 2;
@@ -124,6 +125,10 @@ template <int MP, int PACK, int T_> struct Cfg8 {
     static constexpr int G = PACK == kPackG64 ? 64 : 128;   // weight group size
     static constexpr int kGPP = 128 / G;                    // groups per plane of a span
     static constexpr int kU = (MP == 16 && G == 128 && T == 2) ? 1 : 2; // units per span
+    // two dequant sets, each a k half of every plane (2-bit layouts) or one packed box (4-bit
+    // head), for the whole-span units of 16-row launches (for 32-row launches the second set
+    // measured slower)
+    static constexpr int kDqSets = kU == 1 ? 2 : 1;
     static constexpr int kPP = 4 / kU;                      // planes per unit
     static constexpr uint32_t kACols = 32 * kPP;
     static constexpr uint32_t kSlotCols = kACols + kPP * kGPP * N; // one accumulator per group
@@ -324,7 +329,7 @@ __device__ __forceinline__ void select_pair2(bool live, const float *vals0, cons
 }
 
 // Two dequant sets exactly when the two-term body has one unit per span.
-template <int MP, int PACK> constexpr bool two_sets() { return Cfg8<MP, PACK, 2>::kU == 1; }
+template <int MP, int PACK> constexpr bool two_sets() { return Cfg8<MP, PACK, 2>::kDqSets == 2; }
 
 // The kernel body for a launch whose rows take TT x terms (see Cfg8).
 template <int MP, int PACK, int TT>
@@ -339,7 +344,7 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
     constexpr int N = C::N, T = C::T, K = C::K, kU = C::kU, kPP = C::kPP;
     constexpr int kGU = kPP * kGPP;         // weight groups (accumulators) of a unit
     using R = Roles<two_sets<MP, PACK>()>;
-    constexpr int kDqSets = kU == 1 ? 2 : 1; // dequant warp sets (split each span's planes)
+    constexpr int kDqSets = C::kDqSets; // dequant warp sets (split each span's planes)
     static_assert(kDqSets == 1 || two_sets<MP, PACK>(), "a second dequant set needs its warps");
     constexpr int kWarpEp0 = R::kEp0;
     constexpr uint32_t kSlotCols = C::kSlotCols, kACols = C::kACols;
