@@ -104,6 +104,12 @@ template <bool kTwoSets> struct Roles {
     static constexpr int kRegsEp = (kRegsLaunch * (kWarps / 4) - 2 * kRegsLight -
                                     (kTwoSets ? 2 : 1) * kRegsDq) / 2;
     static_assert(kWarps % 4 == 0, "whole warpgroups");
+    // the dequant branch sets no budget: its warpgroups keep the launch's, and only the light
+    // and epilogue branches move registers (a setmaxnreg.inc that asks for more than the decs
+    // free waits forever)
+    static_assert(kRegsDq == kRegsLaunch, "the dequant warpgroups keep the launch budget");
+    static_assert(2 * (kRegsLaunch - kRegsLight) == 2 * (kRegsEp - kRegsLaunch),
+                  "the epilogue takes exactly what the light warpgroups free");
     static_assert(2 * kRegsLight + (kTwoSets ? 2 : 1) * kRegsDq + 2 * kRegsEp ==
                       kRegsLaunch * (kWarps / 4), "register budgets must add up");
     __device__ static int issuer_plane(int warp)
