@@ -464,19 +464,24 @@ def time_e2e(sets, M, steps):
     """The same call end to end with host buffers: pinned x in, dh_forward, idx/logit out."""
     import torch
     dev = sets[0].x.device
-    ws, idx, logit = make_outputs(M, dev)
+    ws, _, _ = make_outputs(M, dev)
     xh = [s.x[:M].cpu().pin_memory() for s in sets]
     xd = torch.empty(M, H_FULL, dtype=torch.bfloat16, device=dev)
-    ih = torch.empty(M, TOPK, dtype=torch.int32).pin_memory()
-    lh = torch.empty(M, TOPK, dtype=torch.float32).pin_memory()
+    # idx and logit side by side in one device buffer (each part 16-byte aligned), read back
+    # with one copy
+    n = M * TOPK
+    half = (n + 3) // 4 * 4
+    out = torch.empty(2 * half, dtype=torch.int32, device=dev)
+    idx = out[:n].view(M, TOPK)
+    logit = out[half:half + n].view(torch.float32).view(M, TOPK)
+    outh = torch.empty(2 * half, dtype=torch.int32).pin_memory()
     import quantised_speculative_draft_gb300 as dh
 
     def one(i):
         s = sets[i % len(sets)]
         xd.copy_(xh[i % len(sets)], non_blocking=True)
         dh.dh_forward(xd, s.packed, s.S, s.ZS, s.W, KCAND, RERANK, TOPK, idx, logit, ws)
-        ih.copy_(idx, non_blocking=True)
-        lh.copy_(logit, non_blocking=True)
+        outh.copy_(out, non_blocking=True)
 
     for i in range(5):
         one(i)
@@ -487,7 +492,7 @@ def time_e2e(sets, M, steps):
         one(i)
     e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / steps, M * H_FULL * 2, M * TOPK * 8
+    return e0.elapsed_time(e1) * 1e3 / steps, M * H_FULL * 2, 2 * half * 4
 
 
 def exact_topk_ids(x, W, k):
