@@ -160,6 +160,21 @@ struct Tc8Params {
     int *timeout_flag;
 };
 
+// L2 prefetch of one [128 rows x 128 B] box of a 2-D tensor map (x a multiple of 16 bytes),
+// and of a contiguous byte range (address and size multiples of 16).
+__device__ __forceinline__ void prefetch_l2_box(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2_bytes(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // kind::f8f6f4 instruction descriptor: D f32, A e4m3, B e4m3, both K-major, M = 128, N.
 __host__ __device__ constexpr uint32_t make_idesc_f8(int N)
 {
@@ -379,7 +394,8 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
     uint64_t *const red_free = red_full + 1;  // [1]      selection -> epilogue: `red` free
     uint64_t *const sz_full = red_free + 1;   // [2]      bulk copy -> epilogue: S, ZS of a tile
     uint64_t *const sz_empty = sz_full + 2;   // [2]      epilogue (8 warps) -> bulk copy
-    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(sz_empty + 2);
+    uint64_t *const xs_full = sz_empty + 2;   // [1]      epilogue (8 warps): xs, 2^-e, weights
+    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(xs_full + 1);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_packed);
@@ -400,18 +416,11 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
             mbar_init(&sz_full[i], 1);
             mbar_init(&sz_empty[i], kEpWarps);
         }
+        mbar_init(xs_full, kEpWarps);
         fence_barrier_init();
     }
-    const float *const xsrc = T == 3 ? prm.xs3 : prm.xs2;
-    for (int i = threadIdx.x; i < NGt * MP; i += blockDim.x) {
-        const int g = i / MP, m = i - g * MP;
-        xs_s[i] = xsrc[static_cast<long long>(m) * NGt + g];
-    }
-    for (int i = threadIdx.x; i < MP; i += blockDim.x) {
-        inv_s[i] = prm.row_f[i];
-        tw_s[i] = prm.row_f[kTc8MaxMP + i];
-        tw_s[MP + i] = prm.row_f[2 * kTc8MaxMP + i];
-    }
+    // (the group sums, 2^-e and the term weights are read by the epilogue only: its warps load
+    // them, so that their global-memory latency stays off the start of the weight stream)
     if (warp == kWarpTma) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -644,6 +653,24 @@ __device__ __forceinline__ void coarse_tc8_body(const CUtensorMap &tm_packed, co
     } else if (warp >= kWarpEp0 && warp < kWarpEp0 + kEpWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R::kRegsEp));
         // ---------------- epilogue: two halves of four warps, each two groups of every span ---
+        {
+            // the batch rows' group sums (scaled units), 2^-e and term weights, shared by the
+            // eight epilogue warps (written by all of them, read after every one has arrived)
+            const int et = static_cast<int>(threadIdx.x) - 32 * kWarpEp0;
+            const float *const xsrc = T == 3 ? prm.xs3 : prm.xs2;
+            for (int i = et; i < NGt * MP; i += 32 * kEpWarps) {
+                const int g = i / MP, m = i - g * MP;
+                xs_s[i] = xsrc[static_cast<long long>(m) * NGt + g];
+            }
+            for (int i = et; i < MP; i += 32 * kEpWarps) {
+                inv_s[i] = prm.row_f[i];
+                tw_s[i] = prm.row_f[kTc8MaxMP + i];
+                tw_s[MP + i] = prm.row_f[2 * kTc8MaxMP + i];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xs_full);
+            if (!warp_wait(xs_full, 0, prm.timeout_flag)) failed = true;
+        }
         const int h = (warp - kWarpEp0) >> 2; // planes 2h, 2h + 1
         const int row = ((warp & 3) << 5) | lane;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
@@ -849,6 +876,22 @@ __global__ void __launch_bounds__(Roles<two_sets<MP, PACK>()>::kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_x3, const Tc8Params prm)
 {
     extern __shared__ uint8_t smem_raw[];
+    // before the x staging is known to be done: the weights are the caller's, so the first
+    // two spans of this CTA's first tile and the tile's S / ZS rows can already move to L2
+    if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < prm.ntiles) {
+        constexpr int kBoxes = PACK == kPackHalf4 ? 2 : 1;
+        const int tile = blockIdx.x;
+        prefetch_tensormap(&tm_packed);
+#pragma unroll
+        for (int b = 0; b < 2 * kBoxes; ++b) prefetch_l2_box(&tm_packed, b * kSpanBytes, tile * kTileRows);
+        const int NGt = prm.H / (PACK == kPackG64 ? 64 : 128);
+        if ((tile + 1) * kTileRows <= prm.V) {
+            const size_t off = static_cast<size_t>(tile) * kTileRows * NGt;
+            const uint32_t bytes = static_cast<uint32_t>(kTileRows) * NGt * 2;
+            prefetch_l2_bytes(prm.S + off, bytes);
+            prefetch_l2_bytes(prm.ZS + off, bytes);
+        }
+    }
     // launched while the x staging may still run: everything below reads its output
     pdl_wait();
     int need = 2;
