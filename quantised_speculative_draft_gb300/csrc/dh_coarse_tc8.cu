@@ -23,7 +23,7 @@
 //     with xs' the group sums of the represented x (in the scaled units): the scale and zero
 //     are applied to the fp32 partial of every group, never to the weight.
 //
-// Roles (23 or 19 warps, one CTA per SM, persistent over 128-row vocabulary tiles).  The unit of
+// Roles (24 or 20 warps, one CTA per SM, persistent over 128-row vocabulary tiles).  The unit of
 // handoff is a span (N = 32: the four planes of 512 k) or half a span (larger N: planes 2u,
 // 2u+1); unit q uses tensor-memory slot q % 2 (an A buffer and one accumulator per group).
 // Issuing a tcgen05.mma holds the issuing warp for many cycles, so each plane has its own issuer
@@ -47,9 +47,12 @@
 //                 planes 2h, 2h+1 of every span -- tcgen05.ld of the partials, recombination of
 //                 the terms, scale/zero fold into fp32 registers -- and at the tile end writes its
 //                 half of the coarse values; the selection warp adds the halves
-//   last 2 warps  block top-KCAND of the previous tile (overlaps the current one): two lanes
+//   next 2 warps  block top-KCAND of the previous tile (overlaps the current one): two lanes
 //                 per (batch column, block) pair each keep an insertion list of the best 8 of
 //                 their 32 rows, then merge
+//   last warp     idle: it completes the last warpgroup, so that each warpgroup can set its own
+//                 register budget (setmaxnreg: the TMA / issuer and issuer / selection / idle
+//                 warpgroups give registers to the epilogue's)
 // Every handoff is an mbarrier; every wait is bounded.
 //
 // The 4-bit head (BITS = 4, half split, bias 16; _quantize_head_now's 4-bit variant) runs the
