@@ -11,7 +11,7 @@
 // Every arithmetic step uses the explicitly rounded intrinsics (no contraction into FMA),
 // division is correctly rounded, rintf rounds half to even: the result is bit-exact with the
 // definition.  The per-weight division is replaced by a product with the group's reciprocal
-// wherever that provably gives the same code (quant_code), because a correctly rounded
+// wherever that provably gives the same code (quant_pair), because a correctly rounded
 // division per weight -- a reciprocal on the SM's few special-function units, a rounding and a
 // float-to-int conversion -- bound the kernel far below the HBM rate (2 bytes read per weight,
 // BITS/8 + 1/32 written).
@@ -50,29 +50,109 @@ __device__ __forceinline__ float lanes_max(float v)
     return v;
 }
 
-// The code q = clamp(rne(fl32(fl32(w / sc) + zp)), 0, L) of one weight, without a division in the
-// common case.  With rcp = fl32(1 / sc), t = fma(w, rcp, zp) (one rounding) differs from the
-// defining t* = fl32(fl32(w / sc) + zp) by less than 2^-24 (4 |t| + 4 L + 4) (the reciprocal's
-// and the quotient's roundings of |w / sc| <= |t| + L, the sums' of |t|), below the margin
-// 2^-21 (|t| + 16) for L <= 15; so where t lies farther than the margin from every
-// half-integer, rne(t) = rne(t*) and the cheap code is the exact one.  t is clamped to [0, L]
-// first (the code's own clamp: no boundary is left at the ends, and a clamped t sits half a
-// unit from the nearest one), then rounded to an integer by adding 1.5 2^23 (round to nearest
-// even on the unit grid), whose bits give the code.  Within the margin the defining division
-// decides (a few weights in ten thousand).
-__device__ __forceinline__ uint32_t quant_code(float w, float sc, float rcp, float zp, float L)
+// The group's scale and zero point, as defined (both correctly rounded divisions).
+struct GroupParams {
+    float sc, zp;
+};
+
+__device__ __forceinline__ GroupParams group_params(float lo, float hi, float L)
 {
-    constexpr float kMagic = 12582912.0f; // 1.5 2^23
-    const float tc = fminf(fmaxf(__fmaf_rn(w, rcp, zp), 0.0f), L);
-    const float sm = __fadd_rn(tc, kMagic);
-    const float r = __fsub_rn(sm, kMagic);
-    uint32_t q = static_cast<uint32_t>(__float_as_int(sm) - __float_as_int(kMagic));
-    // distance to the nearest half-integer: | |tc - r| - 1/2 |
-    if (fabsf(__fsub_rn(fabsf(__fsub_rn(tc, r)), 0.5f)) <= __fmaf_rn(tc, 0x1p-21f, 0x1p-17f)) {
-        const float re = rintf(__fadd_rn(__fdiv_rn(w, sc), zp));
-        q = static_cast<uint32_t>(fminf(fmaxf(re, 0.0f), L));
-    }
-    return q;
+    const float sc = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), L), 1e-8f);
+    const float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), L);
+    return {sc, zp};
+}
+
+// The defining code of one weight: clamp(rne(fl32(fl32(w / sc) + zp)), 0, L).
+__device__ __forceinline__ uint32_t code_by_definition(float w, GroupParams g, float L)
+{
+    const float re = rintf(__fadd_rn(__fdiv_rn(w, g.sc), g.zp));
+    return static_cast<uint32_t>(fminf(fmaxf(re, 0.0f), L));
+}
+
+// The fast codes of a pair of weights of one group, added into a packed word.
+//
+// With ra = fl32(fl32(1 / sc) fl32(1 / L)) and zb = fl32(zp fl32(1 / L)) (once per group),
+// y = fl32(w ra + zb) is the code's argument divided by L, clamped to [0, 1] by the FMA's
+// saturation (the code's own clamp: clamping to integer ends commutes with rounding to the
+// nearest integer).  Against the defining t* = fl32(fl32(w / sc) + zp), L y is off by at most
+// 2^-24 (6 |w / sc| + 4 zp) (four roundings on the w / sc term and three on zp in L y, two and
+// one in t*).  Where t* lies within one unit of a rounding boundary of [0, L], t* and zp both
+// lie in [0, L], so |w / sc| <= L and the difference is below 10 L 2^-24 <= 2^-16 for L <= 15.
+// So where L y lies farther than 2^-16 from every half-integer, rne(L y) is the defining code;
+// the pair falls back to the definition otherwise (about one weight in a thousand: with bf16
+// weights, sc = (hi - lo) / L often has few significant bits, and exact ties are common).
+//
+// rne(L y) comes from one FMA onto -1.5 2^23, whose bits are those of -1.5 2^23 plus the code in
+// the low mantissa bits; the word adds those bits at each code's position, and the caller
+// removes the constant part once per word (mod 2^32 the magic's bits and the codes add
+// independently, and the codes' fields do not overlap).  The rounding of L y and its distance to
+// the integer run on the paired fp32 units.
+constexpr float kQMagic = 12582912.0f;           // 1.5 2^23
+constexpr uint32_t kQMagicNegBits = 0xCB400000u; // the bits of -1.5 2^23
+constexpr float kQThreshold = 0.5f - 0x1p-16f;   // |L y - rne(L y)| at or above: near a boundary
+
+// The magic's bits summed over n fields at positions 0, step, 2 step, ...
+__host__ __device__ constexpr uint32_t magic_bits_sum(int n, int step)
+{
+    uint32_t c = 0;
+    for (int i = 0; i < n; ++i) c += kQMagicNegBits << (i * step);
+    return c;
+}
+
+__device__ __forceinline__ float fma_sat(float a, float b, float c)
+{
+    float r;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// The correction that turns a pair's fast codes (magic bits b0, b1 at s0, s1) into the defining
+// ones; out of line, so that the rare path costs the unrolled loop no code space.
+__device__ __noinline__ uint32_t pair_by_definition(float w0, float w1, float lo, float hi, float L,
+                                                    uint32_t b0, uint32_t b1, int s0, int s1)
+{
+    const GroupParams g = group_params(lo, hi, L);
+    return ((code_by_definition(w0, g, L) - (b0 - kQMagicNegBits)) << s0) +
+           ((code_by_definition(w1, g, L) - (b1 - kQMagicNegBits)) << s1);
+}
+
+template <int BITS>
+__device__ __forceinline__ void quant_pair(float w0, float w1, float ra, float zb, float lo,
+                                           float hi, int s0, int s1, uint32_t &word)
+{
+    constexpr float L = static_cast<float>((1 << BITS) - 1);
+    const float2 y = make_float2(fma_sat(w0, ra, zb), fma_sat(w1, ra, zb));
+    const float2 m = __ffma2_rn(y, make_float2(-L, -L), make_float2(-kQMagic, -kQMagic));
+    const float2 nr = __fadd2_rn(m, make_float2(kQMagic, kQMagic)); // -rne(L y), exact
+    const float2 d = __ffma2_rn(y, make_float2(L, L), nr);         // L y - rne(L y)
+    const uint32_t b0 = __float_as_uint(m.x), b1 = __float_as_uint(m.y);
+    word += b0 << s0;
+    word += b1 << s1;
+    if (__builtin_expect(fmaxf(fabsf(d.x), fabsf(d.y)) >= kQThreshold, 0))
+        word += pair_by_definition(w0, w1, lo, hi, L, b0, b1, s0, s1);
+}
+
+// The fast path's per-group constants ra, zb.
+template <int BITS>
+__device__ __forceinline__ float2 fast_params(GroupParams g)
+{
+    constexpr float kInvL = 1.0f / static_cast<float>((1 << BITS) - 1); // fl32(1 / L)
+    return make_float2(__fmul_rn(__frcp_rn(g.sc), kInvL), __fmul_rn(g.zp, kInvL));
+}
+
+// Bytes 0 and 1 of v, two e4m3 codes, as fp32: the conversion unit's e4m3 -> f16 pair (every
+// finite e4m3 value is an f16 value), then f16 -> f32; both exact.  (Placing the code's fields
+// in an fp32 word and scaling by 2^120, also exact, measured slower: the integer pipe is the
+// busier one here.)
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t v)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(h2) : "r"(v));
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
 }
 
 // min / max over the whole warp in one instruction each (groups of 128: every lane holds four
@@ -95,7 +175,7 @@ __device__ __forceinline__ float warp_max_f32(float v)
 // G: the group size, 128 (the head) or 64 (the page's group-size ablation: each plane's 128 k
 // of a span are two groups, lanes 0-15 and 16-31).
 template <bool kFp8, int BITS, int G>
-__global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ Wv,
+__global__ void __launch_bounds__(256, 3) quantize_kernel(const void *__restrict__ Wv,
                                                        const float *__restrict__ wsc,
                                                        uint8_t *__restrict__ packed,
                                                        uint16_t *__restrict__ S,
@@ -110,13 +190,17 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
     const int NGt = H / G;      // groups per row
     // work items (n, s) = warp w, w + nwarps, ...: the position advances by (dn, ds) with no
     // division in the loop, and the next two items' weights are in flight while this one is
-    // quantised (2 KB per warp: enough loads outstanding to cover the HBM latency)
+    // quantised (2 KB per warp: enough loads outstanding to cover the HBM latency).  The three
+    // items' registers form a ring that the loop body, unrolled three times, walks without
+    // copies.
     const int nwarps = gridDim.x * (blockDim.x >> 5);
     const int dn = nwarps / NS, ds = nwarps - dn * NS;
     const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    int n = w0 / NS, s = w0 - (w0 / NS) * NS;
     using Raw = typename std::conditional<kFp8, uint32_t, uint2>::type;
-    auto load = [&](int rn, int rs, Raw (&raw)[P]) {
+    // an item's weights and, for the fp8 head, its row scale
+    auto load = [&](int rn, int rs, Raw (&raw)[P], float &rsc) {
+        if (rn >= V) return;
+        if constexpr (kFp8) rsc = __ldg(wsc + rn);
 #pragma unroll
         for (int p = 0; p < P; ++p) {
             if constexpr (kFp8) {
@@ -128,33 +212,26 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
             }
         }
     };
-    auto advance = [&](int &an, int &as) {
-        an += dn;
-        as += ds;
+    auto advance = [&](int &an, int &as, int fn, int fs) {
+        an = fn + dn;
+        as = fs + ds;
         if (as >= NS) {
             as -= NS;
             ++an;
         }
     };
-    Raw raw[P], next[P];
-    if (n < V) load(n, s, raw);
-    int nn = n, ns = s;
-    advance(nn, ns);
-    if (nn < V) load(nn, ns, next);
-    while (n < V) {
-        int n2 = nn, s2 = ns;
-        advance(n2, s2);
-        Raw next2[P];
-        if (n2 < V) load(n2, s2, next2);
-        // four weights of each plane: k = p*PS + 128 s + 4 lane + i
+    // one item: lane l holds four weights of each plane, k = p PS + 128 s + 4 l + i
+    auto process = [&](const Raw (&raw)[P], float rs, int n, int s) {
         float wv[P][4];
         if constexpr (kFp8) {
-            const float rs = __ldg(wsc + n);
 #pragma unroll
             for (int p = 0; p < P; ++p)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    wv[p][i] = __fmul_rn(e4m3_to_f32(raw[p] >> (8 * i)), rs);
+                for (int i = 0; i < 4; i += 2) {
+                    const float2 v = __fmul2_rn(e4m3x2_to_f32x2(raw[p] >> (8 * i)), make_float2(rs, rs));
+                    wv[p][i] = v.x;
+                    wv[p][i + 1] = v.y;
+                }
         } else {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
@@ -165,11 +242,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
             }
         }
         uint32_t word = 0;
+        float lo[P], hi[P];
         if constexpr (G == 128) {
             // the span's P groups each cover the whole warp: one reduction instruction per
-            // extremum, then lane l computes the scale, zero point and reciprocal of group
+            // extremum, then lane l computes the scale, zero point and fast constants of group
             // l % P once (not every lane every group) and the others fetch them
-            float lo[P], hi[P];
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 const float *w = wv[p];
@@ -184,59 +261,71 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
                     glo = lo[p];
                     ghi = hi[p];
                 }
-            const float gsc = fmaxf(__fdiv_rn(__fsub_rn(ghi, glo), L), 1e-8f);
-            const float gzp = fminf(fmaxf(rintf(__fdiv_rn(-glo, gsc)), 0.0f), L);
-            const float grcp = __frcp_rn(gsc);
+            const GroupParams gg = group_params(glo, ghi, L);
+            const float2 gf = fast_params<BITS>(gg);
             if (lane < P) {
-                const float sb = __fmul_rn(B, gsc);
+                const float sb = __fmul_rn(B, gg.sc);
                 const long long gi = static_cast<long long>(lane) * NS + s;
                 S[static_cast<long long>(n) * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
                 ZS[static_cast<long long>(n) * NGt + gi] =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(gzp, gsc))));
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(gg.zp, gg.sc))));
             }
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                const float sc = __shfl_sync(0xffffffffu, gsc, p);
-                const float zp = __shfl_sync(0xffffffffu, gzp, p);
-                const float rcp = __shfl_sync(0xffffffffu, grcp, p);
+                const float ra = __shfl_sync(0xffffffffu, gf.x, p);
+                const float zb = __shfl_sync(0xffffffffu, gf.y, p);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    word |= quant_code(wv[p][i], sc, rcp, zp, L) << (8 * i + BITS * p);
+                for (int i = 0; i < 4; i += 2)
+                    quant_pair<BITS>(wv[p][i], wv[p][i + 1], ra, zb, lo[p], hi[p], 8 * i + BITS * p,
+                                     8 * (i + 1) + BITS * p, word);
             }
         } else {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 const float *w = wv[p];
-                float lo = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
-                float hi = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-                lo = lanes_min<G / 4>(lo);
-                hi = lanes_max<G / 4>(hi);
-                float sc = __fdiv_rn(__fsub_rn(hi, lo), L);
-                sc = fmaxf(sc, 1e-8f);
-                float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), L);
-                const float rcp = __frcp_rn(sc);
+                lo[p] = lanes_min<G / 4>(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
+                hi[p] = lanes_max<G / 4>(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
+                const GroupParams g = group_params(lo[p], hi[p], L);
+                const float2 f = fast_params<BITS>(g);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) word |= quant_code(w[i], sc, rcp, zp, L) << (8 * i + BITS * p);
+                for (int i = 0; i < 4; i += 2)
+                    quant_pair<BITS>(w[i], w[i + 1], f.x, f.y, lo[p], hi[p], 8 * i + BITS * p,
+                                     8 * (i + 1) + BITS * p, word);
                 if ((lane & (G / 4 - 1)) == p) {
-                    const float sb = __fmul_rn(B, sc);
+                    const float sb = __fmul_rn(B, g.sc);
                     const long long gi = (static_cast<long long>(p) * NS + s) * (128 / G) +
                                          lane / (G / 4);
                     S[static_cast<long long>(n) * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
                     ZS[static_cast<long long>(n) * NGt + gi] =
-                        __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(zp, sc))));
+                        __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(g.zp, g.sc))));
                 }
             }
         }
+        // the word's fields are at 8 i + BITS p: every multiple of BITS below 32
+        constexpr uint32_t kFix = magic_bits_sum(32 / BITS, BITS);
+        word -= kFix;
         reinterpret_cast<uint32_t *>(packed + static_cast<long long>(n) * PS + 128 * s)[lane] = word;
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            raw[p] = next[p];
-            next[p] = next2[p];
-        }
-        n = nn;
-        s = ns;
-        nn = n2;
-        ns = s2;
+    };
+    Raw r0[P], r1[P], r2[P];
+    float f0 = 0.0f, f1 = 0.0f, f2 = 0.0f;
+    int n0 = w0 / NS, s0 = w0 - (w0 / NS) * NS, n1, s1, n2, s2;
+    advance(n1, s1, n0, s0);
+    load(n0, s0, r0, f0);
+    load(n1, s1, r1, f1);
+    // items only grow along the walk: once one is past the head, so are the rest
+    for (;;) {
+        if (n0 >= V) break;
+        advance(n2, s2, n1, s1);
+        load(n2, s2, r2, f2);
+        process(r0, f0, n0, s0);
+        if (n1 >= V) break;
+        advance(n0, s0, n2, s2);
+        load(n0, s0, r0, f0);
+        process(r1, f1, n1, s1);
+        if (n2 >= V) break;
+        advance(n1, s1, n0, s0);
+        load(n1, s1, r1, f1);
+        process(r2, f2, n2, s2);
     }
 }
 
@@ -279,19 +368,19 @@ __global__ void __launch_bounds__(256) quantize_c4_kernel(const uint16_t *__rest
             lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
             hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
         }
-        float sc = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
-        sc = fmaxf(sc, 1e-8f);
-        const float zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.0f), 3.0f);
-        const float rcp = __frcp_rn(sc);
+        const GroupParams g = group_params(lo, hi, 3.0f);
+        const float2 f = fast_params<2>(g);
         uint32_t word = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) word |= quant_code(w[i], sc, rcp, zp, 3.0f) << (2 * i);
+        for (int i = 0; i < 16; i += 2) quant_pair<2>(w[i], w[i + 1], f.x, f.y, lo, hi, 2 * i, 2 * i + 2, word);
+        constexpr uint32_t kFix = magic_bits_sum(16, 2);
+        word -= kFix;
         if ((lane & 7) == 0) {
-            const float s4 = __fmul_rn(4.0f, sc);
+            const float s4 = __fmul_rn(4.0f, g.sc);
             const long long gi = 4LL * s + (lane >> 3);
             S[n * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(s4));
             ZS[n * NGt + gi] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(s4, __fmul_rn(zp, sc))));
+                __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(s4, __fmul_rn(g.zp, g.sc))));
         }
         reinterpret_cast<uint32_t *>(packed + n * Q + 128 * s)[lane] = word;
     }
