@@ -103,6 +103,30 @@ int dh_forward(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
                size_t ws_bytes, void *stream);
 
 /*
+ * dh_forward_host -- dh_forward with x, idx and logit in host memory: the call a host-side
+ * caller makes once per step, with the step's transfers inside it.  The pages' counterpart is
+ * the same forward fed from and read back to the host by the serving loop.
+ *
+ *   x_host     [M, H] bf16      pinned host memory, mapped into the device's address space
+ *                               (cudaHostAlloc / cudaMallocHost, or cudaHostRegister with
+ *                               cudaHostRegisterMapped), 16-byte aligned               (input)
+ *   idx_host   [M, topk] int32  pinned, mapped host memory, 16-byte aligned            (output)
+ *   logit_host [M, topk] fp32   pinned, mapped host memory, 16-byte aligned            (output)
+ *   everything else as dh_forward: the head and the workspace in device memory.
+ * On the 8-bit tcgen05 path the staging kernel reads x across the host link and keeps a
+ * device copy for the rerank (in the workspace); on the other coarse paths x is first copied
+ * to the workspace on the stream.  The last kernel writes idx and logit into the host
+ * buffers: they hold the result once the stream has been synchronised, and must not be read
+ * or written before.  Results are bit-identical to dh_forward's for the same inputs.
+ * Returns DH_ERR_ARG (before anything runs) if a host buffer is not pinned and mapped, and
+ * otherwise what dh_forward returns.
+ */
+int dh_forward_host(const uint16_t *x_host, const uint8_t *packed, const uint16_t *scales,
+                    const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                    int kcand, int rerank, int topk, int32_t *idx_host, float *logit_host,
+                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * dh_forward_debug -- dh_forward that also writes the intermediates, for parity checks.
  * Any of the extra outputs may be NULL.
  *   coarse    [M, V] fp32                 coarse values c[m, n]
@@ -213,7 +237,8 @@ int dh_device_status(int reset);
 const char *dh_last_error(void);
 
 /* ABI version: (major << 16) | minor.  1.0: the head and its sharded calls; 1.2: the fp8
- * head; 1.3: the 4-bit head and the design-choice ablations.  Minor versions only add calls. */
+ * head; 1.3: the 4-bit head and the design-choice ablations; 1.4: dh_forward_host.  Minor
+ * versions only add calls. */
 int dh_version(void);
 
 /*

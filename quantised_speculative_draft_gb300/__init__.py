@@ -117,6 +117,8 @@ def _load():
         lib.dh_forward_c4_debug.restype = I
         lib.dh_quantize_g64.argtypes = [P, I, I, P, P, P, P]
         lib.dh_quantize_g64.restype = I
+        lib.dh_forward_host.argtypes = fwd + [P]
+        lib.dh_forward_host.restype = I
         lib.dh_forward_g64_debug.argtypes = fwd + [P, P, P, P, P, P, P]
         lib.dh_forward_g64_debug.restype = I
         lib.dh_forward_wside_debug.argtypes = fwd + [P, P, P, P, P, P, P]
@@ -179,6 +181,18 @@ def dh_forward(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, wor
                stream=None):
     args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
     _check(_load().dh_forward(*args, _stream(stream)))
+
+
+def dh_forward_host(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,
+                    stream=None):
+    """dh_forward with x [M, H] bf16, idx [M, topk] int32 and logit [M, topk] fp32 in pinned
+    host memory (CPU tensors with ``pin_memory()``); the head and the workspace stay on the
+    device.  idx and logit hold the result once the stream has been synchronised."""
+    for name, t in (("x", x), ("idx", idx), ("logit", logit)):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous pinned host tensor")
+    args = _fwd_args(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace)
+    _check(_load().dh_forward_host(*args, _stream(stream)))
 
 
 def dh_forward_debug(x, packed, scales, zeros, W, kcand, rerank, topk, idx, logit, workspace,

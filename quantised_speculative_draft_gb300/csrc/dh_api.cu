@@ -101,7 +101,7 @@ struct Layout {
     long long nblk = 0, ncand = 0, scratch_entries = 0;
     int passes = 0;
     size_t xs = 0, xw = 0, xt = 0, cval = 0, cidx = 0, sval[2] = {0, 0}, sidx[2] = {0, 0},
-           sel = 0, ex = 0, counters = 0, xt8 = 0, small8 = 0, total = 0;
+           sel = 0, ex = 0, counters = 0, xt8 = 0, small8 = 0, xcopy = 0, total = 0;
 };
 
 
@@ -137,6 +137,8 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     // the most launches (16 rows each)
     L.xt8 = take(tc8_x_bytes(M, H));
     L.small8 = take(static_cast<size_t>(tc8_chunks(M, kPackHalf4)) * tc8_small_floats(H) * 4);
+    // a device copy of x for the calls that take x in host memory (dh_forward_host)
+    L.xcopy = take(static_cast<size_t>(M) * H * 2);
     L.total = off;
     return L;
 }
@@ -184,8 +186,11 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
                  size_t ws_bytes, float *coarse, float *cand_val, int32_t *cand_idx,
                  int32_t *sel_idx, float *sel_exact, void *const *events, cudaStream_t stream,
                  float *sel_val = nullptr, int id_offset = 0, bool candidates_only = false,
-                 const float *w_scale = nullptr, int pack = kPackQuarter2)
+                 const float *w_scale = nullptr, int pack = kPackQuarter2,
+                 uint16_t *x_copy = nullptr)
 {
+    // x_copy (8-bit tcgen05 path only): the staging kernel writes a device copy of x there as
+    // it reads x (which may then be pinned host memory), and the rerank reads the copy
     // candidates_only: stop after the top-R selection (a vocabulary shard's local candidates,
     // indices offset by id_offset, values into sel_val); W, idx and logit are not used
     if (candidates_only) {
@@ -243,8 +248,11 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     w8.xt8 = ws + L.xt8;
     w8.small = reinterpret_cast<float *>(ws + L.small8);
     w8.group = pack == kPackG64 ? 64 : 128;
+    if (x_copy && path != DH_PATH_TC)
+        return fail(DH_ERR_ARG, "x_copy needs the 8-bit tcgen05 path");
+    const uint16_t *x_rr = x_copy ? x_copy : x; // the x the rerank reads
     if (path == DH_PATH_TC)
-        err = launch_prep_fp8(x, M, H, pack, w8, counters, kNumCounters, stream);
+        err = launch_prep_fp8(x, M, H, pack, w8, counters, kNumCounters, stream, x_copy);
     else if (path == DH_PATH_CORE)
         err = launch_prep(x, M, H, core_mpad(M), xs, nullptr, nullptr, 0, counters,
                           kNumCounters, stream);
@@ -289,8 +297,8 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     if (!candidates_only && select_rerank_fits(rerank, kcand)) {
         // one launch for the selection, the rerank and the top-k (the stage events 3 and 4
         // then enclose nothing)
-        err = launch_select_rerank(cval, cidx, M, L.ncand, kcand, rerank, x, W, w_scale, H, V,
-                                   sel, ex, topk, idx, logit, stream);
+        err = launch_select_rerank(cval, cidx, M, L.ncand, kcand, rerank, x_rr, W, w_scale, H,
+                                   V, sel, ex, topk, idx, logit, stream);
         if (err != cudaSuccess)
             return fail(DH_ERR_CUDA, "select/rerank launch: %s", cudaGetErrorString(err));
         if (!rec(3) || !rec(4) || !rec(5)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
@@ -301,8 +309,8 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "select launch: %s", cudaGetErrorString(err));
     if (candidates_only) return ok();
     if (!rec(3)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
-    err = launch_rerank_topk(x, W, w_scale, M, H, V, sel, rerank, ex, counters + kRowDoneOffset,
-                             topk, idx, logit, 0, stream);
+    err = launch_rerank_topk(x_rr, W, w_scale, M, H, V, sel, rerank, ex,
+                             counters + kRowDoneOffset, topk, idx, logit, 0, stream);
     if (err != cudaSuccess) return fail(DH_ERR_CUDA, "rerank launch: %s", cudaGetErrorString(err));
     if (!rec(4)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
     if (!rec(5)) return fail(DH_ERR_CUDA, "cudaEventRecord failed");
@@ -393,6 +401,54 @@ int dh_forward(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
     return forward_impl(x, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, idx,
                         logit, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
                         nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int dh_forward_host(const uint16_t *x_host, const uint8_t *packed, const uint16_t *scales,
+                    const uint16_t *zeros, const uint16_t *W_bf16, int M, int H, int V,
+                    int kcand, int rerank, int topk, int32_t *idx_host, float *logit_host,
+                    void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!x_host || !idx_host || !logit_host || !workspace)
+        return fail(DH_ERR_NULL, "a required pointer is NULL");
+    // every host buffer must be pinned and mapped into the device's address space; its device
+    // address is what the kernels use (checked here, before anything runs)
+    const void *host_ptrs[3] = {x_host, idx_host, logit_host};
+    void *dev_ptrs[3] = {nullptr, nullptr, nullptr};
+    for (int i = 0; i < 3; ++i) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, host_ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(DH_ERR_ARG, "cannot query pointer %p", host_ptrs[i]);
+        }
+        if (a.type != cudaMemoryTypeHost || !a.devicePointer)
+            return fail(DH_ERR_ARG,
+                        "%s at %p is not pinned host memory mapped into the device's address space",
+                        i == 0 ? "x" : (i == 1 ? "idx" : "logit"), host_ptrs[i]);
+        dev_ptrs[i] = a.devicePointer;
+    }
+    int rc = check_shapes(M, H, V, kcand, rerank, topk);
+    if (rc != DH_OK) return rc;
+    if (!aligned16(workspace)) return fail(DH_ERR_ALIGN, "workspace is not 16-byte aligned");
+    const Layout L = layout_for(M, H, V, kcand, rerank);
+    if (ws_bytes < L.total)
+        return fail(DH_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
+    uint16_t *xc = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(workspace) + L.xcopy);
+    const auto *xd = static_cast<const uint16_t *>(dev_ptrs[0]);
+    auto *id = static_cast<int32_t *>(dev_ptrs[1]);
+    auto *ld = static_cast<float *>(dev_ptrs[2]);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (choose_path(M, H) == DH_PATH_TC) // the staging kernel reads x across the host link
+        return forward_impl(xd, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, id,
+                            ld, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
+                            nullptr, st, nullptr, 0, false, nullptr, kPackQuarter2, xc);
+    // the other coarse paths: one copy of x to the device first
+    if (!aligned16(xd)) return fail(DH_ERR_ALIGN, "x is not 16-byte aligned");
+    const cudaError_t e = cudaMemcpyAsync(xc, x_host, static_cast<size_t>(M) * H * 2,
+                                          cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return fail(DH_ERR_CUDA, "copy of x: %s", cudaGetErrorString(e));
+    return forward_impl(xc, packed, scales, zeros, W_bf16, M, H, V, kcand, rerank, topk, id, ld,
+                        workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        st);
 }
 
 int dh_quantize_fp8(const uint8_t *W_e4m3, const float *row_scale, int V, int H, uint8_t *packed,
@@ -680,7 +736,7 @@ const char *dh_last_error(void)
 
 int dh_version(void)
 {
-    return (1 << 16) | 3;
+    return (1 << 16) | 4;
 }
 
 

@@ -156,8 +156,11 @@ struct Tc8Workspace {
     float *small;  // per launch tc8_small_floats(H) floats
     int group = 128; // group size of xs (64: the group-size ablation)
 };
+// xcopy (nullable): a device copy [M, H] of x, written as the rows are read (x may then be
+// pinned host memory read across the host link: the rerank reads the copy)
 cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, int pack, const Tc8Workspace &w,
-                            int *counters, int ncounters, cudaStream_t stream);
+                            int *counters, int ncounters, cudaStream_t stream,
+                            uint16_t *xcopy = nullptr);
 cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaStream_t stream);
 // the 8-bit tcgen05 path runs these sizes (shared memory and tensor memory fit)
 bool tc8_supported(int M, int H, int bits = 2, int group = 128);

@@ -227,7 +227,8 @@ template <int G>
 __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_t *__restrict__ x,
                                                                    int H, const PrepChunks ch,
                                                                    int *__restrict__ counters,
-                                                                   int ncounters)
+                                                                   int ncounters,
+                                                                   uint16_t *__restrict__ xcopy)
 {
     __shared__ float wred[kPrepMaxThreads / 32];
     __shared__ float wred2[kPrepMaxThreads / 32];
@@ -258,7 +259,11 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
     for (int j = 0; j < kPrepOcts; ++j) {
         const int o = threadIdx.x + j * blockDim.x;
         xv[j] = make_uint4(0, 0, 0, 0);
-        if (valid && o < octs) xv[j] = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
+        if (valid && o < octs) {
+            xv[j] = __ldg(reinterpret_cast<const uint4 *>(xr) + o);
+            if (xcopy)
+                reinterpret_cast<uint4 *>(xcopy + static_cast<long long>(m0 + m) * H)[o] = xv[j];
+        }
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
 }
 
 cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, int pack, const Tc8Workspace &w,
-                            int *counters, int ncounters, cudaStream_t stream)
+                            int *counters, int ncounters, cudaStream_t stream, uint16_t *xcopy)
 {
     PrepChunks ch;
     ch.n = tc8_chunks(M, pack);
@@ -391,7 +396,7 @@ cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, int pack, const Tc8
     // one thread per 16-byte slice of the row (a multiple of 32 threads)
     int threads = ((H / 8 + 31) / 32) * 32;
     if (threads > kPrepMaxThreads) threads = kPrepMaxThreads;
-    kern<<<blocks, threads, 0, stream>>>(x, H, ch, counters, ncounters);
+    kern<<<blocks, threads, 0, stream>>>(x, H, ch, counters, ncounters, xcopy);
     return cudaGetLastError();
 }
 
