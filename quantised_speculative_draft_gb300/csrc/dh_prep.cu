@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
 {
     __shared__ float wred[kPrepMaxThreads / 32];
     __shared__ float wred2[kPrepMaxThreads / 32];
+    __shared__ float wred3[kPrepMaxThreads / 32];
     // the coarse pass may be scheduled now: it waits for this grid before it reads x
     pdl_trigger();
     int c = 0;
@@ -249,9 +250,10 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
         for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
     const uint16_t *xr = x + static_cast<long long>(m0 + (valid ? m : 0)) * H;
 
-    // the row stays in registers between the passes (H <= 1024 * 8 * kPrepOcts); the second
-    // slice of every thread exists only when the row has more slices than the CTA has threads
-    // (CTA-uniform)
+    // the row stays in registers between the passes (H <= 1024 * 8 * kPrepOcts), and so do the
+    // split's intermediate values: each pass takes one rounding further (the second slice of
+    // every thread exists only when the row has more slices than the CTA has threads:
+    // CTA-uniform)
     const int nj = octs > static_cast<int>(blockDim.x) ? 2 : 1;
     uint4 xv[kPrepOcts];
     float mx = 0.f;
@@ -271,8 +273,9 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
     const int e = range_shift(cta_max(mx, wred));
     const float scale = pow2f(e);
 
-    // pass 2: the largest first-term residual -> s2; pass 3: the largest second-term one -> s3
-    float m1 = 0.f;
+    // pass 2: r0 = x 2^e, its first term and residual; the largest residual -> s2
+    float t1v[kPrepOcts][8], rv[kPrepOcts][8];
+    float m1 = 0.f, l1 = 0.f; // and sum |x 2^e|
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
         if (j >= nj) break;
@@ -280,53 +283,84 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
-            m1 = fmaxf(m1, fabsf(r0 - round_e4m3(r0)));
+            t1v[j][i] = round_e4m3(r0);
+            rv[j][i] = r0 - t1v[j][i];
+            m1 = fmaxf(m1, fabsf(rv[j][i]));
+            l1 += fabsf(r0);
         }
     }
     const int s2 = range_shift(cta_max(m1, wred));
     const float k2 = pow2f(s2), ik2 = pow2f(-s2);
-    float m2 = 0.f;
+
+    // pass 3: the second term of every residual, the residual after it (rv), the largest of
+    // those -> s3, and the two sums that decide the row's term count, in one reduction
+    float u2v[kPrepOcts][8];
+    float m2 = 0.f, b2 = 0.f; // and the two-term residual sum |r2|
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
         if (j >= nj) break;
-        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
-            const Split3 sp = split3<2>(r0, k2, ik2, 0.f, 0.f);
-            m2 = fmaxf(m2, fabsf(sp.r2));
+            u2v[j][i] = round_e4m3(rv[j][i] * k2);
+            rv[j][i] = rv[j][i] - u2v[j][i] * ik2;
+            m2 = fmaxf(m2, fabsf(rv[j][i]));
+            b2 += fabsf(rv[j][i]);
         }
     }
-    const int s3 = range_shift(cta_max(m2, wred));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, off));
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        b2 += __shfl_xor_sync(0xffffffffu, b2, off);
+    }
+    __syncthreads(); // the previous use of wred is over
+    if ((threadIdx.x & 31) == 0) {
+        wred[threadIdx.x >> 5] = m2;
+        wred2[threadIdx.x >> 5] = l1;
+        wred3[threadIdx.x >> 5] = b2;
+    }
+    __syncthreads();
+    {
+        const int lane = threadIdx.x & 31;
+        float v = lane < static_cast<int>(blockDim.x >> 5) ? wred[lane] : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        m2 = v;
+    }
+    const int s3 = range_shift(m2);
     const float k3 = pow2f(s3), ik3 = pow2f(-s3);
     if (threadIdx.x == 0) {
         // per-row factors: 2^-e, then the weights of terms 2 and 3 (see the coarse kernel)
         row_f[m] = valid ? pow2f(-e) : 1.0f;
         row_f[kTc8MaxMP + m] = ik2;
         row_f[2 * kTc8MaxMP + m] = ik3;
+        float L = 0.f, B = 0.f;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) {
+            L += wred2[i];
+            B += wred3[i];
+        }
+        row_terms[m] = (valid && B > kTermsThreshold * L) ? 3 : 2;
     }
 
-    float l1 = 0.f, b2 = 0.f; // sum |x 2^e| and the two-term residual sum |r2|
+    // pass 4: the third terms, the terms' bytes and the group sums
 #pragma unroll
     for (int j = 0; j < kPrepOcts; ++j) {
         if (j >= nj) break; // CTA-uniform
         const int o = threadIdx.x + j * blockDim.x;
         // every lane of a warp takes part in the group shuffles: lanes past the row add 0
         const bool live = o < octs;
-        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
         float u[kTc8Terms][8];
         float sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float r0 = ((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1])) * scale;
-            const Split3 sp = split3<3>(r0, k2, ik2, k3, ik3);
-            const float rep2 = sp.t1 + sp.t2;
+            const float t2 = u2v[j][i] * ik2;
+            const float u3 = round_e4m3(rv[j][i] * k3);
+            const float rep2 = t1v[j][i] + t2;
             sum2 += rep2;
-            sum3 += rep2 + sp.t3;
-            l1 += fabsf(r0);
-            b2 += fabsf(sp.r2);
-#pragma unroll
-            for (int t = 0; t < kTc8Terms; ++t) u[t][i] = sp.u[t];
+            sum3 += rep2 + u3 * ik3;
+            u[0][i] = t1v[j][i];
+            u[1][i] = u2v[j][i];
+            u[2][i] = u3;
         }
         // the terms' bytes, element i in byte i of the 8-byte slice
         uint32_t lo[kTc8Terms], hi[kTc8Terms];
@@ -350,27 +384,6 @@ __global__ void __launch_bounds__(kPrepMaxThreads) prep_fp8_kernel(const uint16_
             xs2[static_cast<long long>(m) * NGt + o / (G / 8)] = sum2;
             xs3[static_cast<long long>(m) * NGt + o / (G / 8)] = sum3;
         }
-    }
-    // the decision needs sums, not maxima: reduce (l1, b2) through the same buffer
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        b2 += __shfl_xor_sync(0xffffffffu, b2, off);
-    }
-    // (wred's last use, the third maximum, ended at a barrier; wred2 is fresh)
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) {
-        wred[threadIdx.x >> 5] = l1;
-        wred2[threadIdx.x >> 5] = b2;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float L = 0.f, B = 0.f;
-        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) {
-            L += wred[i];
-            B += wred2[i];
-        }
-        row_terms[m] = (valid && B > kTermsThreshold * L) ? 3 : 2;
     }
 }
 
