@@ -433,9 +433,20 @@ class DraftHead:
         return self._ws
 
     def forward(self, x, topk: int = 1, stream=None):
-        """x [M, H] bf16 -> (idx int32 [M, topk], logit fp32 [M, topk])."""
+        """x [M, H] bf16 -> (idx int32 [M, topk], logit fp32 [M, topk]).  A pinned host x (the
+        bf16 2-bit head) goes through dh_forward_host: the results come back in pinned host
+        tensors, complete on return (the stream is synchronised)."""
         import torch
         M = x.shape[0]
+        if not x.is_cuda:
+            if self.bits == 4 or self.row_scale is not None:
+                raise ValueError("a host x is taken by the bf16 2-bit head only")
+            idx = torch.empty(M, topk, dtype=torch.int32).pin_memory()
+            logit = torch.empty(M, topk, dtype=torch.float32).pin_memory()
+            dh_forward_host(x, self.packed, self.scales, self.zeros, self.W, self.kcand,
+                            self.rerank, topk, idx, logit, self.workspace(M), stream)
+            (torch.cuda.current_stream() if stream is None else stream).synchronize()
+            return idx, logit
         idx = torch.empty(M, topk, dtype=torch.int32, device=x.device)
         logit = torch.empty(M, topk, dtype=torch.float32, device=x.device)
         if self.bits == 4:

@@ -97,3 +97,17 @@ def test_unpinned_host_buffers_are_rejected():
         dh.dh_forward_host(xh, packed, S, ZS, W, kcand, R, topk, ih, lh, ws)
     torch.cuda.synchronize()
     assert dh.dh_device_status(reset=True) == 0
+
+
+def test_draft_head_takes_a_pinned_host_x():
+    M, H, V = 5, 1024, 9000 + 13
+    wl = synth.custom(M, H, V, hot_rows=V // 50, hot_scale=4.0)
+    x, W = synth.make_x(wl, 1, DEV), synth.make_w(wl, 1, DEV)
+    head = dh.DraftHead(W, kcand=8, rerank=32)
+    idx, logit = head.forward(x, topk=4)
+    hidx, hlogit = head.forward(x.cpu().pin_memory(), topk=4)
+    assert not hidx.is_cuda and hidx.is_pinned()
+    assert torch.equal(hidx, idx.cpu())
+    assert torch.equal(hlogit.view(torch.int32), logit.cpu().view(torch.int32))
+    with pytest.raises(ValueError):
+        head.forward(x.cpu(), topk=4)                # pageable
