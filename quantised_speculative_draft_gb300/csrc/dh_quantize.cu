@@ -132,6 +132,42 @@ __device__ __forceinline__ void quant_pair(float w0, float w1, float ra, float z
         word += pair_by_definition(w0, w1, lo, hi, L, b0, b1, s0, s1);
 }
 
+// The same for four weights of one group at bit positions s0, s0 + step, s0 + 2 step, s0 + 3
+// step, with one boundary test for the four (two pairs on the paired units).
+__device__ __noinline__ uint32_t quad_by_definition(float w0, float w1, float w2, float w3, float lo,
+                                                    float hi, float L, uint32_t b0, uint32_t b1,
+                                                    uint32_t b2, uint32_t b3, int s0, int step)
+{
+    const GroupParams g = group_params(lo, hi, L);
+    return ((code_by_definition(w0, g, L) - (b0 - kQMagicNegBits)) << s0) +
+           ((code_by_definition(w1, g, L) - (b1 - kQMagicNegBits)) << (s0 + step)) +
+           ((code_by_definition(w2, g, L) - (b2 - kQMagicNegBits)) << (s0 + 2 * step)) +
+           ((code_by_definition(w3, g, L) - (b3 - kQMagicNegBits)) << (s0 + 3 * step));
+}
+
+// Returns true when one of the four lies within the margin of a rounding boundary; the caller
+// then adds quad_by_definition's correction (with the group's extrema).
+template <int BITS>
+__device__ __forceinline__ bool quant_quad(const float (&w)[4], float ra, float zb, int s0, int step,
+                                           uint32_t &word, uint32_t (&b)[4])
+{
+    constexpr float L = static_cast<float>((1 << BITS) - 1);
+    const float2 ya = make_float2(fma_sat(w[0], ra, zb), fma_sat(w[1], ra, zb));
+    const float2 yb = make_float2(fma_sat(w[2], ra, zb), fma_sat(w[3], ra, zb));
+    const float2 ma = __ffma2_rn(ya, make_float2(-L, -L), make_float2(-kQMagic, -kQMagic));
+    const float2 mb = __ffma2_rn(yb, make_float2(-L, -L), make_float2(-kQMagic, -kQMagic));
+    const float2 da = __ffma2_rn(ya, make_float2(L, L), __fadd2_rn(ma, make_float2(kQMagic, kQMagic)));
+    const float2 db = __ffma2_rn(yb, make_float2(L, L), __fadd2_rn(mb, make_float2(kQMagic, kQMagic)));
+    b[0] = __float_as_uint(ma.x);
+    b[1] = __float_as_uint(ma.y);
+    b[2] = __float_as_uint(mb.x);
+    b[3] = __float_as_uint(mb.y);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) word += b[i] << (s0 + i * step);
+    const float dm = fmaxf(fmaxf(fabsf(da.x), fabsf(da.y)), fmaxf(fabsf(db.x), fabsf(db.y)));
+    return __builtin_expect(dm >= kQThreshold, 0);
+}
+
 // The fast path's per-group constants ra, zb.
 template <int BITS>
 __device__ __forceinline__ float2 fast_params(GroupParams g)
@@ -184,113 +220,140 @@ __global__ void __launch_bounds__(256, 3) quantize_kernel(const void *__restrict
     constexpr int P = 8 / BITS;                          // planes (codes per byte)
     constexpr float L = static_cast<float>((1 << BITS) - 1);
     constexpr float B = static_cast<float>(1 << BITS);
+    // spans per work item: two with groups of 128 (the per-group work -- extrema, scale and
+    // zero point, fast constants, the S / ZS stores -- is then shared by 8 groups' lanes at
+    // once), one with groups of 64
+    constexpr int SPI = G == 128 ? 2 : 1;
+    constexpr int NGI = SPI * P; // groups of 128 k per item
     const int lane = threadIdx.x & 31;
     const int PS = H / P;       // k stride between planes = packed bytes per row
     const int NS = PS / 128;    // spans per row
+    const int NSI = (NS + SPI - 1) / SPI; // items per row (the last may hold one span)
     const int NGt = H / G;      // groups per row
-    // work items (n, s) = warp w, w + nwarps, ...: the position advances by (dn, ds) with no
-    // division in the loop, and the next two items' weights are in flight while this one is
-    // quantised (2 KB per warp: enough loads outstanding to cover the HBM latency).  The three
-    // items' registers form a ring that the loop body, unrolled three times, walks without
-    // copies.
+    // the extrema of the item's groups, for the rare codes taken by their definition
+    __shared__ float lohi_s[8][2 * NGI];
+    float *const lohi = lohi_s[threadIdx.x >> 5];
+    // work items (n, si) = warp w, w + nwarps, ...: the position advances by (dn, ds) with no
+    // division in the loop, and the next item's weights are in flight while this one is
+    // quantised (2 KB per warp); the two items' registers alternate, the loop body unrolled
+    // twice
     const int nwarps = gridDim.x * (blockDim.x >> 5);
-    const int dn = nwarps / NS, ds = nwarps - dn * NS;
+    const int dn = nwarps / NSI, ds = nwarps - dn * NSI;
     const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     using Raw = typename std::conditional<kFp8, uint32_t, uint2>::type;
     // an item's weights and, for the fp8 head, its row scale
-    auto load = [&](int rn, int rs, Raw (&raw)[P], float &rsc) {
+    auto load = [&](int rn, int ri, Raw (&raw)[SPI][P], float &rsc) {
         if (rn >= V) return;
         if constexpr (kFp8) rsc = __ldg(wsc + rn);
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-            if constexpr (kFp8) {
-                const uint8_t *row = static_cast<const uint8_t *>(Wv) + static_cast<long long>(rn) * H;
-                raw[p] = __ldg(reinterpret_cast<const uint32_t *>(row + p * PS + 128 * rs + 4 * lane));
-            } else {
-                const uint16_t *row = static_cast<const uint16_t *>(Wv) + static_cast<long long>(rn) * H;
-                raw[p] = __ldg(reinterpret_cast<const uint2 *>(row + p * PS + 128 * rs + 4 * lane));
+        for (int j = 0; j < SPI; ++j) {
+            const int rs = SPI * ri + j;
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (rs >= NS) { // the row's last item holds one span: the other reads as zero
+                    raw[j][p] = Raw{};
+                } else if constexpr (kFp8) {
+                    const uint8_t *row = static_cast<const uint8_t *>(Wv) + static_cast<long long>(rn) * H;
+                    raw[j][p] = __ldg(reinterpret_cast<const uint32_t *>(row + p * PS + 128 * rs + 4 * lane));
+                } else {
+                    const uint16_t *row = static_cast<const uint16_t *>(Wv) + static_cast<long long>(rn) * H;
+                    raw[j][p] = __ldg(reinterpret_cast<const uint2 *>(row + p * PS + 128 * rs + 4 * lane));
+                }
             }
         }
     };
-    auto advance = [&](int &an, int &as, int fn, int fs) {
+    auto advance = [&](int &an, int &ai, int fn, int fi) {
         an = fn + dn;
-        as = fs + ds;
-        if (as >= NS) {
-            as -= NS;
+        ai = fi + ds;
+        if (ai >= NSI) {
+            ai -= NSI;
             ++an;
         }
     };
-    // one item: lane l holds four weights of each plane, k = p PS + 128 s + 4 l + i
-    auto process = [&](const Raw (&raw)[P], float rs, int n, int s) {
-        float wv[P][4];
-        if constexpr (kFp8) {
+    // one item: lane l holds four weights of each plane of each span, k = p PS + 128 s + 4 l + i
+    auto process = [&](const Raw (&raw)[SPI][P], float rs, int n, int si) {
+        const int nsp = min(SPI, NS - SPI * si); // spans in this item (warp-uniform)
+        float wv[SPI][P][4];
 #pragma unroll
-            for (int p = 0; p < P; ++p)
-#pragma unroll
-                for (int i = 0; i < 4; i += 2) {
-                    const float2 v = __fmul2_rn(e4m3x2_to_f32x2(raw[p] >> (8 * i)), make_float2(rs, rs));
-                    wv[p][i] = v.x;
-                    wv[p][i + 1] = v.y;
-                }
-        } else {
+        for (int j = 0; j < SPI; ++j)
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                wv[p][0] = __uint_as_float(raw[p].x << 16);
-                wv[p][1] = __uint_as_float(raw[p].x & 0xFFFF0000u);
-                wv[p][2] = __uint_as_float(raw[p].y << 16);
-                wv[p][3] = __uint_as_float(raw[p].y & 0xFFFF0000u);
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int i = 0; i < 4; i += 2) {
+                        const float2 v =
+                            __fmul2_rn(e4m3x2_to_f32x2(raw[j][p] >> (8 * i)), make_float2(rs, rs));
+                        wv[j][p][i] = v.x;
+                        wv[j][p][i + 1] = v.y;
+                    }
+                } else {
+                    wv[j][p][0] = __uint_as_float(raw[j][p].x << 16);
+                    wv[j][p][1] = __uint_as_float(raw[j][p].x & 0xFFFF0000u);
+                    wv[j][p][2] = __uint_as_float(raw[j][p].y << 16);
+                    wv[j][p][3] = __uint_as_float(raw[j][p].y & 0xFFFF0000u);
+                }
             }
-        }
-        uint32_t word = 0;
-        float lo[P], hi[P];
+        uint32_t word[SPI];
+#pragma unroll
+        for (int j = 0; j < SPI; ++j) word[j] = 0;
         if constexpr (G == 128) {
-            // the span's P groups each cover the whole warp: one reduction instruction per
-            // extremum, then lane l computes the scale, zero point and fast constants of group
-            // l % P once (not every lane every group) and the others fetch them
+            // every group covers the whole warp: one reduction instruction per extremum, then
+            // lane l computes the scale, zero point and fast constants of group l % NGI (span
+            // (l / P) % SPI, plane l % P) once and the others fetch them
+            const int gl = lane & (NGI - 1);
+            float glo = 0.f, ghi = 0.f;
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const float *w = wv[p];
-                lo[p] = warp_min_f32(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
-                hi[p] = warp_max_f32(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
-            }
-            const int gp = lane & (P - 1);
-            float glo = lo[0], ghi = hi[0];
+            for (int j = 0; j < SPI; ++j)
 #pragma unroll
-            for (int p = 1; p < P; ++p)
-                if (gp == p) {
-                    glo = lo[p];
-                    ghi = hi[p];
+                for (int p = 0; p < P; ++p) {
+                    const float *w = wv[j][p];
+                    const float lo = warp_min_f32(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
+                    const float hi = warp_max_f32(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
+                    if (gl == j * P + p) {
+                        glo = lo;
+                        ghi = hi;
+                    }
                 }
+            if (lane < NGI) {
+                lohi[2 * lane] = glo;
+                lohi[2 * lane + 1] = ghi;
+            }
             const GroupParams gg = group_params(glo, ghi, L);
             const float2 gf = fast_params<BITS>(gg);
-            if (lane < P) {
+            if (lane < NGI && gl / P < nsp) {
                 const float sb = __fmul_rn(B, gg.sc);
-                const long long gi = static_cast<long long>(lane) * NS + s;
+                const long long gi = static_cast<long long>(gl % P) * NS + SPI * si + gl / P;
                 S[static_cast<long long>(n) * NGt + gi] = __bfloat16_as_ushort(__float2bfloat16_rn(sb));
                 ZS[static_cast<long long>(n) * NGt + gi] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sb, __fmul_rn(gg.zp, gg.sc))));
             }
+            __syncwarp();
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const float ra = __shfl_sync(0xffffffffu, gf.x, p);
-                const float zb = __shfl_sync(0xffffffffu, gf.y, p);
+            for (int j = 0; j < SPI; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; i += 2)
-                    quant_pair<BITS>(wv[p][i], wv[p][i + 1], ra, zb, lo[p], hi[p], 8 * i + BITS * p,
-                                     8 * (i + 1) + BITS * p, word);
-            }
+                for (int p = 0; p < P; ++p) {
+                    const int g = j * P + p;
+                    const float ra = __shfl_sync(0xffffffffu, gf.x, g);
+                    const float zb = __shfl_sync(0xffffffffu, gf.y, g);
+                    uint32_t bq[4];
+                    if (quant_quad<BITS>(wv[j][p], ra, zb, BITS * p, 8, word[j], bq))
+                        word[j] += quad_by_definition(wv[j][p][0], wv[j][p][1], wv[j][p][2],
+                                                      wv[j][p][3], lohi[2 * g], lohi[2 * g + 1], L,
+                                                      bq[0], bq[1], bq[2], bq[3], BITS * p, 8);
+                }
         } else {
+            const int s = si; // one span per item
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                const float *w = wv[p];
-                lo[p] = lanes_min<G / 4>(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
-                hi[p] = lanes_max<G / 4>(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
-                const GroupParams g = group_params(lo[p], hi[p], L);
+                const float *w = wv[0][p];
+                const float lo = lanes_min<G / 4>(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
+                const float hi = lanes_max<G / 4>(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
+                const GroupParams g = group_params(lo, hi, L);
                 const float2 f = fast_params<BITS>(g);
-#pragma unroll
-                for (int i = 0; i < 4; i += 2)
-                    quant_pair<BITS>(w[i], w[i + 1], f.x, f.y, lo[p], hi[p], 8 * i + BITS * p,
-                                     8 * (i + 1) + BITS * p, word);
+                uint32_t bq[4];
+                if (quant_quad<BITS>(wv[0][p], f.x, f.y, BITS * p, 8, word[0], bq))
+                    word[0] += quad_by_definition(w[0], w[1], w[2], w[3], lo, hi, L, bq[0], bq[1],
+                                                  bq[2], bq[3], BITS * p, 8);
                 if ((lane & (G / 4 - 1)) == p) {
                     const float sb = __fmul_rn(B, g.sc);
                     const long long gi = (static_cast<long long>(p) * NS + s) * (128 / G) +
@@ -301,31 +364,29 @@ __global__ void __launch_bounds__(256, 3) quantize_kernel(const void *__restrict
                 }
             }
         }
-        // the word's fields are at 8 i + BITS p: every multiple of BITS below 32
+        // a word's fields are at 8 i + BITS p: every multiple of BITS below 32
         constexpr uint32_t kFix = magic_bits_sum(32 / BITS, BITS);
-        word -= kFix;
-        reinterpret_cast<uint32_t *>(packed + static_cast<long long>(n) * PS + 128 * s)[lane] = word;
+#pragma unroll
+        for (int j = 0; j < SPI; ++j)
+            if (j < nsp)
+                reinterpret_cast<uint32_t *>(packed + static_cast<long long>(n) * PS +
+                                             128 * (SPI * si + j))[lane] = word[j] - kFix;
+        __syncwarp(); // the extrema scratch is reused by the next item
     };
-    Raw r0[P], r1[P], r2[P];
-    float f0 = 0.0f, f1 = 0.0f, f2 = 0.0f;
-    int n0 = w0 / NS, s0 = w0 - (w0 / NS) * NS, n1, s1, n2, s2;
-    advance(n1, s1, n0, s0);
-    load(n0, s0, r0, f0);
-    load(n1, s1, r1, f1);
+    Raw r0[SPI][P], r1[SPI][P];
+    float f0 = 0.0f, f1 = 0.0f;
+    int n0 = w0 / NSI, i0 = w0 - (w0 / NSI) * NSI, n1, i1;
+    load(n0, i0, r0, f0);
     // items only grow along the walk: once one is past the head, so are the rest
     for (;;) {
         if (n0 >= V) break;
-        advance(n2, s2, n1, s1);
-        load(n2, s2, r2, f2);
-        process(r0, f0, n0, s0);
+        advance(n1, i1, n0, i0);
+        load(n1, i1, r1, f1);
+        process(r0, f0, n0, i0);
         if (n1 >= V) break;
-        advance(n0, s0, n2, s2);
-        load(n0, s0, r0, f0);
-        process(r1, f1, n1, s1);
-        if (n2 >= V) break;
-        advance(n1, s1, n0, s0);
-        load(n1, s1, r1, f1);
-        process(r2, f2, n2, s2);
+        advance(n0, i0, n1, i1);
+        load(n0, i0, r0, f0);
+        process(r1, f1, n1, i1);
     }
 }
 
@@ -403,7 +464,8 @@ template <bool kFp8, int BITS, int G>
 cudaError_t launch_quantize_cfg(const void *W, const float *wsc, int V, int H, uint8_t *packed,
                                 uint16_t *S, uint16_t *ZS, cudaStream_t stream)
 {
-    const long long total = static_cast<long long>(V) * (H / (128 * (8 / BITS)));
+    const int ns = H / (128 * (8 / BITS));                    // spans per row
+    const long long total = static_cast<long long>(V) * (G == 128 ? (ns + 1) / 2 : ns); // items
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, quantize_kernel<kFp8, BITS, G>, 256, 0);
