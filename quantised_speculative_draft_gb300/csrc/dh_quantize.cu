@@ -273,26 +273,34 @@ __global__ void __launch_bounds__(256, 3) quantize_kernel(const void *__restrict
     // one item: lane l holds four weights of each plane of each span, k = p PS + 128 s + 4 l + i
     auto process = [&](const Raw (&raw)[SPI][P], float rs, int n, int si) {
         const int nsp = min(SPI, NS - SPI * si); // spans in this item (warp-uniform)
-        float wv[SPI][P][4];
+        // the fp8 head's weights are decoded once and kept; bf16 weights are re-read from the
+        // raw words where they are used (one shift or mask each), which keeps the register
+        // count within three blocks per SM without spills
+        float wv8[kFp8 ? SPI : 1][kFp8 ? P : 1][4];
+        if constexpr (kFp8) {
 #pragma unroll
-        for (int j = 0; j < SPI; ++j)
+            for (int j = 0; j < SPI; ++j)
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                if constexpr (kFp8) {
+                for (int p = 0; p < P; ++p)
 #pragma unroll
                     for (int i = 0; i < 4; i += 2) {
                         const float2 v =
                             __fmul2_rn(e4m3x2_to_f32x2(raw[j][p] >> (8 * i)), make_float2(rs, rs));
-                        wv[j][p][i] = v.x;
-                        wv[j][p][i + 1] = v.y;
+                        wv8[j][p][i] = v.x;
+                        wv8[j][p][i + 1] = v.y;
                     }
-                } else {
-                    wv[j][p][0] = __uint_as_float(raw[j][p].x << 16);
-                    wv[j][p][1] = __uint_as_float(raw[j][p].x & 0xFFFF0000u);
-                    wv[j][p][2] = __uint_as_float(raw[j][p].y << 16);
-                    wv[j][p][3] = __uint_as_float(raw[j][p].y & 0xFFFF0000u);
-                }
+        }
+        auto weights = [&](int j, int p, float (&w)[4]) {
+            if constexpr (kFp8) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) w[i] = wv8[j][p][i];
+            } else {
+                w[0] = __uint_as_float(raw[j][p].x << 16);
+                w[1] = __uint_as_float(raw[j][p].x & 0xFFFF0000u);
+                w[2] = __uint_as_float(raw[j][p].y << 16);
+                w[3] = __uint_as_float(raw[j][p].y & 0xFFFF0000u);
             }
+        };
         uint32_t word[SPI];
 #pragma unroll
         for (int j = 0; j < SPI; ++j) word[j] = 0;
@@ -306,7 +314,8 @@ __global__ void __launch_bounds__(256, 3) quantize_kernel(const void *__restrict
             for (int j = 0; j < SPI; ++j)
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
-                    const float *w = wv[j][p];
+                    float w[4];
+                    weights(j, p, w);
                     const float lo = warp_min_f32(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
                     const float hi = warp_max_f32(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
                     if (gl == j * P + p) {
@@ -335,23 +344,26 @@ __global__ void __launch_bounds__(256, 3) quantize_kernel(const void *__restrict
                     const int g = j * P + p;
                     const float ra = __shfl_sync(0xffffffffu, gf.x, g);
                     const float zb = __shfl_sync(0xffffffffu, gf.y, g);
+                    float w[4];
+                    weights(j, p, w);
                     uint32_t bq[4];
-                    if (quant_quad<BITS>(wv[j][p], ra, zb, BITS * p, 8, word[j], bq))
-                        word[j] += quad_by_definition(wv[j][p][0], wv[j][p][1], wv[j][p][2],
-                                                      wv[j][p][3], lohi[2 * g], lohi[2 * g + 1], L,
-                                                      bq[0], bq[1], bq[2], bq[3], BITS * p, 8);
+                    if (quant_quad<BITS>(w, ra, zb, BITS * p, 8, word[j], bq))
+                        word[j] += quad_by_definition(w[0], w[1], w[2], w[3], lohi[2 * g],
+                                                      lohi[2 * g + 1], L, bq[0], bq[1], bq[2],
+                                                      bq[3], BITS * p, 8);
                 }
         } else {
             const int s = si; // one span per item
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                const float *w = wv[0][p];
+                float w[4];
+                weights(0, p, w);
                 const float lo = lanes_min<G / 4>(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
                 const float hi = lanes_max<G / 4>(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
                 const GroupParams g = group_params(lo, hi, L);
                 const float2 f = fast_params<BITS>(g);
                 uint32_t bq[4];
-                if (quant_quad<BITS>(wv[0][p], f.x, f.y, BITS * p, 8, word[0], bq))
+                if (quant_quad<BITS>(w, f.x, f.y, BITS * p, 8, word[0], bq))
                     word[0] += quad_by_definition(w[0], w[1], w[2], w[3], lo, hi, L, bq[0], bq[1],
                                                   bq[2], bq[3], BITS * p, 8);
                 if ((lane & (G / 4 - 1)) == p) {
