@@ -21,11 +21,11 @@
 // per-row scale before the group statistics), each rounded once; the steps above then run on
 // those values.
 //
-// Work unit: one warp per (row n, span s), where span s is packed bytes [128 s, 128 s + 128)
-// of the row -- one group per plane p (P = 8 / BITS planes): group p NS + s, NS = H / (128 P)
-// spans per row.  Lane l owns packed bytes 4l .. 4l+3 of the span, i.e. four consecutive
-// weights of each of the span's groups, so the packed word it writes needs nothing from other
-// lanes.
+// Work unit: one warp per (row n, two spans) with groups of 128 (one span with groups of 64),
+// where span s is packed bytes [128 s, 128 s + 128) of the row -- one group per plane p
+// (P = 8 / BITS planes): group p NS + s, NS = H / (128 P) spans per row.  Lane l owns packed
+// bytes 4l .. 4l+3 of each span, i.e. four consecutive weights of each of the span's groups, so
+// the packed words it writes need nothing from other lanes.
 #include "dh_common.cuh"
 #include "dh_internal.h"
 
