@@ -223,3 +223,13 @@ def test_draft_head_rejects_bad_heads_on_the_host():
         dh.DraftHead(W)                                           # not a CUDA tensor
     with pytest.raises(ValueError):
         dh.DraftHead(W.to(torch.uint8), row_scale=torch.ones(64))  # fp8 head off the device
+
+
+def test_forward_host_rejects_missing_buffers_before_any_cuda_call(lib):
+    # dh_forward_host(x, packed, scales, zeros, W, M, H, V, kcand, rerank, topk, idx, logit,
+    #                 workspace, ws_bytes, stream): NULL host buffers or workspace -> -1
+    args = [FAKE] * 5 + [4, 1024, 8192, 8, 32, 1, FAKE, FAKE, FAKE, 1 << 40]
+    for i in (0, 11, 12, 13):
+        bad = list(args)
+        bad[i] = None
+        assert lib.dh_forward_host(*bad, None) == -1
