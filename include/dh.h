@@ -339,8 +339,8 @@ int dh_forward_fp8w(const uint16_t *x, const uint8_t *packed, const uint16_t *sc
  *   rerank (against W_bf16), workspace (dh_workspace_bytes) and ranking rules unchanged.
  *   Runs on the 8-bit tcgen05 coarse path only: DH_ERR_ARG when another path is forced by
  *   dh_set_coarse_path or the sizes do not fit it (two pipeline stages of 32 KB of packed
- *   bytes plus the staged x next to the fixed buffers: H <= 7168 for M > 16, H <= 13312
- *   for M <= 16 -- the check runs before any launch).
+ *   bytes plus the staged x next to the fixed buffers, in launches of 16 rows: H <= 11264 at
+ *   any M -- the check runs before any launch).
  */
 int dh_quantize4(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
                  uint16_t *zeros, void *stream);

@@ -136,7 +136,7 @@ Layout layout_for(int M, int H, int V, int kcand, int rerank)
     // small per-row data (group sums, 2^-e, term weights and counts); the 4-bit layout takes
     // the most launches (16 rows each)
     L.xt8 = take(tc8_x_bytes(M, H));
-    L.small8 = take(static_cast<size_t>(tc8_chunks(M, kPackHalf4)) * tc8_small_floats(H) * 4);
+    L.small8 = take(static_cast<size_t>(tc8_chunks(M, kPackHalf4, H)) * tc8_small_floats(H) * 4);
     // a device copy of x for the calls that take x in host memory (dh_forward_host)
     L.xcopy = take(static_cast<size_t>(M) * H * 2);
     L.total = off;
@@ -172,11 +172,11 @@ int choose_path(int M, int H)
     }
     if (p == DH_PATH_TC) return tc8_supported(M, H) ? p : -1;
     if (p == DH_PATH_TC_BF16) return tc_supported(M, H) ? p : -1;
-    if (p == DH_PATH_WARP) return DH_PATH_WARP;
+    if (p == DH_PATH_WARP) return warp_supported(M, H) ? p : -1;
     if (p == DH_PATH_CORE) return core_supported(M, H) ? p : -1;
     // automatic: the 8-bit tcgen05 path where it is available, else the warp path
     if (tc8_supported(M, H)) return DH_PATH_TC;
-    return DH_PATH_WARP;
+    return warp_supported(M, H) ? DH_PATH_WARP : -1;
 }
 
 // W: the head's rows for the rerank, bf16 (w_scale null) or e4m3 with per-row fp32 scales.
@@ -212,7 +212,9 @@ int forward_impl(const uint16_t *x, const uint8_t *packed, const uint16_t *scale
     int path = choose_path(M, H);
     if (pack == kPackWside) // the weight-side ablation runs on the bf16 tcgen05 path
         path = tc_supported(M, H) ? DH_PATH_TC_BF16 : -1;
-    if (path < 0) return fail(DH_ERR_ARG, "the tcgen05 path does not support M=%d, H=%d", M, H);
+    if (path < 0)
+        return fail(DH_ERR_ARG, "no coarse path takes M=%d, H=%d (the one set by dh_set_coarse_path, "
+                                "or with the automatic choice none fits its shared memory)", M, H);
     if (pack != kPackQuarter2 && pack != kPackWside &&
         (path != DH_PATH_TC || !tc8_supported(M, H, pack == kPackHalf4 ? 4 : 2,
                                               pack == kPackG64 ? 64 : 128)))
@@ -704,7 +706,7 @@ int dh_forward_launch_count(int M, int H, int V, int kcand, int rerank)
     const int path = choose_path(M, H);
     if (path < 0) return 0;
     int prep = 1, coarse = (M + kWarpBatch - 1) / kWarpBatch;
-    if (path == DH_PATH_TC) coarse = tc8_chunks(M, kPackQuarter2); // one staging launch
+    if (path == DH_PATH_TC) coarse = tc8_chunks(M, kPackQuarter2, H); // one staging launch
     else if (path == DH_PATH_TC_BF16) coarse = tc_launches(M);
     else if (path == DH_PATH_CORE) coarse = 1;
     if (select_rerank_fits(rerank, kcand)) return prep + coarse + 1; // fused select + rerank

@@ -980,22 +980,24 @@ bool fits(int MP, int H)
 
 } // namespace
 
-int tc8_max_rows(int pack)
+int tc8_max_rows(int pack, int H)
 {
     // groups of 64 need two accumulators per plane; the 4-bit head's 32 KB packed boxes leave
-    // no room for two stages of 32 rows in three terms
-    return (pack == kPackG64 || pack == kPackHalf4) ? 16 : 32;
+    // no room for two stages of 32 rows in three terms; 2-bit rows wider than a 32-row launch's
+    // shared memory holds run in 16-row launches too
+    if (pack == kPackG64 || pack == kPackHalf4) return 16;
+    return fits<kPackQuarter2>(32, H) && fits<kPackContig2>(32, H) ? 32 : 16;
 }
 
-int tc8_chunks(int M, int pack)
+int tc8_chunks(int M, int pack, int H)
 {
-    const int r = tc8_max_rows(pack);
+    const int r = tc8_max_rows(pack, H);
     return (M + r - 1) / r;
 }
 
 Tc8Chunk tc8_chunk(int M, int c, int pack, int H)
 {
-    const int r = tc8_max_rows(pack);
+    const int r = tc8_max_rows(pack, H);
     Tc8Chunk k;
     k.m0 = c * r;
     k.rows = M - k.m0 < r ? M - k.m0 : r;
@@ -1010,7 +1012,7 @@ size_t tc8_x_bytes(int M, int H)
     size_t most = 0;
     const int packs[2] = {kPackQuarter2, kPackHalf4};
     for (int pack : packs) {
-        const int n = tc8_chunks(M, pack);
+        const int n = tc8_chunks(M, pack, H);
         const Tc8Chunk last = tc8_chunk(M, n - 1, pack, H);
         const size_t b = last.x_off + static_cast<size_t>(kTc8Terms) * last.MP * H;
         if (b > most) most = b;
@@ -1026,7 +1028,7 @@ bool tc8_supported(int M, int H, int bits, int group)
     // groups of 64 need two accumulators per plane: only the 16-row launch
     if (group != 128 && (group != 64 || bits != 2 || M > 16)) return false;
     const int pack = bits == 4 ? kPackHalf4 : (group == 64 ? kPackG64 : kPackQuarter2);
-    for (int c = 0; c < tc8_chunks(M, pack); ++c) {
+    for (int c = 0; c < tc8_chunks(M, pack, H); ++c) {
         const int MP = tc8_chunk(M, c, pack, H).MP;
         bool ok;
         if (pack == kPackHalf4) ok = fits<kPackHalf4>(MP, H);
@@ -1061,7 +1063,7 @@ cudaError_t launch_coarse_tc8(const CoarseArgs &a, const Tc8Workspace &w, cudaSt
     base.coarse = a.coarse;
     base.timeout_flag = a.timeout_flag;
     base.nstage2 = base.nstage3 = 2;
-    for (int c = 0; c < tc8_chunks(a.M, a.pack); ++c) {
+    for (int c = 0; c < tc8_chunks(a.M, a.pack, a.H); ++c) {
         const Tc8Chunk k = tc8_chunk(a.M, c, a.pack, a.H);
         const float *const small = w.small + static_cast<size_t>(c) * tc8_small_floats(a.H);
         base.m0 = k.m0;

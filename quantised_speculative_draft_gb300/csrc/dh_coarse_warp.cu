@@ -331,14 +331,22 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta, 1)
     }
 }
 
+// Shared memory a launch needs besides its stage rings: the staged x of NT n8 tiles, the group
+// sums and small scratch.
+size_t warp_fixed_smem(int NT, int H)
+{
+    const size_t xw_bytes = static_cast<size_t>(H / 512) * 4 * NT * 2048;
+    return 1024 /*alignment slack*/ + xw_bytes + static_cast<size_t>(8 * NT) * (H / kGroup + 1) * 4 +
+           16 + 8 * 64;
+}
+
 template <int NT>
 cudaError_t launch_nt(const CoarseArgs &a, const CUtensorMap &tm, cudaStream_t stream)
 {
-    const int H = a.H, NG = H / 512, NGt = H / kGroup;
+    const int H = a.H, NG = H / 512;
     const int nblk = (a.V + kBlockN - 1) / kBlockN;
     const uint32_t xw_bytes = static_cast<uint32_t>(NG) * 4 * NT * 2048;
-    const size_t fixed = 1024 /*alignment slack*/ + xw_bytes +
-                         static_cast<size_t>(8 * NT) * (NGt + 1) * 4 + 16 + 8 * 64;
+    const size_t fixed = warp_fixed_smem(NT, H);
     const int nstage = NG >= 3 ? 3 : NG; // never more stages than spans per item
     int nwarps = static_cast<int>((kSmemLimit - static_cast<long long>(fixed)) /
                                   (static_cast<long long>(nstage) * kStageBytes));
@@ -391,6 +399,14 @@ cudaError_t launch_nt(const CoarseArgs &a, const CUtensorMap &tm, cudaStream_t s
 }
 
 } // namespace
+
+bool warp_supported(int M, int H)
+{
+    if (M < 1 || M > kMaxM || H <= 0 || H % 512 != 0) return false;
+    const int NT = M <= 8 ? 1 : 2;
+    return warp_fixed_smem(NT, H) + 2 * static_cast<size_t>(kStageBytes) <=
+           static_cast<size_t>(kSmemLimit);
+}
 
 cudaError_t launch_coarse_warp(const CoarseArgs &a, cudaStream_t stream)
 {

@@ -129,19 +129,21 @@ bool core_supported(int M, int H);
 int core_mpad(int M);
 cudaError_t launch_coarse_core(const CoarseArgs &a, cudaStream_t stream);
 size_t warp_xw_elems(int M, int H); // bf16 elements of the warp-path operand
+// the warp path's shared memory holds its staged x and at least two stages of one warp
+bool warp_supported(int M, int H);
 
-// tcgen05 path with 8-bit operands.  The batch runs in launches of at most tc8_max_rows(pack)
-// rows; launch c pads its rows to MP in {16, 32, 64} and stages them as kTc8Terms e4m3 terms
+// tcgen05 path with 8-bit operands.  The batch runs in launches of at most
+// tc8_max_rows(pack, H) rows; launch c pads its rows to MP in {16, 32, 64} and stages them as kTc8Terms e4m3 terms
 // ([kTc8Terms * MP, H], term t in rows t * MP ..), of which it uses 2 or 3 (chosen on the
 // device from the staged rows' representation error).
 constexpr int kTc8Terms = 3;
 constexpr int kTc8MaxMP = 64;
-int tc8_max_rows(int pack);
+int tc8_max_rows(int pack, int H);
 struct Tc8Chunk {
     int m0, rows, MP;
     size_t x_off; // byte offset of the launch's staged x in Tc8Workspace::xt8
 };
-int tc8_chunks(int M, int pack);
+int tc8_chunks(int M, int pack, int H);
 Tc8Chunk tc8_chunk(int M, int c, int pack, int H);
 size_t tc8_x_bytes(int M, int H); // staged-x bytes, enough for every pack
 // Per launch, tc8_small_floats(H) floats: xs of the 2-term and of the 3-term representation

@@ -391,7 +391,7 @@ cudaError_t launch_prep_fp8(const uint16_t *x, int M, int H, int pack, const Tc8
                             int *counters, int ncounters, cudaStream_t stream, uint16_t *xcopy)
 {
     PrepChunks ch;
-    ch.n = tc8_chunks(M, pack);
+    ch.n = tc8_chunks(M, pack, H);
     if (ch.n > kMaxPrepChunks) return cudaErrorInvalidValue;
     int blocks = 0;
     for (int c = 0; c < ch.n; ++c) {

@@ -233,3 +233,17 @@ def test_forward_host_rejects_missing_buffers_before_any_cuda_call(lib):
         bad = list(args)
         bad[i] = None
         assert lib.dh_forward_host(*bad, None) == -1
+
+
+def test_every_width_up_to_14336_has_a_coarse_path(lib):
+    """Launch counts (staging + coarse launches + selection) from the host-side plan: the 8-bit
+    path runs 32-row launches up to H = 7168 and 16-row launches above, at any batch size; wider
+    rows have no path, and the forward refuses them before any CUDA call."""
+    count = dh.dh_forward_launch_count
+    assert count(100, 5120, 248320, 8, 32) == 1 + 4 + 1      # 32 + 32 + 32 + 4 rows
+    assert count(100, 8192, 248320, 8, 32) == 1 + 7 + 1      # 16-row launches
+    assert count(128, 14336, 248320, 8, 32) == 1 + 8 + 1
+    assert count(1, 16384, 248320, 8, 32) == 0
+    args = [FAKE] * 5 + [4, 16384, 8192, 8, 32, 1, FAKE, FAKE, FAKE, 1 << 40]
+    assert lib.dh_forward(*args, None) == -8
+    assert "no coarse path" in dh.dh_last_error()

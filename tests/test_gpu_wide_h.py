@@ -1,7 +1,8 @@
 """GPU parity of the 8-bit tcgen05 path at the widest hidden sizes it takes.
 
-At H = 8192 the tile's S/ZS copies leave room for fewer TMA stages, and above 8192 the x staging
-kernel holds a second 16-byte slice of the row per thread.  Each case runs every check of
+At H = 8192 the tile's S/ZS copies leave room for fewer TMA stages, above 7168 the batch runs in
+16-row launches whatever its size, and above 8192 the x staging kernel holds a second 16-byte
+slice of the row per thread.  Each case runs every check of
 parity.py against the oracle on the tcgen05 path explicitly; a size the path does not take is
 skipped (the automatic choice would run another path there).
 """
@@ -27,6 +28,7 @@ def _build():
     (16, 8192, 20000 + 37, 8, 32, 1),   # fewer stages; 157 tiles: some CTAs run two
     (33, 6144, 9000, 8, 32, 4),         # 32-row and 16-row launches at H = 6144
     (16, 12288, 9000, 8, 32, 1),        # the staging kernel's second slice per thread
+    (40, 8192, 9000 + 5, 8, 32, 4),     # wider than a 32-row launch holds: 16 + 16 + 8 rows
 ])
 def test_wide_rows_on_the_tensor_path(M, H, V, kcand, rerank, topk):
     wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
