@@ -1,8 +1,9 @@
 """GPU parity on seeded random configurations: every check of parity.py against the oracle.
 
 The hand-picked cases elsewhere cover the edges one at a time; these draw the batch size,
-hidden size, vocabulary size, KCAND, RERANK and top-k together (seed 2024), on whichever coarse
-path the library chooses for the sizes, so that combinations nobody wrote down are exercised
+hidden size, vocabulary size, KCAND, RERANK and top-k together (seeded), on whichever coarse
+path the library chooses for the sizes -- for the bf16 2-bit head, the 4-bit head and the fp8
+head -- so that combinations nobody wrote down are exercised
 too: ragged tail blocks with small KCAND, RERANK above 32 (the radix selection and the
 standalone rerank) next to batch chunks, wide rows with small heads.  The product M H V is
 capped so that the oracle finishes each case in seconds.
@@ -14,7 +15,8 @@ import torch
 import quantised_speculative_draft_gb300 as dh
 from quantised_speculative_draft_gb300 import synth
 
-from parity import full_compare, gpu_quantize
+from oracle import oracle as orc
+from parity import check_result, full_compare, gpu_quantize, host
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -25,12 +27,12 @@ def _valid_candidates(V, kcand):
     return full * kcand + min(tail, kcand)
 
 
-def _cases(n=14, seed=2024):
+def _cases(n=14, seed=2024, max_h=8192):
     rng = np.random.default_rng(seed)
     out = []
     while len(out) < n:
         M = int(rng.choice([1, 2, 3, 5, 8, 13, 16, 17, 24, 32, 33, 48, 64, 72, 100, 128]))
-        H = 512 * int(rng.integers(1, 17))
+        H = 512 * int(rng.integers(1, max_h // 512 + 1))
         V = int(rng.integers(64, 30000))
         if M * H * V > 4e9:
             continue
@@ -51,7 +53,7 @@ def _build():
     torch.cuda.init()
 
 
-@pytest.mark.parametrize("M, H, V, kcand, R, topk", _cases())
+@pytest.mark.parametrize("M, H, V, kcand, R, topk", _cases() + _cases(8, seed=7, max_h=15360))
 def test_random_configuration(M, H, V, kcand, R, topk):
     wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
     x, W = synth.make_x(wl, M + V, DEV), synth.make_w(wl, H + V, DEV)
@@ -59,3 +61,37 @@ def test_random_configuration(M, H, V, kcand, R, topk):
     rep, gpu, ref = full_compare(x, W, packed, S, ZS, kcand, R, topk)
     print((M, H, V, kcand, R, topk), "path", dh.dh_coarse_path_for(M), rep["coarse_worst"],
           rep["exact_worst"], "tie rows", len(rep["ties"]))
+
+
+@pytest.mark.parametrize("M, H, V, kcand, R, topk", _cases(6, seed=11, max_h=11264))
+def test_random_configuration_4bit_head(M, H, V, kcand, R, topk):
+    wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    x, W = synth.make_x(wl, M + V, DEV), synth.make_w(wl, H + V, DEV)
+    packed = torch.empty(V, H // 2, dtype=torch.uint8, device=DEV)
+    S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=DEV)
+    ZS = torch.empty_like(S)
+    dh.dh_quantize4(W, packed, S, ZS)
+    rep, gpu, ref = full_compare(x, W, packed, S, ZS, kcand, R, topk, bits=4)
+    print((M, H, V, kcand, R, topk), "4-bit", rep["coarse_worst"], "tie rows", len(rep["ties"]))
+
+
+@pytest.mark.parametrize("M, H, V, kcand, R, topk", _cases(6, seed=13))
+def test_random_configuration_fp8_head(M, H, V, kcand, R, topk):
+    wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    x = synth.make_x(wl, M + V, DEV)
+    W8, rs = synth.make_w_fp8(wl, H + V, DEV)
+    packed = torch.empty(V, H // 4, dtype=torch.uint8, device=DEV)
+    S = torch.empty(V, H // 128, dtype=torch.bfloat16, device=DEV)
+    ZS = torch.empty_like(S)
+    dh.dh_quantize_fp8(W8, rs, packed, S, ZS)
+    ws = torch.empty(dh.dh_workspace_bytes(M, H, V, kcand, R), dtype=torch.uint8, device=DEV)
+    idx = torch.empty(M, topk, dtype=torch.int32, device=DEV)
+    logit = torch.empty(M, topk, dtype=torch.float32, device=DEV)
+    dh.dh_forward_fp8w(x, packed, S, ZS, W8, rs, kcand, R, topk, idx, logit, ws)
+    torch.cuda.synchronize()
+    assert dh.dh_device_status(reset=True) == 0
+    xb, W8h, rsh = host(x), W8.cpu().numpy(), rs.cpu().numpy()
+    ref = orc.forward_fp8(xb, host(packed), host(S), host(ZS), W8h, rsh, kcand, R, topk)
+    ties = check_result({"idx": idx.cpu().numpy(), "logit": logit.cpu().numpy()}, ref, kcand,
+                        topk, xb, None, rerank_fn=lambda xr, ix: orc.rerank_fp8(xr, W8h, rsh, ix))
+    print((M, H, V, kcand, R, topk), "fp8", "tie rows", len(ties))
