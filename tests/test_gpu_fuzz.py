@@ -95,3 +95,57 @@ def test_random_configuration_fp8_head(M, H, V, kcand, R, topk):
     ties = check_result({"idx": idx.cpu().numpy(), "logit": logit.cpu().numpy()}, ref, kcand,
                         topk, xb, None, rerank_fn=lambda xr, ix: orc.rerank_fp8(xr, W8h, rsh, ix))
     print((M, H, V, kcand, R, topk), "fp8", "tie rows", len(ties))
+
+
+def _forced_cases():
+    out = []
+    for path, Ms in ((dh.PATH_CORE, [1, 2, 3, 4]), (dh.PATH_TC_BF16, [1, 5, 16, 17, 40]),
+                     (dh.PATH_WARP, [1, 7, 16, 33, 64])):
+        rng = np.random.default_rng(100 + path)
+        for _ in range(4):
+            M = int(rng.choice(Ms))
+            H = 512 * int(rng.integers(1, 13))
+            V = int(rng.integers(64, 20000))
+            kcand = int(rng.integers(1, 65))
+            top = min(_valid_candidates(V, kcand), 1024, V)
+            R = int(rng.integers(1, min(top, 64) + 1))
+            topk = int(rng.integers(1, min(R, 16) + 1))
+            out.append((path, M, H, V, kcand, R, topk))
+    return out
+
+
+@pytest.mark.parametrize("path, M, H, V, kcand, R, topk", _forced_cases())
+def test_random_configuration_forced_path(path, M, H, V, kcand, R, topk):
+    """The other coarse implementations, each forced, on sizes it takes (skipped otherwise)."""
+    wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    x, W = synth.make_x(wl, M + V, DEV), synth.make_w(wl, H + V, DEV)
+    packed, S, ZS = gpu_quantize(W)
+    try:
+        rep, gpu, ref = full_compare(x, W, packed, S, ZS, kcand, R, topk, path=path)
+    except dh.DHError as e:
+        pytest.skip(f"path {path} does not take M={M}, H={H}: {e}")
+    print((path, M, H, V, kcand, R, topk), rep["coarse_worst"], "tie rows", len(rep["ties"]))
+
+
+@pytest.mark.parametrize("M, H, V, kcand, R, topk", _cases(6, seed=17))
+def test_random_configuration_entry_points_agree(M, H, V, kcand, R, topk):
+    """dh_forward, dh_forward_host and dh_forward_noalloc run the same kernels: bit for bit."""
+    wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    x, W = synth.make_x(wl, M + V, DEV), synth.make_w(wl, H + V, DEV)
+    packed, S, ZS = gpu_quantize(W)
+    ws = torch.empty(dh.dh_workspace_bytes(M, H, V, kcand, R), dtype=torch.uint8, device=DEV)
+    idx = torch.empty(M, topk, dtype=torch.int32, device=DEV)
+    logit = torch.empty(M, topk, dtype=torch.float32, device=DEV)
+    dh.dh_forward(x, packed, S, ZS, W, kcand, R, topk, idx, logit, ws)
+    ih = torch.empty(M, topk, dtype=torch.int32).pin_memory()
+    lh = torch.empty(M, topk, dtype=torch.float32).pin_memory()
+    dh.dh_forward_host(x.cpu().pin_memory(), packed, S, ZS, W, kcand, R, topk, ih, lh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(ih, idx.cpu())
+    assert torch.equal(lh.view(torch.int32), logit.cpu().view(torch.int32))
+    if ws.numel() <= dh.NOALLOC_WORKSPACE_BYTES:
+        i2, l2 = torch.empty_like(idx), torch.empty_like(logit)
+        dh.dh_forward_noalloc(x, packed, S, ZS, W, kcand, R, topk, i2, l2)
+        torch.cuda.synchronize()
+        assert torch.equal(i2, idx) and torch.equal(l2.view(torch.int32), logit.view(torch.int32))
+    assert dh.dh_device_status(reset=True) == 0
