@@ -149,3 +149,68 @@ def test_random_configuration_entry_points_agree(M, H, V, kcand, R, topk):
         torch.cuda.synchronize()
         assert torch.equal(i2, idx) and torch.equal(l2.view(torch.int32), logit.view(torch.int32))
     assert dh.dh_device_status(reset=True) == 0
+
+
+def _shard_cases(n=5, seed=23):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        P = int(rng.integers(2, 5))
+        M = int(rng.choice([1, 3, 16, 17, 40]))
+        H = 512 * int(rng.integers(1, 11))
+        kcand = int(rng.integers(1, 17))
+        R = int(rng.integers(1, 65))
+        topk = int(rng.integers(1, min(R, 16) + 1))
+        # every shard holds at least R valid candidates
+        V = int(rng.integers(P * 64 * (R // kcand + 2), 30000))
+        if M * H * V > 2e9:
+            continue
+        out.append((P, M, H, V, kcand, R, topk))
+    return out
+
+
+@pytest.mark.parametrize("P, M, H, V, kcand, R, topk", _shard_cases())
+def test_random_configuration_sharded_head(P, M, H, V, kcand, R, topk):
+    """P sequential vocabulary shards through the C ABI equal the unsharded forward bit for
+    bit."""
+    from quantised_speculative_draft_gb300.sharded import (DeviceShard,
+                                                           sharded_forward_sequential, split_rows)
+    wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    x, W = synth.make_x(wl, M + V, DEV), synth.make_w(wl, H + V, DEV)
+    packed, S, ZS = gpu_quantize(W)
+    ws = torch.empty(dh.dh_workspace_bytes(M, H, V, kcand, R), dtype=torch.uint8, device=DEV)
+    idx = torch.empty(M, topk, dtype=torch.int32, device=DEV)
+    logit = torch.empty(M, topk, dtype=torch.float32, device=DEV)
+    dh.dh_forward(x, packed, S, ZS, W, kcand, R, topk, idx, logit, ws)
+    shards = [DeviceShard(packed[a:b], S[a:b], ZS[a:b], W[a:b], a, kcand, R)
+              for a, b in split_rows(V, P)]
+    sidx, slogit = sharded_forward_sequential(x, shards, topk)
+    torch.cuda.synchronize()
+    assert dh.dh_device_status(reset=True) == 0
+    assert torch.equal(sidx, idx)
+    assert torch.equal(slogit.view(torch.int32), logit.view(torch.int32))
+
+
+@pytest.mark.parametrize("layout", ["c4", "g64"])
+@pytest.mark.parametrize("case", range(3))
+def test_random_configuration_packing_ablations(layout, case):
+    """The contiguous-4 and group-64 heads on random sizes they take (skipped otherwise)."""
+    rng = np.random.default_rng(31 + case + (10 if layout == "g64" else 0))
+    M = int(rng.choice([1, 5, 16] if layout == "g64" else [1, 5, 16, 17, 33]))
+    H = 512 * int(rng.integers(1, 11))
+    V = int(rng.integers(64, 20000))
+    kcand = int(rng.integers(1, 65))
+    R = int(rng.integers(1, min(_valid_candidates(V, kcand), 64, V) + 1))
+    topk = int(rng.integers(1, min(R, 16) + 1))
+    wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    x, W = synth.make_x(wl, M + V, DEV), synth.make_w(wl, H + V, DEV)
+    G = 64 if layout == "g64" else 128
+    packed = torch.empty(V, H // 4, dtype=torch.uint8, device=DEV)
+    S = torch.empty(V, H // G, dtype=torch.bfloat16, device=DEV)
+    ZS = torch.empty_like(S)
+    (dh.dh_quantize_g64 if layout == "g64" else dh.dh_quantize_c4)(W, packed, S, ZS)
+    try:
+        rep, gpu, ref = full_compare(x, W, packed, S, ZS, kcand, R, topk, bits=layout)
+    except dh.DHError as e:
+        pytest.skip(f"{layout} does not take M={M}, H={H}: {e}")
+    print((layout, M, H, V, kcand, R, topk), rep["coarse_worst"], "tie rows", len(rep["ties"]))
