@@ -214,3 +214,16 @@ def test_random_configuration_packing_ablations(layout, case):
     except dh.DHError as e:
         pytest.skip(f"{layout} does not take M={M}, H={H}: {e}")
     print((layout, M, H, V, kcand, R, topk), rep["coarse_worst"], "tie rows", len(rep["ties"]))
+
+
+@pytest.mark.parametrize("M, H, V, kcand, R, topk", [
+    (2, 1024, 70000, 16, 1024, 1024),   # the largest RERANK, every reranked entry returned
+    (5, 2048, 20011, 64, 700, 333),     # a large top-k from a ragged head
+    (17, 512, 9000, 8, 100, 65),        # top-k just above two warps' worth
+])
+def test_large_topk(M, H, V, kcand, R, topk):
+    wl = synth.custom(M, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    x, W = synth.make_x(wl, M + V, DEV), synth.make_w(wl, H + V, DEV)
+    packed, S, ZS = gpu_quantize(W)
+    rep, gpu, ref = full_compare(x, W, packed, S, ZS, kcand, R, topk)
+    print((M, H, V, kcand, R, topk), rep["coarse_worst"], "tie rows", len(rep["ties"]))
