@@ -227,3 +227,39 @@ def test_large_topk(M, H, V, kcand, R, topk):
     packed, S, ZS = gpu_quantize(W)
     rep, gpu, ref = full_compare(x, W, packed, S, ZS, kcand, R, topk)
     print((M, H, V, kcand, R, topk), rep["coarse_worst"], "tie rows", len(rep["ties"]))
+
+
+def _quant_shapes(n=6, seed=41):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.choice([1, 2, 3, 7, int(rng.integers(8, 5000))])),
+             512 * int(rng.integers(1, 21))) for _ in range(n)]
+
+
+@pytest.mark.parametrize("kind", ["quarter", "half4", "c4", "g64", "fp8"])
+@pytest.mark.parametrize("V, H", _quant_shapes())
+def test_random_quantiser_shapes(kind, V, H):
+    """Every quantiser bit-exact with the oracle on random head shapes: tiny heads, odd span
+    counts per row (the two-span work items end on one span), widths up to 10240."""
+    from parity import host as hbits
+    wl = synth.custom(1, H, V, hot_rows=max(1, V // 50), hot_scale=4.0)
+    G = 64 if kind == "g64" else 128
+    packed = torch.empty(V, H // (2 if kind == "half4" else 4), dtype=torch.uint8, device=DEV)
+    S = torch.empty(V, H // G, dtype=torch.bfloat16, device=DEV)
+    ZS = torch.empty_like(S)
+    if kind == "fp8":
+        W8, rs = synth.make_w_fp8(wl, V + H, DEV)
+        dh.dh_quantize_fp8(W8, rs, packed, S, ZS)
+        ref = orc.quantize_fp8(W8.cpu().numpy(), rs.cpu().numpy())
+    else:
+        W = synth.make_w(wl, V + H, DEV)
+        fn, rf = {"quarter": (dh.dh_quantize, orc.quantize),
+                  "half4": (dh.dh_quantize4, orc.quantize4),
+                  "c4": (dh.dh_quantize_c4, orc.quantize_c4),
+                  "g64": (dh.dh_quantize_g64, orc.quantize_g64)}[kind]
+        fn(W, packed, S, ZS)
+        ref = rf(hbits(W))
+    torch.cuda.synchronize()
+    rp, rS, rZS = ref
+    assert np.array_equal(hbits(packed), rp)
+    assert np.array_equal(hbits(S), rS)
+    assert np.array_equal(hbits(ZS), rZS)
