@@ -95,6 +95,10 @@ size_t dh_workspace_bytes(int M, int H, int V, int kcand, int rerank);
  *   workspace, ws_bytes      device scratch of at least dh_workspace_bytes(...)
  * Ranking: coarse values and exact values are compared in fp32; equal values go to the
  * lower vocabulary index.  Only reranked entries are eligible for the result.
+ * Sizes: every M with H <= 15360 has a coarse path (the 8-bit tcgen05 path in launches of 32
+ * rows up to H = 7168 and of 16 rows above; the warp path where its shared memory holds the
+ * staged x); wider rows, or a forced path (dh_set_coarse_path) that does not take the sizes,
+ * give DH_ERR_ARG.
  * Returns DH_OK or a negative DH_ERR_* (checked before any launch).
  */
 int dh_forward(const uint16_t *x, const uint8_t *packed, const uint16_t *scales,
@@ -366,8 +370,8 @@ int dh_forward4_timed(const uint16_t *x, const uint8_t *packed, const uint16_t *
  *
  * dh_quantize_c4 -- dh_quantize with packed [V, H/4] u8 holding k = 4j .. 4j+3 in byte j
  *   (code of k = 4j + f in bits 2f .. 2f+1); scales and zeros as dh_quantize.  Bit-exact.
- * dh_forward_c4_debug -- the forward on that packing (8-bit tcgen05 path only, DH_ERR_ARG
- *   otherwise), with dh_forward_debug's optional outputs and, when `events` is not NULL,
+ * dh_forward_c4_debug -- the forward on that packing (8-bit tcgen05 path only, H <= 15360;
+ *   DH_ERR_ARG otherwise, before any launch), with dh_forward_debug's optional outputs and, when `events` is not NULL,
  *   dh_forward_timed's stage events.  Everything else as dh_forward.
  */
 int dh_quantize_c4(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
@@ -386,7 +390,7 @@ int dh_forward_c4_debug(const uint16_t *x, const uint8_t *packed, const uint16_t
  *
  * dh_quantize_g64 -- dh_quantize with groups of 64 consecutive k: scales, zeros [V, H/64] bf16
  *   (S = bf16(4 sc), ZS = bf16(4 sc + zp sc) per 64-group); packed [V, H/4] quarter split.
- * dh_forward_g64_debug -- the forward on that head, M <= 16, 8-bit tcgen05 path only
+ * dh_forward_g64_debug -- the forward on that head, M <= 16, H <= 7680, 8-bit tcgen05 path only
  *   (DH_ERR_ARG otherwise); optional debug outputs and stage events as dh_forward_c4_debug.
  */
 int dh_quantize_g64(const uint16_t *W_bf16, int V, int H, uint8_t *packed, uint16_t *scales,
