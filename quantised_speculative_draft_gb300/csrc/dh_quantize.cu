@@ -191,6 +191,23 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t v)
     return make_float2(lo, hi);
 }
 
+// Element-wise minimum / maximum of two bf16 pairs (each result is one of its inputs; the sign
+// of a zero result may differ from fminf's, which changes no code, S or ZS: the extrema enter
+// only as hi - lo and -lo / sc, rounded to an integer and clamped at 0).
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // min / max over the whole warp in one instruction each (groups of 128: every lane holds four
 // weights of each group of the span)
 __device__ __forceinline__ float warp_min_f32(float v)
@@ -314,10 +331,21 @@ __global__ void __launch_bounds__(256, 3) quantize_kernel(const void *__restrict
             for (int j = 0; j < SPI; ++j)
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
-                    float w[4];
-                    weights(j, p, w);
-                    const float lo = warp_min_f32(fminf(fminf(w[0], w[1]), fminf(w[2], w[3])));
-                    const float hi = warp_max_f32(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])));
+                    float tmin, tmax; // the lane's four weights' extrema
+                    if constexpr (kFp8 || BITS == 4) { // (the packed form measured slower here)
+                        float w[4];
+                        weights(j, p, w);
+                        tmin = fminf(fminf(w[0], w[1]), fminf(w[2], w[3]));
+                        tmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+                    } else {
+                        // on the packed bf16 pairs first (exact selections), then the halves
+                        const uint32_t mn = bf16x2_min(raw[j][p].x, raw[j][p].y);
+                        const uint32_t mx = bf16x2_max(raw[j][p].x, raw[j][p].y);
+                        tmin = fminf(__uint_as_float(mn << 16), __uint_as_float(mn & 0xFFFF0000u));
+                        tmax = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
+                    }
+                    const float lo = warp_min_f32(tmin);
+                    const float hi = warp_max_f32(tmax);
                     if (gl == j * P + p) {
                         glo = lo;
                         ghi = hi;
